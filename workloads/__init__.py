@@ -1,0 +1,373 @@
+"""Seeded synthetic decode-attention workloads.
+
+This module only *generates inputs*: request lengths, block tables, prefix
+groups, and K/V pools filled with N(0, 1) values encoded as fp32, bf16 or
+fp8-e4m3 codes with per-head scales.  It holds none of the attention
+arithmetic; both the CUDA library's tests/bench and the CPU oracle read the
+arrays it returns.
+
+Layouts (shared by every consumer):
+  q       [B, Hq, d]                     q_dtype   (fp32 or bf16 bit patterns as uint16)
+  k_pool  [num_pages, page_size, Hkv, d] kv_dtype  (fp32, bf16 bits as uint16, or e4m3 codes as uint8)
+  v_pool  same as k_pool
+  k_scale, v_scale [Hkv] float32 (fp8 only; dequantised value = code * scale)
+  block table as CSR: page_indptr[B+1], page_indices[...] int32, logical page order
+  kv_len[B] int32 (context length including the token being decoded)
+  prefix_group[B] int32 (-1 = no shared prefix), group_prefix_len[num_groups] int32 tokens
+
+Workload shapes follow the five cells of the study: a tiny fp32 case, a
+Llama-3.1-8B-shaped layer without sharing at page sizes 1/16/128, a 256-request
+agent batch sharing a 4096-token prefix, a short-prefix dispatcher case and a
+large fp8 shared-prefix case ("GraniKV: asymmetric KV cache paging for
+shared-prefix agents", sections 2-4; "The 25% Page-Size Slowdown That Wasn't",
+"Scope and evidence boundaries").
+
+Generation recipe (seeded, platform independent for a given numpy):
+  1. Lengths from numpy.random.default_rng([seed, 0]) (uniform, inclusive
+     bounds); Q, then the logical K and V rows of every stored token (shared
+     prefix tokens first, then each request's private tokens in request
+     order), all N(0, 1) float32 from the chunked streams of normal_f32
+     (streams 1, 2, 3).
+  2. Layout uses its own generator seeded (seed, page_size, layout): the pool
+     holds ceil(1.25 x pages needed) pages (or a fixed count); physical ids
+     come from a random permutation (shared-prefix pages first, then each
+     request's private pages).  The logical content therefore does not depend
+     on the page size or the permutation.
+  3. Block-aligned sharing: only floor(P / page_size) full pages of a
+     P-token prefix are stored once; the remaining prefix tokens are copied
+     into each member's first private page ("Track C Document 10", block
+     size discussion: 2,003 tokens at block 16 share 125 blocks).
+  4. Every pool slot no request references, and the unused tail of each
+     partially filled last page, holds NaN (fp32/bf16) or the e4m3 NaN code
+     0x7F, so that any unmasked or out-of-bounds read poisons the output.
+  5. Encoding: bf16 by round-to-nearest-even of the float32 value; fp8 with
+     scale_h = amax_h / 448 over all logical tokens of KV head h and codes =
+     RNE(clip(x / scale_h, -448, 448)) in the OCP e4m3 ("fn") format.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+import os
+from typing import Optional
+
+import numpy as np
+
+DTYPES = ("f32", "bf16", "fp8_e4m3")
+
+BF16_NAN = np.uint16(0x7FC0)
+FP8_NAN = np.uint8(0x7F)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """Shape and length distribution of one synthetic decode step."""
+
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    q_dtype: str
+    kv_dtype: str
+    o_dtype: str
+    prefix_len: int           # shared prefix tokens (0 = no sharing)
+    private_lo: int           # private (suffix) length, uniform in [lo, hi]
+    private_hi: int
+    page_size: int
+    num_pages: Optional[int] = None   # None = ceil(1.25 x needed)
+    description: str = ""
+
+
+WORKLOADS = {
+    "tiny": Workload(
+        "tiny", 4, 8, 2, 64, "f32", "f32", "f32", 64, 1, 48, 16, 64,
+        "B=4, 8 q / 2 KV heads, d=64, fp32; 64-token shared prefix, suffixes U[1,48]; "
+        "page size 16 in a pool of 64 permuted pages"),
+    "llama8b_noshare": Workload(
+        "llama8b_noshare", 32, 32, 8, 128, "bf16", "bf16", "bf16", 0, 2048, 4096, 16, None,
+        "Llama-3.1-8B-shaped layer, no sharing: B=32, 32 q / 8 KV heads, d=128, bf16; "
+        "contexts U[2048,4096]; page sizes 1/16/128, pages scattered"),
+    "agent": Workload(
+        "agent", 256, 32, 8, 128, "bf16", "bf16", "bf16", 4096, 128, 1024, 16, None,
+        "shared-prefix agent batch: B=256, 32 q / 8 KV heads (M_eff=1024), d=128, bf16; "
+        "4096-token prefix stored once, suffixes U[128,1024]; page size 16"),
+    "short_prefix": Workload(
+        "short_prefix", 64, 16, 8, 128, "bf16", "bf16", "bf16", 512, 256, 2048, 16, None,
+        "short-prefix dispatcher case: B=64, 16 q / 8 KV heads (GQA 2, M_eff=128), d=128, bf16; "
+        "512-token prefix, suffixes U[256,2048]; page size 16"),
+    "fp8_large": Workload(
+        "fp8_large", 512, 64, 8, 128, "bf16", "fp8_e4m3", "bf16", 16384, 1, 2048, 16, None,
+        "large shared prefix, fp8 cache: B=512, 64 q / 8 KV heads (GQA 8, M_eff=4096), d=128; "
+        "e4m3 KV with per-head fp32 scales, bf16 Q; 16384-token prefix, suffixes U[1,2048]; "
+        "page size 16, pages permuted"),
+}
+
+
+@dataclasses.dataclass
+class Case:
+    """One generated decode step: configuration, block tables and tensors (numpy)."""
+
+    workload: Workload
+    seed: int
+    page_size: int
+    num_pages: int
+    layout: str
+    kv_len: np.ndarray            # [B] int32
+    page_indptr: np.ndarray       # [B+1] int32
+    page_indices: np.ndarray      # [nnz] int32
+    prefix_group: np.ndarray      # [B] int32
+    group_prefix_len: np.ndarray  # [G] int32
+    q: np.ndarray
+    k_pool: np.ndarray
+    v_pool: np.ndarray
+    k_scale: Optional[np.ndarray]
+    v_scale: Optional[np.ndarray]
+    # optional: encoded logical rows before paging, and each request's row ids into them
+    k_logical: Optional[np.ndarray] = None
+    v_logical: Optional[np.ndarray] = None
+    logical_rows: Optional[list] = None
+
+    @property
+    def batch(self) -> int:
+        return int(self.kv_len.shape[0])
+
+    @property
+    def num_groups(self) -> int:
+        return int(self.group_prefix_len.shape[0])
+
+    def without_sharing(self) -> "Case":
+        """Same step with every request reading its prefix through its own block table."""
+        return dataclasses.replace(
+            self,
+            prefix_group=np.full_like(self.prefix_group, -1),
+            group_prefix_len=np.zeros((0,), np.int32))
+
+    def kv_token_bytes(self) -> int:
+        """Bytes of K plus V for one token over all KV heads."""
+        w = self.workload
+        return 2 * w.num_kv_heads * w.head_dim * elem_bytes(w.kv_dtype)
+
+
+def elem_bytes(dtype: str) -> int:
+    return {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[dtype]
+
+
+_CHUNK = 1 << 22
+
+
+def normal_f32(shape, seed: int, stream: int) -> np.ndarray:
+    """N(0, 1) float32 array drawn in fixed 4 Mi-element chunks.
+
+    Chunk i comes from numpy.random.default_rng([seed, stream, i]), so the
+    values do not depend on how many threads fill the chunks.
+    """
+    n = int(np.prod(shape))
+    out = np.empty(n, np.float32)
+    n_chunks = (n + _CHUNK - 1) // _CHUNK
+
+    def fill(i):
+        g = np.random.default_rng([seed, stream, i])
+        g.standard_normal(dtype=np.float32, out=out[i * _CHUNK:(i + 1) * _CHUNK])
+
+    if n_chunks <= 1:
+        for i in range(n_chunks):
+            fill(i)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
+            list(ex.map(fill, range(n_chunks)))
+    return out.reshape(shape)
+
+
+def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); returns uint16 bit patterns."""
+    import torch  # dtype conversion only
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def fp8_codes_from_f32(x: np.ndarray) -> np.ndarray:
+    """Encode float32 values (already within +-448) as OCP e4m3 codes, nearest-even."""
+    import torch  # dtype conversion only
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _encode(x: np.ndarray, dtype: str, scale: Optional[np.ndarray] = None) -> np.ndarray:
+    if dtype == "f32":
+        return np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == "bf16":
+        return bf16_bits_from_f32(x)
+    if dtype == "fp8_e4m3":
+        assert scale is not None
+        y = x / scale.reshape((1,) * (x.ndim - 2) + (-1, 1)).astype(np.float32)
+        np.clip(y, -448.0, 448.0, out=y)
+        return fp8_codes_from_f32(y)
+    raise ValueError(dtype)
+
+
+def _poison(dtype: str):
+    return {"f32": np.float32(np.nan), "bf16": BF16_NAN, "fp8_e4m3": FP8_NAN}[dtype]
+
+
+def _np_dtype(dtype: str):
+    return {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8}[dtype]
+
+
+def make_case(name: str, seed: int = 0, *, page_size: Optional[int] = None,
+              batch: Optional[int] = None, prefix_len: Optional[int] = None,
+              private_range: Optional[tuple] = None, num_pages: Optional[int] = None,
+              layout: str = "scatter", num_q_heads: Optional[int] = None,
+              num_kv_heads: Optional[int] = None, head_dim: Optional[int] = None,
+              kv_dtype: Optional[str] = None, private_lengths: Optional[list] = None,
+              keep_logical: bool = False) -> Case:
+    """Generate one seeded decode step of workload `name`.
+
+    Overrides shrink or reshape a workload for tests (batch, prefix length,
+    private length range or explicit private lengths, page size, heads).
+    `layout` is "scatter" (random physical permutation), "contiguous"
+    (physical ids in logical order) or "block128" (runs of 128 consecutive
+    token slots in shuffled order; page size must divide 128).  With
+    `keep_logical`, the encoded rows before paging are kept (contiguous
+    per-request K/V for brute-force checks).
+    """
+    w = WORKLOADS[name]
+    w = dataclasses.replace(
+        w,
+        batch=batch if batch is not None else w.batch,
+        prefix_len=prefix_len if prefix_len is not None else w.prefix_len,
+        private_lo=private_range[0] if private_range else w.private_lo,
+        private_hi=private_range[1] if private_range else w.private_hi,
+        num_q_heads=num_q_heads or w.num_q_heads,
+        num_kv_heads=num_kv_heads or w.num_kv_heads,
+        head_dim=head_dim or w.head_dim,
+        kv_dtype=kv_dtype or w.kv_dtype,
+        num_pages=num_pages if num_pages is not None else w.num_pages,
+    )
+    ps = int(page_size if page_size is not None else w.page_size)
+    if ps < 1:
+        raise ValueError("page size must be >= 1")
+    B, Hq, Hkv, d = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    rng = np.random.default_rng([seed, 0])
+
+    # 1. lengths, Q, logical K/V (independent of page size and layout)
+    if private_lengths is not None:
+        priv = np.asarray(private_lengths, dtype=np.int64)
+        assert priv.shape == (B,)
+    else:
+        priv = rng.integers(w.private_lo, w.private_hi + 1, size=B).astype(np.int64)
+    P = int(w.prefix_len)
+    kv_len = (P + priv).astype(np.int32)
+    q32 = normal_f32((B, Hq, d), seed, 1)
+    n_tok = P + int(priv.sum())
+    k_log = normal_f32((n_tok, Hkv, d), seed, 2)
+    v_log = normal_f32((n_tok, Hkv, d), seed, 3)
+
+    k_scale = v_scale = None
+    if w.kv_dtype == "fp8_e4m3":
+        k_scale = (np.abs(k_log).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
+        v_scale = (np.abs(v_log).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
+    k_enc = _encode(k_log, w.kv_dtype, k_scale)
+    del k_log
+    v_enc = _encode(v_log, w.kv_dtype, v_scale)
+    del v_log
+    offsets = P + np.concatenate([[0], np.cumsum(priv)[:-1]]) if B else np.zeros(0, np.int64)
+    rows_of = [np.concatenate([np.arange(P), offsets[b] + np.arange(int(priv[b]))]).astype(np.int64)
+               for b in range(B)] if keep_logical else None
+    q = _encode(q32, w.q_dtype)
+
+    # 2. layout: block-aligned sharing of the prefix
+    n_sh = P // ps if P > 0 else 0
+    tail = P - n_sh * ps                       # prefix tokens every member stores privately
+    own_tokens = tail + priv                   # tokens in each request's private pages
+    own_pages = (own_tokens + ps - 1) // ps
+    needed = n_sh + int(own_pages.sum())
+    if w.num_pages is not None:
+        n_pages = int(w.num_pages)
+        if n_pages < needed:
+            raise ValueError(f"pool of {n_pages} pages cannot hold {needed}")
+    else:
+        n_pages = int(math.ceil(1.25 * needed))
+    lrng = np.random.default_rng([seed, ps, {"scatter": 0, "contiguous": 1, "block128": 2}[layout]])
+    if layout == "scatter":
+        phys = lrng.permutation(n_pages).astype(np.int64)
+    elif layout == "contiguous":
+        phys = np.arange(n_pages, dtype=np.int64)
+    elif layout == "block128":
+        if 128 % ps:
+            raise ValueError("block128 layout needs a page size dividing 128")
+        ppb = 128 // ps
+        n_blk = (n_pages + ppb - 1) // ppb
+        order = lrng.permutation(n_blk)
+        phys = (order[:, None] * ppb + np.arange(ppb)[None, :]).reshape(-1)
+        phys = phys[phys < n_pages]
+        if phys.shape[0] < n_pages:
+            raise ValueError("block128 layout needs the pool to be a whole number of blocks")
+    else:
+        raise ValueError(layout)
+    prefix_pages = phys[:n_sh]
+    pos = n_sh
+    page_lists = []
+    for b in range(B):
+        mine = phys[pos:pos + own_pages[b]]
+        pos += int(own_pages[b])
+        page_lists.append(np.concatenate([prefix_pages, mine]))
+    page_indptr = np.zeros(B + 1, np.int32)
+    page_indptr[1:] = np.cumsum([len(p) for p in page_lists])
+    page_indices = (np.concatenate(page_lists) if B else np.zeros(0, np.int64)).astype(np.int32)
+
+    # 3. fill the pool (flat slot view), poisoned everywhere first
+    elem = _np_dtype(w.kv_dtype)
+    k_pool = np.full((n_pages * ps, Hkv, d), _poison(w.kv_dtype), dtype=elem)
+    v_pool = np.full((n_pages * ps, Hkv, d), _poison(w.kv_dtype), dtype=elem)
+    if n_sh:
+        t = np.arange(n_sh * ps)
+        slots = prefix_pages[t // ps] * ps + t % ps
+        k_pool[slots] = k_enc[:n_sh * ps]
+        v_pool[slots] = v_enc[:n_sh * ps]
+    src = P
+    for b in range(B):
+        u = np.arange(int(own_tokens[b]))
+        mine = page_lists[b][n_sh:]
+        slots = mine[u // ps] * ps + u % ps
+        rows = np.concatenate([np.arange(n_sh * ps, P), src + np.arange(int(priv[b]))])
+        k_pool[slots] = k_enc[rows]
+        v_pool[slots] = v_enc[rows]
+        src += int(priv[b])
+    k_pool = k_pool.reshape(n_pages, ps, Hkv, d)
+    v_pool = v_pool.reshape(n_pages, ps, Hkv, d)
+
+    if P > 0:
+        prefix_group = np.zeros(B, np.int32)
+        group_prefix_len = np.array([P], np.int32)
+    else:
+        prefix_group = np.full(B, -1, np.int32)
+        group_prefix_len = np.zeros(0, np.int32)
+    return Case(w, seed, ps, n_pages, layout, kv_len, page_indptr, page_indices,
+                prefix_group, group_prefix_len, q, k_pool, v_pool, k_scale, v_scale,
+                k_enc if keep_logical else None, v_enc if keep_logical else None, rows_of)
+
+
+def unique_kv_bytes(case: Case) -> int:
+    """Distinct stored token slots a step must read, times K+V bytes per token.
+
+    A page referenced by several block tables (a shared prefix page) is counted
+    once; per-head fp8 scales are added.
+    """
+    ps = case.page_size
+    counts = np.zeros(case.num_pages, np.int64)
+    for b in range(case.batch):
+        pages = case.page_indices[case.page_indptr[b]:case.page_indptr[b + 1]].astype(np.int64)
+        L = int(case.kv_len[b])
+        used = np.minimum(ps, L - ps * np.arange(pages.shape[0]))
+        np.maximum.at(counts, pages, used)
+    extra = 2 * 4 * case.workload.num_kv_heads if case.k_scale is not None else 0
+    return int(counts.sum()) * case.kv_token_bytes() + extra
+
+
+def paged_kv_bytes(case: Case) -> int:
+    """K+V bytes when every request reads its whole context through its block table."""
+    return int(case.kv_len.astype(np.int64).sum()) * case.kv_token_bytes()
