@@ -1,0 +1,319 @@
+// kernel_suffix.cu -- split-KV paged decode over each request's private suffix.
+//
+// One CTA per (split, KV head).  The CTA serves all G query heads of its KV
+// head, so every suffix K/V byte is read from HBM exactly once per step.
+// Keys and values are gathered token by token through the block table (page
+// granularity 1 << page_shift; at page size 1, or in token-flat mode, the
+// list is the per-token kv_indices) with 16-byte cp.async copies into a
+// per-warp multi-stage shared-memory ring ("The 25% Page-Size Slowdown That
+// Wasn't", "When source beats intuition": each token's K/V row is a contiguous
+// burst, so only the address generation depends on the page size).
+//
+// Each warp owns 16-token sub-tiles w, w+NW, ... of the split.  Scores are the
+// tensor-core product S^T = K Q^T (m16n8k16, tokens on M, the <= 8 query
+// heads on N), the online softmax runs on the accumulator fragments with a
+// three-step shuffle max per tile, P^T is turned into the B operand of the
+// second product by an in-register 8x8 transpose (movmatrix), and the value
+// product is O^T = V^T P^T.  fp8-e4m3 keys/values are converted to f16 in
+// registers (exact); the per-head scales fold into the score and output
+// scalars.  The warps' partial states are combined through shared memory and
+// written as one normalised fp32 partial (O, log2-LSE) per (split, head, q).
+#include <cuda_runtime.h>
+
+#include "psp_device.cuh"
+#include "psp_internal.h"
+
+namespace psp {
+namespace {
+
+using namespace dev;
+
+template <int KV, int D>
+struct SufCfg {
+  static constexpr int kElem = (KV == PSP_KV_BF16) ? 2 : 1;
+  static constexpr int kRowBytes = D * kElem;
+  static constexpr int kChunks = kRowBytes / 16;
+  static constexpr int kTileBytes = 16 * kRowBytes;   // one 16-token sub-tile of K (or V)
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K + V
+  static constexpr int kMTiles = D / 16;              // m16 tiles of the value product
+};
+
+template <int KV, int D, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
+  using C = SufCfg<KV, D>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int h = blockIdx.y;
+  const int b = p.split_req[split];
+  const int t0 = p.split_begin[split];
+  const int t1 = p.split_end[split];
+  const int G = p.group;
+
+  const int32_t* list;
+  int shift;
+  if (p.token_flat) {
+    list = p.kv_indices + p.kv_indptr[b] + p.suffix_start[b];
+    shift = 0;
+  } else {
+    list = p.suffix_page_indices + p.suffix_page_indptr[b];
+    shift = p.page_shift;
+  }
+  const int64_t row_stride = static_cast<int64_t>(p.hkv) * C::kRowBytes;
+  const unsigned char* kbase = static_cast<const unsigned char*>(p.k_pool) + static_cast<int64_t>(h) * C::kRowBytes;
+  const unsigned char* vbase = static_cast<const unsigned char*>(p.v_pool) + static_cast<int64_t>(h) * C::kRowBytes;
+  unsigned char* ring = smem + warp * (NST * C::kStageBytes);
+
+  const int n_sub = (t1 - t0 + 15) >> 4;
+  const int my_n = n_sub > warp ? (n_sub - warp + NW - 1) / NW : 0;
+
+  // -------- query fragments: B operand of S^T = K Q^T (k = head dim, n = query head)
+  const int qg = lane >> 2;  // query head within the group (B fragment column)
+  const int qc = lane & 3;
+  uint32_t qf[D / 16][2];
+  {
+    const bool live = qg < G;
+    const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                (static_cast<int64_t>(b) * p.hq + h * G + (live ? qg : 0)) * D;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      if constexpr (KV == PSP_KV_BF16) {
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow + ks * 16);
+        qf[ks][0] = live ? __ldg(q32 + qc) : 0u;
+        qf[ks][1] = live ? __ldg(q32 + 4 + qc) : 0u;
+      } else {
+        // k-slots (2c, 2c+1) <- d = 4c, 4c+1 and (2c+8, 2c+9) <- d = 4c+2, 4c+3 (matches the
+        // byte order the fp8 key fragments arrive in)
+        const uint2 v = live ? __ldg(reinterpret_cast<const uint2*>(qrow + ks * 16 + 4 * qc)) : make_uint2(0u, 0u);
+        qf[ks][0] = pack_f16(bf16_bits_to_float(v.x & 0xffff), bf16_bits_to_float(v.x >> 16));
+        qf[ks][1] = pack_f16(bf16_bits_to_float(v.y & 0xffff), bf16_bits_to_float(v.y >> 16));
+      }
+    }
+  }
+  float score_scale = p.scale_log2;
+  float out_scale = 1.f;
+  if constexpr (KV == PSP_KV_FP8) {
+    score_scale *= __ldg(p.k_scale + h);
+    out_scale = __ldg(p.v_scale + h);
+  }
+
+  // -------- asynchronous gather of one 16-token sub-tile (K and V) into ring stage i % NST
+  auto issue = [&](int i) {
+    const int tb = t0 + (warp + i * NW) * 16;
+    unsigned char* kdst = ring + (i % NST) * C::kStageBytes;
+    constexpr int kRowsPerPass = 32 / C::kChunks;
+    const int c = lane % C::kChunks;
+#pragma unroll
+    for (int k = 0; k < 16 / kRowsPerPass; ++k) {
+      const int r = lane / C::kChunks + k * kRowsPerPass;
+      const int t = tb + r;
+      const bool valid = t < t1;
+      const int64_t off = valid ? slot_of(list, t, shift) * row_stride + c * 16 : 0;
+      const uint32_t d = smem_u32(kdst + r * C::kRowBytes + swz<C::kChunks>(r, c) * 16);
+      cp_async_16(d, kbase + off, valid);
+      cp_async_16(d + C::kTileBytes, vbase + off, valid);
+    }
+  };
+
+  float o[C::kMTiles][4];
+#pragma unroll
+  for (int mt = 0; mt < C::kMTiles; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float m0 = neg_inf(), m1 = neg_inf();  // running max of query heads 2c, 2c+1 (log2 domain)
+  float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
+
+#pragma unroll
+  for (int i = 0; i < NST - 1; ++i) {
+    if (i < my_n) issue(i);
+    cp_async_commit();
+  }
+
+  for (int i = 0; i < my_n; ++i) {
+    cp_async_wait<NST - 2>();
+    __syncwarp();
+    const unsigned char* kt = ring + (i % NST) * C::kStageBytes;
+    const unsigned char* vt = kt + C::kTileBytes;
+
+    // ---- S^T (16 tokens x 8 query heads)
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const int j = lane >> 3;
+      const int row = (lane & 7) + (j & 1) * 8;
+      if constexpr (KV == PSP_KV_BF16) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t a[4];
+          const int ch = 2 * ks + (j >> 1);
+          ldsm_x4(a, smem_u32(kt + row * C::kRowBytes + swz<C::kChunks>(row, ch) * 16));
+          mma_bf16(s, a, qf[ks][0], qf[ks][1]);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+          uint32_t r[4];
+          const int ch = 2 * kk + (j >> 1);
+          ldsm_x4(r, smem_u32(kt + row * C::kRowBytes + swz<C::kChunks>(row, ch) * 16));
+          const uint32_t a0[4] = {e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[1]), e4m3x2_to_f16x2(r[0] >> 16),
+                                  e4m3x2_to_f16x2(r[1] >> 16)};
+          const uint32_t a1[4] = {e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[3]), e4m3x2_to_f16x2(r[2] >> 16),
+                                  e4m3x2_to_f16x2(r[3] >> 16)};
+          mma_f16(s, a0, qf[2 * kk][0], qf[2 * kk][1]);
+          mma_f16(s, a1, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
+        }
+      }
+    }
+
+    // ---- online softmax on the fragments: rows = tokens (lane>>2, +8), cols = heads (2c, 2c+1)
+    const int tb = t0 + (warp + i * NW) * 16;
+    const bool v_lo = tb + (lane >> 2) < t1;
+    const bool v_hi = tb + (lane >> 2) + 8 < t1;
+    const float s0 = v_lo ? s[0] * score_scale : neg_inf();
+    const float s1 = v_lo ? s[1] * score_scale : neg_inf();
+    const float s2 = v_hi ? s[2] * score_scale : neg_inf();
+    const float s3 = v_hi ? s[3] * score_scale : neg_inf();
+    const float mx0 = xor_max<4, 16>(fmaxf(s0, s2));
+    const float mx1 = xor_max<4, 16>(fmaxf(s1, s3));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+    const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
+    const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
+    l0 = l0 * a0 + p0 + p2;
+    l1 = l1 * a1 + p1 + p3;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int mt = 0; mt < C::kMTiles; ++mt) {
+      o[mt][0] *= a0;
+      o[mt][1] *= a1;
+      o[mt][2] *= a0;
+      o[mt][3] *= a1;
+    }
+    uint32_t pb0, pb1;  // P^T as the B operand (k = token, n = query head)
+    if constexpr (KV == PSP_KV_BF16) {
+      pb0 = movmatrix_t(pack_bf16(p0, p1));
+      pb1 = movmatrix_t(pack_bf16(p2, p3));
+    } else {
+      pb0 = movmatrix_t(pack_f16(p0, p1));
+      pb1 = movmatrix_t(pack_f16(p2, p3));
+    }
+
+    // ---- O^T += V^T P^T
+    {
+      const int j = lane >> 3;
+      const int row = (lane & 7) + (j >> 1) * 8;
+      if constexpr (KV == PSP_KV_BF16) {
+#pragma unroll
+        for (int mt = 0; mt < C::kMTiles; ++mt) {
+          uint32_t a[4];
+          const int ch = 2 * mt + (j & 1);
+          ldsm_x4_t(a, smem_u32(vt + row * C::kRowBytes + swz<C::kChunks>(row, ch) * 16));
+          mma_bf16(o[mt], a, pb0, pb1);
+        }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[4];
+          const int ch = 2 * cc + (j & 1);
+          ldsm_x4_t(r, smem_u32(vt + row * C::kRowBytes + swz<C::kChunks>(row, ch) * 16));
+          // each register: (token 2c: d 2p, 2p+1), (token 2c+1: d 2p, 2p+1); split even / odd d
+          const uint32_t ax[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, 0x20)),
+                                  e4m3x2_to_f16x2(__byte_perm(r[1], 0, 0x20)),
+                                  e4m3x2_to_f16x2(__byte_perm(r[2], 0, 0x20)),
+                                  e4m3x2_to_f16x2(__byte_perm(r[3], 0, 0x20))};
+          const uint32_t ay[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, 0x31)),
+                                  e4m3x2_to_f16x2(__byte_perm(r[1], 0, 0x31)),
+                                  e4m3x2_to_f16x2(__byte_perm(r[2], 0, 0x31)),
+                                  e4m3x2_to_f16x2(__byte_perm(r[3], 0, 0x31))};
+          mma_f16(o[2 * cc], ax, pb0, pb1);
+          mma_f16(o[2 * cc + 1], ay, pb0, pb1);
+        }
+      }
+    }
+    __syncwarp();
+    const int nx = i + NST - 1;
+    if (nx < my_n) issue(nx);
+    cp_async_commit();
+  }
+  cp_async_wait<0>();
+
+  // -------- combine the warps' partial states through shared memory
+  l0 = xor_sum<4, 16>(l0);
+  l1 = xor_sum<4, 16>(l1);
+  __syncthreads();
+  float* red = reinterpret_cast<float*>(smem);  // [NW][8][D]
+  float* ms = red + NW * 8 * D;                 // [NW][8]
+  float* ls = ms + NW * 8;                      // [NW][8]
+  const int c2 = 2 * (lane & 3);
+  if (lane < 4) {
+    ms[warp * 8 + c2] = m0;
+    ms[warp * 8 + c2 + 1] = m1;
+    ls[warp * 8 + c2] = l0;
+    ls[warp * 8 + c2 + 1] = l1;
+  }
+  {
+    const int rr = lane >> 2;
+#pragma unroll
+    for (int mt = 0; mt < C::kMTiles; ++mt) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        int d;
+        if constexpr (KV == PSP_KV_BF16) {
+          d = 16 * mt + 8 * half + rr;
+        } else {
+          d = 32 * (mt >> 1) + 16 * half + 2 * rr + (mt & 1);
+        }
+        red[(warp * 8 + c2) * D + d] = o[mt][2 * half];
+        red[(warp * 8 + c2 + 1) * D + d] = o[mt][2 * half + 1];
+      }
+    }
+  }
+  __syncthreads();
+  const int64_t row0 = (static_cast<int64_t>(split) * p.hkv + h) * G;
+  for (int e = threadIdx.x; e < G * D; e += NW * 32) {
+    const int g = e / D;
+    const int d = e - g * D;
+    float mmax = neg_inf();
+#pragma unroll
+    for (int w = 0; w < NW; ++w) mmax = fmaxf(mmax, ms[w * 8 + g]);
+    float acc = 0.f, sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float sc = exp2f(ms[w * 8 + g] - mmax);
+      sum += ls[w * 8 + g] * sc;
+      acc += red[(w * 8 + g) * D + d] * sc;
+    }
+    p.o_suf[(row0 + g) * D + d] = acc / sum * out_scale;
+    if (d == 0) p.lse_suf[row0 + g] = mmax + log2f(sum);
+  }
+}
+
+template <int KV, int D, int NW, int NST>
+cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
+  using C = SufCfg<KV, D>;
+  const int ring = NW * NST * C::kStageBytes;
+  const int epi = (NW * 8 * D + 2 * NW * 8) * 4;
+  const int bytes = ring > epi ? ring : epi;
+  auto kern = suffix_kernel<KV, D, NW, NST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(num_splits, p.hkv);
+  kern<<<grid, NW * 32, bytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
+  if (num_splits <= 0) return cudaSuccess;
+  if (p.kv_dtype == PSP_KV_BF16) {
+    return p.head_dim == 128 ? launch_t<PSP_KV_BF16, 128, 4, 3>(p, num_splits, s)
+                             : launch_t<PSP_KV_BF16, 64, 4, 4>(p, num_splits, s);
+  }
+  if (p.kv_dtype == PSP_KV_FP8) {
+    return p.head_dim == 128 ? launch_t<PSP_KV_FP8, 128, 4, 5>(p, num_splits, s)
+                             : launch_t<PSP_KV_FP8, 64, 4, 6>(p, num_splits, s);
+  }
+  return launch_suffix_simt(p, num_splits, s);
+}
+
+}  // namespace psp

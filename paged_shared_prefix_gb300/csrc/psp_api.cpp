@@ -1,0 +1,793 @@
+// psp_api.cpp -- the C ABI of the paged shared-prefix decode step: handle and
+// configuration checks, the host-side plan (block-aligned prefix split,
+// dispatcher, split-KV partition), workspace layout, plan upload and the
+// ordered kernel launches of one step.
+#include "psp.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "psp_internal.h"
+
+namespace {
+
+using psp::PlanLayout;
+using psp::StepParams;
+
+// Dense/cascade threshold used when the configuration passes 0.  The pages fit
+// 1024 on A100 and ask for a refit per GPU ("GraniKV", section 3); this value
+// is the GB300 refit from the M_eff sweep of the benchmark.
+constexpr int32_t kDefaultDenseThreshold = 1024;
+
+constexpr int32_t kSplitMinTiles = 4;
+constexpr int32_t kSplitCtasPerSm = 4;
+constexpr int32_t kPrefixMinTiles = 4;
+constexpr int32_t kPrefixCtasPerSm = 1;
+
+thread_local std::string g_create_error;
+
+int env_int(const char* name, int fallback) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return fallback;
+  char* end = nullptr;
+  long x = std::strtol(v, &end, 10);
+  return (end && *end == 0 && x > 0 && x < (1L << 30)) ? static_cast<int>(x) : fallback;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align_up(size_t x) { return (x + psp::kWorkspaceAlign - 1) / psp::kWorkspaceAlign * psp::kWorkspaceAlign; }
+
+int dtype_bytes(int32_t t) {
+  switch (t) {
+    case PSP_DTYPE_F32: return 4;
+    case PSP_DTYPE_BF16: return 2;
+    case PSP_DTYPE_FP8_E4M3: return 1;
+  }
+  return 0;
+}
+
+struct HostPlan {
+  int32_t B = 0, NG = 0, NS = 0, NC = 0;
+  std::vector<int32_t> suffix_page_indptr, suffix_page_indices, suffix_start, suffix_len;
+  std::vector<int32_t> split_indptr, split_req, split_begin, split_end;
+  std::vector<int32_t> req_group, req_member;
+  std::vector<int32_t> group_page_indptr, group_page_indices, group_m_eff, group_shared_len;
+  std::vector<int32_t> group_branch, group_row_blocks;
+  std::vector<int32_t> group_member_indptr, group_members, group_chunk_indptr;
+  std::vector<int32_t> chunk_group, chunk_begin, chunk_end, chunk_row_offset;
+  std::vector<int32_t> item_chunk_dense, item_rb_dense, item_chunk_cascade, item_rb_cascade;
+  std::vector<int32_t> kv_indptr;
+  int64_t kv_indices_len = 0, suffix_tokens = 0, shared_tokens = 0, pre_rows = 0;
+  PlanLayout layout{};
+  psp_plan_info info{};
+};
+
+}  // namespace
+
+struct psp_handle {
+  psp_config cfg{};
+  int32_t group = 1;
+  int32_t page_shift = 0;
+  int32_t split_min_tiles = kSplitMinTiles;
+  int32_t split_ctas_per_sm = kSplitCtasPerSm;
+  int32_t prefix_min_tiles = kPrefixMinTiles;
+  int32_t prefix_ctas_per_sm = kPrefixCtasPerSm;
+  int32_t num_sms_resolved = 0;
+
+  bool planned = false;
+  HostPlan plan;
+
+  // upload state
+  unsigned char* staging = nullptr;
+  size_t staging_bytes = 0;
+  cudaEvent_t staging_done = nullptr;
+  unsigned char* workspace = nullptr;
+  size_t workspace_bytes = 0;
+  bool uploaded = false;
+
+  // per-kernel timing
+  bool timing = false;
+  std::vector<cudaEvent_t> events;       // 2 per launch
+  std::vector<const char*> event_names;
+  int recorded = 0;
+
+  std::string last_error;
+};
+
+namespace {
+
+psp_status fail(psp_handle* h, psp_status code, const std::string& msg) {
+  if (h) h->last_error = msg;
+  else g_create_error = msg;
+  return code;
+}
+
+psp_status cuda_fail(psp_handle* h, cudaError_t e, const char* what) {
+  std::string msg = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return fail(h, PSP_ERR_CUDA, msg);
+}
+
+// ----------------------------------------------------------------- planning
+
+psp_status validate_batch(psp_handle* h, const psp_batch* bt) {
+  const psp_config& c = h->cfg;
+  if (!bt) return fail(h, PSP_ERR_INVALID_ARGUMENT, "batch is NULL");
+  if (bt->batch_size < 0) return fail(h, PSP_ERR_INVALID_ARGUMENT, "negative batch size");
+  if (bt->num_groups < 0) return fail(h, PSP_ERR_INVALID_ARGUMENT, "negative group count");
+  const int B = bt->batch_size;
+  if (B > 0 && (!bt->kv_len || !bt->page_indptr || !bt->page_indices))
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "kv_len/page_indptr/page_indices NULL");
+  if (bt->num_groups > 0 && !bt->group_prefix_len)
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "group_prefix_len NULL");
+  if (B > 0 && bt->page_indptr[0] != 0) return fail(h, PSP_ERR_INVALID_ARGUMENT, "page_indptr[0] != 0");
+  const int64_t ps = c.page_size;
+  int64_t total = 0;
+  for (int b = 0; b < B; ++b) {
+    const int64_t L = bt->kv_len[b];
+    if (L < 1) return fail(h, PSP_ERR_LENGTH, "kv_len[" + std::to_string(b) + "] < 1");
+    const int64_t n = static_cast<int64_t>(bt->page_indptr[b + 1]) - bt->page_indptr[b];
+    if (n != cdiv(L, ps))
+      return fail(h, PSP_ERR_LENGTH, "request " + std::to_string(b) + " has " + std::to_string(n) +
+                                         " pages for kv_len " + std::to_string(L));
+    for (int64_t i = bt->page_indptr[b]; i < bt->page_indptr[b + 1]; ++i) {
+      const int32_t pg = bt->page_indices[i];
+      if (pg < 0 || pg >= c.num_pages)
+        return fail(h, PSP_ERR_PAGE_OUT_OF_RANGE,
+                    "page id " + std::to_string(pg) + " of request " + std::to_string(b) + " outside [0, num_pages)");
+    }
+    total += L;
+    if (total > INT32_MAX) return fail(h, PSP_ERR_INVALID_ARGUMENT, "sum of kv_len exceeds int32");
+  }
+  for (int g = 0; g < bt->num_groups; ++g)
+    if (bt->group_prefix_len[g] < 0) return fail(h, PSP_ERR_INVALID_ARGUMENT, "negative group prefix length");
+  return PSP_OK;
+}
+
+psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
+  const psp_config& c = h->cfg;
+  const int B = bt->batch_size, NG = bt->num_groups, Hkv = c.num_kv_heads, G = h->group;
+  const int64_t ps = c.page_size;
+  const int64_t tile = psp::kTileTokens;
+  const int32_t threshold = c.dense_threshold > 0 ? c.dense_threshold : kDefaultDenseThreshold;
+  const int64_t sms = h->num_sms_resolved;
+  P = HostPlan();
+  P.B = B;
+  P.NG = NG;
+
+  // --- groups: members (increasing request id) and agreement on shared pages
+  std::vector<int32_t> first(NG, -1), count(NG, 0);
+  P.req_group.assign(B, -1);
+  P.req_member.assign(B, -1);
+  for (int b = 0; b < B; ++b) {
+    const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
+    if (g == -1) continue;
+    if (g < -1 || g >= NG) return fail(h, PSP_ERR_INVALID_ARGUMENT, "prefix_group out of range");
+    const int64_t plen = bt->group_prefix_len[g];
+    if (plen > bt->kv_len[b])
+      return fail(h, PSP_ERR_PREFIX_MISMATCH, "group prefix longer than the context of request " + std::to_string(b));
+    const int64_t n_sh = plen / ps;
+    if (first[g] < 0) {
+      first[g] = b;
+    } else {
+      const int32_t* mine = bt->page_indices + bt->page_indptr[b];
+      const int32_t* ref = bt->page_indices + bt->page_indptr[first[g]];
+      if (!std::equal(mine, mine + n_sh, ref))
+        return fail(h, PSP_ERR_PREFIX_MISMATCH,
+                    "request " + std::to_string(b) + " does not share the prefix pages of its group");
+    }
+    P.req_member[b] = count[g]++;
+  }
+  P.group_member_indptr.assign(NG + 1, 0);
+  for (int g = 0; g < NG; ++g) P.group_member_indptr[g + 1] = P.group_member_indptr[g] + count[g];
+  P.group_members.assign(std::max<int64_t>(P.group_member_indptr[NG], 0), 0);
+  for (int b = 0; b < B; ++b) {
+    const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
+    if (g >= 0) P.group_members[P.group_member_indptr[g] + P.req_member[b]] = b;
+  }
+
+  // --- per group: shared pages, M_eff, branch, row blocks, prefix chunks
+  P.group_shared_len.assign(NG, 0);
+  P.group_m_eff.assign(NG, 0);
+  P.group_branch.assign(NG, PSP_BRANCH_NONE);
+  P.group_row_blocks.assign(NG, 0);
+  P.group_page_indptr.assign(NG + 1, 0);
+  P.group_chunk_indptr.assign(NG + 1, 0);
+  for (int g = 0; g < NG; ++g) {
+    const int64_t n_sh = count[g] > 0 ? bt->group_prefix_len[g] / ps : 0;
+    const int64_t shared = n_sh * ps;
+    const int64_t m_eff = static_cast<int64_t>(count[g]) * G;
+    P.group_shared_len[g] = static_cast<int32_t>(shared);
+    P.group_m_eff[g] = static_cast<int32_t>(m_eff);
+    if (n_sh > 0) {
+      const int32_t* src = bt->page_indices + bt->page_indptr[first[g]];
+      P.group_page_indices.insert(P.group_page_indices.end(), src, src + n_sh);
+    }
+    P.group_page_indptr[g + 1] = static_cast<int32_t>(P.group_page_indices.size());
+    int branch = PSP_BRANCH_NONE;
+    if (m_eff > 0 && n_sh > 0) branch = m_eff >= threshold ? PSP_BRANCH_DENSE : PSP_BRANCH_CASCADE;
+    P.group_branch[g] = branch;
+    if (branch != PSP_BRANCH_NONE) {
+      const int64_t rows = branch == PSP_BRANCH_DENSE ? psp::kDenseRows : psp::kCascadeRows;
+      const int64_t rb = cdiv(m_eff, rows);
+      const int64_t tiles = cdiv(shared, tile);
+      const int64_t fit = (static_cast<int64_t>(h->prefix_ctas_per_sm) * sms) / (Hkv * rb);
+      const int64_t most = tiles / h->prefix_min_tiles;
+      int64_t n = std::max<int64_t>(1, std::min(fit, most));
+      const int64_t per = cdiv(tiles, n);
+      n = cdiv(tiles, per);
+      P.group_row_blocks[g] = static_cast<int32_t>(rb);
+      for (int64_t ci = 0; ci < n; ++ci) {
+        const int32_t chunk_id = static_cast<int32_t>(P.chunk_begin.size());
+        P.chunk_group.push_back(g);
+        P.chunk_begin.push_back(static_cast<int32_t>(ci * per * tile));
+        P.chunk_end.push_back(static_cast<int32_t>(std::min((ci + 1) * per * tile, shared)));
+        P.chunk_row_offset.push_back(static_cast<int32_t>(P.pre_rows));
+        P.pre_rows += static_cast<int64_t>(Hkv) * m_eff;
+        for (int64_t r = 0; r < rb; ++r) {
+          if (branch == PSP_BRANCH_DENSE) {
+            P.item_chunk_dense.push_back(chunk_id);
+            P.item_rb_dense.push_back(static_cast<int32_t>(r));
+          } else {
+            P.item_chunk_cascade.push_back(chunk_id);
+            P.item_rb_cascade.push_back(static_cast<int32_t>(r));
+          }
+        }
+      }
+      P.shared_tokens += shared;
+    }
+    P.group_chunk_indptr[g + 1] = static_cast<int32_t>(P.chunk_begin.size());
+  }
+  if (P.pre_rows > INT32_MAX) return fail(h, PSP_ERR_INVALID_ARGUMENT, "prefix partial rows exceed int32");
+  P.NC = static_cast<int32_t>(P.chunk_begin.size());
+  // requests whose group runs no prefix kernel read everything as suffix
+  for (int b = 0; b < B; ++b) {
+    const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
+    if (g >= 0 && P.group_branch[g] == PSP_BRANCH_NONE) P.req_group[b] = -1;
+    else P.req_group[b] = g;
+  }
+
+  // --- per request: suffix after the group's shared pages
+  P.suffix_page_indptr.assign(B + 1, 0);
+  P.suffix_start.assign(B, 0);
+  P.suffix_len.assign(B, 0);
+  P.kv_indptr.assign(B + 1, 0);
+  for (int b = 0; b < B; ++b) {
+    const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
+    const int64_t n_sh = g >= 0 ? bt->group_prefix_len[g] / ps : 0;
+    P.suffix_start[b] = static_cast<int32_t>(n_sh * ps);
+    P.suffix_len[b] = static_cast<int32_t>(bt->kv_len[b] - n_sh * ps);
+    const int32_t* pages = bt->page_indices + bt->page_indptr[b];
+    const int64_t npg = bt->page_indptr[b + 1] - bt->page_indptr[b];
+    P.suffix_page_indices.insert(P.suffix_page_indices.end(), pages + n_sh, pages + npg);
+    P.suffix_page_indptr[b + 1] = static_cast<int32_t>(P.suffix_page_indices.size());
+    P.kv_indptr[b + 1] = P.kv_indptr[b] + bt->kv_len[b];
+    P.suffix_tokens += P.suffix_len[b];
+  }
+  P.kv_indices_len = P.kv_indptr[B];
+
+  // --- split-KV partition of the suffixes (token units, page-size independent)
+  int64_t granules = 0;
+  for (int b = 0; b < B; ++b) granules += cdiv(P.suffix_len[b], tile);
+  const int64_t target = static_cast<int64_t>(h->split_ctas_per_sm) * sms;
+  const int64_t per_split = std::max<int64_t>(h->split_min_tiles, cdiv(static_cast<int64_t>(Hkv) * granules, target));
+  P.split_indptr.assign(B + 1, 0);
+  for (int b = 0; b < B; ++b) {
+    const int64_t S = P.suffix_len[b];
+    for (int64_t lo = 0; lo < S; lo += per_split * tile) {
+      P.split_req.push_back(b);
+      P.split_begin.push_back(static_cast<int32_t>(lo));
+      P.split_end.push_back(static_cast<int32_t>(std::min(lo + per_split * tile, S)));
+    }
+    P.split_indptr[b + 1] = static_cast<int32_t>(P.split_req.size());
+  }
+  P.NS = static_cast<int32_t>(P.split_req.size());
+  if (static_cast<int64_t>(P.NS) * Hkv > INT32_MAX / psp::kMaxGroupSize)
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "too many splits");
+
+  // --- workspace layout
+  PlanLayout& L = P.layout;
+  size_t off = 0;
+  auto place = [&](size_t& field, size_t bytes) { field = off; off = align_up(off + std::max<size_t>(bytes, 4)); };
+  auto n32 = [](const std::vector<int32_t>& v) { return v.size() * sizeof(int32_t); };
+  place(L.suffix_page_indptr, n32(P.suffix_page_indptr));
+  place(L.suffix_page_indices, n32(P.suffix_page_indices));
+  place(L.suffix_start, n32(P.suffix_start));
+  place(L.suffix_len, n32(P.suffix_len));
+  place(L.split_indptr, n32(P.split_indptr));
+  place(L.split_req, n32(P.split_req));
+  place(L.split_begin, n32(P.split_begin));
+  place(L.split_end, n32(P.split_end));
+  place(L.req_group, n32(P.req_group));
+  place(L.req_member, n32(P.req_member));
+  place(L.group_page_indptr, n32(P.group_page_indptr));
+  place(L.group_page_indices, n32(P.group_page_indices));
+  place(L.group_m_eff, n32(P.group_m_eff));
+  place(L.group_shared_len, n32(P.group_shared_len));
+  place(L.group_member_indptr, n32(P.group_member_indptr));
+  place(L.group_members, n32(P.group_members));
+  place(L.group_chunk_indptr, n32(P.group_chunk_indptr));
+  place(L.chunk_group, n32(P.chunk_group));
+  place(L.chunk_begin, n32(P.chunk_begin));
+  place(L.chunk_end, n32(P.chunk_end));
+  place(L.chunk_row_offset, n32(P.chunk_row_offset));
+  place(L.item_chunk_dense, n32(P.item_chunk_dense));
+  place(L.item_rb_dense, n32(P.item_rb_dense));
+  place(L.item_chunk_cascade, n32(P.item_chunk_cascade));
+  place(L.item_rb_cascade, n32(P.item_rb_cascade));
+  place(L.kv_indptr, n32(P.kv_indptr));
+  L.plan_bytes = off;
+  place(L.status, 64);
+  const size_t D = c.head_dim;
+  const size_t suf_rows = static_cast<size_t>(P.NS) * Hkv * G;
+  place(L.o_suf, suf_rows * D * sizeof(float));
+  place(L.lse_suf, suf_rows * sizeof(float));
+  place(L.o_pre, static_cast<size_t>(P.pre_rows) * D * sizeof(float));
+  place(L.lse_pre, static_cast<size_t>(P.pre_rows) * sizeof(float));
+  place(L.kv_indices, (c.flags & PSP_FLAG_TOKEN_FLAT) ? static_cast<size_t>(P.kv_indices_len) * 4 : 0);
+  L.total = off;
+
+  psp_plan_info& I = P.info;
+  I.batch_size = B;
+  I.num_groups = NG;
+  I.num_splits = P.NS;
+  I.num_chunks = P.NC;
+  I.suffix_pages = static_cast<int64_t>(P.suffix_page_indices.size());
+  I.group_pages = static_cast<int64_t>(P.group_page_indices.size());
+  I.kv_indices_len = P.kv_indices_len;
+  I.suffix_tokens = P.suffix_tokens;
+  I.shared_tokens = P.shared_tokens;
+  I.workspace_bytes = static_cast<int64_t>(L.total);
+  I.suffix_ctas = P.NS * Hkv;
+  I.prefix_dense_ctas = static_cast<int32_t>(P.item_chunk_dense.size()) * Hkv;
+  I.prefix_cascade_ctas = static_cast<int32_t>(P.item_chunk_cascade.size()) * Hkv;
+  I.merge_rows = B * c.num_q_heads;
+  I.num_sms = static_cast<int32_t>(sms);
+  I.dense_threshold = threshold;
+  I.tile_tokens = psp::kTileTokens;
+  I.split_min_tiles = h->split_min_tiles;
+  I.split_ctas_per_sm = h->split_ctas_per_sm;
+  I.prefix_rows_dense = psp::kDenseRows;
+  I.prefix_rows_cascade = psp::kCascadeRows;
+  I.prefix_min_tiles = h->prefix_min_tiles;
+  I.prefix_ctas_per_sm = h->prefix_ctas_per_sm;
+  return PSP_OK;
+}
+
+const std::vector<int32_t>* field_vector(const HostPlan& P, int32_t field) {
+  switch (field) {
+    case PSP_FIELD_SUFFIX_START: return &P.suffix_start;
+    case PSP_FIELD_SUFFIX_LEN: return &P.suffix_len;
+    case PSP_FIELD_SUFFIX_PAGE_INDPTR: return &P.suffix_page_indptr;
+    case PSP_FIELD_SUFFIX_PAGE_INDICES: return &P.suffix_page_indices;
+    case PSP_FIELD_SPLIT_INDPTR: return &P.split_indptr;
+    case PSP_FIELD_SPLIT_BEGIN: return &P.split_begin;
+    case PSP_FIELD_SPLIT_END: return &P.split_end;
+    case PSP_FIELD_GROUP_SHARED_LEN: return &P.group_shared_len;
+    case PSP_FIELD_GROUP_PAGE_INDPTR: return &P.group_page_indptr;
+    case PSP_FIELD_GROUP_PAGE_INDICES: return &P.group_page_indices;
+    case PSP_FIELD_GROUP_M_EFF: return &P.group_m_eff;
+    case PSP_FIELD_GROUP_BRANCH: return &P.group_branch;
+    case PSP_FIELD_GROUP_ROW_BLOCKS: return &P.group_row_blocks;
+    case PSP_FIELD_GROUP_CHUNK_INDPTR: return &P.group_chunk_indptr;
+    case PSP_FIELD_CHUNK_BEGIN: return &P.chunk_begin;
+    case PSP_FIELD_CHUNK_END: return &P.chunk_end;
+    case PSP_FIELD_KV_INDPTR: return &P.kv_indptr;
+  }
+  return nullptr;
+}
+
+StepParams make_params(const psp_handle* h, const psp_tensors* t) {
+  const psp_config& c = h->cfg;
+  const HostPlan& P = h->plan;
+  const PlanLayout& L = P.layout;
+  unsigned char* ws = h->workspace;
+  StepParams p{};
+  p.batch = P.B;
+  p.hq = c.num_q_heads;
+  p.hkv = c.num_kv_heads;
+  p.group = h->group;
+  p.head_dim = c.head_dim;
+  p.page_size = c.page_size;
+  p.page_shift = h->page_shift;
+  p.kv_dtype = c.kv_dtype;
+  p.q_dtype = c.q_dtype;
+  p.o_dtype = c.o_dtype;
+  p.num_pages = c.num_pages;
+  p.token_flat = (c.flags & PSP_FLAG_TOKEN_FLAT) ? 1 : 0;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
+  if (t) {
+    p.q = t->q;
+    p.k_pool = t->k_pool;
+    p.v_pool = t->v_pool;
+    p.k_scale = t->k_scale;
+    p.v_scale = t->v_scale;
+    p.o = t->o;
+    p.lse = t->lse;
+  }
+  auto I = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  p.suffix_page_indptr = I(L.suffix_page_indptr);
+  p.suffix_page_indices = I(L.suffix_page_indices);
+  p.suffix_start = I(L.suffix_start);
+  p.suffix_len = I(L.suffix_len);
+  p.split_indptr = I(L.split_indptr);
+  p.split_req = I(L.split_req);
+  p.split_begin = I(L.split_begin);
+  p.split_end = I(L.split_end);
+  p.req_group = I(L.req_group);
+  p.req_member = I(L.req_member);
+  p.group_page_indptr = I(L.group_page_indptr);
+  p.group_page_indices = I(L.group_page_indices);
+  p.group_m_eff = I(L.group_m_eff);
+  p.group_shared_len = I(L.group_shared_len);
+  p.group_member_indptr = I(L.group_member_indptr);
+  p.group_members = I(L.group_members);
+  p.group_chunk_indptr = I(L.group_chunk_indptr);
+  p.chunk_group = I(L.chunk_group);
+  p.chunk_begin = I(L.chunk_begin);
+  p.chunk_end = I(L.chunk_end);
+  p.chunk_row_offset = I(L.chunk_row_offset);
+  p.item_chunk_dense = I(L.item_chunk_dense);
+  p.item_rb_dense = I(L.item_rb_dense);
+  p.item_chunk_cascade = I(L.item_chunk_cascade);
+  p.item_rb_cascade = I(L.item_rb_cascade);
+  p.kv_indptr = I(L.kv_indptr);
+  p.kv_indices = I(L.kv_indices);
+  p.o_suf = F(L.o_suf);
+  p.lse_suf = F(L.lse_suf);
+  p.o_pre = F(L.o_pre);
+  p.lse_pre = F(L.lse_pre);
+  p.status = I(L.status);
+  return p;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+const char* psp_version(void) { return "psp 0.1 sm_103a"; }
+
+const char* psp_status_string(psp_status s) {
+  switch (s) {
+    case PSP_OK: return "ok";
+    case PSP_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case PSP_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PSP_ERR_PAGE_OUT_OF_RANGE: return "page id out of range";
+    case PSP_ERR_LENGTH: return "context length and page count disagree";
+    case PSP_ERR_PREFIX_MISMATCH: return "prefix group members disagree";
+    case PSP_ERR_NO_PLAN: return "no plan";
+    case PSP_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case PSP_ERR_CUDA: return "CUDA error";
+    case PSP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case PSP_ERR_HOST_ALLOC: return "host allocation failed";
+    case PSP_ERR_CAPACITY: return "buffer too small";
+  }
+  return "unknown status";
+}
+
+psp_status psp_create(const psp_config* cfg, psp_handle** out) {
+  if (!cfg || !out) return fail(nullptr, PSP_ERR_INVALID_ARGUMENT, "cfg or out is NULL");
+  *out = nullptr;
+  const psp_config& c = *cfg;
+  if (c.num_q_heads < 1 || c.num_kv_heads < 1 || c.head_dim < 1 || c.page_size < 1 || c.num_pages < 1 ||
+      c.num_sms < 0 || c.dense_threshold < 0)
+    return fail(nullptr, PSP_ERR_INVALID_ARGUMENT, "non-positive size in psp_config");
+  if (c.num_q_heads % c.num_kv_heads)
+    return fail(nullptr, PSP_ERR_INVALID_ARGUMENT, "num_q_heads is not a multiple of num_kv_heads");
+  const int G = c.num_q_heads / c.num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(nullptr, PSP_ERR_UNSUPPORTED, "GQA group size must be 1, 2, 4 or 8");
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(nullptr, PSP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if ((c.page_size & (c.page_size - 1)) || c.page_size > 1024)
+    return fail(nullptr, PSP_ERR_UNSUPPORTED, "page_size must be a power of two in [1, 1024]");
+  const bool f32 = c.kv_dtype == PSP_DTYPE_F32 && c.q_dtype == PSP_DTYPE_F32;
+  const bool low = (c.kv_dtype == PSP_DTYPE_BF16 || c.kv_dtype == PSP_DTYPE_FP8_E4M3) && c.q_dtype == PSP_DTYPE_BF16;
+  if (!f32 && !low) return fail(nullptr, PSP_ERR_UNSUPPORTED, "unsupported q/kv dtype combination");
+  if (c.o_dtype != PSP_DTYPE_F32 && c.o_dtype != PSP_DTYPE_BF16)
+    return fail(nullptr, PSP_ERR_UNSUPPORTED, "o_dtype must be F32 or BF16");
+  if (c.flags & ~PSP_FLAG_TOKEN_FLAT) return fail(nullptr, PSP_ERR_INVALID_ARGUMENT, "unknown flag");
+  const int64_t slots = static_cast<int64_t>(c.num_pages) * c.page_size;
+  if (slots * c.num_kv_heads * c.head_dim > (int64_t{1} << 40))
+    return fail(nullptr, PSP_ERR_INVALID_ARGUMENT, "pool too large");
+  if (slots > INT32_MAX) return fail(nullptr, PSP_ERR_INVALID_ARGUMENT, "pool slots exceed int32");
+  psp_handle* h = new (std::nothrow) psp_handle();
+  if (!h) return fail(nullptr, PSP_ERR_HOST_ALLOC, "handle allocation failed");
+  h->cfg = c;
+  h->group = G;
+  while ((1 << h->page_shift) < c.page_size) ++h->page_shift;
+  h->split_min_tiles = env_int("PSP_SPLIT_MIN_TILES", kSplitMinTiles);
+  h->split_ctas_per_sm = env_int("PSP_SPLIT_CTAS_PER_SM", kSplitCtasPerSm);
+  h->prefix_min_tiles = env_int("PSP_PREFIX_MIN_TILES", kPrefixMinTiles);
+  h->prefix_ctas_per_sm = env_int("PSP_PREFIX_CTAS_PER_SM", kPrefixCtasPerSm);
+  if (c.dense_threshold == 0) {
+    const int t = env_int("PSP_DENSE_THRESHOLD", 0);
+    if (t > 0) h->cfg.dense_threshold = t;
+  }
+  *out = h;
+  return PSP_OK;
+}
+
+void psp_destroy(psp_handle* h) {
+  if (!h) return;
+  if (h->staging) cudaFreeHost(h->staging);
+  if (h->staging_done) cudaEventDestroy(h->staging_done);
+  for (cudaEvent_t e : h->events) cudaEventDestroy(e);
+  delete h;
+}
+
+const char* psp_last_error(const psp_handle* h) {
+  return h ? h->last_error.c_str() : g_create_error.c_str();
+}
+
+psp_status psp_plan(psp_handle* h, const psp_batch* batch) {
+  if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  h->planned = false;
+  h->uploaded = false;
+  if (h->num_sms_resolved == 0) {
+    if (h->cfg.num_sms > 0) {
+      h->num_sms_resolved = h->cfg.num_sms;
+    } else {
+      int dev = 0, n = 0;
+      cudaError_t e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(h, e, "querying the SM count");
+      h->num_sms_resolved = std::max(1, n);
+    }
+  }
+  psp_status st = validate_batch(h, batch);
+  if (st) return st;
+  try {
+    st = build_plan(h, batch, h->plan);
+  } catch (const std::bad_alloc&) {
+    return fail(h, PSP_ERR_HOST_ALLOC, "plan allocation failed");
+  }
+  if (st) return st;
+  h->planned = true;
+  h->last_error.clear();
+  return PSP_OK;
+}
+
+psp_status psp_plan_info_get(const psp_handle* h, psp_plan_info* out) {
+  if (!h || !out) return PSP_ERR_INVALID_ARGUMENT;
+  if (!h->planned) return PSP_ERR_NO_PLAN;
+  *out = h->plan.info;
+  return PSP_OK;
+}
+
+psp_status psp_workspace_size(const psp_handle* h, size_t* bytes) {
+  if (!h || !bytes) return PSP_ERR_INVALID_ARGUMENT;
+  if (!h->planned) return PSP_ERR_NO_PLAN;
+  *bytes = h->plan.layout.total;
+  return PSP_OK;
+}
+
+psp_status psp_plan_query(const psp_handle* h, int32_t field, void* dst, size_t cap_bytes, size_t* needed) {
+  if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  if (!h->planned) return PSP_ERR_NO_PLAN;
+  const std::vector<int32_t>* v = field_vector(h->plan, field);
+  if (!v) return PSP_ERR_INVALID_ARGUMENT;
+  const size_t bytes = v->size() * sizeof(int32_t);
+  if (needed) *needed = bytes;
+  if (bytes == 0) return PSP_OK;
+  if (!dst || cap_bytes < bytes) return PSP_ERR_CAPACITY;
+  std::memcpy(dst, v->data(), bytes);
+  return PSP_OK;
+}
+
+psp_status psp_upload(psp_handle* h, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  if (!h->planned) return fail(h, PSP_ERR_NO_PLAN, "psp_upload before psp_plan");
+  const HostPlan& P = h->plan;
+  const PlanLayout& L = P.layout;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % psp::kWorkspaceAlign) || workspace_bytes < L.total)
+    return fail(h, PSP_ERR_WORKSPACE, "workspace needs " + std::to_string(L.total) + " bytes, 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (h->staging_done) {
+    e = cudaEventSynchronize(h->staging_done);   // the previous upload has left the staging
+    if (e != cudaSuccess) return cuda_fail(h, e, "waiting for the previous upload");
+  } else {
+    e = cudaEventCreateWithFlags(&h->staging_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventCreate");
+  }
+  if (h->staging_bytes < L.plan_bytes) {
+    if (h->staging) cudaFreeHost(h->staging);
+    h->staging = nullptr;
+    h->staging_bytes = 0;
+    const size_t want = std::max<size_t>(L.plan_bytes, 1 << 16) * 5 / 4;
+    e = cudaHostAlloc(reinterpret_cast<void**>(&h->staging), want, cudaHostAllocDefault);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaHostAlloc (plan staging)");
+    h->staging_bytes = want;
+  }
+  auto put = [&](size_t off, const std::vector<int32_t>& v) {
+    if (!v.empty()) std::memcpy(h->staging + off, v.data(), v.size() * sizeof(int32_t));
+  };
+  std::memset(h->staging, 0, L.plan_bytes);
+  put(L.suffix_page_indptr, P.suffix_page_indptr);
+  put(L.suffix_page_indices, P.suffix_page_indices);
+  put(L.suffix_start, P.suffix_start);
+  put(L.suffix_len, P.suffix_len);
+  put(L.split_indptr, P.split_indptr);
+  put(L.split_req, P.split_req);
+  put(L.split_begin, P.split_begin);
+  put(L.split_end, P.split_end);
+  put(L.req_group, P.req_group);
+  put(L.req_member, P.req_member);
+  put(L.group_page_indptr, P.group_page_indptr);
+  put(L.group_page_indices, P.group_page_indices);
+  put(L.group_m_eff, P.group_m_eff);
+  put(L.group_shared_len, P.group_shared_len);
+  put(L.group_member_indptr, P.group_member_indptr);
+  put(L.group_members, P.group_members);
+  put(L.group_chunk_indptr, P.group_chunk_indptr);
+  put(L.chunk_group, P.chunk_group);
+  put(L.chunk_begin, P.chunk_begin);
+  put(L.chunk_end, P.chunk_end);
+  put(L.chunk_row_offset, P.chunk_row_offset);
+  put(L.item_chunk_dense, P.item_chunk_dense);
+  put(L.item_rb_dense, P.item_rb_dense);
+  put(L.item_chunk_cascade, P.item_chunk_cascade);
+  put(L.item_rb_cascade, P.item_rb_cascade);
+  put(L.kv_indptr, P.kv_indptr);
+  e = cudaMemcpyAsync(workspace, h->staging, L.plan_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "plan upload");
+  e = cudaEventRecord(h->staging_done, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventRecord");
+  e = cudaMemsetAsync(static_cast<unsigned char*>(workspace) + L.status, 0, 64, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "clearing the device status word");
+  h->workspace = static_cast<unsigned char*>(workspace);
+  h->workspace_bytes = workspace_bytes;
+  h->uploaded = true;
+  return PSP_OK;
+}
+
+psp_status psp_set_kernel_timing(psp_handle* h, int32_t enable) {
+  if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  h->timing = enable != 0;
+  h->recorded = 0;
+  return PSP_OK;
+}
+
+psp_status psp_kernel_times(psp_handle* h, float* ms, const char** names, int32_t cap, int32_t* count) {
+  if (!h || !count || cap < 0 || (cap > 0 && !ms)) return PSP_ERR_INVALID_ARGUMENT;
+  *count = h->recorded;
+  for (int i = 0; i < h->recorded && i < cap; ++i) {
+    float t = 0.f;
+    cudaError_t e = cudaEventElapsedTime(&t, h->events[2 * i], h->events[2 * i + 1]);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventElapsedTime");
+    ms[i] = t;
+    if (names) names[i] = h->event_names[i];
+  }
+  return PSP_OK;
+}
+
+static psp_status timed_launch(psp_handle* h, cudaStream_t s, const char* name, int& slot,
+                               cudaError_t (*fn)(const StepParams&, int, cudaStream_t), const StepParams& p,
+                               int n) {
+  cudaError_t e;
+  if (h->timing) {
+    while (static_cast<int>(h->events.size()) < 2 * (slot + 1)) {
+      cudaEvent_t ev;
+      e = cudaEventCreate(&ev);
+      if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventCreate");
+      h->events.push_back(ev);
+    }
+    if (static_cast<int>(h->event_names.size()) < slot + 1) h->event_names.resize(slot + 1);
+    h->event_names[slot] = name;
+    e = cudaEventRecord(h->events[2 * slot], s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventRecord");
+  }
+  e = fn(p, n, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, name);
+  if (h->timing) {
+    e = cudaEventRecord(h->events[2 * slot + 1], s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventRecord");
+    ++slot;
+    h->recorded = slot;
+  }
+  return PSP_OK;
+}
+
+static cudaError_t expand_entry(const StepParams& p, int, cudaStream_t s) {
+  return psp::launch_expand_kv_indices(p, p.kv_indices, s);
+}
+static cudaError_t merge_entry(const StepParams& p, int, cudaStream_t s) { return psp::launch_merge(p, s); }
+
+psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
+  if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  if (!h->planned || !h->uploaded) return fail(h, PSP_ERR_NO_PLAN, "psp_run needs psp_plan and psp_upload first");
+  if (!t || !t->q || !t->k_pool || !t->v_pool || !t->o)
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "q, k_pool, v_pool and o must be set");
+  if (h->cfg.kv_dtype == PSP_DTYPE_FP8_E4M3 && (!t->k_scale || !t->v_scale))
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "fp8 KV needs k_scale and v_scale");
+  if (!aligned16(t->q) || !aligned16(t->k_pool) || !aligned16(t->v_pool) || !aligned16(t->o))
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  const HostPlan& P = h->plan;
+  if (P.B == 0) return PSP_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const StepParams p = make_params(h, t);
+  int slot = 0;
+  h->recorded = 0;
+  psp_status st;
+  if (p.token_flat) {
+    st = timed_launch(h, s, "expand_kv_indices", slot, expand_entry, p, 0);
+    if (st) return st;
+  }
+  const int nd = static_cast<int>(P.item_chunk_dense.size());
+  const int nc = static_cast<int>(P.item_chunk_cascade.size());
+  if (nd > 0) {
+    st = timed_launch(h, s, "prefix_dense", slot, psp::launch_prefix_dense, p, nd);
+    if (st) return st;
+  }
+  if (nc > 0) {
+    st = timed_launch(h, s, "prefix_cascade", slot, psp::launch_prefix_cascade, p, nc);
+    if (st) return st;
+  }
+  if (P.NS > 0) {
+    st = timed_launch(h, s, "suffix_splitkv", slot, psp::launch_suffix, p, P.NS);
+    if (st) return st;
+  }
+  return timed_launch(h, s, "merge", slot, merge_entry, p, 0);
+}
+
+psp_status psp_step_host(psp_handle* h, const psp_batch* batch, const void* q_host, void* o_host, float* lse_host,
+                         const psp_tensors* dev, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  if (!q_host || !o_host || !dev || !dev->q || !dev->o || (lse_host && !dev->lse))
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "host and device staging buffers must be set");
+  psp_status st = psp_plan(h, batch);
+  if (st) return st;
+  st = psp_upload(h, workspace, workspace_bytes, stream);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const psp_config& c = h->cfg;
+  const size_t rows = static_cast<size_t>(batch->batch_size) * c.num_q_heads;
+  cudaError_t e = cudaMemcpyAsync(const_cast<void*>(dev->q), q_host, rows * c.head_dim * dtype_bytes(c.q_dtype),
+                                  cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "copying q to the device");
+  st = psp_run(h, dev, stream);
+  if (st) return st;
+  e = cudaMemcpyAsync(o_host, dev->o, rows * c.head_dim * dtype_bytes(c.o_dtype), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "copying o to the host");
+  if (lse_host) {
+    e = cudaMemcpyAsync(lse_host, dev->lse, rows * sizeof(float), cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "copying lse to the host");
+  }
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+  return PSP_OK;
+}
+
+psp_status psp_expand_kv_indices(psp_handle* h, int32_t* kv_indices, int64_t cap, void* stream) {
+  if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  if (!h->planned || !h->uploaded) return fail(h, PSP_ERR_NO_PLAN, "psp_expand_kv_indices needs an uploaded plan");
+  if (cap < h->plan.kv_indices_len) return fail(h, PSP_ERR_CAPACITY, "kv_indices capacity too small");
+  if (h->plan.kv_indices_len == 0) return PSP_OK;
+  if (!kv_indices || !aligned16(kv_indices)) return fail(h, PSP_ERR_INVALID_ARGUMENT, "kv_indices NULL or misaligned");
+  StepParams p = make_params(h, nullptr);
+  cudaError_t e = psp::launch_expand_kv_indices(p, kv_indices, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "expand_kv_indices");
+  return PSP_OK;
+}
+
+psp_status psp_device_status(psp_handle* h, int32_t* code) {
+  if (!h || !code) return PSP_ERR_INVALID_ARGUMENT;
+  if (!h->uploaded) return fail(h, PSP_ERR_NO_PLAN, "no workspace bound");
+  cudaError_t e = cudaMemcpy(code, h->workspace + h->plan.layout.status, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "reading the device status word");
+  return PSP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// psp_internal.h -- structures shared by the host side (plan, C ABI) and the
+// kernels of the paged shared-prefix decode step.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+// Element type codes (same values as the public PSP_DTYPE_*).
+#define PSP_KV_F32 0
+#define PSP_KV_BF16 1
+#define PSP_KV_FP8 2
+
+namespace psp {
+
+constexpr int kMaxGroupSize = 8;        // query heads per KV head handled per CTA row set
+constexpr int kTileTokens = 64;         // partition granule (tokens)
+constexpr int kCascadeRows = 64;        // stacked query rows per cascade prefix CTA
+constexpr int kDenseRows = 128;         // stacked query rows per dense prefix CTA
+constexpr int kWorkspaceAlign = 256;
+
+// Device status codes written instead of faulting.
+constexpr int32_t kDevOk = 0;
+constexpr int32_t kDevTimeout = 1;
+constexpr int32_t kDevBadIndex = 2;
+
+// Everything a kernel of the step reads: configuration, caller tensors, the
+// uploaded plan and the partial-result buffers in the workspace.
+struct StepParams {
+  // configuration
+  int32_t batch;
+  int32_t hq, hkv, group, head_dim;
+  int32_t page_size, page_shift;     // page_size == 1 << page_shift
+  int32_t kv_dtype, q_dtype, o_dtype;
+  int32_t num_pages;
+  int32_t token_flat;                // read K/V through kv_indices (page size 1 view)
+  float scale_log2;                  // log2(e) / sqrt(head_dim)
+
+  // caller tensors (device)
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const float* k_scale;
+  const float* v_scale;
+  void* o;
+  float* lse;
+
+  // plan (device int32 arrays, see plan layout)
+  const int32_t* suffix_page_indptr;   // [B+1]
+  const int32_t* suffix_page_indices;
+  const int32_t* suffix_start;         // [B]
+  const int32_t* suffix_len;           // [B]
+  const int32_t* split_indptr;         // [B+1]
+  const int32_t* split_req;            // [S]
+  const int32_t* split_begin;          // [S]
+  const int32_t* split_end;            // [S]
+  const int32_t* req_group;            // [B] group with a prefix branch, else -1
+  const int32_t* req_member;           // [B] index of b among its group's members
+  const int32_t* group_page_indptr;    // [NG+1]
+  const int32_t* group_page_indices;
+  const int32_t* group_m_eff;          // [NG]
+  const int32_t* group_shared_len;     // [NG]
+  const int32_t* group_member_indptr;  // [NG+1]
+  const int32_t* group_members;        // members, increasing request id
+  const int32_t* group_chunk_indptr;   // [NG+1]
+  const int32_t* chunk_group;          // [NC]
+  const int32_t* chunk_begin;          // [NC]
+  const int32_t* chunk_end;            // [NC]
+  const int32_t* chunk_row_offset;     // [NC] first prefix-partial row of the chunk
+  const int32_t* item_chunk_dense;     // dense prefix work items: (chunk, row block)
+  const int32_t* item_rb_dense;
+  const int32_t* item_chunk_cascade;   // cascade prefix work items
+  const int32_t* item_rb_cascade;
+  const int32_t* kv_indptr;            // [B+1] token-flat offsets
+  int32_t* kv_indices;                 // [sum kv_len] (token-flat mode)
+
+  // partial results: O normalised (fp32) and log2-domain LSE
+  float* o_suf;                        // [(S * Hkv + h) * G + j][D]
+  float* lse_suf;
+  float* o_pre;                        // [chunk_row_offset[c] + h * M_eff + r][D]
+  float* lse_pre;
+  int32_t* status;                     // device status word
+};
+
+// Byte offsets of every array inside the workspace (256-byte aligned each).
+struct PlanLayout {
+  size_t suffix_page_indptr, suffix_page_indices, suffix_start, suffix_len;
+  size_t split_indptr, split_req, split_begin, split_end;
+  size_t req_group, req_member;
+  size_t group_page_indptr, group_page_indices, group_m_eff, group_shared_len;
+  size_t group_member_indptr, group_members, group_chunk_indptr;
+  size_t chunk_group, chunk_begin, chunk_end, chunk_row_offset;
+  size_t item_chunk_dense, item_rb_dense, item_chunk_cascade, item_rb_cascade;
+  size_t kv_indptr;
+  size_t plan_bytes;       // end of the uploaded integer region
+  size_t status;
+  size_t o_suf, lse_suf, o_pre, lse_pre;
+  size_t kv_indices;
+  size_t total;
+};
+
+// Launchers (each returns the launch's cudaError_t; nothing is launched for 0 items).
+cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s);
+cudaError_t launch_prefix_cascade(const StepParams& p, int num_items, cudaStream_t s);
+cudaError_t launch_prefix_dense(const StepParams& p, int num_items, cudaStream_t s);
+cudaError_t launch_merge(const StepParams& p, cudaStream_t s);
+cudaError_t launch_expand_kv_indices(const StepParams& p, int32_t* out, cudaStream_t s);
+cudaError_t launch_suffix_simt(const StepParams& p, int num_splits, cudaStream_t s);
+cudaError_t launch_prefix_simt(const StepParams& p, int num_items, bool dense, cudaStream_t s);
+cudaError_t launch_prefix_dense_mma(const StepParams& p, int num_items, cudaStream_t s);
+
+}  // namespace psp

@@ -1,0 +1,253 @@
+"""Host-side checks of the C ABI (no GPU): exported symbols, configuration and
+batch validation, and the integer plan against the oracle, bit for bit."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_shared_prefix_gb300 as psp
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+NUM_SMS = 152
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "psp.h")).read()
+    return sorted(set(re.findall(r"^PSP_API\s+[\w\s\*]+?\b(psp_\w+)\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(psp.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/psp.h but not exported"
+    assert set(names) == set(psp.EXPORTED), "binding and header disagree"
+
+
+def test_version_and_status_strings():
+    assert "sm_103a" in psp.version()
+    for code in psp.STATUS_NAMES:
+        assert psp.psp_status_string(code)
+
+
+def _create_status(**over):
+    base = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, q_dtype=1, kv_dtype=1, o_dtype=1,
+                page_size=16, num_pages=100, num_sms=NUM_SMS, dense_threshold=0, flags=0)
+    base.update(over)
+    cfg = psp.psp_config(**base)
+    h = ctypes.c_void_p()
+    st = psp.psp_create(ctypes.byref(cfg), ctypes.byref(h))
+    if st == 0:
+        psp.psp_destroy(h)
+    return st
+
+
+@pytest.mark.parametrize("over,expect", [
+    ({}, 0),
+    (dict(num_q_heads=24), -2),            # G = 3 is not built
+    (dict(num_q_heads=30), -1),            # not a multiple of Hkv
+    (dict(head_dim=96), -2),
+    (dict(page_size=24), -2),              # not a power of two: refused, never coerced
+    (dict(page_size=2048), -2),
+    (dict(page_size=1), 0),
+    (dict(page_size=128), 0),
+    (dict(q_dtype=2), -2),                 # fp8 queries are not supported
+    (dict(kv_dtype=0), -2),                # fp32 KV with bf16 Q
+    (dict(kv_dtype=0, q_dtype=0, o_dtype=0), 0),
+    (dict(kv_dtype=2), 0),
+    (dict(o_dtype=2), -2),
+    (dict(num_pages=0), -1),
+    (dict(flags=4), -1),
+    (dict(flags=1), 0),
+])
+def test_create_validation(over, expect):
+    assert _create_status(**over) == expect
+
+
+def _lib_plan(case, threshold=0, num_sms=NUM_SMS):
+    step = psp.DecodeStep.for_case(case, num_sms=num_sms, dense_threshold=threshold)
+    step.plan_case(case)
+    return step
+
+
+PLAN_FIELDS = ["suffix_start", "suffix_len", "suffix_page_indptr", "suffix_page_indices",
+               "split_indptr", "split_begin", "split_end", "group_shared_len", "group_page_indptr",
+               "group_page_indices", "group_m_eff", "group_branch", "group_row_blocks",
+               "group_chunk_indptr", "chunk_begin", "chunk_end"]
+
+
+def _check_plan_matches_oracle(case, threshold=0, num_sms=NUM_SMS):
+    step = _lib_plan(case, threshold, num_sms)
+    info = step.plan_info()
+    params = {k: info[k] for k, _ in oracle.PlanParams._fields_}
+    ref = oracle.plan(case, params)
+    for f in PLAN_FIELDS:
+        got = step.plan_query(f)
+        want = np.asarray(ref[f], np.int32)
+        assert np.array_equal(got, want), f"{f}: library {got[:12]} oracle {want[:12]}"
+    indptr, _ = oracle.expand_kv_indices(case)
+    assert np.array_equal(step.plan_query("kv_indptr"), indptr)
+    assert info["num_splits"] == len(ref["split_begin"])
+    assert info["num_chunks"] == len(ref["chunk_begin"])
+    assert info["suffix_tokens"] == int(ref["suffix_len"].sum())
+    assert info["kv_indices_len"] == int(case.kv_len.sum())
+    assert info["workspace_bytes"] > 0
+    step.close()
+    return info, ref
+
+
+def _table_cases():
+    out = []
+    for name in ("tiny", "llama8b_noshare", "agent", "short_prefix", "fp8_large"):
+        out.append((f"{name}-full", dict(name=name)))
+    for ps in (1, 16, 128):
+        out.append((f"llama-ps{ps}", dict(name="llama8b_noshare", page_size=ps)))
+    out += [
+        ("agent-ps1", dict(name="agent", page_size=1, batch=40)),
+        ("agent-ps128-unaligned", dict(name="agent", page_size=128, prefix_len=1000, batch=20)),
+        ("prefix-2003-ps16", dict(name="agent", prefix_len=2003, batch=9, private_range=(1, 50))),
+        ("prefix-shorter-than-page", dict(name="agent", prefix_len=10, batch=5, page_size=16)),
+        ("agent-ps32", dict(name="agent", page_size=32, batch=33)),
+        ("agent-ps1024", dict(name="agent", page_size=1024, batch=12, prefix_len=4096)),
+        ("one-request", dict(name="short_prefix", batch=1)),
+        ("single-token-suffixes", dict(name="fp8_large", batch=64, private_range=(1, 1))),
+    ]
+    return out
+
+
+@pytest.mark.parametrize("label,kw", _table_cases(), ids=[c[0] for c in _table_cases()])
+def test_plan_matches_oracle(label, kw):
+    kw = dict(kw)
+    name = kw.pop("name")
+    case = workloads.make_case(name, 3, tables_only=True, **kw)
+    _check_plan_matches_oracle(case)
+    _check_plan_matches_oracle(case.without_sharing())
+    _check_plan_matches_oracle(case, threshold=1)          # every group dense
+    _check_plan_matches_oracle(case, threshold=1 << 20)    # every group cascade
+    _check_plan_matches_oracle(case, num_sms=7)
+
+
+def test_plan_identical_across_page_sizes():
+    plans = []
+    for ps in (1, 16, 128):
+        case = workloads.make_case("llama8b_noshare", 1, page_size=ps, tables_only=True)
+        step = _lib_plan(case)
+        plans.append([step.plan_query(f).tolist() for f in ("split_indptr", "split_begin", "split_end")])
+    assert plans[0] == plans[1] == plans[2]
+
+
+def _multi_group_case():
+    """Three prefix groups of different lengths plus ungrouped requests, one pool."""
+    import dataclasses
+    rng = np.random.default_rng(5)
+    ps, B = 16, 23
+    groups = np.array([-1, 0, 0, 1, 2, 1, 0, -1, 2, 2, 1, 0, 0, -1, 1, 2, 0, 1, 1, 2, -1, 0, 2], np.int32)
+    gl = np.array([160, 37, 512], np.int32)
+    priv = rng.integers(1, 300, B)
+    kv_len = np.where(groups >= 0, gl[np.maximum(groups, 0)], 0) + priv
+    n_pages = 4000
+    perm = rng.permutation(n_pages)
+    pos = 0
+    shared = []
+    for g in range(3):
+        n = gl[g] // ps
+        shared.append(perm[pos:pos + n])
+        pos += n
+    tables = []
+    for b in range(B):
+        g = groups[b]
+        pre = shared[g] if g >= 0 else np.zeros(0, np.int64)
+        need = -(-int(kv_len[b]) // ps) - len(pre)
+        tables.append(np.concatenate([pre, perm[pos:pos + need]]))
+        pos += need
+    indptr = np.concatenate([[0], np.cumsum([len(t) for t in tables])]).astype(np.int32)
+    base = workloads.make_case("agent", 0, batch=B, tables_only=True)
+    return dataclasses.replace(base, num_pages=n_pages, kv_len=kv_len.astype(np.int32),
+                               page_indptr=indptr, page_indices=np.concatenate(tables).astype(np.int32),
+                               prefix_group=groups, group_prefix_len=gl)
+
+
+def test_plan_multi_group_matches_oracle():
+    case = _multi_group_case()
+    for thr in (0, 1, 40, 1 << 20):
+        info, ref = _check_plan_matches_oracle(case, threshold=thr)
+    assert info["num_groups"] == 3
+
+
+def _status_of_plan(case):
+    step = psp.DecodeStep.for_case(case, num_sms=NUM_SMS)
+    b, keep = step.make_batch(case.kv_len, case.page_indptr, case.page_indices, case.prefix_group,
+                              case.group_prefix_len)
+    st = psp.psp_plan(step.handle, ctypes.byref(b))
+    step.close()
+    return st
+
+
+def _oracle_status(case):
+    try:
+        oracle.plan(case, dict(num_sms=NUM_SMS, dense_threshold=1024, tile_tokens=64, split_min_tiles=4,
+                               split_ctas_per_sm=4, prefix_rows_dense=128, prefix_rows_cascade=64,
+                               prefix_min_tiles=4, prefix_ctas_per_sm=1))
+    except oracle.OracleError as e:
+        return e.code
+    return 0
+
+
+def test_invalid_batches_rejected_like_the_oracle():
+    import dataclasses
+    c = workloads.make_case("agent", 1, batch=5, prefix_len=64, private_range=(1, 40), tables_only=True)
+    bad_cases = []
+    pi = c.page_indices.copy()
+    pi[-1] = c.num_pages
+    bad_cases.append(("page id == num_pages", dataclasses.replace(c, page_indices=pi), -3))
+    pi = c.page_indices.copy()
+    pi[3] = -1
+    bad_cases.append(("negative page id", dataclasses.replace(c, page_indices=pi), -3))
+    kl = c.kv_len.copy()
+    kl[1] += 16
+    bad_cases.append(("kv_len beyond its pages", dataclasses.replace(c, kv_len=kl), -4))
+    kl = c.kv_len.copy()
+    kl[2] = 0
+    bad_cases.append(("empty context", dataclasses.replace(c, kv_len=kl), -4))
+    pi = c.page_indices.copy()
+    b1 = c.page_indptr[1]
+    pi[b1], pi[-1] = pi[-1], pi[b1]
+    bad_cases.append(("members disagree", dataclasses.replace(c, page_indices=pi), -5))
+    pg = c.prefix_group.copy()
+    pg[0] = 1
+    bad_cases.append(("group id out of range", dataclasses.replace(c, prefix_group=pg), -1))
+    bad_cases.append(("prefix longer than a context",
+                      dataclasses.replace(c, group_prefix_len=np.array([int(c.kv_len.min()) + 1], np.int32)), -5))
+    for label, case, code in bad_cases:
+        assert _status_of_plan(case) == code, label
+        assert _oracle_status(case) == code, label
+
+
+def test_calls_before_plan_report_no_plan():
+    step = psp.DecodeStep(8, 2, 64, "f32", "f32", "f32", 16, 64, num_sms=NUM_SMS)
+    n = ctypes.c_size_t(0)
+    assert psp.psp_workspace_size(step.handle, ctypes.byref(n)) == -6
+    t = psp.psp_tensors()
+    assert psp.psp_run(step.handle, ctypes.byref(t), None) == -6
+    assert psp.psp_upload(step.handle, None, 0, None) == -6
+    info = psp.psp_plan_info()
+    assert psp.psp_plan_info_get(step.handle, ctypes.byref(info)) == -6
+    step.close()
+
+
+def test_plan_query_capacity_and_empty_batch():
+    case = workloads.make_case("tiny", 0, tables_only=True)
+    step = _lib_plan(case)
+    need = ctypes.c_size_t(0)
+    small = np.zeros(1, np.int32)
+    st = psp.psp_plan_query(step.handle, 3, small.ctypes.data, 4, ctypes.byref(need))
+    assert st == -11 and need.value == 4 * len(step.plan_query("suffix_page_indices"))
+    assert psp.psp_plan_query(step.handle, 99, None, 0, None) == -1
+    step.plan(np.zeros(0, np.int32), np.zeros(1, np.int32), np.zeros(0, np.int32))
+    assert step.plan_info()["num_splits"] == 0
+    step.close()

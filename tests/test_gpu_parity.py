@@ -1,0 +1,217 @@
+"""GPU parity: the CUDA decode step against the fp64 oracle on the same seeded
+inputs, through the C ABI.
+
+Small cases (every output row compared) span several 64-token tiles and
+ragged tails for each workload shape; full-size workloads compare sampled
+rows in the launch configuration the benchmark times.  Tolerances are the
+max |O_gpu - O_oracle| bounds of the target: 2e-3 (fp32 KV), 1.5e-2 (bf16
+KV), 6e-2 (fp8 KV); LSE uses the same bound.  Indexing outputs are bit-exact.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_shared_prefix_gb300 as psp
+import workloads
+from gpu_util import TOL, device_tensors, max_err, run_case
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    ("tiny", dict()),
+    ("tiny-seed7", dict(name="tiny", seed=7)),
+    ("llama", dict(name="llama8b_noshare", batch=4, private_range=(100, 700))),
+    ("agent", dict(name="agent", batch=12, prefix_len=256, private_range=(1, 300))),
+    ("short_prefix", dict(name="short_prefix", batch=8, private_range=(1, 400))),
+    ("fp8_large", dict(name="fp8_large", batch=6, prefix_len=1024, private_range=(1, 300))),
+    ("agent-d64", dict(name="agent", batch=5, prefix_len=128, private_range=(1, 200), head_dim=64)),
+    ("fp8-d64", dict(name="fp8_large", batch=4, prefix_len=192, private_range=(1, 150), head_dim=64)),
+    ("fp32-d128", dict(name="tiny", head_dim=128, private_range=(1, 200))),
+    ("agent-g1", dict(name="agent", batch=7, prefix_len=64, private_range=(1, 100), num_q_heads=8)),
+    ("agent-g8", dict(name="agent", batch=4, prefix_len=80, private_range=(1, 100), num_q_heads=64)),
+    ("fp8-g2", dict(name="fp8_large", batch=5, prefix_len=96, private_range=(1, 70), num_q_heads=16)),
+]
+
+
+def _make(kw):
+    kw = dict(kw)
+    name = kw.pop("name", None)
+    seed = kw.pop("seed", 0)
+    return workloads.make_case(name, seed, **kw)
+
+
+@pytest.mark.parametrize("label,kw", SMALL, ids=[s[0] for s in SMALL])
+@pytest.mark.parametrize("branch", ["dense", "cascade"])
+def test_small_matches_oracle(label, kw, branch):
+    kw = dict(kw)
+    kw.setdefault("name", label)
+    case = _make(kw)
+    thr = 1 if branch == "dense" else 1 << 20
+    o, lse = run_case(case, threshold=thr)
+    ref_o, ref_lse = oracle.attend_all(case)
+    tol = TOL[case.workload.kv_dtype]
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert max_err(o, ref_o) <= tol
+    assert max_err(lse, ref_lse) <= tol
+
+
+def test_page_sizes_and_layouts_bit_identical():
+    outs = []
+    for ps in (1, 16, 128):
+        for layout in ("scatter", "contiguous"):
+            case = workloads.make_case("llama8b_noshare", 2, batch=3, private_range=(200, 900), page_size=ps,
+                                       layout=layout)
+            outs.append(run_case(case))
+    case = workloads.make_case("llama8b_noshare", 2, batch=3, private_range=(200, 900), page_size=16,
+                               layout="block128")
+    outs.append(run_case(case))
+    for o, l in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
+    ref_o, ref_lse = oracle.attend_all(case)
+    assert max_err(outs[0][0], ref_o) <= TOL["bf16"]
+
+
+def test_token_flat_lowering_bit_identical():
+    for name, kw in (("agent", dict(batch=6, prefix_len=160, private_range=(1, 200))),
+                     ("fp8_large", dict(batch=4, prefix_len=128, private_range=(1, 150))),
+                     ("tiny", {})):
+        case = workloads.make_case(name, 4, **kw)
+        a = run_case(case)
+        b = run_case(case, token_flat=True)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), name
+
+
+def test_expand_kv_indices_bit_exact():
+    for ps in (1, 16, 128):
+        case = workloads.make_case("agent", 1, batch=9, prefix_len=300, private_range=(1, 500), page_size=ps)
+        step = psp.DecodeStep.for_case(case)
+        step.plan_case(case)
+        ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device="cuda:0")
+        step.upload(ws)
+        n = step.plan_info()["kv_indices_len"]
+        out = torch.full((n + 7,), -7, dtype=torch.int32, device="cuda:0")
+        step.expand_kv_indices(out)
+        torch.cuda.synchronize()
+        indptr, idx = oracle.expand_kv_indices(case)
+        got = out.cpu().numpy()
+        assert np.array_equal(got[:n], idx) and np.all(got[n:] == -7)
+        assert np.array_equal(step.plan_query("kv_indptr"), indptr)
+        step.close()
+
+
+def test_shared_equals_per_request_paged():
+    case = workloads.make_case("agent", 5, batch=16, prefix_len=512, private_range=(1, 256))
+    a = run_case(case)
+    b = run_case(case.without_sharing())
+    ref_o, ref_lse = oracle.attend_all(case)
+    for o, l in (a, b):
+        assert max_err(o, ref_o) <= TOL["bf16"] and max_err(l, ref_lse) <= TOL["bf16"]
+
+
+def test_edge_cases():
+    # empty suffix: a context that ends exactly at the page-aligned shared prefix
+    case = workloads.make_case("agent", 6, batch=5, prefix_len=128, private_lengths=[0, 3, 0, 17, 64])
+    o, lse = run_case(case)
+    ro, rl = oracle.attend_all(case)
+    assert max_err(o, ro) <= TOL["bf16"] and max_err(lse, rl) <= TOL["bf16"]
+    # prefix shorter than one page: nothing shared, everything is suffix
+    case = workloads.make_case("agent", 6, batch=4, prefix_len=9, private_range=(1, 30))
+    o, lse = run_case(case)
+    ro, rl = oracle.attend_all(case)
+    assert max_err(o, ro) <= TOL["bf16"]
+    # one-token contexts
+    case = workloads.make_case("llama8b_noshare", 6, batch=5, private_lengths=[1, 1, 2, 1, 3])
+    o, lse = run_case(case)
+    ro, rl = oracle.attend_all(case)
+    assert max_err(o, ro) <= TOL["bf16"] and max_err(lse, rl) <= TOL["bf16"]
+    # unaligned prefix at page size 128 (tail of the prefix stays private)
+    case = workloads.make_case("fp8_large", 6, batch=4, prefix_len=300, private_range=(1, 90), page_size=128)
+    o, lse = run_case(case)
+    ro, rl = oracle.attend_all(case)
+    assert max_err(o, ro) <= TOL["fp8_e4m3"] and max_err(lse, rl) <= TOL["fp8_e4m3"]
+
+
+def test_step_host_matches_run():
+    case = workloads.make_case("agent", 8, batch=10, prefix_len=192, private_range=(1, 200))
+    w = case.workload
+    (o_ref, l_ref), step, ws = run_case(case, return_step=True)
+    tens = device_tensors(case)
+    q_host = torch.from_numpy(case.q.view(np.int16)).pin_memory()
+    o_host = torch.empty((case.batch, w.num_q_heads, w.head_dim), dtype=torch.int16).pin_memory()
+    l_host = torch.empty((case.batch, w.num_q_heads), dtype=torch.float32).pin_memory()
+    o_dev = torch.empty((case.batch, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda:0")
+    l_dev = torch.empty((case.batch, w.num_q_heads), dtype=torch.float32, device="cuda:0")
+    q_dev = torch.empty_like(tens["q"])
+    batch, keep = step.make_batch(case.kv_len, case.page_indptr, case.page_indices, case.prefix_group,
+                                  case.group_prefix_len)
+    dev = step.tensors(q_dev, tens["k_pool"], tens["v_pool"], o_dev, l_dev)
+    step.step_host(batch, q_host, o_host, l_host, dev, ws)
+    o = o_host.view(torch.bfloat16).float().double().numpy()
+    assert np.array_equal(o, o_ref) and np.array_equal(l_host.double().numpy(), l_ref)
+    step.close()
+
+
+def test_kernel_timing_reports_launches():
+    case = workloads.make_case("agent", 9, batch=8, prefix_len=256, private_range=(1, 200))
+    tens = device_tensors(case)
+    step = psp.DecodeStep.for_case(case, dense_threshold=1)
+    step.plan_case(case)
+    ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device="cuda:0")
+    step.upload(ws)
+    w = case.workload
+    o = torch.empty((case.batch, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda:0")
+    step.set_kernel_timing(True)
+    step.run(tens["q"], tens["k_pool"], tens["v_pool"], o)
+    torch.cuda.synchronize()
+    names = [n for n, _ in step.kernel_times()]
+    assert names == ["prefix_dense", "suffix_splitkv", "merge"]
+    assert all(t > 0 for _, t in step.kernel_times())
+    step.close()
+
+
+# ---------------------------------------------------------------- full size
+
+FULL = [("llama8b_noshare", 16), ("agent", 16), ("short_prefix", 16), ("fp8_large", 16),
+        ("tiny", 16), ("llama8b_noshare", 1), ("llama8b_noshare", 128)]
+
+
+def _sample_rows(case, n, seed=0):
+    rng = np.random.default_rng(seed)
+    B, Hq = case.batch, case.workload.num_q_heads
+    rows = rng.choice(B * Hq, size=min(n, B * Hq), replace=False)
+    # always include the longest and the shortest request
+    L = case.kv_len
+    extra = [int(np.argmax(L)) * Hq, int(np.argmin(L)) * Hq + Hq - 1]
+    rows = np.unique(np.concatenate([rows, extra]))
+    return rows // Hq, rows % Hq
+
+
+@pytest.mark.parametrize("name,ps", FULL, ids=[f"{n}-ps{p}" for n, p in FULL])
+def test_full_size_sampled_rows(name, ps):
+    case = workloads.make_case(name, 0, page_size=ps)
+    o, lse = run_case(case)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    bb, hh = _sample_rows(case, 96)
+    ro, rl = oracle.attend(case, bb, hh)
+    tol = TOL[case.workload.kv_dtype]
+    assert max_err(o[bb, hh], ro) <= tol
+    assert max_err(lse[bb, hh], rl) <= tol
+
+
+def test_full_size_page_sizes_bit_identical():
+    outs = [run_case(workloads.make_case("llama8b_noshare", 0, page_size=ps)) for ps in (1, 16, 128)]
+    for o, l in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
+
+
+def test_full_size_paged_comparator_matches():
+    case = workloads.make_case("agent", 0)
+    a = run_case(case)
+    b = run_case(case.without_sharing())
+    bb, hh = _sample_rows(case, 64, seed=1)
+    ro, rl = oracle.attend(case, bb, hh)
+    for o, l in (a, b):
+        assert max_err(o[bb, hh], ro) <= TOL["bf16"] and max_err(l[bb, hh], rl) <= TOL["bf16"]

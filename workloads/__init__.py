@@ -223,7 +223,7 @@ def make_case(name: str, seed: int = 0, *, page_size: Optional[int] = None,
               layout: str = "scatter", num_q_heads: Optional[int] = None,
               num_kv_heads: Optional[int] = None, head_dim: Optional[int] = None,
               kv_dtype: Optional[str] = None, private_lengths: Optional[list] = None,
-              keep_logical: bool = False) -> Case:
+              keep_logical: bool = False, tables_only: bool = False) -> Case:
     """Generate one seeded decode step of workload `name`.
 
     Overrides shrink or reshape a workload for tests (batch, prefix length,
@@ -232,7 +232,8 @@ def make_case(name: str, seed: int = 0, *, page_size: Optional[int] = None,
     (physical ids in logical order) or "block128" (runs of 128 consecutive
     token slots in shuffled order; page size must divide 128).  With
     `keep_logical`, the encoded rows before paging are kept (contiguous
-    per-request K/V for brute-force checks).
+    per-request K/V for brute-force checks).  With `tables_only`, only the
+    lengths and block tables are generated (q and the pools are None).
     """
     w = WORKLOADS[name]
     w = dataclasses.replace(
@@ -261,23 +262,28 @@ def make_case(name: str, seed: int = 0, *, page_size: Optional[int] = None,
         priv = rng.integers(w.private_lo, w.private_hi + 1, size=B).astype(np.int64)
     P = int(w.prefix_len)
     kv_len = (P + priv).astype(np.int32)
-    q32 = normal_f32((B, Hq, d), seed, 1)
     n_tok = P + int(priv.sum())
-    k_log = normal_f32((n_tok, Hkv, d), seed, 2)
-    v_log = normal_f32((n_tok, Hkv, d), seed, 3)
+    if tables_only:
+        k_log = v_log = q32 = None
+    else:
+        q32 = normal_f32((B, Hq, d), seed, 1)
+        k_log = normal_f32((n_tok, Hkv, d), seed, 2)
+        v_log = normal_f32((n_tok, Hkv, d), seed, 3)
 
     k_scale = v_scale = None
-    if w.kv_dtype == "fp8_e4m3":
+    if tables_only:
+        pass
+    elif w.kv_dtype == "fp8_e4m3":
         k_scale = (np.abs(k_log).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
         v_scale = (np.abs(v_log).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
-    k_enc = _encode(k_log, w.kv_dtype, k_scale)
+    k_enc = _encode(k_log, w.kv_dtype, k_scale) if not tables_only else None
     del k_log
-    v_enc = _encode(v_log, w.kv_dtype, v_scale)
+    v_enc = _encode(v_log, w.kv_dtype, v_scale) if not tables_only else None
     del v_log
     offsets = P + np.concatenate([[0], np.cumsum(priv)[:-1]]) if B else np.zeros(0, np.int64)
     rows_of = [np.concatenate([np.arange(P), offsets[b] + np.arange(int(priv[b]))]).astype(np.int64)
                for b in range(B)] if keep_logical else None
-    q = _encode(q32, w.q_dtype)
+    q = _encode(q32, w.q_dtype) if not tables_only else None
 
     # 2. layout: block-aligned sharing of the prefix
     n_sh = P // ps if P > 0 else 0
@@ -319,6 +325,16 @@ def make_case(name: str, seed: int = 0, *, page_size: Optional[int] = None,
     page_indptr[1:] = np.cumsum([len(p) for p in page_lists])
     page_indices = (np.concatenate(page_lists) if B else np.zeros(0, np.int64)).astype(np.int32)
 
+    if P > 0:
+        prefix_group = np.zeros(B, np.int32)
+        group_prefix_len = np.array([P], np.int32)
+    else:
+        prefix_group = np.full(B, -1, np.int32)
+        group_prefix_len = np.zeros(0, np.int32)
+    if tables_only:
+        return Case(w, seed, ps, n_pages, layout, kv_len, page_indptr, page_indices,
+                    prefix_group, group_prefix_len, None, None, None, None, None)
+
     # 3. fill the pool (flat slot view), poisoned everywhere first
     elem = _np_dtype(w.kv_dtype)
     k_pool = np.full((n_pages * ps, Hkv, d), _poison(w.kv_dtype), dtype=elem)
@@ -339,13 +355,6 @@ def make_case(name: str, seed: int = 0, *, page_size: Optional[int] = None,
         src += int(priv[b])
     k_pool = k_pool.reshape(n_pages, ps, Hkv, d)
     v_pool = v_pool.reshape(n_pages, ps, Hkv, d)
-
-    if P > 0:
-        prefix_group = np.zeros(B, np.int32)
-        group_prefix_len = np.array([P], np.int32)
-    else:
-        prefix_group = np.full(B, -1, np.int32)
-        group_prefix_len = np.zeros(0, np.int32)
     return Case(w, seed, ps, n_pages, layout, kv_len, page_indptr, page_indices,
                 prefix_group, group_prefix_len, q, k_pool, v_pool, k_scale, v_scale,
                 k_enc if keep_logical else None, v_enc if keep_logical else None, rows_of)
