@@ -302,10 +302,19 @@ PSP_API psp_status psp_set_kernel_timing(psp_handle* h, int32_t enable);
 PSP_API psp_status psp_kernel_times(psp_handle* h, float* ms, const char** names, int32_t cap,
                             int32_t* count);
 
-/* Reads (synchronously) the device status word in the bound workspace: 0, or
- * the code a kernel recorded instead of faulting (a bounded wait that ran out,
- * an index found out of range).  Errors: NO_PLAN, CUDA. */
+/* Reads (synchronously) the device status word in the bound workspace into
+ * *code: 0, or the code a kernel recorded instead of faulting -- low byte 1 =
+ * a bounded mbarrier wait ran out (upper bits: the wait site), 2 = an index
+ * found out of range.  Returns PSP_ERR_DEVICE_TIMEOUT when a wait ran out.
+ * Errors: NO_PLAN, CUDA, DEVICE_TIMEOUT. */
 PSP_API psp_status psp_device_status(psp_handle* h, int32_t* code);
+
+/* Failure-detection self test: launches one kernel that waits, with a budget
+ * of `polls` polls, on an mbarrier nothing completes, so that the wait runs out
+ * and records its timeout (site 99) in the status word instead of hanging.
+ * Read the result with psp_device_status after the stream completes.  Needs
+ * an uploaded plan (for the workspace).  Errors: INVALID_ARGUMENT, NO_PLAN, CUDA. */
+PSP_API psp_status psp_wait_selftest(psp_handle* h, int32_t polls, void* stream);
 
 #ifdef __cplusplus
 }

@@ -100,6 +100,7 @@ _sig = {
     "psp_kernel_times": (_S, [_H, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_char_p), _S,
                               ctypes.POINTER(_S)]),
     "psp_device_status": (_S, [_H, ctypes.POINTER(_S)]),
+    "psp_wait_selftest": (_S, [_H, _S, ctypes.c_void_p]),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -253,7 +254,12 @@ class DecodeStep:
         self._check(psp_kernel_times(self.handle, ms, names, cap, ctypes.byref(n)), "psp_kernel_times")
         return [(names[i].decode(), float(ms[i])) for i in range(min(n.value, cap))]
 
-    def device_status(self) -> int:
+    def device_status(self, raise_on_timeout: bool = True) -> int:
         code = _S(0)
-        self._check(psp_device_status(self.handle, ctypes.byref(code)), "psp_device_status")
+        st = psp_device_status(self.handle, ctypes.byref(code))
+        if st != PSP_OK and (raise_on_timeout or st != -9):
+            self._check(st, "psp_device_status")
         return int(code.value)
+
+    def wait_selftest(self, polls: int, stream=None):
+        self._check(psp_wait_selftest(self.handle, int(polls), _stream_ptr(stream)), "psp_wait_selftest")

@@ -19,6 +19,7 @@
 
 #include "psp_device.cuh"
 #include "psp_internal.h"
+#include "psp_sm100.cuh"
 
 namespace psp {
 namespace {
@@ -115,7 +116,26 @@ __global__ void __launch_bounds__(256) expand_kernel(const StepParams p, int32_t
   }
 }
 
+// Failure-detection self test: waits on an mbarrier that nothing completes,
+// with the given poll budget, and must come back with the timeout recorded in
+// the status word (site 99) instead of hanging.
+__global__ void wait_selftest_kernel(int32_t* status, uint32_t polls) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    sm100::mbar_init(b, 1);
+    sm100::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sm100::mbar_wait_polls(b, 0, status, 99, polls);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(int32_t* status, uint32_t polls, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, polls);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const StepParams& p, cudaStream_t s) {
   const int rows = p.batch * p.hq;
@@ -135,6 +155,7 @@ cudaError_t launch_expand_kv_indices(const StepParams& p, int32_t* out, cudaStre
 cudaError_t launch_prefix_dense(const StepParams& p, int num_items, cudaStream_t s) {
   if (num_items <= 0) return cudaSuccess;
   if (p.kv_dtype == PSP_KV_F32) return launch_prefix_simt(p, num_items, true, s);
+  if (dense_tc_supported(p)) return launch_prefix_dense_tc(p, num_items, s);
   return launch_prefix_dense_mma(p, num_items, s);
 }
 

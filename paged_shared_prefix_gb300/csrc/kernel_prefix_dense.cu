@@ -1,0 +1,370 @@
+// kernel_prefix_dense.cu -- dense shared-prefix attention on the 5th-generation
+// tensor cores (tcgen05), the branch the dispatcher takes at large M_eff
+// ("GraniKV", section 3: above the threshold the shared prefix runs as a dense
+// matmul over all stacked queries; section 2: the prefix is read once per
+// step instead of once per request).
+//
+// One CTA = 128 stacked query rows (rows R = member * G + j of one KV head)
+// x one chunk of the shared prefix, in 128-token tiles:
+//   warp 4 (producer)  TMA-loads each K and V tile page by page from the paged
+//                      pool (3-D tensor map [slot][kv head][d], boxes of up to
+//                      64 tokens x 64 dims, 128-byte swizzle) into a 2-stage ring;
+//   warp 5 (MMA)       one thread issues S_j = Q K_j^T (M=128, N=128, K=128,
+//                      bf16 operands from shared memory, fp32 accumulator in
+//                      tensor memory, two S buffers) and O += P_j V_j (P from
+//                      tensor memory, V as an MN-major shared operand);
+//   warps 0-3 (softmax) each thread owns one row: reads its S row from tensor
+//                      memory, applies the online softmax with lazy rescaling
+//                      (the running max is only moved when it grows by more
+//                      than 2^8, and O is rescaled in tensor memory only then),
+//                      writes P back over S as bf16, and at the end normalises
+//                      O and writes the fp32 partial row and its log2-LSE.
+// Every mbarrier wait is bounded; on timeout the kernel records the site in
+// the device status word and unwinds (draining its own TMA copies, freeing its
+// tensor memory) instead of hanging.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "psp_device.cuh"
+#include "psp_internal.h"
+#include "psp_sm100.cuh"
+
+namespace psp {
+namespace {
+
+using namespace dev;
+using namespace sm100;
+
+constexpr int kRows = 128;                 // UMMA M (stacked query rows)
+constexpr int kTok = 128;                  // tokens per tile (N of S, K of PV)
+constexpr int kD = 128;                    // head dim (K of S, N of PV)
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;        // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t kTileBytes = kTok * kD * 2;   // 32 KB, two 16 KB halves (d 0-63, 64-127)
+constexpr uint32_t kHalf = kTileBytes / 2;
+constexpr float kRescaleLog2 = 8.f;
+
+// shared-memory carve-up (offsets from a 1024-byte aligned base)
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;          // 2 stages
+constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;      // 2 stages
+constexpr uint32_t kOffBar = kOffV + 2 * kTileBytes;
+enum Bar { kQReady, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
+           kSFull0, kSFull1, kPFull0, kPFull1, kPvDone, kOFull, kFinal, kNumBars };
+constexpr uint32_t kOffTmem = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffTmem + 16 + 1024;   // + alignment slack
+
+constexpr uint32_t kIdescS = idesc_f16(kRows, kTok, 1, false);
+constexpr uint32_t kIdescPV = idesc_f16(kRows, kD, 1, true);
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefix_dense_kernel(const StepParams p, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, int num_slots) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw);
+  auto bar = [&](int i) { return base + kOffBar + 8u * i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ci = p.item_chunk_dense[blockIdx.x];
+  const int rb = p.item_rb_dense[blockIdx.x];
+  const int h = blockIdx.y;
+  const int g = p.chunk_group[ci];
+  const int t0 = p.chunk_begin[ci];
+  const int t1 = p.chunk_end[ci];
+  const int n_tiles = (t1 - t0 + kTok - 1) / kTok;
+  const int G = p.group;
+  const int m_eff = p.group_m_eff[g];
+  const int32_t* members = p.group_members + p.group_member_indptr[g];
+  int32_t* status = p.status;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kQReady), 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kKFull0 + s), 1);
+      mbar_init(bar(kKEmpty0 + s), 1);
+      mbar_init(bar(kVFull0 + s), 1);
+      mbar_init(bar(kVEmpty0 + s), 1);
+      mbar_init(bar(kSFull0 + s), 1);
+      mbar_init(bar(kPFull0 + s), 128);
+    }
+    mbar_init(bar(kPvDone), 1);
+    mbar_init(bar(kOFull), 1);
+    mbar_init(bar(kFinal), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(base + kOffTmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffTmem);
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
+      const int32_t* list;
+      int shift;
+      if (p.token_flat) {
+        list = p.kv_indices + p.kv_indptr[members[0]];
+        shift = 0;
+      } else {
+        list = p.group_page_indices + p.group_page_indptr[g];
+        shift = p.page_shift;
+      }
+      const int mask = (1 << shift) - 1;
+      const int br = min(1 << shift, 64);  // rows per TMA box; boxes never straddle a page
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j & 1;
+        for (int which = 0; which < 2 && ok; ++which) {  // K then V
+          const int full = (which ? kVFull0 : kKFull0) + s;
+          const int empty = (which ? kVEmpty0 : kKEmpty0) + s;
+          if (j >= 2 && !mbar_wait(bar(empty), ((j >> 1) - 1) & 1, status, 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_tx(bar(full), kTileBytes);
+          const uint32_t dst = base + (which ? kOffV : kOffK) + s * kTileBytes;
+          const CUtensorMap* map = which ? &vmap : &kmap;
+          for (int r = 0; r < kTok; r += br) {
+            const int tok = t0 + j * kTok + r;
+            const int slot = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
+            tma_load_3d(dst + r * 128, map, 0, h, slot, bar(full));
+            tma_load_3d(dst + kHalf + r * 128, map, 64, h, slot, bar(full));
+          }
+        }
+        issued = j + 1;
+      }
+      // drain: the last load issued on each stage must have landed before the CTA may exit
+      for (int j = max(0, issued - 2); j < issued; ++j) {
+        mbar_wait(bar(kKFull0 + (j & 1)), (j >> 1) & 1, status, 2);
+        mbar_wait(bar(kVFull0 + (j & 1)), (j >> 1) & 1, status, 3);
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(kQReady), 0, status, 4);
+      tc_fence_after();
+      auto issue_pv = [&](int jj) -> bool {
+        const int s = jj & 1;
+        if (!mbar_wait(bar(kPFull0 + s), (jj >> 1) & 1, status, 5)) return false;
+        if (!mbar_wait(bar(kVFull0 + s), (jj >> 1) & 1, status, 6)) return false;
+        tc_fence_after();
+        const uint32_t vbase = base + kOffV + s * kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kTok / 16; ++ks) {
+          const uint64_t bdesc = sw128_desc(vbase + ks * 16 * 128, kHalf, 1024);
+          mma_ts(tmem + 256, tmem + s * 128 + ks * 8, bdesc, kIdescPV, (jj > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(kPvDone));
+        mma_commit(bar(kVEmpty0 + s));
+        return true;
+      };
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(bar(kKFull0 + s), (j >> 1) & 1, status, 7)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kbase = base + kOffK + s * kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
+          const uint64_t adesc = sw128_desc(base + kOffQ + off, 16, 1024);
+          const uint64_t bdesc = sw128_desc(kbase + off, 16, 1024);
+          mma_ss(tmem + s * 128, adesc, bdesc, kIdescS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kSFull0 + s));
+        mma_commit(bar(kKEmpty0 + s));
+        if (j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
+      mma_commit(bar(kOFull));
+      mma_commit(bar(kFinal));
+      mbar_wait(bar(kFinal), 0, status, 8);  // every MMA of this CTA has completed
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- softmax warps
+    const int r = threadIdx.x;  // row of the block = TMEM lane
+    const int R = rb * kRows + r;
+    const bool live = R < m_eff;
+    {
+      const uint4* qrow = nullptr;
+      if (live) {
+        const int mem = R / G, jq = R - mem * G;
+        qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                              (static_cast<int64_t>(members[mem]) * p.hq + h * G + jq) * kD);
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = live ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t off = kOffQ + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(gbase + off) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kQReady));
+    }
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float scale = p.scale_log2;
+    float m_used = neg_inf(), l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int s = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull0 + s), (j >> 1) & 1, status, 9));
+      if (!ok) break;
+      tc_fence_after();
+      float x[kTok];
+      {
+        uint32_t u[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + s * 128 + c * 32, u[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[c][i]);
+      }
+      const int valid = min(kTok, t1 - (t0 + j * kTok));
+      float mt = neg_inf();
+#pragma unroll
+      for (int i = 0; i < kTok; ++i) {
+        x[i] = i < valid ? x[i] * scale : neg_inf();
+        mt = fmaxf(mt, x[i]);
+      }
+      const bool need = mt > m_used + kRescaleLog2;
+      float alpha = 1.f;
+      if (need) {
+        alpha = exp2f(m_used - mt);
+        m_used = mt;
+        l *= alpha;
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t u[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float a = exp2f(x[c * 64 + 2 * i] - m_used);
+          const float b = exp2f(x[c * 64 + 2 * i + 1] - m_used);
+          sum += a + b;
+          u[i] = pack_bf16(a, b);
+        }
+        tmem_st32(lane_addr + s * 128 + c * 32, u);
+      }
+      l += sum;
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O holds the products of tiles < j; wait for the last of them, then rescale this row
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kPvDone), (j - 1) & 1, status, 10));
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < kD / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(lane_addr + 256 + c * 32, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            tmem_st32(lane_addr + 256 + c * 32, u);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kPFull0 + s));
+    }
+    // epilogue: O / l -> fp32 partial row, log2-LSE
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kOFull), 0, status, 11));
+    if (ok) {
+      tc_fence_after();
+      const int64_t row = p.chunk_row_offset[ci] + static_cast<int64_t>(h) * m_eff + R;
+      float4* dst = live ? reinterpret_cast<float4*>(p.o_pre + row * kD) : nullptr;
+      const float inv = 1.f / l;
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(lane_addr + 256 + c * 32, u);
+        tmem_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[c * 8 + i] = make_float4(__uint_as_float(u[4 * i]) * inv, __uint_as_float(u[4 * i + 1]) * inv,
+                                         __uint_as_float(u[4 * i + 2]) * inv, __uint_as_float(u[4 * i + 3]) * inv);
+        }
+      }
+      if (live) p.lse_pre[row] = m_used + log2f(l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Pool [slots][Hkv][d] (bf16) as a 3-D tensor; box = 64 dims x 1 head x rows tokens, 128-byte swizzle.
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int64_t slots, int hkv, int rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(slots)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(hkv) * kD * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+// True when the tcgen05 dense kernel serves this configuration (bf16 K/V, d = 128).
+bool dense_tc_supported(const StepParams& p) { return p.kv_dtype == PSP_KV_BF16 && p.head_dim == kD; }
+
+cudaError_t launch_prefix_dense_tc(const StepParams& p, int num_items, cudaStream_t s) {
+  if (num_items <= 0) return cudaSuccess;
+  const int64_t slots = static_cast<int64_t>(p.num_pages) * p.page_size;
+  if (slots >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  const int rows = p.token_flat ? 1 : (p.page_size < 64 ? p.page_size : 64);
+  CUtensorMap kmap, vmap;
+  cudaError_t e = make_pool_map(&kmap, p.k_pool, slots, p.hkv, rows);
+  if (e != cudaSuccess) return e;
+  e = make_pool_map(&vmap, p.v_pool, slots, p.hkv, rows);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefix_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(num_items, p.hkv);
+  prefix_dense_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, kmap, vmap, static_cast<int>(slots));
+  return cudaGetLastError();
+}
+
+}  // namespace psp

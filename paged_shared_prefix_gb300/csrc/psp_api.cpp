@@ -782,11 +782,21 @@ psp_status psp_expand_kv_indices(psp_handle* h, int32_t* kv_indices, int64_t cap
   return PSP_OK;
 }
 
+psp_status psp_wait_selftest(psp_handle* h, int32_t polls, void* stream) {
+  if (!h || polls < 1) return PSP_ERR_INVALID_ARGUMENT;
+  if (!h->uploaded) return fail(h, PSP_ERR_NO_PLAN, "no workspace bound");
+  int32_t* status = reinterpret_cast<int32_t*>(h->workspace + h->plan.layout.status);
+  cudaError_t e = psp::launch_wait_selftest(status, static_cast<uint32_t>(polls), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "wait self test");
+  return PSP_OK;
+}
+
 psp_status psp_device_status(psp_handle* h, int32_t* code) {
   if (!h || !code) return PSP_ERR_INVALID_ARGUMENT;
   if (!h->uploaded) return fail(h, PSP_ERR_NO_PLAN, "no workspace bound");
   cudaError_t e = cudaMemcpy(code, h->workspace + h->plan.layout.status, sizeof(int32_t), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e, "reading the device status word");
+  if ((*code & 0xff) == psp::kDevTimeout) return fail(h, PSP_ERR_DEVICE_TIMEOUT, "a bounded device wait ran out");
   return PSP_OK;
 }
 

@@ -109,5 +109,8 @@ cudaError_t launch_expand_kv_indices(const StepParams& p, int32_t* out, cudaStre
 cudaError_t launch_suffix_simt(const StepParams& p, int num_splits, cudaStream_t s);
 cudaError_t launch_prefix_simt(const StepParams& p, int num_items, bool dense, cudaStream_t s);
 cudaError_t launch_prefix_dense_mma(const StepParams& p, int num_items, cudaStream_t s);
+cudaError_t launch_prefix_dense_tc(const StepParams& p, int num_items, cudaStream_t s);
+bool dense_tc_supported(const StepParams& p);
+cudaError_t launch_wait_selftest(int32_t* status, uint32_t polls, cudaStream_t s);
 
 }  // namespace psp

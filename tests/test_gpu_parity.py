@@ -215,3 +215,24 @@ def test_full_size_paged_comparator_matches():
     ro, rl = oracle.attend(case, bb, hh)
     for o, l in (a, b):
         assert max_err(o[bb, hh], ro) <= TOL["bf16"] and max_err(l[bb, hh], rl) <= TOL["bf16"]
+
+
+def test_bounded_wait_reports_timeout_instead_of_hanging():
+    case = workloads.make_case("tiny", 0)
+    step = psp.DecodeStep.for_case(case)
+    step.plan_case(case)
+    ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device="cuda:0")
+    step.upload(ws)
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    step.wait_selftest(2000)
+    torch.cuda.synchronize()
+    code = step.device_status(raise_on_timeout=False)
+    assert code & 0xff == 1 and code >> 8 == 99
+    # the context stays usable and a fresh upload clears the word
+    step.upload(ws)
+    o, lse = run_case(case)
+    ref_o, _ = oracle.attend_all(case)
+    assert max_err(o, ref_o) <= TOL["f32"]
+    assert step.device_status() == 0
+    step.close()
