@@ -70,6 +70,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle CPU time for the baseline")
+    ap.add_argument("--sweep-threshold", action="store_true",
+                    help="time the dense and cascade prefix kernels over an M_eff sweep and report the refit threshold")
     return ap.parse_args()
 
 
@@ -243,10 +245,58 @@ def run_reference(args):
     return 0
 
 
+def sweep_threshold(args):
+    """Dispatcher refit: for a 4096-token prefix and 8 KV heads, time the prefix kernel of
+    both branches over batch x GQA group; the threshold is the smallest swept M_eff from
+    which the dense branch is never slower than the cascade branch."""
+    import torch
+
+    import paged_shared_prefix_gb300 as psp
+    dev = torch.device("cuda:0")
+    rows = []
+    for G in (1, 2, 4, 8):
+        for B in (4, 8, 16, 32, 64, 128, 256, 512):
+            m_eff = B * G
+            if m_eff < 16 or m_eff > 4096:
+                continue
+            case = workloads.make_case("agent", 11, batch=B, prefix_len=4096, private_range=(1, 16),
+                                       num_q_heads=8 * G, num_kv_heads=8)
+            tens = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev))
+                    for k, v in dict(q=case.q, k=case.k_pool, v=case.v_pool).items()}
+            o = torch.empty((B, 8 * G, 128), dtype=torch.bfloat16, device=dev)
+            res = {}
+            for branch, thr in (("dense", 1), ("cascade", 1 << 30)):
+                step = psp.DecodeStep.for_case(case, dense_threshold=thr)
+                step.plan_case(case)
+                ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device=dev)
+                step.upload(ws)
+                step.set_kernel_timing(True)
+                times = []
+                for i in range(8):
+                    step.run(tens["q"], tens["k"], tens["v"], o)
+                    torch.cuda.synchronize()
+                    if i >= 3:
+                        times += [ms for n, ms in step.kernel_times() if n.startswith("prefix")]
+                res[branch] = statistics.median(times) * 1e3
+                step.close()
+            rows.append({"G": G, "B": B, "m_eff": m_eff, "dense_us": res["dense"], "cascade_us": res["cascade"]})
+    rows.sort(key=lambda r: r["m_eff"])
+    thr = None
+    for i, r in enumerate(rows):
+        if all(x["dense_us"] <= x["cascade_us"] for x in rows[i:]):
+            thr = r["m_eff"]
+            break
+    print(json.dumps({"sweep": rows, "refit_threshold": thr,
+                      "gpu": torch.cuda.get_device_name(0), "prefix_tokens": 4096, "kv_heads": 8}))
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep_threshold:
+        return sweep_threshold(args)
 
     import torch
     import torch.distributed as dist

@@ -19,6 +19,12 @@
 //                      than 2^8, and O is rescaled in tensor memory only then),
 //                      writes P back over S as bf16, and at the end normalises
 //                      O and writes the fp32 partial row and its log2-LSE.
+// fp8-e4m3 caches use kind::f8f6f4: the e4m3 K/V tiles are loaded as stored
+// (one 128-byte box row per token), each query row is quantised to e4m3 with
+// its own scale amax/448 (folded, with the per-head key scale, into the
+// softmax scale), and P is written to tensor memory as e4m3 (P <= 2^8 under
+// the lazy rescaling bound, inside the e4m3 range); the value scale is
+// applied to the normalised output.
 // Every mbarrier wait is bounded; on timeout the kernel records the site in
 // the device status word and unwinds (draining its own TMA copies, freeing its
 // tensor memory) instead of hanging.
@@ -43,26 +49,38 @@ constexpr int kTok = 128;                  // tokens per tile (N of S, K of PV)
 constexpr int kD = 128;                    // head dim (K of S, N of PV)
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;        // S0 [0,128), S1 [128,256), O [256,384)
-constexpr uint32_t kTileBytes = kTok * kD * 2;   // 32 KB, two 16 KB halves (d 0-63, 64-127)
-constexpr uint32_t kHalf = kTileBytes / 2;
 constexpr float kRescaleLog2 = 8.f;
-
-// shared-memory carve-up (offsets from a 1024-byte aligned base)
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;          // 2 stages
-constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;      // 2 stages
-constexpr uint32_t kOffBar = kOffV + 2 * kTileBytes;
 enum Bar { kQReady, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
            kSFull0, kSFull1, kPFull0, kPFull1, kPvDone, kOFull, kFinal, kNumBars };
-constexpr uint32_t kOffTmem = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffTmem + 16 + 1024;   // + alignment slack
 
-constexpr uint32_t kIdescS = idesc_f16(kRows, kTok, 1, false);
-constexpr uint32_t kIdescPV = idesc_f16(kRows, kD, 1, true);
+// Tile geometry for bf16 (FP8 = false) and e4m3 (FP8 = true) operands.
+template <bool FP8>
+struct DenseCfg {
+  static constexpr uint32_t kElem = FP8 ? 1 : 2;
+  static constexpr uint32_t kTileBytes = kTok * kD * kElem;  // one Q, K or V tile
+  static constexpr uint32_t kHalves = FP8 ? 1 : 2;           // 128-byte column blocks of a row
+  static constexpr uint32_t kHalf = kTileBytes / kHalves;    // 16 KB
+  static constexpr int kBoxElems = 128 / kElem;              // d elements per TMA box row
+  static constexpr int kKStep = 32 / kElem;                  // K elements per MMA instruction
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + kTileBytes;      // 2 stages
+  static constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;  // 2 stages
+  static constexpr uint32_t kOffBar = kOffV + 2 * kTileBytes;
+  static constexpr uint32_t kOffTmem = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kOffTmem + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(kRows, kTok, false) : idesc_f16(kRows, kTok, 1, false);
+  static constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3(kRows, kD, true) : idesc_f16(kRows, kD, 1, true);
+};
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_dense_kernel(const StepParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, int num_slots) {
+  using C = DenseCfg<FP8>;
+  constexpr uint32_t kTileBytes = C::kTileBytes;
+  constexpr uint32_t kHalf = C::kHalf;
+  constexpr uint32_t kOffQ = C::kOffQ, kOffK = C::kOffK, kOffV = C::kOffV, kOffBar = C::kOffBar;
+  constexpr uint32_t kOffTmem = C::kOffTmem;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -140,8 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < kTok; r += br) {
             const int tok = t0 + j * kTok + r;
             const int slot = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
-            tma_load_3d(dst + r * 128, map, 0, h, slot, bar(full));
-            tma_load_3d(dst + kHalf + r * 128, map, 64, h, slot, bar(full));
+#pragma unroll
+            for (uint32_t hf = 0; hf < C::kHalves; ++hf)
+              tma_load_3d(dst + hf * kHalf + r * 128, map, hf * C::kBoxElems, h, slot, bar(full));
           }
         }
         issued = j + 1;
@@ -164,9 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t vbase = base + kOffV + s * kTileBytes;
 #pragma unroll
-        for (int ks = 0; ks < kTok / 16; ++ks) {
-          const uint64_t bdesc = sw128_desc(vbase + ks * 16 * 128, kHalf, 1024);
-          mma_ts(tmem + 256, tmem + s * 128 + ks * 8, bdesc, kIdescPV, (jj > 0 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < kTok / C::kKStep; ++ks) {
+          // V is the MN-major B operand: K (tokens) advances by whole 128-byte rows
+          const uint64_t bdesc = sw128_desc(vbase + ks * C::kKStep * 128, kHalf, 1024);
+          const uint32_t acc = (jj > 0 || ks > 0) ? 1u : 0u;
+          if constexpr (FP8) {
+            mma_ts_f8(tmem + 256, tmem + s * 128 + ks * 8, bdesc, C::kIdescPV, acc);
+          } else {
+            mma_ts(tmem + 256, tmem + s * 128 + ks * 8, bdesc, C::kIdescPV, acc);
+          }
         }
         mma_commit(bar(kPvDone));
         mma_commit(bar(kVEmpty0 + s));
@@ -181,11 +206,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t kbase = base + kOffK + s * kTileBytes;
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
+        for (int ks = 0; ks < kD / C::kKStep; ++ks) {
+          // K-major operands: 32 bytes of K per instruction inside a 128-byte swizzled row
           const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
           const uint64_t adesc = sw128_desc(base + kOffQ + off, 16, 1024);
           const uint64_t bdesc = sw128_desc(kbase + off, 16, 1024);
-          mma_ss(tmem + s * 128, adesc, bdesc, kIdescS, ks > 0 ? 1u : 0u);
+          if constexpr (FP8) {
+            mma_ss_f8(tmem + s * 128, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
+          } else {
+            mma_ss(tmem + s * 128, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
+          }
         }
         mma_commit(bar(kSFull0 + s));
         mma_commit(bar(kKEmpty0 + s));
@@ -202,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x;  // row of the block = TMEM lane
     const int R = rb * kRows + r;
     const bool live = R < m_eff;
+    float q_scale = 1.f;  // fp8: this row's quantisation scale
     {
       const uint4* qrow = nullptr;
       if (live) {
@@ -209,17 +240,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
                                               (static_cast<int64_t>(members[mem]) * p.hq + h * G + jq) * kD);
       }
+      if constexpr (FP8) {
+        uint4 raw[16];
+        float amax = 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = live ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t off = kOffQ + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(gbase + off) = v;
+        for (int c = 0; c < 16; ++c) {
+          raw[c] = live ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[k] & 0xffff)), fabsf(bf16_bits_to_float(w[k] >> 16))));
+        }
+        q_scale = amax > 0.f ? amax / 448.f : 1.f;
+        const float inv = 1.f / q_scale;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16 e4m3 codes per 16-byte chunk
+          uint32_t out[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t w0 = (k < 2) ? (&raw[2 * c].x)[2 * k] : (&raw[2 * c + 1].x)[2 * (k - 2)];
+            const uint32_t w1 = (k < 2) ? (&raw[2 * c].x)[2 * k + 1] : (&raw[2 * c + 1].x)[2 * (k - 2) + 1];
+            out[k] = e4m3x4_from_floats(bf16_bits_to_float(w0 & 0xffff) * inv, bf16_bits_to_float(w0 >> 16) * inv,
+                                        bf16_bits_to_float(w1 & 0xffff) * inv, bf16_bits_to_float(w1 >> 16) * inv);
+          }
+          const uint32_t off = kOffQ + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(gbase + off) = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint4 v = live ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t off = kOffQ + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(gbase + off) = v;
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(kQReady));
     }
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const float scale = p.scale_log2;
+    float scale = p.scale_log2;
+    float out_scale = 1.f;
+    if constexpr (FP8) {
+      scale *= __ldg(p.k_scale + h) * q_scale;
+      out_scale = __ldg(p.v_scale + h);
+    }
     float m_used = neg_inf(), l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
@@ -253,17 +317,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
       }
       float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t u[32];
+      if constexpr (FP8) {
+        uint32_t u[32];  // four e4m3 probabilities per column
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float a = exp2f(x[c * 64 + 2 * i] - m_used);
-          const float b = exp2f(x[c * 64 + 2 * i + 1] - m_used);
-          sum += a + b;
-          u[i] = pack_bf16(a, b);
+          const float a = exp2f(x[4 * i] - m_used), b = exp2f(x[4 * i + 1] - m_used);
+          const float c2 = exp2f(x[4 * i + 2] - m_used), d2 = exp2f(x[4 * i + 3] - m_used);
+          sum += (a + b) + (c2 + d2);
+          u[i] = e4m3x4_from_floats(a, b, c2, d2);
         }
-        tmem_st32(lane_addr + s * 128 + c * 32, u);
+        tmem_st32(lane_addr + s * 128, u);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t u[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = exp2f(x[c * 64 + 2 * i] - m_used);
+            const float b = exp2f(x[c * 64 + 2 * i + 1] - m_used);
+            sum += a + b;
+            u[i] = pack_bf16(a, b);
+          }
+          tmem_st32(lane_addr + s * 128 + c * 32, u);
+        }
       }
       l += sum;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -292,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t row = p.chunk_row_offset[ci] + static_cast<int64_t>(h) * m_eff + R;
       float4* dst = live ? reinterpret_cast<float4*>(p.o_pre + row * kD) : nullptr;
-      const float inv = 1.f / l;
+      const float inv = out_scale / l;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t u[32];
@@ -331,40 +407,49 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Pool [slots][Hkv][d] (bf16) as a 3-D tensor; box = 64 dims x 1 head x rows tokens, 128-byte swizzle.
-cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int64_t slots, int hkv, int rows) {
+// Pool [slots][Hkv][d] as a 3-D tensor; box = 128 bytes of d x 1 head x rows tokens, 128-byte swizzle.
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int64_t slots, int hkv, int rows, bool fp8) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t elem = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(slots)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(hkv) * kD * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * elem, static_cast<cuuint64_t>(hkv) * kD * elem};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 1, static_cast<cuuint32_t>(rows)};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-}  // namespace
-
-// True when the tcgen05 dense kernel serves this configuration (bf16 K/V, d = 128).
-bool dense_tc_supported(const StepParams& p) { return p.kv_dtype == PSP_KV_BF16 && p.head_dim == kD; }
-
-cudaError_t launch_prefix_dense_tc(const StepParams& p, int num_items, cudaStream_t s) {
-  if (num_items <= 0) return cudaSuccess;
+template <bool FP8>
+cudaError_t launch_t(const StepParams& p, int num_items, cudaStream_t s) {
   const int64_t slots = static_cast<int64_t>(p.num_pages) * p.page_size;
   if (slots >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
   const int rows = p.token_flat ? 1 : (p.page_size < 64 ? p.page_size : 64);
   CUtensorMap kmap, vmap;
-  cudaError_t e = make_pool_map(&kmap, p.k_pool, slots, p.hkv, rows);
+  cudaError_t e = make_pool_map(&kmap, p.k_pool, slots, p.hkv, rows, FP8);
   if (e != cudaSuccess) return e;
-  e = make_pool_map(&vmap, p.v_pool, slots, p.hkv, rows);
+  e = make_pool_map(&vmap, p.v_pool, slots, p.hkv, rows, FP8);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prefix_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  constexpr uint32_t bytes = DenseCfg<FP8>::kSmemBytes;
+  e = cudaFuncSetAttribute(prefix_dense_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   dim3 grid(num_items, p.hkv);
-  prefix_dense_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, kmap, vmap, static_cast<int>(slots));
+  prefix_dense_kernel<FP8><<<grid, kThreads, bytes, s>>>(p, kmap, vmap, static_cast<int>(slots));
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// True when the tcgen05 dense kernel serves this configuration (bf16 or e4m3 K/V, d = 128).
+bool dense_tc_supported(const StepParams& p) {
+  return (p.kv_dtype == PSP_KV_BF16 || p.kv_dtype == PSP_KV_FP8) && p.head_dim == kD;
+}
+
+cudaError_t launch_prefix_dense_tc(const StepParams& p, int num_items, cudaStream_t s) {
+  if (num_items <= 0) return cudaSuccess;
+  return p.kv_dtype == PSP_KV_FP8 ? launch_t<true>(p, num_items, s) : launch_t<false>(p, num_items, s);
 }
 
 }  // namespace psp
