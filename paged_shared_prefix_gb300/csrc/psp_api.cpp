@@ -68,6 +68,7 @@ struct HostPlan {
   int64_t kv_indices_len = 0, suffix_tokens = 0, shared_tokens = 0, pre_rows = 0;
   PlanLayout layout{};
   psp_plan_info info{};
+  std::vector<unsigned char> image;  // the uploaded integer region, laid out as in the workspace
 };
 
 }  // namespace
@@ -333,6 +334,38 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   place(L.lse_pre, static_cast<size_t>(P.pre_rows) * sizeof(float));
   place(L.kv_indices, (c.flags & PSP_FLAG_TOKEN_FLAT) ? static_cast<size_t>(P.kv_indices_len) * 4 : 0);
   L.total = off;
+
+  // host image of the integer region
+  P.image.assign(L.plan_bytes, 0);
+  auto put = [&](size_t off, const std::vector<int32_t>& v) {
+    if (!v.empty()) std::memcpy(P.image.data() + off, v.data(), v.size() * sizeof(int32_t));
+  };
+  put(L.suffix_page_indptr, P.suffix_page_indptr);
+  put(L.suffix_page_indices, P.suffix_page_indices);
+  put(L.suffix_start, P.suffix_start);
+  put(L.suffix_len, P.suffix_len);
+  put(L.split_indptr, P.split_indptr);
+  put(L.split_req, P.split_req);
+  put(L.split_begin, P.split_begin);
+  put(L.split_end, P.split_end);
+  put(L.req_group, P.req_group);
+  put(L.req_member, P.req_member);
+  put(L.group_page_indptr, P.group_page_indptr);
+  put(L.group_page_indices, P.group_page_indices);
+  put(L.group_m_eff, P.group_m_eff);
+  put(L.group_shared_len, P.group_shared_len);
+  put(L.group_member_indptr, P.group_member_indptr);
+  put(L.group_members, P.group_members);
+  put(L.group_chunk_indptr, P.group_chunk_indptr);
+  put(L.chunk_group, P.chunk_group);
+  put(L.chunk_begin, P.chunk_begin);
+  put(L.chunk_end, P.chunk_end);
+  put(L.chunk_row_offset, P.chunk_row_offset);
+  put(L.item_chunk_dense, P.item_chunk_dense);
+  put(L.item_rb_dense, P.item_rb_dense);
+  put(L.item_chunk_cascade, P.item_chunk_cascade);
+  put(L.item_rb_cascade, P.item_rb_cascade);
+  put(L.kv_indptr, P.kv_indptr);
 
   psp_plan_info& I = P.info;
   I.batch_size = B;
@@ -611,36 +644,7 @@ psp_status psp_upload(psp_handle* h, void* workspace, size_t workspace_bytes, vo
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaHostAlloc (plan staging)");
     h->staging_bytes = want;
   }
-  auto put = [&](size_t off, const std::vector<int32_t>& v) {
-    if (!v.empty()) std::memcpy(h->staging + off, v.data(), v.size() * sizeof(int32_t));
-  };
-  std::memset(h->staging, 0, L.plan_bytes);
-  put(L.suffix_page_indptr, P.suffix_page_indptr);
-  put(L.suffix_page_indices, P.suffix_page_indices);
-  put(L.suffix_start, P.suffix_start);
-  put(L.suffix_len, P.suffix_len);
-  put(L.split_indptr, P.split_indptr);
-  put(L.split_req, P.split_req);
-  put(L.split_begin, P.split_begin);
-  put(L.split_end, P.split_end);
-  put(L.req_group, P.req_group);
-  put(L.req_member, P.req_member);
-  put(L.group_page_indptr, P.group_page_indptr);
-  put(L.group_page_indices, P.group_page_indices);
-  put(L.group_m_eff, P.group_m_eff);
-  put(L.group_shared_len, P.group_shared_len);
-  put(L.group_member_indptr, P.group_member_indptr);
-  put(L.group_members, P.group_members);
-  put(L.group_chunk_indptr, P.group_chunk_indptr);
-  put(L.chunk_group, P.chunk_group);
-  put(L.chunk_begin, P.chunk_begin);
-  put(L.chunk_end, P.chunk_end);
-  put(L.chunk_row_offset, P.chunk_row_offset);
-  put(L.item_chunk_dense, P.item_chunk_dense);
-  put(L.item_rb_dense, P.item_rb_dense);
-  put(L.item_chunk_cascade, P.item_chunk_cascade);
-  put(L.item_rb_cascade, P.item_rb_cascade);
-  put(L.kv_indptr, P.kv_indptr);
+  std::memcpy(h->staging, P.image.data(), L.plan_bytes);
   e = cudaMemcpyAsync(workspace, h->staging, L.plan_bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "plan upload");
   e = cudaEventRecord(h->staging_done, s);
