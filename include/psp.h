@@ -309,6 +309,31 @@ PSP_API psp_status psp_kernel_times(psp_handle* h, float* ms, const char** names
  * Errors: NO_PLAN, CUDA, DEVICE_TIMEOUT. */
 PSP_API psp_status psp_device_status(psp_handle* h, int32_t* code);
 
+/* Workspace-free variant of psp_run, for callers that cannot allocate device
+ * memory where they run the step: an engine that has reserved nearly all HBM
+ * for its KV pool and weights, a framework plugin or custom-op callback that
+ * must not allocate on that path, or a latency-critical loop that cannot take
+ * the synchronisation an allocation may cause.  (It has no counterpart on the
+ * pages; the step it runs is exactly psp_run's.)
+ * Needs a successful psp_plan; instead of psp_upload's caller workspace it
+ * uses one file-scope static device array of 64 MiB, held for the life of the
+ * process on every GPU where the library's device code is loaded.  It copies
+ * the plan into that array from the handle's host image (pageable copy, no
+ * staging), clears the status word, binds the array as the handle's workspace
+ * (psp_device_status reads it afterwards) and launches the step on `stream`.
+ * It calls no cudaMalloc, cudaFree or other allocating routine and records no
+ * kernel timing events.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call, from any handle, shares the one
+ * array, which keeps the last call's contents: calls whose work overlaps on
+ * the GPU race with each other, so serialise them (one stream, or events).
+ * A plan whose workspace (psp_workspace_size) exceeds 64 MiB is rejected with
+ * PSP_ERR_WORKSPACE before anything is copied or launched.
+ * Errors: INVALID_ARGUMENT, NO_PLAN, WORKSPACE, UNSUPPORTED (device ordinal >
+ * 63), CUDA. */
+PSP_API psp_status psp_run_noalloc(psp_handle* h, const psp_tensors* t, void* stream);
+
 /* Failure-detection self test: launches one kernel that waits, with a budget
  * of `polls` polls, on an mbarrier nothing completes, so that the wait runs out
  * and records its timeout (site 99) in the status word instead of hanging.

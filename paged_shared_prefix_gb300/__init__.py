@@ -101,6 +101,7 @@ _sig = {
                               ctypes.POINTER(_S)]),
     "psp_device_status": (_S, [_H, ctypes.POINTER(_S)]),
     "psp_wait_selftest": (_S, [_H, _S, ctypes.c_void_p]),
+    "psp_run_noalloc": (_S, [_H, ctypes.POINTER(psp_tensors), ctypes.c_void_p]),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -232,6 +233,11 @@ class DecodeStep:
     def run(self, q, k_pool, v_pool, o, lse=None, k_scale=None, v_scale=None, stream=None):
         t = self.tensors(q, k_pool, v_pool, o, lse, k_scale, v_scale)
         self._check(psp_run(self.handle, ctypes.byref(t), _stream_ptr(stream)), "psp_run")
+
+    def run_noalloc(self, q, k_pool, v_pool, o, lse=None, k_scale=None, v_scale=None, stream=None):
+        """psp_run_noalloc: the same step with the library's static scratch as workspace."""
+        t = self.tensors(q, k_pool, v_pool, o, lse, k_scale, v_scale)
+        self._check(psp_run_noalloc(self.handle, ctypes.byref(t), _stream_ptr(stream)), "psp_run_noalloc")
 
     def step_host(self, batch: psp_batch, q_host, o_host, lse_host, dev: psp_tensors, workspace, stream=None):
         nbytes = workspace.numel() * workspace.element_size()

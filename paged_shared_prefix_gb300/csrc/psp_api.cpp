@@ -805,3 +805,40 @@ psp_status psp_device_status(psp_handle* h, int32_t* code) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- workspace-free entry point support
+
+namespace psp {
+
+psp_status set_error(psp_handle* h, psp_status code, const char* msg) { return fail(h, code, msg); }
+
+// Copies the plan's host image into caller-provided device scratch without any
+// allocation (pageable source, no pinned staging), clears the status word, binds
+// the scratch as the handle's workspace and launches the step.  Kernel timing
+// events are not recorded on this path (creating them would allocate).
+psp_status bind_image_and_run(psp_handle* h, unsigned char* ws, size_t cap, const psp_tensors* t,
+                              cudaStream_t s) {
+  if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  if (!h->planned) return fail(h, PSP_ERR_NO_PLAN, "psp_run_noalloc before psp_plan");
+  const PlanLayout& L = h->plan.layout;
+  if (L.total > cap)
+    return fail(h, PSP_ERR_WORKSPACE,
+                "the plan needs " + std::to_string(L.total) + " bytes of scratch but the static scratch holds " +
+                    std::to_string(cap) + " bytes; plan a smaller batch or use psp_upload with a workspace");
+  if (!t || !t->q || !t->k_pool || !t->v_pool || !t->o)
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "q, k_pool, v_pool and o must be set");
+  cudaError_t e = cudaMemcpyAsync(ws, h->plan.image.data(), L.plan_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "plan copy into the static scratch");
+  e = cudaMemsetAsync(ws + L.status, 0, 64, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "clearing the device status word");
+  h->workspace = ws;
+  h->workspace_bytes = cap;
+  h->uploaded = true;
+  const bool timing = h->timing;
+  h->timing = false;
+  const psp_status st = psp_run(h, t, s);
+  h->timing = timing;
+  return st;
+}
+
+}  // namespace psp

@@ -113,4 +113,14 @@ cudaError_t launch_prefix_dense_tc(const StepParams& p, int num_items, cudaStrea
 bool dense_tc_supported(const StepParams& p);
 cudaError_t launch_wait_selftest(int32_t* status, uint32_t polls, cudaStream_t s);
 
+// Workspace-free entry point support (defined in psp_api.cpp).
+}  // namespace psp
+
+struct psp_handle;
+typedef int32_t psp_status;
+struct psp_tensors;
+
+namespace psp {
+psp_status set_error(psp_handle* h, psp_status code, const char* msg);
+psp_status bind_image_and_run(psp_handle* h, unsigned char* ws, size_t cap, const psp_tensors* t, cudaStream_t s);
 }  // namespace psp

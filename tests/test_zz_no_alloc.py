@@ -1,0 +1,66 @@
+"""psp_run_noalloc: the decode step for callers that cannot allocate device
+memory (an engine whose KV pool and weights already hold nearly all of HBM, a
+plugin callback that must not allocate, a latency-critical loop).  It must give
+the same result as psp_run with a caller workspace, call after call, while the
+library's static scratch keeps the previous call's contents.
+
+Kept in a file that pytest collects last, so that a run stopping at the first
+failure has already run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_shared_prefix_gb300 as psp
+import workloads
+from gpu_util import TOL, device_tensors, max_err, run_case
+
+pytestmark = pytest.mark.gpu
+
+
+def _fresh_outputs(case):
+    w = case.workload
+    dt = torch.float32 if w.o_dtype == "f32" else torch.bfloat16
+    o = torch.full((case.batch, w.num_q_heads, w.head_dim), float("nan"), dtype=dt, device="cuda:0")
+    lse = torch.full((case.batch, w.num_q_heads), float("nan"), dtype=torch.float32, device="cuda:0")
+    return o, lse
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("agent", dict(batch=24, prefix_len=512, private_range=(1, 300))),
+    ("fp8_large", dict(batch=10, prefix_len=384, private_range=(1, 200))),
+    ("tiny", dict()),
+])
+def test_noalloc_matches_workspace_run_twice(name, kw):
+    case = workloads.make_case(name, 3, **kw)
+    ref_o, ref_lse = run_case(case)                # psp_run with a caller workspace
+    tens = device_tensors(case)
+    step = psp.DecodeStep.for_case(case)
+    step.plan_case(case)
+    tol = TOL[case.workload.kv_dtype]
+    for _ in range(2):                             # the second call reuses the scratch as left
+        o, lse = _fresh_outputs(case)
+        step.run_noalloc(tens["q"], tens["k_pool"], tens["v_pool"], o, lse, tens["k_scale"], tens["v_scale"])
+        torch.cuda.synchronize()
+        assert step.device_status() == 0
+        got_o = o.float().cpu().double().numpy()
+        got_lse = lse.cpu().double().numpy()
+        assert max_err(got_o, ref_o) <= tol and max_err(got_lse, ref_lse) <= tol
+    o_ref, _ = oracle.attend_all(case)
+    assert max_err(got_o, o_ref) <= tol
+    step.close()
+
+
+def test_noalloc_rejects_a_plan_larger_than_the_scratch():
+    case = workloads.make_case("fp8_large", 0, batch=4096, tables_only=True)
+    step = psp.DecodeStep.for_case(case)
+    step.plan_case(case)
+    assert step.workspace_size() > 64 << 20
+    dummy = torch.zeros(16, dtype=torch.uint8, device="cuda:0")
+    t = step.tensors(dummy, dummy, dummy, dummy)
+    st = psp.psp_run_noalloc(step.handle, ctypes.byref(t), None)
+    assert st == -7                                # PSP_ERR_WORKSPACE, nothing launched
+    assert b"static scratch" in psp.psp_last_error(step.handle)
+    step.close()
