@@ -50,7 +50,6 @@ KERNEL_SOURCES = {
     "suffix_splitkv": "paged_shared_prefix_gb300/csrc/kernel_suffix.cu",
     "prefix_cascade": "paged_shared_prefix_gb300/csrc/kernel_prefix_cascade.cu",
     "prefix_dense": "paged_shared_prefix_gb300/csrc/kernel_prefix_dense.cu",
-    "merge": "paged_shared_prefix_gb300/csrc/kernel_merge.cu",
     "expand_kv_indices": "paged_shared_prefix_gb300/csrc/kernel_merge.cu",
 }
 
@@ -58,7 +57,7 @@ KERNEL_SOURCES = {
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="agent", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--page-size", type=int, default=None)
@@ -132,7 +131,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -393,11 +392,6 @@ def main():
         if dom == "suffix_splitkv":
             alg = info["suffix_tokens"] * tok_bytes
             desc = f"{alg} B per launch = {info['suffix_tokens']} suffix tokens x {tok_bytes} B (K+V, all KV heads)"
-        elif dom == "merge":
-            rows = case.batch * w.num_q_heads
-            parts = (info["num_splits"] * Hkv * (w.num_q_heads // Hkv) + info["num_chunks"] * 0)
-            alg = rows * d * workloads.elem_bytes(w.o_dtype)
-            desc = f"{alg} B output per launch"
         else:
             alg = ub
             desc = f"{alg} unique K/V bytes"

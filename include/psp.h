@@ -251,7 +251,8 @@ PSP_API psp_status psp_plan(psp_handle* h, const psp_batch* batch);
 PSP_API psp_status psp_plan_info_get(const psp_handle* h, psp_plan_info* out);
 
 /* Device workspace bytes the current plan needs (plan arrays, fp32 partial
- * results, the token-flat indices in TOKEN_FLAT mode, a device status word).
+ * results, the token-flat indices in TOKEN_FLAT mode, a device status word and
+ * per-(request, KV head) merge counters).
  * Errors: NO_PLAN. */
 PSP_API psp_status psp_workspace_size(const psp_handle* h, size_t* bytes);
 
@@ -264,15 +265,16 @@ PSP_API psp_status psp_plan_query(const psp_handle* h, int32_t field, void* dst,
 /* Binds a caller-allocated device workspace (>= psp_workspace_size bytes,
  * 256-byte aligned) to the current plan and enqueues the plan's host-to-device
  * copy on `stream` (from pinned staging the library owns).  Clears the device
- * status word.  The staging is reused by the next upload of this handle after
+ * status word and the merge counters.  The staging is reused by the next upload of this handle after
  * the previous copy has completed (the call synchronises on its own event).
  * Errors: NO_PLAN, WORKSPACE, CUDA, HOST_ALLOC. */
 PSP_API psp_status psp_upload(psp_handle* h, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Launches one decode step on `stream`: the prefix kernel of every group
- * (dense or cascade branch), the split-KV suffix kernel, and the log-sum-exp
- * merge that writes o and lse (and, in TOKEN_FLAT mode, first the device
- * kv_indices expansion).  Reads the uploaded plan; t must match the planned
+ * (dense or cascade branch), then the split-KV suffix kernel (in TOKEN_FLAT
+ * mode, first the device kv_indices expansion).  The log-sum-exp merge that
+ * writes o and lse runs inside those kernels: the CTA that delivers the last
+ * partial result of a (request, KV head) merges its rows.  Reads the uploaded plan; t must match the planned
  * batch and configuration.  Errors: NO_PLAN, INVALID_ARGUMENT, CUDA. */
 PSP_API psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream);
 
@@ -319,7 +321,8 @@ PSP_API psp_status psp_device_status(psp_handle* h, int32_t* code);
  * uses one file-scope static device array of 64 MiB, held for the life of the
  * process on every GPU where the library's device code is loaded.  It copies
  * the plan into that array from the handle's host image (pageable copy, no
- * staging), clears the status word, binds the array as the handle's workspace
+ * staging), clears the status word and the merge counters, binds the array
+ * as the handle's workspace
  * (psp_device_status reads it afterwards) and launches the step on `stream`.
  * It calls no cudaMalloc, cudaFree or other allocating routine and records no
  * kernel timing events.

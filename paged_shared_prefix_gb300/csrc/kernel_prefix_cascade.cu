@@ -19,6 +19,7 @@
 
 #include "psp_device.cuh"
 #include "psp_internal.h"
+#include "psp_merge.cuh"
 
 namespace psp {
 namespace {
@@ -290,6 +291,11 @@ __global__ void __launch_bounds__(NW * 32) prefix_cascade_kernel(const StepParam
     }
     if (qc == 0) p.lse_pre[base + R] = (half ? m_hi : m_lo) + log2f(half ? l_hi : l_lo);
   }
+  // arrive for every member of this row block; the arrival that completes a member merges it
+  __threadfence();
+  __syncthreads();
+  const int row0 = rb * NW * 16;
+  prefix_arrive_and_merge<D>(p, members, h, row0, min(NW * 16, m_eff - row0), reinterpret_cast<int*>(smem));
 }
 
 template <int KV, int D, int NW, int NST>

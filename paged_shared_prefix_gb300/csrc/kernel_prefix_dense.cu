@@ -6,9 +6,10 @@
 //
 // One CTA = 128 stacked query rows (rows R = member * G + j of one KV head)
 // x one chunk of the shared prefix, in 128-token tiles:
-//   warp 4 (producer)  TMA-loads each K and V tile page by page from the paged
-//                      pool (3-D tensor map [slot][kv head][d], boxes of up to
-//                      64 tokens x 64 dims, 128-byte swizzle) into a 2-stage ring;
+//   warps 4 and 6     (producers, keys and values) TMA-load each K and V tile
+//                      page by page from the paged pool (3-D tensor map
+//                      [slot][kv head][d], boxes of up to 64 tokens x 128 bytes,
+//                      128-byte swizzle) into rings of 3 (bf16) or 5 (e4m3) stages;
 //   warp 5 (MMA)       one thread issues S_j = Q K_j^T (M=128, N=128, K=128,
 //                      bf16 operands from shared memory, fp32 accumulator in
 //                      tensor memory, two S buffers) and O += P_j V_j (P from
@@ -36,6 +37,7 @@
 
 #include "psp_device.cuh"
 #include "psp_internal.h"
+#include "psp_merge.cuh"
 #include "psp_sm100.cuh"
 
 namespace psp {
@@ -47,25 +49,35 @@ using namespace sm100;
 constexpr int kRows = 128;                 // UMMA M (stacked query rows)
 constexpr int kTok = 128;                  // tokens per tile (N of S, K of PV)
 constexpr int kD = 128;                    // head dim (K of S, N of PV)
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;              // warps 0-3 softmax, 4 K producer, 5 MMA, 6 V producer
 constexpr uint32_t kTmemCols = 512;        // S0 [0,128), S1 [128,256), O [256,384)
 constexpr float kRescaleLog2 = 8.f;
-enum Bar { kQReady, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
-           kSFull0, kSFull1, kPFull0, kPFull1, kPvDone, kOFull, kFinal, kNumBars };
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Tile geometry for bf16 (FP8 = false) and e4m3 (FP8 = true) operands.
 template <bool FP8>
 struct DenseCfg {
   static constexpr uint32_t kElem = FP8 ? 1 : 2;
+  static constexpr int kStages = FP8 ? 5 : 3;                // K and V ring depth
   static constexpr uint32_t kTileBytes = kTok * kD * kElem;  // one Q, K or V tile
   static constexpr uint32_t kHalves = FP8 ? 1 : 2;           // 128-byte column blocks of a row
   static constexpr uint32_t kHalf = kTileBytes / kHalves;    // 16 KB
   static constexpr int kBoxElems = 128 / kElem;              // d elements per TMA box row
   static constexpr int kKStep = 32 / kElem;                  // K elements per MMA instruction
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOffQ + kTileBytes;      // 2 stages
-  static constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;  // 2 stages
-  static constexpr uint32_t kOffBar = kOffV + 2 * kTileBytes;
+  static constexpr uint32_t kOffK = kOffQ + kTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+  // barriers: q_ready, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done, o_full, final
+  static constexpr int kBarQ = 0, kBarKFull = 1, kBarKEmpty = 1 + kStages, kBarVFull = 1 + 2 * kStages,
+                       kBarVEmpty = 1 + 3 * kStages, kBarSFull = 1 + 4 * kStages, kBarPFull = 3 + 4 * kStages,
+                       kBarPvDone = 5 + 4 * kStages, kBarOFull = 6 + 4 * kStages, kBarFinal = 7 + 4 * kStages,
+                       kNumBars = 8 + 4 * kStages;
   static constexpr uint32_t kOffTmem = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffTmem + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(kRows, kTok, false) : idesc_f16(kRows, kTok, 1, false);
@@ -77,15 +89,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefix_dense_kernel(const StepParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, int num_slots) {
   using C = DenseCfg<FP8>;
+  constexpr int NS = C::kStages;
   constexpr uint32_t kTileBytes = C::kTileBytes;
   constexpr uint32_t kHalf = C::kHalf;
-  constexpr uint32_t kOffQ = C::kOffQ, kOffK = C::kOffK, kOffV = C::kOffV, kOffBar = C::kOffBar;
-  constexpr uint32_t kOffTmem = C::kOffTmem;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
-  auto bar = [&](int i) { return base + kOffBar + 8u * i; };
+  auto bar = [&](int i) { return base + C::kOffBar + 8u * i; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -100,36 +111,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_eff = p.group_m_eff[g];
   const int32_t* members = p.group_members + p.group_member_indptr[g];
   int32_t* status = p.status;
+  __shared__ int epilogue_failed;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kQReady), 128);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kKFull0 + s), 1);
-      mbar_init(bar(kKEmpty0 + s), 1);
-      mbar_init(bar(kVFull0 + s), 1);
-      mbar_init(bar(kVEmpty0 + s), 1);
-      mbar_init(bar(kSFull0 + s), 1);
-      mbar_init(bar(kPFull0 + s), 128);
+    epilogue_failed = 0;
+    mbar_init(bar(C::kBarQ), 128);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar(C::kBarKFull + s), 1);
+      mbar_init(bar(C::kBarKEmpty + s), 1);
+      mbar_init(bar(C::kBarVFull + s), 1);
+      mbar_init(bar(C::kBarVEmpty + s), 1);
     }
-    mbar_init(bar(kPvDone), 1);
-    mbar_init(bar(kOFull), 1);
-    mbar_init(bar(kFinal), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::kBarSFull + s), 1);
+      mbar_init(bar(C::kBarPFull + s), 128);
+    }
+    mbar_init(bar(C::kBarPvDone), 1);
+    mbar_init(bar(C::kBarOFull), 1);
+    mbar_init(bar(C::kBarFinal), 1);
     fence_mbar_init();
   }
   if (warp == 5) {
-    tmem_alloc(base + kOffTmem, kTmemCols);
+    tmem_alloc(base + C::kOffTmem, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffTmem);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kOffTmem);
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == 4 || warp == 6) {
+    // ------------------------------------------------- producers: warp 4 keys, warp 6 values
     if (lane == 0) {
-      prefetch_tmap(&kmap);
-      prefetch_tmap(&vmap);
+      const bool is_v = warp == 6;
+      const CUtensorMap* map = is_v ? &vmap : &kmap;
+      prefetch_tmap(map);
+      const int full0 = is_v ? C::kBarVFull : C::kBarKFull;
+      const int empty0 = is_v ? C::kBarVEmpty : C::kBarKEmpty;
+      const uint32_t ring = base + (is_v ? C::kOffV : C::kOffK);
       const int32_t* list;
       int shift;
       if (p.token_flat) {
@@ -141,90 +160,78 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int mask = (1 << shift) - 1;
       const int br = min(1 << shift, 64);  // rows per TMA box; boxes never straddle a page
-      bool ok = true;
       int issued = 0;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s = j & 1;
-        for (int which = 0; which < 2 && ok; ++which) {  // K then V
-          const int full = (which ? kVFull0 : kKFull0) + s;
-          const int empty = (which ? kVEmpty0 : kKEmpty0) + s;
-          if (j >= 2 && !mbar_wait(bar(empty), ((j >> 1) - 1) & 1, status, 1)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_tx(bar(full), kTileBytes);
-          const uint32_t dst = base + (which ? kOffV : kOffK) + s * kTileBytes;
-          const CUtensorMap* map = which ? &vmap : &kmap;
-          for (int r = 0; r < kTok; r += br) {
-            const int tok = t0 + j * kTok + r;
-            const int slot = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % NS;
+        if (j >= NS && !mbar_wait(bar(empty0 + s), ((j / NS) - 1) & 1, status, is_v ? 2 : 1)) break;
+        mbar_arrive_tx(bar(full0 + s), kTileBytes);
+        const uint32_t dst = ring + s * kTileBytes;
+        for (int r = 0; r < kTok; r += br) {
+          const int tok = t0 + j * kTok + r;
+          const int slot = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
 #pragma unroll
-            for (uint32_t hf = 0; hf < C::kHalves; ++hf)
-              tma_load_3d(dst + hf * kHalf + r * 128, map, hf * C::kBoxElems, h, slot, bar(full));
-          }
+          for (uint32_t hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(dst + hf * kHalf + r * 128, map, hf * C::kBoxElems, h, slot, bar(full0 + s));
         }
         issued = j + 1;
       }
       // drain: the last load issued on each stage must have landed before the CTA may exit
-      for (int j = max(0, issued - 2); j < issued; ++j) {
-        mbar_wait(bar(kKFull0 + (j & 1)), (j >> 1) & 1, status, 2);
-        mbar_wait(bar(kVFull0 + (j & 1)), (j >> 1) & 1, status, 3);
-      }
+      for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(bar(full0 + j % NS), (j / NS) & 1, status, 3);
     }
   } else if (warp == 5) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      bool ok = mbar_wait(bar(kQReady), 0, status, 4);
+      bool ok = mbar_wait(bar(C::kBarQ), 0, status, 4);
       tc_fence_after();
       auto issue_pv = [&](int jj) -> bool {
-        const int s = jj & 1;
-        if (!mbar_wait(bar(kPFull0 + s), (jj >> 1) & 1, status, 5)) return false;
-        if (!mbar_wait(bar(kVFull0 + s), (jj >> 1) & 1, status, 6)) return false;
+        const int sb = jj & 1, sv = jj % NS;
+        if (!mbar_wait(bar(C::kBarPFull + sb), (jj >> 1) & 1, status, 5)) return false;
+        if (!mbar_wait(bar(C::kBarVFull + sv), (jj / NS) & 1, status, 6)) return false;
         tc_fence_after();
-        const uint32_t vbase = base + kOffV + s * kTileBytes;
+        const uint32_t vbase = base + C::kOffV + sv * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kTok / C::kKStep; ++ks) {
           // V is the MN-major B operand: K (tokens) advances by whole 128-byte rows
           const uint64_t bdesc = sw128_desc(vbase + ks * C::kKStep * 128, kHalf, 1024);
           const uint32_t acc = (jj > 0 || ks > 0) ? 1u : 0u;
           if constexpr (FP8) {
-            mma_ts_f8(tmem + 256, tmem + s * 128 + ks * 8, bdesc, C::kIdescPV, acc);
+            mma_ts_f8(tmem + 256, tmem + sb * 128 + ks * 8, bdesc, C::kIdescPV, acc);
           } else {
-            mma_ts(tmem + 256, tmem + s * 128 + ks * 8, bdesc, C::kIdescPV, acc);
+            mma_ts(tmem + 256, tmem + sb * 128 + ks * 8, bdesc, C::kIdescPV, acc);
           }
         }
-        mma_commit(bar(kPvDone));
-        mma_commit(bar(kVEmpty0 + s));
+        mma_commit(bar(C::kBarPvDone));
+        mma_commit(bar(C::kBarVEmpty + sv));
         return true;
       };
       for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(bar(kKFull0 + s), (j >> 1) & 1, status, 7)) {
+        const int sb = j & 1, sk = j % NS;
+        if (!mbar_wait(bar(C::kBarKFull + sk), (j / NS) & 1, status, 7)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t kbase = base + kOffK + s * kTileBytes;
+        const uint32_t kbase = base + C::kOffK + sk * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kD / C::kKStep; ++ks) {
           // K-major operands: 32 bytes of K per instruction inside a 128-byte swizzled row
           const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-          const uint64_t adesc = sw128_desc(base + kOffQ + off, 16, 1024);
+          const uint64_t adesc = sw128_desc(base + C::kOffQ + off, 16, 1024);
           const uint64_t bdesc = sw128_desc(kbase + off, 16, 1024);
           if constexpr (FP8) {
-            mma_ss_f8(tmem + s * 128, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
+            mma_ss_f8(tmem + sb * 128, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
           } else {
-            mma_ss(tmem + s * 128, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
+            mma_ss(tmem + sb * 128, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
           }
         }
-        mma_commit(bar(kSFull0 + s));
-        mma_commit(bar(kKEmpty0 + s));
+        mma_commit(bar(C::kBarSFull + sb));
+        mma_commit(bar(C::kBarKEmpty + sk));
         if (j >= 1) ok = issue_pv(j - 1);
       }
       if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
-      mma_commit(bar(kOFull));
-      mma_commit(bar(kFinal));
-      mbar_wait(bar(kFinal), 0, status, 8);  // every MMA of this CTA has completed
+      mma_commit(bar(C::kBarOFull));
+      mma_commit(bar(C::kBarFinal));
+      mbar_wait(bar(C::kBarFinal), 0, status, 8);  // every MMA of this CTA has completed
     }
     __syncwarp();
   } else {
@@ -263,22 +270,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             out[k] = e4m3x4_from_floats(bf16_bits_to_float(w0 & 0xffff) * inv, bf16_bits_to_float(w0 >> 16) * inv,
                                         bf16_bits_to_float(w1 & 0xffff) * inv, bf16_bits_to_float(w1 >> 16) * inv);
           }
-          const uint32_t off = kOffQ + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          const uint32_t off = C::kOffQ + r * 128 + (((c & 7) ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(gbase + off) = make_uint4(out[0], out[1], out[2], out[3]);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const uint4 v = live ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t off = kOffQ + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          const uint32_t off = C::kOffQ + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(gbase + off) = v;
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar(kQReady));
+      mbar_arrive(bar(C::kBarQ));
     }
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float scale = p.scale_log2;
+    float scale = p.scale_log2;  // > 0, so max(x) * scale = max(x * scale)
     float out_scale = 1.f;
     if constexpr (FP8) {
       scale *= __ldg(p.k_scale + h) * q_scale;
@@ -288,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
       const int s = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kSFull0 + s), (j >> 1) & 1, status, 9));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarSFull + s), (j >> 1) & 1, status, 9));
       if (!ok) break;
       tc_fence_after();
       float x[kTok];
@@ -302,28 +309,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[c][i]);
       }
-      const int valid = min(kTok, t1 - (t0 + j * kTok));
-      float mt = neg_inf();
+      const int valid = t1 - (t0 + j * kTok);
+      if (valid < kTok) {
 #pragma unroll
-      for (int i = 0; i < kTok; ++i) {
-        x[i] = i < valid ? x[i] * scale : neg_inf();
-        mt = fmaxf(mt, x[i]);
+        for (int i = 0; i < kTok; ++i) x[i] = i < valid ? x[i] : neg_inf();
       }
+      // tile max with eight independent accumulators (short dependency chains)
+      float mx[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mx[a] = x[a];
+#pragma unroll
+      for (int i = 8; i < kTok; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * scale;
       const bool need = mt > m_used + kRescaleLog2;
       float alpha = 1.f;
       if (need) {
-        alpha = exp2f(m_used - mt);
+        alpha = ex2(m_used - mt);
         m_used = mt;
         l *= alpha;
       }
-      float sum = 0.f;
+      const float neg_m = -m_used;
+      float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if constexpr (FP8) {
         uint32_t u[32];  // four e4m3 probabilities per column
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float a = exp2f(x[4 * i] - m_used), b = exp2f(x[4 * i + 1] - m_used);
-          const float c2 = exp2f(x[4 * i + 2] - m_used), d2 = exp2f(x[4 * i + 3] - m_used);
-          sum += (a + b) + (c2 + d2);
+          const float a = ex2(fmaf(x[4 * i], scale, neg_m)), b = ex2(fmaf(x[4 * i + 1], scale, neg_m));
+          const float c2 = ex2(fmaf(x[4 * i + 2], scale, neg_m)), d2 = ex2(fmaf(x[4 * i + 3], scale, neg_m));
+          sm[i & 7] += (a + b) + (c2 + d2);
           u[i] = e4m3x4_from_floats(a, b, c2, d2);
         }
         tmem_st32(lane_addr + s * 128, u);
@@ -333,18 +347,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t u[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float a = exp2f(x[c * 64 + 2 * i] - m_used);
-            const float b = exp2f(x[c * 64 + 2 * i + 1] - m_used);
-            sum += a + b;
+            const float a = ex2(fmaf(x[c * 64 + 2 * i], scale, neg_m));
+            const float b = ex2(fmaf(x[c * 64 + 2 * i + 1], scale, neg_m));
+            sm[i & 7] += a + b;
             u[i] = pack_bf16(a, b);
           }
           tmem_st32(lane_addr + s * 128 + c * 32, u);
         }
       }
-      l += sum;
+      l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // O holds the products of tiles < j; wait for the last of them, then rescale this row
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kPvDone), (j - 1) & 1, status, 10));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarPvDone), (j - 1) & 1, status, 10));
         if (ok) {
           tc_fence_after();
 #pragma unroll
@@ -360,10 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(kPFull0 + s));
+      mbar_arrive(bar(C::kBarPFull + s));
     }
     // epilogue: O / l -> fp32 partial row, log2-LSE
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kOFull), 0, status, 11));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarOFull), 0, status, 11));
     if (ok) {
       tc_fence_after();
       const int64_t row = p.chunk_row_offset[ci] + static_cast<int64_t>(h) * m_eff + R;
@@ -381,8 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          __uint_as_float(u[4 * i + 2]) * inv, __uint_as_float(u[4 * i + 3]) * inv);
         }
       }
-      if (live) p.lse_pre[row] = m_used + log2f(l);
+      if (live) p.lse_pre[row] = m_used + __log2f(l);
+      __threadfence();
     }
+    if (!ok) epilogue_failed = 1;
   }
 
   tc_fence_before();
@@ -390,6 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  // arrive for every member of this row block (shared memory is free now: every MMA and
+  // TMA copy of this CTA has completed); the arrival that completes a member merges it
+  if (!epilogue_failed) {
+    const int row0 = rb * kRows;
+    prefix_arrive_and_merge<kD>(p, members, h, row0, min(kRows, m_eff - row0), reinterpret_cast<int*>(gbase));
   }
 }
 

@@ -12,6 +12,7 @@
 
 #include "psp_device.cuh"
 #include "psp_internal.h"
+#include "psp_merge.cuh"
 
 namespace psp {
 namespace {
@@ -74,6 +75,8 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
   }
   const int64_t row_stride = static_cast<int64_t>(p.hkv) * D;
   constexpr int kPer = D / 32;
+  // a request with a single partial (no shared prefix, one split) writes its output directly
+  const bool direct = mode == 0 && expected_parts(p, b_suffix) == 1;
 
   for (int rbase = 0; rbase < n_rows; rbase += kWarps) {
     const int r = rbase + warp;
@@ -137,12 +140,30 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
         for (int k = 0; k < kPer; ++k) acc[k] = fmaf(pt, vs[tt][lane + 32 * k], acc[k]);
       }
     }
-    if (live) {
+    if (live && direct) {
+      const int64_t orow = static_cast<int64_t>(b_suffix) * p.hq + h * G + r;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) store_final(p, orow, lane + 32 * k, acc[k] / l);
+      if (lane == 0 && p.lse) p.lse[orow] = (m + log2f(l)) * 0.6931471805599453f;
+    } else if (live) {
       float* orow = (mode == 0 ? p.o_suf : p.o_pre) + (out_base + r) * D;
 #pragma unroll
       for (int k = 0; k < kPer; ++k) orow[lane + 32 * k] = acc[k] / l;
       if (lane == 0) (mode == 0 ? p.lse_suf : p.lse_pre)[out_base + r] = m + log2f(l);
     }
+  }
+  if (direct) return;
+  // arrive once per (request, KV head) this CTA contributed to; the completing arrival merges
+  __threadfence();
+  __syncthreads();
+  __shared__ int flags[128];
+  if (mode == 0) {
+    if (threadIdx.x == 0) flags[0] = arrive_is_last(p, b_suffix, h) ? 1 : 0;
+    __syncthreads();
+    if (flags[0])
+      for (int rr = warp; rr < G; rr += kWarps) merge_row<D>(p, b_suffix, h * G + rr, lane);
+  } else {
+    prefix_arrive_and_merge<D>(p, members, h, row0, n_rows, flags);
   }
 }
 

@@ -22,6 +22,7 @@
 
 #include "psp_device.cuh"
 #include "psp_internal.h"
+#include "psp_merge.cuh"
 
 namespace psp {
 namespace {
@@ -268,7 +269,11 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     }
   }
   __syncthreads();
+  // a request with a single partial (no shared prefix, one split) writes its output directly;
+  // otherwise write the partial and let the last arrival of (b, h) merge
+  const bool direct = expected_parts(p, b) == 1;
   const int64_t row0 = (static_cast<int64_t>(split) * p.hkv + h) * G;
+  const int64_t orow0 = static_cast<int64_t>(b) * p.hq + h * G;
   for (int e = threadIdx.x; e < G * D; e += NW * 32) {
     const int g = e / D;
     const int d = e - g * D;
@@ -282,9 +287,22 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
       sum += ls[w * 8 + g] * sc;
       acc += red[(w * 8 + g) * D + d] * sc;
     }
-    p.o_suf[(row0 + g) * D + d] = acc / sum * out_scale;
-    if (d == 0) p.lse_suf[row0 + g] = mmax + log2f(sum);
+    if (direct) {
+      store_final(p, orow0 + g, d, acc / sum * out_scale);
+      if (d == 0 && p.lse) p.lse[orow0 + g] = (mmax + log2f(sum)) * 0.6931471805599453f;
+    } else {
+      p.o_suf[(row0 + g) * D + d] = acc / sum * out_scale;
+      if (d == 0) p.lse_suf[row0 + g] = mmax + log2f(sum);
+    }
   }
+  if (direct) return;
+  __threadfence();
+  __syncthreads();
+  __shared__ int last;
+  if (threadIdx.x == 0) last = arrive_is_last(p, b, h) ? 1 : 0;
+  __syncthreads();
+  if (last)
+    for (int rr = warp; rr < G; rr += NW) merge_row<D>(p, b, h * G + rr, lane);
 }
 
 template <int KV, int D, int NW, int NST>

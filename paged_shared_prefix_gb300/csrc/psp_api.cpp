@@ -325,7 +325,10 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   place(L.item_rb_cascade, n32(P.item_rb_cascade));
   place(L.kv_indptr, n32(P.kv_indptr));
   L.plan_bytes = off;
-  place(L.status, 64);
+  L.status = off;
+  L.counters = off + 64;
+  L.zero_end = L.counters + static_cast<size_t>(B) * Hkv * sizeof(int32_t);
+  off = align_up(L.zero_end);
   const size_t D = c.head_dim;
   const size_t suf_rows = static_cast<size_t>(P.NS) * Hkv * G;
   place(L.o_suf, suf_rows * D * sizeof(float));
@@ -479,6 +482,7 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.o_pre = F(L.o_pre);
   p.lse_pre = F(L.lse_pre);
   p.status = I(L.status);
+  p.counters = I(L.counters);
   return p;
 }
 
@@ -649,8 +653,8 @@ psp_status psp_upload(psp_handle* h, void* workspace, size_t workspace_bytes, vo
   if (e != cudaSuccess) return cuda_fail(h, e, "plan upload");
   e = cudaEventRecord(h->staging_done, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventRecord");
-  e = cudaMemsetAsync(static_cast<unsigned char*>(workspace) + L.status, 0, 64, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "clearing the device status word");
+  e = cudaMemsetAsync(static_cast<unsigned char*>(workspace) + L.status, 0, L.zero_end - L.status, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "clearing the device status word and merge counters");
   h->workspace = static_cast<unsigned char*>(workspace);
   h->workspace_bytes = workspace_bytes;
   h->uploaded = true;
@@ -707,7 +711,6 @@ static psp_status timed_launch(psp_handle* h, cudaStream_t s, const char* name, 
 static cudaError_t expand_entry(const StepParams& p, int, cudaStream_t s) {
   return psp::launch_expand_kv_indices(p, p.kv_indices, s);
 }
-static cudaError_t merge_entry(const StepParams& p, int, cudaStream_t s) { return psp::launch_merge(p, s); }
 
 psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
   if (!h) return PSP_ERR_INVALID_ARGUMENT;
@@ -743,7 +746,7 @@ psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
     st = timed_launch(h, s, "suffix_splitkv", slot, psp::launch_suffix, p, P.NS);
     if (st) return st;
   }
-  return timed_launch(h, s, "merge", slot, merge_entry, p, 0);
+  return PSP_OK;
 }
 
 psp_status psp_step_host(psp_handle* h, const psp_batch* batch, const void* q_host, void* o_host, float* lse_host,
@@ -829,8 +832,8 @@ psp_status bind_image_and_run(psp_handle* h, unsigned char* ws, size_t cap, cons
     return fail(h, PSP_ERR_INVALID_ARGUMENT, "q, k_pool, v_pool and o must be set");
   cudaError_t e = cudaMemcpyAsync(ws, h->plan.image.data(), L.plan_bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "plan copy into the static scratch");
-  e = cudaMemsetAsync(ws + L.status, 0, 64, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "clearing the device status word");
+  e = cudaMemsetAsync(ws + L.status, 0, L.zero_end - L.status, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "clearing the device status word and merge counters");
   h->workspace = ws;
   h->workspace_bytes = cap;
   h->uploaded = true;

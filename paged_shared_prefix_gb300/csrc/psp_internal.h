@@ -81,6 +81,7 @@ struct StepParams {
   float* o_pre;                        // [chunk_row_offset[c] + h * M_eff + r][D]
   float* lse_pre;
   int32_t* status;                     // device status word
+  int32_t* counters;                   // [B * Hkv] arrivals of partial results (zero between steps)
 };
 
 // Byte offsets of every array inside the workspace (256-byte aligned each).
@@ -95,6 +96,8 @@ struct PlanLayout {
   size_t kv_indptr;
   size_t plan_bytes;       // end of the uploaded integer region
   size_t status;
+  size_t counters;         // right after status; both cleared at every upload
+  size_t zero_end;
   size_t o_suf, lse_suf, o_pre, lse_pre;
   size_t kv_indices;
   size_t total;
@@ -104,7 +107,6 @@ struct PlanLayout {
 cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s);
 cudaError_t launch_prefix_cascade(const StepParams& p, int num_items, cudaStream_t s);
 cudaError_t launch_prefix_dense(const StepParams& p, int num_items, cudaStream_t s);
-cudaError_t launch_merge(const StepParams& p, cudaStream_t s);
 cudaError_t launch_expand_kv_indices(const StepParams& p, int32_t* out, cudaStream_t s);
 cudaError_t launch_suffix_simt(const StepParams& p, int num_splits, cudaStream_t s);
 cudaError_t launch_prefix_simt(const StepParams& p, int num_items, bool dense, cudaStream_t s);

@@ -1,0 +1,145 @@
+// psp_merge.cuh -- log-sum-exp merge of the partial results of one
+// (request, query head) row, performed by whichever CTA delivers the last
+// partial of its (request, KV head).
+//
+// Every (b, h) expects one partial per prefix chunk of b's group plus one per
+// suffix split of b.  A CTA that has written its partials fences them and adds
+// one arrival on the (b, h) counter; the CTA that brings the count to the
+// expected total merges the G rows of (b, h) and resets the counter to zero
+// for the next step.  No CTA ever waits for another.
+//
+// Merge of a row: with every O_i normalised and lse_i its log2 normaliser,
+//   M = max_i lse_i,  w_i = 2^(lse_i - M),  O = sum_i w_i O_i / sum_i w_i,
+//   LSE = (M + log2 sum_i w_i) * ln 2,
+// in a fixed order (prefix chunks, then splits), so the result does not depend
+// on which CTA merges ("GraniKV", section 3: the prefix result is merged with
+// each request's suffix attention).
+#pragma once
+
+#include "psp_device.cuh"
+#include "psp_internal.h"
+
+namespace psp {
+namespace dev {
+
+// Number of partial results (b, h) receives this step.
+__device__ __forceinline__ int expected_parts(const StepParams& p, int b) {
+  const int g = p.req_group[b];
+  const int chunks = g >= 0 ? p.group_chunk_indptr[g + 1] - p.group_chunk_indptr[g] : 0;
+  return chunks + p.split_indptr[b + 1] - p.split_indptr[b];
+}
+
+// One arrival on (b, h) after this CTA's partials for it are written and fenced.
+// Returns true for the arrival that completes (b, h).
+__device__ __forceinline__ bool arrive_is_last(const StepParams& p, int b, int h) {
+  int32_t* cnt = p.counters + static_cast<int64_t>(b) * p.hkv + h;
+  const int expected = expected_parts(p, b);
+  const int old = atomicAdd(cnt, 1);
+  if (old + 1 == expected) {
+    __threadfence();   // see every other CTA's partials before reading them
+    *cnt = 0;          // ready for the next step (later kernels are stream-ordered)
+    return true;
+  }
+  return false;
+}
+
+// Warp-cooperative merge of row (b, hq): lane l owns D/32 consecutive elements.
+template <int D>
+__device__ __forceinline__ void merge_row(const StepParams& p, int b, int hq, int lane) {
+  constexpr int kPer = D / 32;
+  const int G = p.group;
+  const int h = hq / G;
+  const int j = hq - h * G;
+  const int g = p.req_group[b];
+  int c0 = 0, c1 = 0, m_eff = 0, prow = 0;
+  if (g >= 0) {
+    c0 = p.group_chunk_indptr[g];
+    c1 = p.group_chunk_indptr[g + 1];
+    m_eff = p.group_m_eff[g];
+    prow = p.req_member[b] * G + j;
+  }
+  const int s0 = p.split_indptr[b], s1 = p.split_indptr[b + 1];
+  float mmax = neg_inf();
+  for (int c = c0; c < c1; ++c)
+    mmax = fmaxf(mmax, __ldcg(p.lse_pre + p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow));
+  for (int s = s0; s < s1; ++s) mmax = fmaxf(mmax, __ldcg(p.lse_suf + (static_cast<int64_t>(s) * p.hkv + h) * G + j));
+  float acc[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  float sum = 0.f;
+  auto add = [&](int64_t r, const float* obuf, const float* lbuf) {
+    const float w = exp2f(__ldcg(lbuf + r) - mmax);
+    sum += w;
+    const float* src = obuf + r * D + lane * kPer;
+    if constexpr (kPer == 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+      acc[0] = fmaf(w, v.x, acc[0]);
+      acc[1] = fmaf(w, v.y, acc[1]);
+      acc[2] = fmaf(w, v.z, acc[2]);
+      acc[3] = fmaf(w, v.w, acc[3]);
+    } else {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+      acc[0] = fmaf(w, v.x, acc[0]);
+      acc[1] = fmaf(w, v.y, acc[1]);
+    }
+  };
+  for (int c = c0; c < c1; ++c) add(p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow, p.o_pre, p.lse_pre);
+  for (int s = s0; s < s1; ++s) add((static_cast<int64_t>(s) * p.hkv + h) * G + j, p.o_suf, p.lse_suf);
+  const float inv = 1.f / sum;
+  const int64_t row = static_cast<int64_t>(b) * p.hq + hq;
+  const int64_t obase = row * D + lane * kPer;
+  if (p.o_dtype == PSP_KV_BF16) {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o) + obase;
+    if constexpr (kPer == 4) {
+      uint2 v;
+      v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+      v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(o) = v;
+    } else {
+      *reinterpret_cast<uint32_t*>(o) = pack_bf16(acc[0] * inv, acc[1] * inv);
+    }
+  } else {
+    float* o = static_cast<float*>(p.o) + obase;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) o[k] = acc[k] * inv;
+  }
+  if (p.lse && lane == 0) p.lse[row] = (mmax + log2f(sum)) * 0.6931471805599453f;
+}
+
+// Writes one row's final result directly (the row has exactly one partial).
+__device__ __forceinline__ void store_final(const StepParams& p, int64_t row, int d, float value) {
+  if (p.o_dtype == PSP_KV_BF16) {
+    static_cast<__nv_bfloat16*>(p.o)[row * p.head_dim + d] = __float2bfloat16_rn(value);
+  } else {
+    static_cast<float*>(p.o)[row * p.head_dim + d] = value;
+  }
+}
+
+// Prefix kernels: after this CTA's partial rows [row0, row0 + n) of head h are
+// written by the calling warp group, arrive once per member whose G rows all lie
+// in the range and merge the members that this arrival completes.  Called by
+// every thread of the CTA after a __syncthreads() that follows the writes.
+// `flags` is shared scratch of at least n / G ints.
+template <int D>
+__device__ __forceinline__ void prefix_arrive_and_merge(const StepParams& p, const int32_t* members, int h, int row0,
+                                                        int n, int* flags) {
+  const int G = p.group;
+  const int n_members = n / G;  // row blocks hold whole members (G divides the block)
+  for (int m = threadIdx.x; m < n_members; m += blockDim.x) {
+    const int b = members[(row0 / G) + m];
+    flags[m] = arrive_is_last(p, b, h) ? 1 : 0;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int rr = warp; rr < n; rr += nwarps) {
+    const int m = rr / G;
+    if (flags[m]) {
+      const int R = row0 + rr;
+      const int b = members[R / G];
+      merge_row<D>(p, b, h * G + (R - (R / G) * G), lane);
+    }
+  }
+}
+
+}  // namespace dev
+}  // namespace psp

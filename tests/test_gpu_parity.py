@@ -167,7 +167,7 @@ def test_kernel_timing_reports_launches():
     step.run(tens["q"], tens["k_pool"], tens["v_pool"], o)
     torch.cuda.synchronize()
     names = [n for n, _ in step.kernel_times()]
-    assert names == ["prefix_dense", "suffix_splitkv", "merge"]
+    assert names == ["prefix_dense", "suffix_splitkv"]
     assert all(t > 0 for _, t in step.kernel_times())
     step.close()
 
