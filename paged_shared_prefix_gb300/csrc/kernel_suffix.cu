@@ -29,6 +29,8 @@ namespace {
 
 using namespace dev;
 
+constexpr int kPreChunks = 2;  // prefix partials prefetched per single-split request (per query head row)
+
 template <int KV, int D>
 struct SufCfg {
   static constexpr int kElem = (KV == PSP_KV_BF16) ? 2 : 1;
@@ -68,6 +70,34 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
 
   const int n_sub = (t1 - t0 + 15) >> 4;
   const int my_n = n_sub > warp ? (n_sub - warp + NW - 1) / NW : 0;
+
+  // A request with one suffix split merges its shared-prefix partials here: the prefix
+  // kernel ran earlier on the stream, so its rows are complete.  They are prefetched into
+  // a shared-memory area of their own, in the first cp.async group of every thread.
+  const int g_req = p.req_group[b];
+  const bool solo = p.split_indptr[b + 1] - p.split_indptr[b] == 1;
+  const int c0 = g_req >= 0 ? p.group_chunk_indptr[g_req] : 0;
+  const int n_chunks = g_req >= 0 ? p.group_chunk_indptr[g_req + 1] - c0 : 0;
+  const bool pre_smem = solo && n_chunks > 0 && n_chunks <= kPreChunks;
+  float* pre_o = reinterpret_cast<float*>(smem + NW * NST * C::kStageBytes);   // [chunk][G][D]
+  float* pre_l = pre_o + kPreChunks * 8 * D;                                     // [chunk][G]
+  if (pre_smem) {
+    const int m_eff = p.group_m_eff[g_req];
+    const int prow = p.req_member[b] * G;
+    constexpr int kRowChunks = D * 4 / 16;
+    for (int e = threadIdx.x; e < n_chunks * G * (kRowChunks + 1); e += NW * 32) {
+      const int c = e / (G * (kRowChunks + 1));
+      const int rem = e - c * G * (kRowChunks + 1);
+      const int j = rem / (kRowChunks + 1);
+      const int q = rem - j * (kRowChunks + 1);
+      const int64_t row = p.chunk_row_offset[c0 + c] + static_cast<int64_t>(h) * m_eff + prow + j;
+      if (q < kRowChunks) {
+        cp_async_16(smem_u32(pre_o + (c * 8 + j) * D + q * 4), p.o_pre + row * D + q * 4, true);
+      } else {
+        cp_async_4(smem_u32(pre_l + c * 8 + j), p.lse_pre + row);
+      }
+    }
+  }
 
   // -------- query fragments: B operand of S^T = K Q^T (k = head dim, n = query head)
   const int qg = lane >> 2;  // query head within the group (B fragment column)
@@ -269,9 +299,11 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     }
   }
   __syncthreads();
-  // a request with a single partial (no shared prefix, one split) writes its output directly;
-  // otherwise write the partial and let the last arrival of (b, h) merge
-  const bool direct = expected_parts(p, b) == 1;
+  // A single-split request writes its final output here: its own result merged with the
+  // prefetched prefix partials (none without a shared prefix).  Otherwise write the partial
+  // and let the last arrival of (b, h) merge.
+  const bool direct = solo && (n_chunks == 0 || pre_smem);
+  const bool solo_global = solo && !direct;   // too many prefix chunks to prefetch: read them here
   const int64_t row0 = (static_cast<int64_t>(split) * p.hkv + h) * G;
   const int64_t orow0 = static_cast<int64_t>(b) * p.hq + h * G;
   for (int e = threadIdx.x; e < G * D; e += NW * 32) {
@@ -288,8 +320,21 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
       acc += red[(w * 8 + g) * D + d] * sc;
     }
     if (direct) {
-      store_final(p, orow0 + g, d, acc / sum * out_scale);
-      if (d == 0 && p.lse) p.lse[orow0 + g] = (mmax + log2f(sum)) * 0.6931471805599453f;
+      // own part: O_s = acc / sum * out_scale with log2-LSE mmax + log2(sum); prefix chunks first
+      float lse_own = mmax + log2f(sum);
+      float big = lse_own;
+      for (int c = 0; c < n_chunks; ++c) big = fmaxf(big, pre_l[c * 8 + g]);
+      float wsum = 0.f, out = 0.f;
+      for (int c = 0; c < n_chunks; ++c) {
+        const float w = exp2f(pre_l[c * 8 + g] - big);
+        wsum += w;
+        out = fmaf(w, pre_o[(c * 8 + g) * D + d], out);
+      }
+      const float w_own = exp2f(lse_own - big);
+      wsum += w_own;
+      out = fmaf(w_own, acc / sum * out_scale, out);
+      store_final(p, orow0 + g, d, out / wsum);
+      if (d == 0 && p.lse) p.lse[orow0 + g] = (big + log2f(wsum)) * 0.6931471805599453f;
     } else {
       p.o_suf[(row0 + g) * D + d] = acc / sum * out_scale;
       if (d == 0) p.lse_suf[row0 + g] = mmax + log2f(sum);
@@ -298,6 +343,10 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   if (direct) return;
   __threadfence();
   __syncthreads();
+  if (solo_global) {  // every other part of (b, h) is already complete
+    for (int rr = warp; rr < G; rr += NW) merge_row<D>(p, b, h * G + rr, lane);
+    return;
+  }
   __shared__ int last;
   if (threadIdx.x == 0) last = arrive_is_last(p, b, h) ? 1 : 0;
   __syncthreads();
@@ -310,7 +359,7 @@ cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
   using C = SufCfg<KV, D>;
   const int ring = NW * NST * C::kStageBytes;
   const int epi = (NW * 8 * D + 2 * NW * 8) * 4;
-  const int bytes = ring > epi ? ring : epi;
+  const int bytes = (ring > epi ? ring : epi) + kPreChunks * 8 * (D + 1) * 4;
   auto kern = suffix_kernel<KV, D, NW, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;

@@ -6,7 +6,9 @@
 // suffix split of b.  A CTA that has written its partials fences them and adds
 // one arrival on the (b, h) counter; the CTA that brings the count to the
 // expected total merges the G rows of (b, h) and resets the counter to zero
-// for the next step.  No CTA ever waits for another.
+// for the next step.  No CTA ever waits for another.  A request with exactly
+// one suffix split skips the counter: its suffix CTA runs after the prefix
+// kernel has finished (stream order) and merges the prefix partials directly.
 //
 // Merge of a row: with every O_i normalised and lse_i its log2 normaliser,
 //   M = max_i lse_i,  w_i = 2^(lse_i - M),  O = sum_i w_i O_i / sum_i w_i,
@@ -117,9 +119,11 @@ __device__ __forceinline__ void store_final(const StepParams& p, int64_t row, in
 
 // Prefix kernels: after this CTA's partial rows [row0, row0 + n) of head h are
 // written by the calling warp group, arrive once per member whose G rows all lie
-// in the range and merge the members that this arrival completes.  Called by
-// every thread of the CTA after a __syncthreads() that follows the writes.
-// `flags` is shared scratch of at least n / G ints.
+// in the range and merge the members that this arrival completes.  Members with
+// exactly one suffix split are skipped: their suffix CTA (a later launch) merges
+// the prefix partials itself.  Called by every thread of the CTA after a
+// __syncthreads() that follows the writes.  `flags` is shared scratch of at
+// least n / G ints.
 template <int D>
 __device__ __forceinline__ void prefix_arrive_and_merge(const StepParams& p, const int32_t* members, int h, int row0,
                                                         int n, int* flags) {
@@ -127,7 +131,8 @@ __device__ __forceinline__ void prefix_arrive_and_merge(const StepParams& p, con
   const int n_members = n / G;  // row blocks hold whole members (G divides the block)
   for (int m = threadIdx.x; m < n_members; m += blockDim.x) {
     const int b = members[(row0 / G) + m];
-    flags[m] = arrive_is_last(p, b, h) ? 1 : 0;
+    const bool solo = p.split_indptr[b + 1] - p.split_indptr[b] == 1;
+    flags[m] = (!solo && arrive_is_last(p, b, h)) ? 1 : 0;
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
