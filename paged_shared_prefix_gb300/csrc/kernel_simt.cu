@@ -75,8 +75,10 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
   }
   const int64_t row_stride = static_cast<int64_t>(p.hkv) * D;
   constexpr int kPer = D / 32;
-  // a request with a single partial (no shared prefix, one split) writes its output directly
-  const bool direct = mode == 0 && expected_parts(p, b_suffix) == 1;
+  // a request with a single partial (no shared prefix, one split) writes its output directly;
+  // a single-split request of a prefix group merges after its write (the prefix kernel ran earlier)
+  const bool solo = mode == 0 && p.split_indptr[b_suffix + 1] - p.split_indptr[b_suffix] == 1;
+  const bool direct = solo && p.req_group[b_suffix] < 0;
 
   for (int rbase = 0; rbase < n_rows; rbase += kWarps) {
     const int r = rbase + warp;
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
   __syncthreads();
   __shared__ int flags[128];
   if (mode == 0) {
-    if (threadIdx.x == 0) flags[0] = arrive_is_last(p, b_suffix, h) ? 1 : 0;
+    if (threadIdx.x == 0) flags[0] = (solo || arrive_is_last(p, b_suffix, h)) ? 1 : 0;
     __syncthreads();
     if (flags[0])
       for (int rr = warp; rr < G; rr += kWarps) merge_row<D>(p, b_suffix, h * G + rr, lane);
