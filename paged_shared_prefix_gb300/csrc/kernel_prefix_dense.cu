@@ -5,12 +5,14 @@
 // step instead of once per request).
 //
 // One CTA = 128 stacked query rows (rows R = member * G + j of one KV head)
-// x one chunk of the shared prefix, in 128-token tiles:
+// x one chunk of the shared prefix, in 64-token tiles; two CTAs share an SM
+// (256 tensor-memory columns and <= 96 KB of shared memory each), so one CTA's
+// softmax overlaps the other's tensor-core work:
 //   warps 4 and 6     (producers, keys and values) TMA-load each K and V tile
 //                      page by page from the paged pool (3-D tensor map
 //                      [slot][kv head][d], boxes of up to 64 tokens x 128 bytes,
-//                      128-byte swizzle) into rings of 3 (bf16) or 5 (e4m3) stages;
-//   warp 5 (MMA)       one thread issues S_j = Q K_j^T (M=128, N=128, K=128,
+//                      128-byte swizzle) into rings of 2 (bf16) or 4 (e4m3) stages;
+//   warp 5 (MMA)       one thread issues S_j = Q K_j^T (M=128, N=64, K=128,
 //                      bf16 operands from shared memory, fp32 accumulator in
 //                      tensor memory, two S buffers) and O += P_j V_j (P from
 //                      tensor memory, V as an MN-major shared operand);
@@ -47,10 +49,11 @@ using namespace dev;
 using namespace sm100;
 
 constexpr int kRows = 128;                 // UMMA M (stacked query rows)
-constexpr int kTok = 128;                  // tokens per tile (N of S, K of PV)
+constexpr int kTok = 64;                   // tokens per tile (N of S, K of PV)
 constexpr int kD = 128;                    // head dim (K of S, N of PV)
 constexpr int kThreads = 224;              // warps 0-3 softmax, 4 K producer, 5 MMA, 6 V producer
-constexpr uint32_t kTmemCols = 512;        // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t kTmemCols = 256;        // S0 [0,64), S1 [64,128), O [128,256): two CTAs fit one SM
+constexpr uint32_t kOCol = 2 * kTok;
 constexpr float kRescaleLog2 = 8.f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -63,7 +66,7 @@ __device__ __forceinline__ float ex2(float x) {
 template <bool FP8>
 struct DenseCfg {
   static constexpr uint32_t kElem = FP8 ? 1 : 2;
-  static constexpr int kStages = FP8 ? 5 : 3;                // K and V ring depth
+  static constexpr int kStages = FP8 ? 4 : 2;                // K and V ring depth (two CTAs per SM)
   static constexpr uint32_t kTileBytes = kTok * kD * kElem;  // one Q, K or V tile
   static constexpr uint32_t kHalves = FP8 ? 1 : 2;           // 128-byte column blocks of a row
   static constexpr uint32_t kHalf = kTileBytes / kHalves;    // 16 KB
@@ -85,7 +88,7 @@ struct DenseCfg {
 };
 
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     prefix_dense_kernel(const StepParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, int num_slots) {
   using C = DenseCfg<FP8>;
@@ -195,9 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = sw128_desc(vbase + ks * C::kKStep * 128, kHalf, 1024);
           const uint32_t acc = (jj > 0 || ks > 0) ? 1u : 0u;
           if constexpr (FP8) {
-            mma_ts_f8(tmem + 256, tmem + sb * 128 + ks * 8, bdesc, C::kIdescPV, acc);
+            mma_ts_f8(tmem + kOCol, tmem + sb * kTok + ks * 8, bdesc, C::kIdescPV, acc);
           } else {
-            mma_ts(tmem + 256, tmem + sb * 128 + ks * 8, bdesc, C::kIdescPV, acc);
+            mma_ts(tmem + kOCol, tmem + sb * kTok + ks * 8, bdesc, C::kIdescPV, acc);
           }
         }
         mma_commit(bar(C::kBarPvDone));
@@ -219,9 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t adesc = sw128_desc(base + C::kOffQ + off, 16, 1024);
           const uint64_t bdesc = sw128_desc(kbase + off, 16, 1024);
           if constexpr (FP8) {
-            mma_ss_f8(tmem + sb * 128, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
+            mma_ss_f8(tmem + sb * kTok, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
           } else {
-            mma_ss(tmem + sb * 128, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
+            mma_ss(tmem + sb * kTok, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
           }
         }
         mma_commit(bar(C::kBarSFull + sb));
@@ -248,28 +251,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               (static_cast<int64_t>(members[mem]) * p.hq + h * G + jq) * kD);
       }
       if constexpr (FP8) {
-        uint4 raw[16];
+        // pass 1: the row's amax; pass 2: reload (cached) and quantise to e4m3
         float amax = 0.f;
+        if (live) {
+#pragma unroll 4
+          for (int c = 0; c < 16; ++c) {
+            const uint4 v = __ldg(qrow + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          raw[c] = live ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[k] & 0xffff)), fabsf(bf16_bits_to_float(w[k] >> 16))));
+            for (int k = 0; k < 4; ++k)
+              amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[k] & 0xffff)), fabsf(bf16_bits_to_float(w[k] >> 16))));
+          }
         }
         q_scale = amax > 0.f ? amax / 448.f : 1.f;
         const float inv = 1.f / q_scale;
-#pragma unroll
+#pragma unroll 2
         for (int c = 0; c < 8; ++c) {  // 16 e4m3 codes per 16-byte chunk
+          const uint4 lo = live ? __ldg(qrow + 2 * c) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 hi = live ? __ldg(qrow + 2 * c + 1) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
           uint32_t out[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t w0 = (k < 2) ? (&raw[2 * c].x)[2 * k] : (&raw[2 * c + 1].x)[2 * (k - 2)];
-            const uint32_t w1 = (k < 2) ? (&raw[2 * c].x)[2 * k + 1] : (&raw[2 * c + 1].x)[2 * (k - 2) + 1];
-            out[k] = e4m3x4_from_floats(bf16_bits_to_float(w0 & 0xffff) * inv, bf16_bits_to_float(w0 >> 16) * inv,
-                                        bf16_bits_to_float(w1 & 0xffff) * inv, bf16_bits_to_float(w1 >> 16) * inv);
-          }
+          for (int k = 0; k < 4; ++k)
+            out[k] = e4m3x4_from_floats(
+                bf16_bits_to_float(w[2 * k] & 0xffff) * inv, bf16_bits_to_float(w[2 * k] >> 16) * inv,
+                bf16_bits_to_float(w[2 * k + 1] & 0xffff) * inv, bf16_bits_to_float(w[2 * k + 1] >> 16) * inv);
           const uint32_t off = C::kOffQ + r * 128 + (((c & 7) ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(gbase + off) = make_uint4(out[0], out[1], out[2], out[3]);
         }
@@ -300,12 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float x[kTok];
       {
-        uint32_t u[4][32];
+        uint32_t u[kTok / 32][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + s * 128 + c * 32, u[c]);
+        for (int c = 0; c < kTok / 32; ++c) tmem_ld32(lane_addr + s * kTok + c * 32, u[c]);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < kTok / 32; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[c][i]);
       }
@@ -332,28 +338,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float neg_m = -m_used;
       float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if constexpr (FP8) {
-        uint32_t u[32];  // four e4m3 probabilities per column
+        uint32_t u[kTok / 4];  // four e4m3 probabilities per column
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < kTok / 4; ++i) {
           const float a = ex2(fmaf(x[4 * i], scale, neg_m)), b = ex2(fmaf(x[4 * i + 1], scale, neg_m));
           const float c2 = ex2(fmaf(x[4 * i + 2], scale, neg_m)), d2 = ex2(fmaf(x[4 * i + 3], scale, neg_m));
           sm[i & 7] += (a + b) + (c2 + d2);
           u[i] = e4m3x4_from_floats(a, b, c2, d2);
         }
-        tmem_st32(lane_addr + s * 128, u);
+        tmem_st16(lane_addr + s * kTok, u);
       } else {
+        uint32_t u[kTok / 2];  // two bf16 probabilities per column
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t u[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float a = ex2(fmaf(x[c * 64 + 2 * i], scale, neg_m));
-            const float b = ex2(fmaf(x[c * 64 + 2 * i + 1], scale, neg_m));
-            sm[i & 7] += a + b;
-            u[i] = pack_bf16(a, b);
-          }
-          tmem_st32(lane_addr + s * 128 + c * 32, u);
+        for (int i = 0; i < kTok / 2; ++i) {
+          const float a = ex2(fmaf(x[2 * i], scale, neg_m));
+          const float b = ex2(fmaf(x[2 * i + 1], scale, neg_m));
+          sm[i & 7] += a + b;
+          u[i] = pack_bf16(a, b);
         }
+        tmem_st32(lane_addr + s * kTok, u);
       }
       l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -364,11 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kD / 32; ++c) {
             uint32_t u[32];
-            tmem_ld32(lane_addr + 256 + c * 32, u);
+            tmem_ld32(lane_addr + kOCol + c * 32, u);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-            tmem_st32(lane_addr + 256 + c * 32, u);
+            tmem_st32(lane_addr + kOCol + c * 32, u);
           }
         }
       }
@@ -386,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t u[32];
-        tmem_ld32(lane_addr + 256 + c * 32, u);
+        tmem_ld32(lane_addr + kOCol + c * 32, u);
         tmem_wait_ld();
         if (live) {
 #pragma unroll

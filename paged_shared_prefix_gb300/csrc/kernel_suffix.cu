@@ -20,6 +20,8 @@
 // written as one normalised fp32 partial (O, log2-LSE) per (split, head, q).
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include "psp_device.cuh"
 #include "psp_internal.h"
 #include "psp_merge.cuh"
@@ -370,15 +372,33 @@ cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
 
 }  // namespace
 
+// Ring depth per warp for d = 128 (PSP_SUFFIX_STAGES overrides it for tuning sweeps):
+// fewer stages leave room for more resident CTAs per SM.
+int suffix_stages(int fallback) {
+  static const int env = [] {
+    const char* v = std::getenv("PSP_SUFFIX_STAGES");
+    return v ? std::atoi(v) : 0;
+  }();
+  return env > 0 ? env : fallback;
+}
+
 cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
   if (num_splits <= 0) return cudaSuccess;
   if (p.kv_dtype == PSP_KV_BF16) {
-    return p.head_dim == 128 ? launch_t<PSP_KV_BF16, 128, 4, 3>(p, num_splits, s)
-                             : launch_t<PSP_KV_BF16, 64, 4, 4>(p, num_splits, s);
+    if (p.head_dim != 128) return launch_t<PSP_KV_BF16, 64, 4, 4>(p, num_splits, s);
+    switch (suffix_stages(3)) {
+      case 2: return launch_t<PSP_KV_BF16, 128, 4, 2>(p, num_splits, s);
+      case 4: return launch_t<PSP_KV_BF16, 128, 4, 4>(p, num_splits, s);
+      default: return launch_t<PSP_KV_BF16, 128, 4, 3>(p, num_splits, s);
+    }
   }
   if (p.kv_dtype == PSP_KV_FP8) {
-    return p.head_dim == 128 ? launch_t<PSP_KV_FP8, 128, 4, 5>(p, num_splits, s)
-                             : launch_t<PSP_KV_FP8, 64, 4, 6>(p, num_splits, s);
+    if (p.head_dim != 128) return launch_t<PSP_KV_FP8, 64, 4, 6>(p, num_splits, s);
+    switch (suffix_stages(5)) {
+      case 2: return launch_t<PSP_KV_FP8, 128, 4, 2>(p, num_splits, s);
+      case 3: return launch_t<PSP_KV_FP8, 128, 4, 3>(p, num_splits, s);
+      default: return launch_t<PSP_KV_FP8, 128, 4, 5>(p, num_splits, s);
+    }
   }
   return launch_suffix_simt(p, num_splits, s);
 }
