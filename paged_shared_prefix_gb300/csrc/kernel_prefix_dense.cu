@@ -67,13 +67,15 @@ template <bool FP8>
 struct DenseCfg {
   static constexpr uint32_t kElem = FP8 ? 1 : 2;
   static constexpr int kStages = FP8 ? 4 : 2;                // K and V ring depth (two CTAs per SM)
-  static constexpr uint32_t kTileBytes = kTok * kD * kElem;  // one Q, K or V tile
+  static constexpr uint32_t kTileBytes = kTok * kD * kElem;  // one K or V tile
+  static constexpr uint32_t kQBytes = kRows * kD * kElem;    // the Q tile
   static constexpr uint32_t kHalves = FP8 ? 1 : 2;           // 128-byte column blocks of a row
-  static constexpr uint32_t kHalf = kTileBytes / kHalves;    // 16 KB
+  static constexpr uint32_t kHalf = kTileBytes / kHalves;    // column block of a K/V tile
+  static constexpr uint32_t kQHalf = kQBytes / kHalves;      // column block of the Q tile
   static constexpr int kBoxElems = 128 / kElem;              // d elements per TMA box row
   static constexpr int kKStep = 32 / kElem;                  // K elements per MMA instruction
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOffQ + kTileBytes;
+  static constexpr uint32_t kOffK = kOffQ + kQBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
   // barriers: q_ready, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done, o_full, final
@@ -218,9 +220,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int ks = 0; ks < kD / C::kKStep; ++ks) {
           // K-major operands: 32 bytes of K per instruction inside a 128-byte swizzled row
-          const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-          const uint64_t adesc = sw128_desc(base + C::kOffQ + off, 16, 1024);
-          const uint64_t bdesc = sw128_desc(kbase + off, 16, 1024);
+          const uint32_t off = (ks & 3) * 32;
+          const uint64_t adesc = sw128_desc(base + C::kOffQ + (ks >> 2) * C::kQHalf + off, 16, 1024);
+          const uint64_t bdesc = sw128_desc(kbase + (ks >> 2) * kHalf + off, 16, 1024);
           if constexpr (FP8) {
             mma_ss_f8(tmem + sb * kTok, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
           } else {
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const uint4 v = live ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t off = C::kOffQ + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          const uint32_t off = C::kOffQ + (c >> 3) * C::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(gbase + off) = v;
         }
       }
