@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--threshold", type=int, default=0, help="dense/cascade M_eff threshold (0 = built-in)")
     ap.add_argument("--token-flat", action="store_true", help="lower to per-token kv_indices inside the step")
+    ap.add_argument("--concurrent", type=int, default=None,
+                    help="1: prefix kernels on a side stream concurrent with the suffix kernel, 0: one stream "
+                         "(default: the library default for the workload)")
     ap.add_argument("--no-comparator", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -323,7 +326,9 @@ def main():
     o = torch.empty((case.batch, w.num_q_heads, w.head_dim), dtype=odt, device=dev)
     lse = torch.empty((case.batch, w.num_q_heads), dtype=torch.float32, device=dev)
 
-    step = psp.DecodeStep.for_case(case, dense_threshold=args.threshold, token_flat=args.token_flat)
+    concurrent = bool(args.concurrent) if args.concurrent is not None else False
+    step = psp.DecodeStep.for_case(case, dense_threshold=args.threshold, token_flat=args.token_flat,
+                                   concurrent=concurrent)
     t_plan = []
     for _ in range(5):
         t0 = time.perf_counter()
@@ -408,7 +413,8 @@ def main():
         "dtype": {"f32": "f32", "bf16": "bf16", "fp8_e4m3": "fp8_e4m3"}[w.kv_dtype],
         "data": "synthetic",
         "config": {"workload": describe(case), "l2": "flushed between steps (2x L2 buffer written, untimed)",
-                   "parallelism": f"replicas x{world}", "token_flat": bool(args.token_flat)},
+                   "parallelism": f"replicas x{world}", "token_flat": bool(args.token_flat),
+                   "concurrent_prefix": concurrent},
         "unique_kv_bytes": ub, "paged_kv_bytes": paged_b,
         "hbm_frac_of_8tbs": value / world / 8000.0,
         "kernels_ms": kmean, "plan_us": statistics.median(t_plan) * 1e6,

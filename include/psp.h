@@ -89,6 +89,11 @@ typedef int32_t psp_status;
 #define PSP_FLAG_TOKEN_FLAT 1 /* lower block tables to per-token kv_indices on the device
                                  (psp_expand_kv_indices) inside psp_run and read K/V
                                  through them; results are bit-identical to page mode */
+#define PSP_FLAG_CONCURRENT 2 /* run the prefix kernels on an internal stream forked from
+                                 and joined back into the caller's stream, concurrently
+                                 with the suffix kernel (tensor-core work overlapping the
+                                 HBM stream); every multi-part row then merges through
+                                 its arrival counter.  Ignored by psp_run_noalloc. */
 
 /*
  * Step configuration.  Supported (anything else -> PSP_ERR_UNSUPPORTED):

@@ -37,6 +37,7 @@ STATUS_NAMES = {0: "PSP_OK", -1: "PSP_ERR_INVALID_ARGUMENT", -2: "PSP_ERR_UNSUPP
 DTYPES = {"f32": 0, "bf16": 1, "fp8_e4m3": 2}
 BRANCH_NONE, BRANCH_CASCADE, BRANCH_DENSE = 0, 1, 2
 FLAG_TOKEN_FLAT = 1
+FLAG_CONCURRENT = 2
 FIELDS = {
     "suffix_start": 0, "suffix_len": 1, "suffix_page_indptr": 2, "suffix_page_indices": 3,
     "split_indptr": 4, "split_begin": 5, "split_end": 6, "group_shared_len": 7,
@@ -150,10 +151,10 @@ class DecodeStep:
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int, q_dtype: str,
                  kv_dtype: str, o_dtype: str, page_size: int, num_pages: int, num_sms: int = 0,
-                 dense_threshold: int = 0, token_flat: bool = False):
+                 dense_threshold: int = 0, token_flat: bool = False, concurrent: bool = False):
+        flags = (FLAG_TOKEN_FLAT if token_flat else 0) | (FLAG_CONCURRENT if concurrent else 0)
         self.cfg = psp_config(num_q_heads, num_kv_heads, head_dim, DTYPES[q_dtype], DTYPES[kv_dtype],
-                              DTYPES[o_dtype], page_size, num_pages, num_sms, dense_threshold,
-                              FLAG_TOKEN_FLAT if token_flat else 0)
+                              DTYPES[o_dtype], page_size, num_pages, num_sms, dense_threshold, flags)
         h = _H()
         st = psp_create(ctypes.byref(self.cfg), ctypes.byref(h))
         if st != PSP_OK:
@@ -162,10 +163,11 @@ class DecodeStep:
         self._batch_arrays = None
 
     @classmethod
-    def for_case(cls, case, num_sms: int = 0, dense_threshold: int = 0, token_flat: bool = False):
+    def for_case(cls, case, num_sms: int = 0, dense_threshold: int = 0, token_flat: bool = False,
+                 concurrent: bool = False):
         w = case.workload
         return cls(w.num_q_heads, w.num_kv_heads, w.head_dim, w.q_dtype, w.kv_dtype, w.o_dtype,
-                   case.page_size, case.num_pages, num_sms, dense_threshold, token_flat)
+                   case.page_size, case.num_pages, num_sms, dense_threshold, token_flat, concurrent)
 
     def close(self):
         if getattr(self, "handle", None):

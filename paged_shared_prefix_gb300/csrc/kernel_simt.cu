@@ -77,8 +77,9 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
   constexpr int kPer = D / 32;
   // a request with a single partial (no shared prefix, one split) writes its output directly;
   // a single-split request of a prefix group merges after its write (the prefix kernel ran earlier)
-  const bool solo = mode == 0 && p.split_indptr[b_suffix + 1] - p.split_indptr[b_suffix] == 1;
-  const bool direct = solo && p.req_group[b_suffix] < 0;
+  const bool one_split = mode == 0 && p.split_indptr[b_suffix + 1] - p.split_indptr[b_suffix] == 1;
+  const bool direct = one_split && p.req_group[b_suffix] < 0;
+  const bool solo = one_split && !p.concurrent;
 
   for (int rbase = 0; rbase < n_rows; rbase += kWarps) {
     const int r = rbase + warp;

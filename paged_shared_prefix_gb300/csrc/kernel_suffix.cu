@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   // kernel ran earlier on the stream, so its rows are complete.  They are prefetched into
   // a shared-memory area of their own, in the first cp.async group of every thread.
   const int g_req = p.req_group[b];
-  const bool solo = p.split_indptr[b + 1] - p.split_indptr[b] == 1;
+  const bool solo = !p.concurrent && p.split_indptr[b + 1] - p.split_indptr[b] == 1;
   const int c0 = g_req >= 0 ? p.group_chunk_indptr[g_req] : 0;
   const int n_chunks = g_req >= 0 ? p.group_chunk_indptr[g_req + 1] - c0 : 0;
   const bool pre_smem = solo && n_chunks > 0 && n_chunks <= kPreChunks;
@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   // A single-split request writes its final output here: its own result merged with the
   // prefetched prefix partials (none without a shared prefix).  Otherwise write the partial
   // and let the last arrival of (b, h) merge.
-  const bool direct = solo && (n_chunks == 0 || pre_smem);
+  const bool only_part = p.split_indptr[b + 1] - p.split_indptr[b] == 1 && n_chunks == 0;
+  const bool direct = only_part || (solo && pre_smem);
   const bool solo_global = solo && !direct;   // too many prefix chunks to prefetch: read them here
   const int64_t row0 = (static_cast<int64_t>(split) * p.hkv + h) * G;
   const int64_t orow0 = static_cast<int64_t>(b) * p.hq + h * G;
@@ -394,7 +395,7 @@ cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
   }
   if (p.kv_dtype == PSP_KV_FP8) {
     if (p.head_dim != 128) return launch_t<PSP_KV_FP8, 64, 4, 6>(p, num_splits, s);
-    switch (suffix_stages(5)) {
+    switch (suffix_stages(3)) {
       case 2: return launch_t<PSP_KV_FP8, 128, 4, 2>(p, num_splits, s);
       case 3: return launch_t<PSP_KV_FP8, 128, 4, 3>(p, num_splits, s);
       default: return launch_t<PSP_KV_FP8, 128, 4, 5>(p, num_splits, s);

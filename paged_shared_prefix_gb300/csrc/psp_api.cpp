@@ -30,7 +30,7 @@ constexpr int32_t kDefaultDenseThreshold = 1024;
 constexpr int32_t kSplitMinTiles = 4;
 constexpr int32_t kSplitCtasPerSm = 4;
 constexpr int32_t kPrefixMinTiles = 4;
-constexpr int32_t kPrefixCtasPerSm = 1;
+constexpr int32_t kPrefixCtasPerSm = 2;  // dense and cascade prefix CTAs fit two per SM
 
 thread_local std::string g_create_error;
 
@@ -93,6 +93,11 @@ struct psp_handle {
   unsigned char* workspace = nullptr;
   size_t workspace_bytes = 0;
   bool uploaded = false;
+
+  // concurrent prefix: side stream and fork/join events (created on first use)
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+  bool allow_concurrent = true;   // false on the workspace-free path (no object creation)
 
   // per-kernel timing
   bool timing = false;
@@ -438,6 +443,7 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.o_dtype = c.o_dtype;
   p.num_pages = c.num_pages;
   p.token_flat = (c.flags & PSP_FLAG_TOKEN_FLAT) ? 1 : 0;
+  p.concurrent = ((c.flags & PSP_FLAG_CONCURRENT) && h->allow_concurrent) ? 1 : 0;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c.head_dim)));
   if (t) {
     p.q = t->q;
@@ -534,7 +540,8 @@ psp_status psp_create(const psp_config* cfg, psp_handle** out) {
   if (!f32 && !low) return fail(nullptr, PSP_ERR_UNSUPPORTED, "unsupported q/kv dtype combination");
   if (c.o_dtype != PSP_DTYPE_F32 && c.o_dtype != PSP_DTYPE_BF16)
     return fail(nullptr, PSP_ERR_UNSUPPORTED, "o_dtype must be F32 or BF16");
-  if (c.flags & ~PSP_FLAG_TOKEN_FLAT) return fail(nullptr, PSP_ERR_INVALID_ARGUMENT, "unknown flag");
+  if (c.flags & ~(PSP_FLAG_TOKEN_FLAT | PSP_FLAG_CONCURRENT))
+    return fail(nullptr, PSP_ERR_INVALID_ARGUMENT, "unknown flag");
   const int64_t slots = static_cast<int64_t>(c.num_pages) * c.page_size;
   if (slots * c.num_kv_heads * c.head_dim > (int64_t{1} << 40))
     return fail(nullptr, PSP_ERR_INVALID_ARGUMENT, "pool too large");
@@ -560,6 +567,9 @@ void psp_destroy(psp_handle* h) {
   if (!h) return;
   if (h->staging) cudaFreeHost(h->staging);
   if (h->staging_done) cudaEventDestroy(h->staging_done);
+  if (h->fork_ev) cudaEventDestroy(h->fork_ev);
+  if (h->join_ev) cudaEventDestroy(h->join_ev);
+  if (h->side) cudaStreamDestroy(h->side);
   for (cudaEvent_t e : h->events) cudaEventDestroy(e);
   delete h;
 }
@@ -734,17 +744,37 @@ psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
   }
   const int nd = static_cast<int>(P.item_chunk_dense.size());
   const int nc = static_cast<int>(P.item_chunk_cascade.size());
+  const bool fork = p.concurrent && (nd > 0 || nc > 0) && P.NS > 0;
+  cudaStream_t ps = s;  // stream of the prefix kernels
+  cudaError_t e;
+  if (fork) {
+    if (!h->side) {
+      e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->fork_ev, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->join_ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return cuda_fail(h, e, "creating the prefix stream");
+    }
+    e = cudaEventRecord(h->fork_ev, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->fork_ev, 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "forking the prefix stream");
+    ps = h->side;
+  }
   if (nd > 0) {
-    st = timed_launch(h, s, "prefix_dense", slot, psp::launch_prefix_dense, p, nd);
+    st = timed_launch(h, ps, "prefix_dense", slot, psp::launch_prefix_dense, p, nd);
     if (st) return st;
   }
   if (nc > 0) {
-    st = timed_launch(h, s, "prefix_cascade", slot, psp::launch_prefix_cascade, p, nc);
+    st = timed_launch(h, ps, "prefix_cascade", slot, psp::launch_prefix_cascade, p, nc);
     if (st) return st;
   }
   if (P.NS > 0) {
     st = timed_launch(h, s, "suffix_splitkv", slot, psp::launch_suffix, p, P.NS);
     if (st) return st;
+  }
+  if (fork) {
+    e = cudaEventRecord(h->join_ev, ps);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->join_ev, 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "joining the prefix stream");
   }
   return PSP_OK;
 }
@@ -839,7 +869,9 @@ psp_status bind_image_and_run(psp_handle* h, unsigned char* ws, size_t cap, cons
   h->uploaded = true;
   const bool timing = h->timing;
   h->timing = false;
+  h->allow_concurrent = false;
   const psp_status st = psp_run(h, t, s);
+  h->allow_concurrent = true;
   h->timing = timing;
   return st;
 }

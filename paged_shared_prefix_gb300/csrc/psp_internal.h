@@ -35,6 +35,7 @@ struct StepParams {
   int32_t kv_dtype, q_dtype, o_dtype;
   int32_t num_pages;
   int32_t token_flat;                // read K/V through kv_indices (page size 1 view)
+  int32_t concurrent;                // prefix and suffix kernels may run at the same time
   float scale_log2;                  // log2(e) / sqrt(head_dim)
 
   // caller tensors (device)

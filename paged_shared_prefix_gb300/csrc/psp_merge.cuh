@@ -7,8 +7,10 @@
 // one arrival on the (b, h) counter; the CTA that brings the count to the
 // expected total merges the G rows of (b, h) and resets the counter to zero
 // for the next step.  No CTA ever waits for another.  A request with exactly
-// one suffix split skips the counter: its suffix CTA runs after the prefix
-// kernel has finished (stream order) and merges the prefix partials directly.
+// one suffix split skips the counter when the prefix kernels run before the
+// suffix kernel on one stream: its suffix CTA merges the (complete) prefix
+// partials directly.  With concurrent prefix and suffix kernels every row with
+// more than one part goes through its counter.
 //
 // Merge of a row: with every O_i normalised and lse_i its log2 normaliser,
 //   M = max_i lse_i,  w_i = 2^(lse_i - M),  O = sum_i w_i O_i / sum_i w_i,
@@ -131,7 +133,7 @@ __device__ __forceinline__ void prefix_arrive_and_merge(const StepParams& p, con
   const int n_members = n / G;  // row blocks hold whole members (G divides the block)
   for (int m = threadIdx.x; m < n_members; m += blockDim.x) {
     const int b = members[(row0 / G) + m];
-    const bool solo = p.split_indptr[b + 1] - p.split_indptr[b] == 1;
+    const bool solo = !p.concurrent && p.split_indptr[b + 1] - p.split_indptr[b] == 1;
     flags[m] = (!solo && arrive_is_last(p, b, h)) ? 1 : 0;
   }
   __syncthreads();

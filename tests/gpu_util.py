@@ -17,12 +17,14 @@ def device_tensors(case, dev="cuda:0"):
                 v_scale=t(case.v_scale))
 
 
-def run_case(case, *, threshold=0, token_flat=False, tensors=None, num_sms=0, return_step=False):
+def run_case(case, *, threshold=0, token_flat=False, tensors=None, num_sms=0, return_step=False,
+             concurrent=False):
     """One step on cuda:0; returns (O float64 [B, Hq, d], LSE float64 [B, Hq])."""
     w = case.workload
     dev = torch.device("cuda:0")
     tens = tensors or device_tensors(case)
-    step = psp.DecodeStep.for_case(case, num_sms=num_sms, dense_threshold=threshold, token_flat=token_flat)
+    step = psp.DecodeStep.for_case(case, num_sms=num_sms, dense_threshold=threshold, token_flat=token_flat,
+                                   concurrent=concurrent)
     step.plan_case(case)
     ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device=dev)
     step.upload(ws)

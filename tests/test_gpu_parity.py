@@ -265,3 +265,37 @@ def test_dense_prefix_matches_oracle(label, kw):
     # different SM counts change the prefix chunking; the result stays within tolerance
     o3, lse3 = run_case(case, threshold=1, num_sms=37)
     assert max_err(o3, ref_o) <= tol and max_err(lse3, ref_lse) <= tol
+
+
+CONCURRENT = [
+    ("tiny", dict(name="tiny")),
+    ("agent-dense", dict(name="agent", batch=40, prefix_len=512, private_range=(1, 300)), 1),
+    ("agent-cascade", dict(name="agent", batch=12, prefix_len=256, private_range=(1, 300)), 1 << 20),
+    ("fp8-dense", dict(name="fp8_large", batch=20, prefix_len=640, private_range=(1, 600)), 1),
+    ("multi-split", dict(name="short_prefix", batch=6, private_range=(800, 2000)), 0),
+    ("empty-suffix", dict(name="agent", batch=5, prefix_len=128, private_lengths=[0, 3, 0, 17, 64]), 1),
+]
+
+
+@pytest.mark.parametrize("spec", CONCURRENT, ids=[c[0] for c in CONCURRENT])
+def test_concurrent_prefix_matches_oracle(spec):
+    label, kw = spec[0], spec[1]
+    thr = spec[2] if len(spec) > 2 else 0
+    case = _make(kw)
+    tol = TOL[case.workload.kv_dtype]
+    ref_o, ref_lse = oracle.attend_all(case)
+    for num_sms in (0, 11):   # 11 SMs: many splits per request, counters exercised
+        o, lse = run_case(case, threshold=thr, concurrent=True, num_sms=num_sms)
+        assert max_err(o, ref_o) <= tol and max_err(lse, ref_lse) <= tol, (label, num_sms)
+    # a second step through the same workspace: the counters reset themselves
+    (o1, l1), step, ws = run_case(case, threshold=thr, concurrent=True, return_step=True)
+    tens = device_tensors(case)
+    w = case.workload
+    o2 = torch.empty((case.batch, w.num_q_heads, w.head_dim),
+                     dtype=torch.float32 if w.o_dtype == "f32" else torch.bfloat16, device="cuda:0")
+    l2 = torch.empty((case.batch, w.num_q_heads), dtype=torch.float32, device="cuda:0")
+    step.run(tens["q"], tens["k_pool"], tens["v_pool"], o2, l2, tens["k_scale"], tens["v_scale"])
+    torch.cuda.synchronize()
+    assert max_err(o2.float().cpu().double().numpy(), ref_o) <= tol
+    assert max_err(l2.cpu().double().numpy(), ref_lse) <= tol
+    step.close()
