@@ -31,7 +31,7 @@ namespace {
 
 using namespace dev;
 
-constexpr int kPreChunks = 2;  // prefix partials prefetched per single-split request (per query head row)
+constexpr int kPreRows = 16;  // prefix partial rows (chunks x query heads) prefetched per single-split request
 
 template <int KV, int D>
 struct SufCfg {
@@ -80,9 +80,9 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   const bool solo = !p.concurrent && p.split_indptr[b + 1] - p.split_indptr[b] == 1;
   const int c0 = g_req >= 0 ? p.group_chunk_indptr[g_req] : 0;
   const int n_chunks = g_req >= 0 ? p.group_chunk_indptr[g_req + 1] - c0 : 0;
-  const bool pre_smem = solo && n_chunks > 0 && n_chunks <= kPreChunks;
-  float* pre_o = reinterpret_cast<float*>(smem + NW * NST * C::kStageBytes);   // [chunk][G][D]
-  float* pre_l = pre_o + kPreChunks * 8 * D;                                     // [chunk][G]
+  const bool pre_smem = solo && n_chunks > 0 && n_chunks * G <= kPreRows;
+  float* pre_o = reinterpret_cast<float*>(smem + NW * NST * C::kStageBytes);   // [chunk * G + j][D]
+  float* pre_l = pre_o + kPreRows * D;                                           // [chunk * G + j]
   if (pre_smem) {
     const int m_eff = p.group_m_eff[g_req];
     const int prow = p.req_member[b] * G;
@@ -94,9 +94,9 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
       const int q = rem - j * (kRowChunks + 1);
       const int64_t row = p.chunk_row_offset[c0 + c] + static_cast<int64_t>(h) * m_eff + prow + j;
       if (q < kRowChunks) {
-        cp_async_16(smem_u32(pre_o + (c * 8 + j) * D + q * 4), p.o_pre + row * D + q * 4, true);
+        cp_async_16(smem_u32(pre_o + (c * G + j) * D + q * 4), p.o_pre + row * D + q * 4, true);
       } else {
-        cp_async_4(smem_u32(pre_l + c * 8 + j), p.lse_pre + row);
+        cp_async_4(smem_u32(pre_l + c * G + j), p.lse_pre + row);
       }
     }
   }
@@ -326,12 +326,12 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
       // own part: O_s = acc / sum * out_scale with log2-LSE mmax + log2(sum); prefix chunks first
       float lse_own = mmax + log2f(sum);
       float big = lse_own;
-      for (int c = 0; c < n_chunks; ++c) big = fmaxf(big, pre_l[c * 8 + g]);
+      for (int c = 0; c < n_chunks; ++c) big = fmaxf(big, pre_l[c * G + g]);
       float wsum = 0.f, out = 0.f;
       for (int c = 0; c < n_chunks; ++c) {
-        const float w = exp2f(pre_l[c * 8 + g] - big);
+        const float w = exp2f(pre_l[c * G + g] - big);
         wsum += w;
-        out = fmaf(w, pre_o[(c * 8 + g) * D + d], out);
+        out = fmaf(w, pre_o[(c * G + g) * D + d], out);
       }
       const float w_own = exp2f(lse_own - big);
       wsum += w_own;
@@ -362,7 +362,7 @@ cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
   using C = SufCfg<KV, D>;
   const int ring = NW * NST * C::kStageBytes;
   const int epi = (NW * 8 * D + 2 * NW * 8) * 4;
-  const int bytes = (ring > epi ? ring : epi) + kPreChunks * 8 * (D + 1) * 4;
+  const int bytes = (ring > epi ? ring : epi) + kPreRows * (D + 1) * 4;
   auto kern = suffix_kernel<KV, D, NW, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
