@@ -752,9 +752,6 @@ cudaError_t launch_cta(const StepParams& p, int num_splits, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-}  // namespace
-
-
 int num_sms_of_current_device() {
   static int cached[64] = {};
   static std::mutex mu;
