@@ -28,7 +28,7 @@ using psp::StepParams;
 constexpr int32_t kDefaultDenseThreshold = 1024;
 
 constexpr int32_t kSplitMinTiles = 4;
-constexpr int32_t kSplitCtasPerSm = 16;  // suffix work items per SM (one warp each)
+constexpr int32_t kSplitCtasPerSm = 8;  // measured: 8 (split, head) CTAs per SM balance best
 constexpr int32_t kPrefixMinTiles = 4;
 constexpr int32_t kPrefixCtasPerSm = 2;  // dense and cascade prefix CTAs fit two per SM
 
@@ -64,7 +64,6 @@ struct HostPlan {
   std::vector<int32_t> group_member_indptr, group_members, group_chunk_indptr;
   std::vector<int32_t> chunk_group, chunk_begin, chunk_end, chunk_row_offset;
   std::vector<int32_t> item_chunk_dense, item_rb_dense, item_chunk_cascade, item_rb_cascade;
-  std::vector<int32_t> suffix_items;  // split * Hkv + h, longest split first (work order of the suffix warps)
   std::vector<int32_t> kv_indptr;
   int64_t kv_indices_len = 0, suffix_tokens = 0, shared_tokens = 0, pre_rows = 0;
   PlanLayout layout{};
@@ -296,18 +295,6 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
     P.split_indptr[b + 1] = static_cast<int32_t>(P.split_req.size());
   }
   P.NS = static_cast<int32_t>(P.split_req.size());
-  {
-    // suffix work items (split, KV head), longest first so that the persistent warps that
-    // take them in order finish together; ties keep split and head order
-    std::vector<int32_t> order(P.NS);
-    for (int32_t i = 0; i < P.NS; ++i) order[i] = i;
-    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
-      return (P.split_end[a] - P.split_begin[a]) > (P.split_end[b] - P.split_begin[b]);
-    });
-    P.suffix_items.reserve(static_cast<size_t>(P.NS) * Hkv);
-    for (int32_t sp : order)
-      for (int h2 = 0; h2 < Hkv; ++h2) P.suffix_items.push_back(sp * Hkv + h2);
-  }
   if (static_cast<int64_t>(P.NS) * Hkv > INT32_MAX / psp::kMaxGroupSize)
     return fail(h, PSP_ERR_INVALID_ARGUMENT, "too many splits");
 
@@ -341,11 +328,9 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   place(L.item_rb_dense, n32(P.item_rb_dense));
   place(L.item_chunk_cascade, n32(P.item_chunk_cascade));
   place(L.item_rb_cascade, n32(P.item_rb_cascade));
-  place(L.suffix_items, n32(P.suffix_items));
   place(L.kv_indptr, n32(P.kv_indptr));
   L.plan_bytes = off;
   L.status = off;
-  L.work = off + 16;      // suffix work counter and finished-warp counter
   L.counters = off + 64;
   L.zero_end = L.counters + static_cast<size_t>(B) * Hkv * sizeof(int32_t);
   off = align_up(L.zero_end);
@@ -388,7 +373,6 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   put(L.item_rb_dense, P.item_rb_dense);
   put(L.item_chunk_cascade, P.item_chunk_cascade);
   put(L.item_rb_cascade, P.item_rb_cascade);
-  put(L.suffix_items, P.suffix_items);
   put(L.kv_indptr, P.kv_indptr);
 
   psp_plan_info& I = P.info;
@@ -497,7 +481,6 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.item_rb_dense = I(L.item_rb_dense);
   p.item_chunk_cascade = I(L.item_chunk_cascade);
   p.item_rb_cascade = I(L.item_rb_cascade);
-  p.suffix_items = I(L.suffix_items);
   p.kv_indptr = I(L.kv_indptr);
   p.kv_indices = I(L.kv_indices);
   p.o_suf = F(L.o_suf);
@@ -506,7 +489,6 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.lse_pre = F(L.lse_pre);
   p.status = I(L.status);
   p.counters = I(L.counters);
-  p.work = I(L.work);
   return p;
 }
 

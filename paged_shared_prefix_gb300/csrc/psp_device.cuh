@@ -34,25 +34,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Waits until at most `pending` of this thread's most recent cp.async groups are
-// still in flight (pending clamped to [0, MAX - 1]).
-template <int MAX>
-__device__ __forceinline__ void cp_async_wait_upto(int pending) {
-  if (pending <= 0) {
-    cp_async_wait<0>();
-  } else if (pending == 1 || MAX <= 2) {
-    cp_async_wait<1>();
-  } else if (pending == 2 || MAX <= 3) {
-    cp_async_wait<(MAX > 2 ? 2 : 1)>();
-  } else if (pending == 3 || MAX <= 4) {
-    cp_async_wait<(MAX > 3 ? 3 : 1)>();
-  } else if (pending == 4 || MAX <= 5) {
-    cp_async_wait<(MAX > 4 ? 4 : 1)>();
-  } else {
-    cp_async_wait<(MAX > 5 ? 5 : 1)>();
-  }
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])

@@ -73,7 +73,6 @@ struct StepParams {
   const int32_t* item_rb_dense;
   const int32_t* item_chunk_cascade;   // cascade prefix work items
   const int32_t* item_rb_cascade;
-  const int32_t* suffix_items;         // [S * Hkv] split * Hkv + h, longest first
   const int32_t* kv_indptr;            // [B+1] token-flat offsets
   int32_t* kv_indices;                 // [sum kv_len] (token-flat mode)
 
@@ -84,7 +83,6 @@ struct StepParams {
   float* lse_pre;
   int32_t* status;                     // device status word
   int32_t* counters;                   // [B * Hkv] arrivals of partial results (zero between steps)
-  int32_t* work;                       // [2] suffix work counter, finished warps (zero between steps)
 };
 
 // Byte offsets of every array inside the workspace (256-byte aligned each).
@@ -95,11 +93,10 @@ struct PlanLayout {
   size_t group_page_indptr, group_page_indices, group_m_eff, group_shared_len;
   size_t group_member_indptr, group_members, group_chunk_indptr;
   size_t chunk_group, chunk_begin, chunk_end, chunk_row_offset;
-  size_t item_chunk_dense, item_rb_dense, item_chunk_cascade, item_rb_cascade, suffix_items;
+  size_t item_chunk_dense, item_rb_dense, item_chunk_cascade, item_rb_cascade;
   size_t kv_indptr;
   size_t plan_bytes;       // end of the uploaded integer region
   size_t status;
-  size_t work;             // suffix work queue counters, inside the cleared region
   size_t counters;         // right after status; both cleared at every upload
   size_t zero_end;
   size_t o_suf, lse_suf, o_pre, lse_pre;
