@@ -40,13 +40,15 @@ struct PreCfg {
 
 template <int KV, int D, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32) prefix_cascade_kernel(const StepParams p, const int32_t* item_chunk,
-                                                                 const int32_t* item_rb) {
+                                                                 const int32_t* item_rb, int ctas_per_item) {
   using C = PreCfg<KV, D>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ci = item_chunk[blockIdx.x];
-  const int rb = item_rb[blockIdx.x];
+  // an item's row block may span several CTAs of NW * 16 rows each
+  const int item = blockIdx.x / ctas_per_item;
+  const int ci = item_chunk[item];
+  const int rb = item_rb[item] * ctas_per_item + (blockIdx.x - item * ctas_per_item);
   const int h = blockIdx.y;
   const int g = p.chunk_group[ci];
   const int t0 = p.chunk_begin[ci];
@@ -299,24 +301,26 @@ __global__ void __launch_bounds__(NW * 32) prefix_cascade_kernel(const StepParam
 }
 
 template <int KV, int D, int NW, int NST>
-cudaError_t launch_t(const StepParams& p, const int32_t* chunks, const int32_t* rbs, int n, cudaStream_t s) {
+cudaError_t launch_t(const StepParams& p, const int32_t* chunks, const int32_t* rbs, int n, int per_item,
+                     cudaStream_t s) {
   using C = PreCfg<KV, D>;
   const int bytes = NST * C::kStageBytes;
   auto kern = prefix_cascade_kernel<KV, D, NW, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(n, p.hkv);
-  kern<<<grid, NW * 32, bytes, s>>>(p, chunks, rbs);
+  dim3 grid(n * per_item, p.hkv);
+  kern<<<grid, NW * 32, bytes, s>>>(p, chunks, rbs, per_item);
   return cudaGetLastError();
 }
 
 template <int NW>
-cudaError_t launch_rows(const StepParams& p, const int32_t* chunks, const int32_t* rbs, int n, cudaStream_t s) {
+cudaError_t launch_rows(const StepParams& p, const int32_t* chunks, const int32_t* rbs, int n, int per_item,
+                        cudaStream_t s) {
   if (p.kv_dtype == PSP_KV_BF16)
-    return p.head_dim == 128 ? launch_t<PSP_KV_BF16, 128, NW, 3>(p, chunks, rbs, n, s)
-                             : launch_t<PSP_KV_BF16, 64, NW, 4>(p, chunks, rbs, n, s);
-  return p.head_dim == 128 ? launch_t<PSP_KV_FP8, 128, NW, 4>(p, chunks, rbs, n, s)
-                           : launch_t<PSP_KV_FP8, 64, NW, 4>(p, chunks, rbs, n, s);
+    return p.head_dim == 128 ? launch_t<PSP_KV_BF16, 128, NW, 3>(p, chunks, rbs, n, per_item, s)
+                             : launch_t<PSP_KV_BF16, 64, NW, 4>(p, chunks, rbs, n, per_item, s);
+  return p.head_dim == 128 ? launch_t<PSP_KV_FP8, 128, NW, 4>(p, chunks, rbs, n, per_item, s)
+                           : launch_t<PSP_KV_FP8, 64, NW, 4>(p, chunks, rbs, n, per_item, s);
 }
 
 }  // namespace
@@ -324,13 +328,14 @@ cudaError_t launch_rows(const StepParams& p, const int32_t* chunks, const int32_
 cudaError_t launch_prefix_cascade(const StepParams& p, int num_items, cudaStream_t s) {
   if (num_items <= 0) return cudaSuccess;
   if (p.kv_dtype == PSP_KV_F32) return launch_prefix_simt(p, num_items, false, s);
-  return launch_rows<kCascadeRows / 16>(p, p.item_chunk_cascade, p.item_rb_cascade, num_items, s);
+  return launch_rows<kCascadeRows / 16>(p, p.item_chunk_cascade, p.item_rb_cascade, num_items, 1, s);
 }
 
-// Dense branch with the same register pipeline over 128-row blocks (8 warps).
+// Dense branch with the same register pipeline (head_dim 64): each 256-row item as
+// two CTAs of 128 rows (8 warps).
 cudaError_t launch_prefix_dense_mma(const StepParams& p, int num_items, cudaStream_t s) {
   if (num_items <= 0) return cudaSuccess;
-  return launch_rows<kDenseRows / 16>(p, p.item_chunk_dense, p.item_rb_dense, num_items, s);
+  return launch_rows<8>(p, p.item_chunk_dense, p.item_rb_dense, num_items, kDenseRows / 128, s);
 }
 
 }  // namespace psp

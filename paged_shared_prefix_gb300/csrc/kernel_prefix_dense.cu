@@ -1,35 +1,36 @@
 // kernel_prefix_dense.cu -- dense shared-prefix attention on the 5th-generation
 // tensor cores (tcgen05), the branch the dispatcher takes at large M_eff
 // ("GraniKV", section 3: above the threshold the shared prefix runs as a dense
-// matmul over all stacked queries; section 2: the prefix is read once per
-// step instead of once per request).
+// matmul over all stacked queries; section 2: the prefix is read once per step
+// instead of once per request).
 //
-// One CTA = 128 stacked query rows (rows R = member * G + j of one KV head)
-// x one chunk of the shared prefix, in 64-token tiles; two CTAs share an SM
-// (256 tensor-memory columns and <= 96 KB of shared memory each), so one CTA's
-// softmax overlaps the other's tensor-core work:
-//   warps 4 and 6     (producers, keys and values) TMA-load each K and V tile
-//                      page by page from the paged pool (3-D tensor map
-//                      [slot][kv head][d], boxes of up to 64 tokens x 128 bytes,
-//                      128-byte swizzle) into rings of 2 (bf16) or 4 (e4m3) stages;
-//   warp 5 (MMA)       one thread issues S_j = Q K_j^T (M=128, N=64, K=128,
-//                      bf16 operands from shared memory, fp32 accumulator in
-//                      tensor memory, two S buffers) and O += P_j V_j (P from
-//                      tensor memory, V as an MN-major shared operand);
-//   warps 0-3 (softmax) each thread owns one row: reads its S row from tensor
-//                      memory, applies the online softmax with lazy rescaling
-//                      (the running max is only moved when it grows by more
-//                      than 2^8, and O is rescaled in tensor memory only then),
-//                      writes P back over S as bf16, and at the end normalises
-//                      O and writes the fp32 partial row and its log2-LSE.
-// fp8-e4m3 caches use kind::f8f6f4: the e4m3 K/V tiles are loaded as stored
-// (one 128-byte box row per token), each query row is quantised to e4m3 with
-// its own scale amax/448 (folded, with the per-head key scale, into the
-// softmax scale), and P is written to tensor memory as e4m3 (P <= 2^8 under
-// the lazy rescaling bound, inside the e4m3 range); the value scale is
-// applied to the normalised output.
-// Every mbarrier wait is bounded; on timeout the kernel records the site in
-// the device status word and unwinds (draining its own TMA copies, freeing its
+// One CTA = 256 stacked query rows of one KV head (rows R = member * G + j, in
+// two 128-row tiles A and B) x one chunk of the shared prefix, in 128-token
+// K/V tiles that both query tiles share:
+//   warps 8 and 9 (producers, keys and values) TMA-load each K and V tile page
+//                      by page from the paged pool (3-D tensor map [slot][kv
+//                      head][d], boxes of up to 64 tokens x 128 bytes, 128-byte
+//                      swizzle) into rings of 2 (bf16) or 4 (e4m3) stages;
+//   warp 10 (MMA)      one thread issues, per K/V tile j,
+//                        S_A = Q_A K_j^T, S_B = Q_B K_j^T       (M=128, N=128)
+//                        O_A += P_A V_j, S_A(j+1), O_B += P_B V_j, S_B(j+1)
+//                      with fp32 accumulators in tensor memory (S_A, S_B, O_A,
+//                      O_B: all 512 columns) and P read from tensor memory; in
+//                      this order the tensor core runs one tile's products while
+//                      the other tile's softmax warps work;
+//   warps 0-3 / 4-7    (softmax, tiles A / B) one thread per row: read the S
+//                      row, online softmax with lazy rescaling (the running max
+//                      only moves when it grows by more than 2^8, and O is then
+//                      rescaled in tensor memory), write P back over S, and at
+//                      the end normalise O and write the fp32 partial row and
+//                      its log2-LSE.
+// fp8-e4m3 caches use kind::f8f6f4: the e4m3 K/V tiles are loaded as stored,
+// each query row is quantised to e4m3 with its own scale amax/448 (folded, with
+// the per-head key scale, into the softmax scale), and P is written to tensor
+// memory as e4m3 (P <= 2^8 under the lazy bound, inside the e4m3 range); the
+// value scale is applied to the normalised output.
+// Every mbarrier wait is bounded; on timeout the kernel records the site in the
+// device status word and unwinds (draining its own TMA copies, freeing its
 // tensor memory) instead of hanging.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -48,12 +49,11 @@ namespace {
 using namespace dev;
 using namespace sm100;
 
-constexpr int kRows = 128;                 // UMMA M (stacked query rows)
-constexpr int kTok = 64;                   // tokens per tile (N of S, K of PV)
+constexpr int kRows = 128;                 // UMMA M (stacked query rows per tile)
+constexpr int kTok = 128;                  // tokens per K/V tile (N of S, K of PV)
 constexpr int kD = 128;                    // head dim (K of S, N of PV)
-constexpr int kThreads = 224;              // warps 0-3 softmax, 4 K producer, 5 MMA, 6 V producer
-constexpr uint32_t kTmemCols = 256;        // S0 [0,64), S1 [64,128), O [128,256): two CTAs fit one SM
-constexpr uint32_t kOCol = 2 * kTok;
+constexpr int kThreads = 352;              // warps 0-7 softmax, 8 K producer, 9 V producer, 10 MMA
+constexpr uint32_t kTmemCols = 512;        // S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512)
 constexpr float kRescaleLog2 = 8.f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -62,35 +62,35 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Tile geometry for bf16 (FP8 = false) and e4m3 (FP8 = true) operands.
 template <bool FP8>
 struct DenseCfg {
   static constexpr uint32_t kElem = FP8 ? 1 : 2;
-  static constexpr int kStages = FP8 ? 4 : 2;                // K and V ring depth (two CTAs per SM)
+  static constexpr int kStages = FP8 ? 4 : 2;                // K and V ring depth
   static constexpr uint32_t kTileBytes = kTok * kD * kElem;  // one K or V tile
-  static constexpr uint32_t kQBytes = kRows * kD * kElem;    // the Q tile
+  static constexpr uint32_t kQBytes = kRows * kD * kElem;    // one query tile
   static constexpr uint32_t kHalves = FP8 ? 1 : 2;           // 128-byte column blocks of a row
-  static constexpr uint32_t kHalf = kTileBytes / kHalves;    // column block of a K/V tile
-  static constexpr uint32_t kQHalf = kQBytes / kHalves;      // column block of the Q tile
+  static constexpr uint32_t kHalf = kTileBytes / kHalves;
+  static constexpr uint32_t kQHalf = kQBytes / kHalves;
   static constexpr int kBoxElems = 128 / kElem;              // d elements per TMA box row
   static constexpr int kKStep = 32 / kElem;                  // K elements per MMA instruction
-  static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOffQ + kQBytes;
+  static constexpr uint32_t kOffQ = 0;                       // Q_A, Q_B
+  static constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // barriers: q_ready, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done, o_full, final
+  // barriers: q_ready, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done[2], o_full, final
   static constexpr int kBarQ = 0, kBarKFull = 1, kBarKEmpty = 1 + kStages, kBarVFull = 1 + 2 * kStages,
                        kBarVEmpty = 1 + 3 * kStages, kBarSFull = 1 + 4 * kStages, kBarPFull = 3 + 4 * kStages,
-                       kBarPvDone = 5 + 4 * kStages, kBarOFull = 6 + 4 * kStages, kBarFinal = 7 + 4 * kStages,
-                       kNumBars = 8 + 4 * kStages;
+                       kBarPvDone = 5 + 4 * kStages, kBarOFull = 7 + 4 * kStages, kBarFinal = 8 + 4 * kStages,
+                       kNumBars = 9 + 4 * kStages;
   static constexpr uint32_t kOffTmem = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = kOffTmem + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t kOffFlag = kOffTmem + 8;
+  static constexpr uint32_t kSmemBytes = kOffFlag + 8 + 1024;  // + alignment slack
   static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(kRows, kTok, false) : idesc_f16(kRows, kTok, 1, false);
   static constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3(kRows, kD, true) : idesc_f16(kRows, kD, 1, true);
 };
 
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefix_dense_kernel(const StepParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, int num_slots) {
   using C = DenseCfg<FP8>;
@@ -102,11 +102,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   auto bar = [&](int i) { return base + C::kOffBar + 8u * i; };
+  volatile int* failed = reinterpret_cast<volatile int*>(gbase + C::kOffFlag);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ci = p.item_chunk_dense[blockIdx.x];
-  const int rb = p.item_rb_dense[blockIdx.x];
+  const int rb = p.item_rb_dense[blockIdx.x];  // 256-row block
   const int h = blockIdx.y;
   const int g = p.chunk_group[ci];
   const int t0 = p.chunk_begin[ci];
@@ -114,29 +115,30 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int n_tiles = (t1 - t0 + kTok - 1) / kTok;
   const int G = p.group;
   const int m_eff = p.group_m_eff[g];
+  const int row_base = rb * 2 * kRows;
+  const bool tile_b = row_base + kRows < m_eff;  // tile B holds live rows
   const int32_t* members = p.group_members + p.group_member_indptr[g];
   int32_t* status = p.status;
-  __shared__ int epilogue_failed;
 
   if (threadIdx.x == 0) {
-    epilogue_failed = 0;
-    mbar_init(bar(C::kBarQ), 128);
+    *failed = 0;
+    mbar_init(bar(C::kBarQ), tile_b ? 256 : 128);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(C::kBarKFull + s), 1);
       mbar_init(bar(C::kBarKEmpty + s), 1);
       mbar_init(bar(C::kBarVFull + s), 1);
       mbar_init(bar(C::kBarVEmpty + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::kBarSFull + s), 1);
-      mbar_init(bar(C::kBarPFull + s), 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarSFull + t), 1);
+      mbar_init(bar(C::kBarPFull + t), 128);
+      mbar_init(bar(C::kBarPvDone + t), 1);
     }
-    mbar_init(bar(C::kBarPvDone), 1);
     mbar_init(bar(C::kBarOFull), 1);
     mbar_init(bar(C::kBarFinal), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 10) {
     tmem_alloc(base + C::kOffTmem, kTmemCols);
     tmem_relinquish();
   }
@@ -145,10 +147,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kOffTmem);
 
-  if (warp == 4 || warp == 6) {
-    // ------------------------------------------------- producers: warp 4 keys, warp 6 values
+  if (warp == 8 || warp == 9) {
+    // ------------------------------------------------- producers: warp 8 keys, warp 9 values
     if (lane == 0) {
-      const bool is_v = warp == 6;
+      const bool is_v = warp == 9;
       const CUtensorMap* map = is_v ? &vmap : &kmap;
       prefetch_tmap(map);
       const int full0 = is_v ? C::kBarVFull : C::kBarKFull;
@@ -183,57 +185,77 @@ __global__ void __launch_bounds__(kThreads, 2)
       // drain: the last load issued on each stage must have landed before the CTA may exit
       for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(bar(full0 + j % NS), (j / NS) & 1, status, 3);
     }
-  } else if (warp == 5) {
+  } else if (warp == 10) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       bool ok = mbar_wait(bar(C::kBarQ), 0, status, 4);
       tc_fence_after();
-      auto issue_pv = [&](int jj) -> bool {
-        const int sb = jj & 1, sv = jj % NS;
-        if (!mbar_wait(bar(C::kBarPFull + sb), (jj >> 1) & 1, status, 5)) return false;
-        if (!mbar_wait(bar(C::kBarVFull + sv), (jj / NS) & 1, status, 6)) return false;
-        tc_fence_after();
-        const uint32_t vbase = base + C::kOffV + sv * kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < kTok / C::kKStep; ++ks) {
-          // V is the MN-major B operand: K (tokens) advances by whole 128-byte rows
-          const uint64_t bdesc = sw128_desc(vbase + ks * C::kKStep * 128, kHalf, 1024);
-          const uint32_t acc = (jj > 0 || ks > 0) ? 1u : 0u;
-          if constexpr (FP8) {
-            mma_ts_f8(tmem + kOCol, tmem + sb * kTok + ks * 8, bdesc, C::kIdescPV, acc);
-          } else {
-            mma_ts(tmem + kOCol, tmem + sb * kTok + ks * 8, bdesc, C::kIdescPV, acc);
-          }
-        }
-        mma_commit(bar(C::kBarPvDone));
-        mma_commit(bar(C::kBarVEmpty + sv));
-        return true;
-      };
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int sb = j & 1, sk = j % NS;
-        if (!mbar_wait(bar(C::kBarKFull + sk), (j / NS) & 1, status, 7)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kbase = base + C::kOffK + sk * kTileBytes;
+      // S_t = Q_t K_j^T into the S columns of tile t
+      auto issue_s = [&](int t, int j) {
+        const uint32_t kbase = base + C::kOffK + (j % NS) * kTileBytes;
+        const uint32_t qbase = base + C::kOffQ + t * C::kQBytes;
 #pragma unroll
         for (int ks = 0; ks < kD / C::kKStep; ++ks) {
           // K-major operands: 32 bytes of K per instruction inside a 128-byte swizzled row
           const uint32_t off = (ks & 3) * 32;
-          const uint64_t adesc = sw128_desc(base + C::kOffQ + (ks >> 2) * C::kQHalf + off, 16, 1024);
+          const uint64_t adesc = sw128_desc(qbase + (ks >> 2) * C::kQHalf + off, 16, 1024);
           const uint64_t bdesc = sw128_desc(kbase + (ks >> 2) * kHalf + off, 16, 1024);
           if constexpr (FP8) {
-            mma_ss_f8(tmem + sb * kTok, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
+            mma_ss_f8(tmem + t * kTok, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
           } else {
-            mma_ss(tmem + sb * kTok, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
+            mma_ss(tmem + t * kTok, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
           }
         }
-        mma_commit(bar(C::kBarSFull + sb));
-        mma_commit(bar(C::kBarKEmpty + sk));
-        if (j >= 1) ok = issue_pv(j - 1);
+        mma_commit(bar(C::kBarSFull + t));
+      };
+      // O_t += P_t V_j (P from the S columns of tile t)
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vbase = base + C::kOffV + (j % NS) * kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kTok / C::kKStep; ++ks) {
+          // V is the MN-major B operand: K (tokens) advances by whole 128-byte rows
+          const uint64_t bdesc = sw128_desc(vbase + ks * C::kKStep * 128, kHalf, 1024);
+          const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+          if constexpr (FP8) {
+            mma_ts_f8(tmem + 256 + t * kD, tmem + t * kTok + ks * 8, bdesc, C::kIdescPV, acc);
+          } else {
+            mma_ts(tmem + 256 + t * kD, tmem + t * kTok + ks * 8, bdesc, C::kIdescPV, acc);
+          }
+        }
+        mma_commit(bar(C::kBarPvDone + t));
+      };
+      if (ok && n_tiles > 0) {
+        ok = mbar_wait(bar(C::kBarKFull), 0, status, 7);
+        tc_fence_after();
+        if (ok) {
+          issue_s(0, 0);
+          if (tile_b) issue_s(1, 0);
+          mma_commit(bar(C::kBarKEmpty));
+        }
       }
-      if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const bool more = j + 1 < n_tiles;
+        ok = mbar_wait(bar(C::kBarPFull + 0), j & 1, status, 5) &&
+             mbar_wait(bar(C::kBarVFull + j % NS), (j / NS) & 1, status, 6);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(0, j);
+        if (more) {
+          ok = mbar_wait(bar(C::kBarKFull + (j + 1) % NS), ((j + 1) / NS) & 1, status, 7);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(0, j + 1);  // S_A's columns are reused only after PV_A(j) (issued above) has read P_A(j)
+        }
+        if (tile_b) {
+          ok = mbar_wait(bar(C::kBarPFull + 1), j & 1, status, 5);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, j);
+          if (more) issue_s(1, j + 1);
+        }
+        mma_commit(bar(C::kBarVEmpty + j % NS));
+        if (more) mma_commit(bar(C::kBarKEmpty + (j + 1) % NS));
+      }
       mma_commit(bar(C::kBarOFull));
       mma_commit(bar(C::kBarFinal));
       mbar_wait(bar(C::kBarFinal), 0, status, 8);  // every MMA of this CTA has completed
@@ -241,58 +263,60 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncwarp();
   } else {
     // ------------------------------------------------------- softmax warps
-    const int r = threadIdx.x;  // row of the block = TMEM lane
-    const int R = rb * kRows + r;
+    const int t = warp >> 2;                   // query tile (0 = A, 1 = B)
+    const int r = threadIdx.x & 127;           // row of the tile = TMEM lane
+    const int R = row_base + t * kRows + r;
     const bool live = R < m_eff;
+    const bool active = t == 0 || tile_b;
     float q_scale = 1.f;  // fp8: this row's quantisation scale
-    {
+    if (active) {
       const uint4* qrow = nullptr;
       if (live) {
         const int mem = R / G, jq = R - mem * G;
         qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
                                               (static_cast<int64_t>(members[mem]) * p.hq + h * G + jq) * kD);
       }
-      if constexpr (FP8) {
-        // pass 1: the row's amax; pass 2: reload (cached) and quantise to e4m3
-        float amax = 0.f;
-        if (live) {
-#pragma unroll 4
-          for (int c = 0; c < 16; ++c) {
-            const uint4 v = __ldg(qrow + c);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t qoff = C::kOffQ + t * C::kQBytes;
+      // all 16 loads of the row in flight before the first shared store (the compiler
+      // cannot move global loads across generic stores that might alias them)
+      uint4 v[16];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[k] & 0xffff)), fabsf(bf16_bits_to_float(w[k] >> 16))));
-          }
+      for (int c = 0; c < 16; ++c) v[c] = live ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (FP8) {
+        // the row's amax, then e4m3 codes of q / (amax / 448)
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[k] & 0xffff)), fabsf(bf16_bits_to_float(w[k] >> 16))));
         }
         q_scale = amax > 0.f ? amax / 448.f : 1.f;
         const float inv = 1.f / q_scale;
-#pragma unroll 2
+#pragma unroll
         for (int c = 0; c < 8; ++c) {  // 16 e4m3 codes per 16-byte chunk
-          const uint4 lo = live ? __ldg(qrow + 2 * c) : make_uint4(0u, 0u, 0u, 0u);
-          const uint4 hi = live ? __ldg(qrow + 2 * c + 1) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          const uint32_t w[8] = {v[2 * c].x,     v[2 * c].y,     v[2 * c].z,     v[2 * c].w,
+                                 v[2 * c + 1].x, v[2 * c + 1].y, v[2 * c + 1].z, v[2 * c + 1].w};
           uint32_t out[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             out[k] = e4m3x4_from_floats(
                 bf16_bits_to_float(w[2 * k] & 0xffff) * inv, bf16_bits_to_float(w[2 * k] >> 16) * inv,
                 bf16_bits_to_float(w[2 * k + 1] & 0xffff) * inv, bf16_bits_to_float(w[2 * k + 1] >> 16) * inv);
-          const uint32_t off = C::kOffQ + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(gbase + off) = make_uint4(out[0], out[1], out[2], out[3]);
+          *reinterpret_cast<uint4*>(gbase + qoff + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
+              make_uint4(out[0], out[1], out[2], out[3]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 v = live ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t off = C::kOffQ + (c >> 3) * C::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(gbase + off) = v;
-        }
+        for (int c = 0; c < 16; ++c)
+          *reinterpret_cast<uint4*>(gbase + qoff + (c >> 3) * C::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v[c];
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(C::kBarQ));
     }
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_col = t * kTok, o_col = 256 + t * kD;
     float scale = p.scale_log2;  // > 0, so max(x) * scale = max(x * scale)
     float out_scale = 1.f;
     if constexpr (FP8) {
@@ -300,17 +324,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       out_scale = __ldg(p.v_scale + h);
     }
     float m_used = neg_inf(), l = 0.f;
-    bool ok = true;
+    bool ok = active;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      const int s = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarSFull + s), (j >> 1) & 1, status, 9));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarSFull + t), j & 1, status, 9));
       if (!ok) break;
       tc_fence_after();
       float x[kTok];
       {
         uint32_t u[kTok / 32][32];
 #pragma unroll
-        for (int c = 0; c < kTok / 32; ++c) tmem_ld32(lane_addr + s * kTok + c * 32, u[c]);
+        for (int c = 0; c < kTok / 32; ++c) tmem_ld32(lane_addr + s_col + c * 32, u[c]);
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < kTok / 32; ++c)
@@ -348,38 +371,41 @@ __global__ void __launch_bounds__(kThreads, 2)
           sm[i & 7] += (a + b) + (c2 + d2);
           u[i] = e4m3x4_from_floats(a, b, c2, d2);
         }
-        tmem_st16(lane_addr + s * kTok, u);
+        tmem_st32(lane_addr + s_col, u);
       } else {
-        uint32_t u[kTok / 2];  // two bf16 probabilities per column
 #pragma unroll
-        for (int i = 0; i < kTok / 2; ++i) {
-          const float a = ex2(fmaf(x[2 * i], scale, neg_m));
-          const float b = ex2(fmaf(x[2 * i + 1], scale, neg_m));
-          sm[i & 7] += a + b;
-          u[i] = pack_bf16(a, b);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t u[32];  // two bf16 probabilities per column
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = ex2(fmaf(x[c * 64 + 2 * i], scale, neg_m));
+            const float b = ex2(fmaf(x[c * 64 + 2 * i + 1], scale, neg_m));
+            sm[i & 7] += a + b;
+            u[i] = pack_bf16(a, b);
+          }
+          tmem_st32(lane_addr + s_col + c * 32, u);
         }
-        tmem_st32(lane_addr + s * kTok, u);
       }
       l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds the products of tiles < j; wait for the last of them, then rescale this row
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarPvDone), (j - 1) & 1, status, 10));
+        // O_t holds the products of tiles < j; wait for the last of them, then rescale this row
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarPvDone + t), (j - 1) & 1, status, 10));
         if (ok) {
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < kD / 32; ++c) {
             uint32_t u[32];
-            tmem_ld32(lane_addr + kOCol + c * 32, u);
+            tmem_ld32(lane_addr + o_col + c * 32, u);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-            tmem_st32(lane_addr + kOCol + c * 32, u);
+            tmem_st32(lane_addr + o_col + c * 32, u);
           }
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarPFull + s));
+      mbar_arrive(bar(C::kBarPFull + t));
     }
     // epilogue: O / l -> fp32 partial row, log2-LSE
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarOFull), 0, status, 11));
@@ -391,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t u[32];
-        tmem_ld32(lane_addr + kOCol + c * 32, u);
+        tmem_ld32(lane_addr + o_col + c * 32, u);
         tmem_wait_ld();
         if (live) {
 #pragma unroll
@@ -403,20 +429,21 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (live) p.lse_pre[row] = m_used + __log2f(l);
       __threadfence();
     }
-    if (!ok) epilogue_failed = 1;
+    if (active && !ok) *failed = 1;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 10) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
   // arrive for every member of this row block (shared memory is free now: every MMA and
   // TMA copy of this CTA has completed); the arrival that completes a member merges it
-  if (!epilogue_failed) {
-    const int row0 = rb * kRows;
-    prefix_arrive_and_merge<kD>(p, members, h, row0, min(kRows, m_eff - row0), reinterpret_cast<int*>(gbase));
+  if (!*failed) {
+    const int n_rows = min(2 * kRows, m_eff - row_base);
+    __syncthreads();
+    prefix_arrive_and_merge<kD>(p, members, h, row_base, n_rows, reinterpret_cast<int*>(gbase));
   }
 }
 
@@ -460,6 +487,7 @@ cudaError_t launch_t(const StepParams& p, int num_items, cudaStream_t s) {
   e = make_pool_map(&vmap, p.v_pool, slots, p.hkv, rows, FP8);
   if (e != cudaSuccess) return e;
   constexpr uint32_t bytes = DenseCfg<FP8>::kSmemBytes;
+  static_assert(bytes <= 232448, "dense prefix CTA exceeds the shared memory of one SM");
   e = cudaFuncSetAttribute(prefix_dense_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   dim3 grid(num_items, p.hkv);

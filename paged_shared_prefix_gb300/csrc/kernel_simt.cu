@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
   // arrive once per (request, KV head) this CTA contributed to; the completing arrival merges
   __threadfence();
   __syncthreads();
-  __shared__ int flags[128];
+  __shared__ int flags[kDenseRows];  // one per member of a row block (G >= 1)
   if (mode == 0) {
     if (threadIdx.x == 0) flags[0] = (solo || arrive_is_last(p, b_suffix, h)) ? 1 : 0;
     __syncthreads();

@@ -30,7 +30,7 @@ constexpr int32_t kDefaultDenseThreshold = 1024;
 constexpr int32_t kSplitMinTiles = 4;
 constexpr int32_t kSplitCtasPerSm = 8;  // measured: 8 (split, head) CTAs per SM balance best
 constexpr int32_t kPrefixMinTiles = 4;
-constexpr int32_t kPrefixCtasPerSm = 2;  // dense and cascade prefix CTAs fit two per SM
+constexpr int32_t kPrefixCtasPerSm = 1;  // a dense prefix CTA fills an SM (all of tensor memory)
 
 thread_local std::string g_create_error;
 

@@ -17,7 +17,7 @@ namespace psp {
 constexpr int kMaxGroupSize = 8;        // query heads per KV head handled per CTA row set
 constexpr int kTileTokens = 64;         // partition granule (tokens)
 constexpr int kCascadeRows = 64;        // stacked query rows per cascade prefix CTA
-constexpr int kDenseRows = 128;         // stacked query rows per dense prefix CTA
+constexpr int kDenseRows = 256;         // stacked query rows per dense prefix CTA (two 128-row tiles)
 constexpr int kWorkspaceAlign = 256;
 
 // Device status codes written instead of faulting.

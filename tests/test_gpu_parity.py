@@ -239,13 +239,16 @@ def test_bounded_wait_reports_timeout_instead_of_hanging():
 
 
 DENSE = [
-    ("rows-3-blocks", dict(name="agent", batch=80, prefix_len=384, private_range=(1, 64))),
+    ("rows-2-blocks", dict(name="agent", batch=80, prefix_len=384, private_range=(1, 64))),
+    ("rows-exact-256", dict(name="agent", batch=64, prefix_len=256, private_range=(1, 32))),
+    ("rows-400", dict(name="agent", batch=100, prefix_len=320, private_range=(1, 32))),
     ("partial-tile", dict(name="agent", batch=40, prefix_len=208, private_range=(1, 40))),
     ("long-prefix", dict(name="agent", batch=33, prefix_len=2048 + 64, private_range=(1, 30))),
     ("ps128", dict(name="agent", batch=20, prefix_len=640, private_range=(1, 200), page_size=128)),
     ("ps1", dict(name="agent", batch=20, prefix_len=300, private_range=(1, 100), page_size=1)),
     ("g8", dict(name="agent", batch=24, prefix_len=512, private_range=(1, 50), num_q_heads=64)),
     ("fp8-2-blocks", dict(name="fp8_large", batch=20, prefix_len=640, private_range=(1, 60))),
+    ("fp8-3-tiles", dict(name="fp8_large", batch=40, prefix_len=448, private_range=(1, 30))),
     ("fp8-partial-tile", dict(name="fp8_large", batch=9, prefix_len=336, private_range=(1, 30))),
     ("fp8-g4-ps1", dict(name="fp8_large", batch=12, prefix_len=256, private_range=(1, 40), num_q_heads=32,
                         page_size=1)),
