@@ -9,7 +9,7 @@ kernel of the shared-prefix group (dense or cascade branch), the split-KV
 suffix kernel and the log-sum-exp merge, with the K/V pool, the queries and
 the uploaded plan resident in HBM.  The metric is device time per step and
 the achieved HBM bandwidth on the step's unique K/V bytes (a shared prefix
-page counts once).  L2 is flushed (a buffer of twice the L2 size is written)
+page counts once).  L2 is flushed (a buffer of twice the L2 size is written and read back)
 between timed steps, outside the timed events.
 
 Printed (rank 0, one JSON line): value = unique-KV GB/s over all ranks,
@@ -340,9 +340,16 @@ def main():
     step.upload(ws, stream)
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20)
     flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # write a buffer of twice the L2 size (evicts the step's data), then read it back so
+        # no dirty line is left whose write-back would land inside the next timed step
+        flush.fill_(1.0)
+        torch.sum(flush, dim=0, out=sink)
 
     def one(timed_events=None):
-        flush.fill_(1.0)
+        flush_l2()
         if timed_events:
             timed_events[0].record(stream)
         step.run(q, kp, vp, o, lse, ks, vs, stream)
@@ -412,7 +419,7 @@ def main():
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"f32": "f32", "bf16": "bf16", "fp8_e4m3": "fp8_e4m3"}[w.kv_dtype],
         "data": "synthetic",
-        "config": {"workload": describe(case), "l2": "flushed between steps (2x L2 buffer written, untimed)",
+        "config": {"workload": describe(case), "l2": "flushed between steps (2x L2 buffer written then read back, untimed)",
                    "parallelism": f"replicas x{world}", "token_flat": bool(args.token_flat),
                    "concurrent_prefix": concurrent},
         "unique_kv_bytes": ub, "paged_kv_bytes": paged_b,
@@ -432,7 +439,7 @@ def main():
         cstep.upload(cws, stream)
         ce = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
         for i in range(13):
-            flush.fill_(1.0)
+            flush_l2()
             if i >= 3:
                 ce[i - 3][0].record(stream)
             cstep.run(q, kp, vp, o, lse, ks, vs, stream)
@@ -456,7 +463,7 @@ def main():
         devt = step.tensors(qd, kp, vp, o, lse, ks, vs)
         e2e = []
         for i in range(3 + args.steps):
-            flush.fill_(1.0)
+            flush_l2()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             step.step_host(batch, qh, oh, lh, devt, ws, stream)

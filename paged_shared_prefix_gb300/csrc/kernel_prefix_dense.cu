@@ -7,31 +7,36 @@
 // One CTA = 256 stacked query rows of one KV head (rows R = member * G + j, in
 // two 128-row tiles A and B) x one chunk of the shared prefix, in 128-token
 // K/V tiles that both query tiles share:
-//   warps 8 and 9 (producers, keys and values) TMA-load each K and V tile page
-//                      by page from the paged pool (3-D tensor map [slot][kv
-//                      head][d], boxes of up to 64 tokens x 128 bytes, 128-byte
-//                      swizzle) into rings of 2 (bf16) or 4 (e4m3) stages;
-//   warp 10 (MMA)      one thread issues, per K/V tile j,
-//                        S_A = Q_A K_j^T, S_B = Q_B K_j^T       (M=128, N=128)
-//                        O_A += P_A V_j, S_A(j+1), O_B += P_B V_j, S_B(j+1)
-//                      with fp32 accumulators in tensor memory (S_A, S_B, O_A,
-//                      O_B: all 512 columns) and P read from tensor memory; in
-//                      this order the tensor core runs one tile's products while
-//                      the other tile's softmax warps work;
-//   warps 0-3 / 4-7    (softmax, tiles A / B) one thread per row: read the S
-//                      row, online softmax with lazy rescaling (the running max
-//                      only moves when it grows by more than 2^8, and O is then
-//                      rescaled in tensor memory), write P back over S, and at
-//                      the end normalise O and write the fp32 partial row and
-//                      its log2-LSE.
+//   warp 8          (producer) TMA-loads K and V tiles page by page from the
+//                   paged pool (3-D tensor maps [slot][kv head][d], boxes of up to
+//                   64 tokens x 128 bytes, 128-byte swizzle): K_0 into a slot of
+//                   its own, then ring stage j holds V_j and K_{j+1}, the operands
+//                   that one issue step consumes, behind a single barrier;
+//   warp 9          (MMA) one thread issues, per K/V tile j and query tile t,
+//                     O_t += P_t V_j, then S_t = Q_t K_{j+1}^T  (M=128, N=128)
+//                   with fp32 accumulators in tensor memory (S_A, S_B, O_A, O_B:
+//                   all 512 columns) and P read from tensor memory where the
+//                   softmax wrote it over S; tile A's products run while tile B's
+//                   softmax works and the other way round;
+//   warps 0-3 / 4-7 (softmax, tiles A / B) one thread per row: read the S row,
+//                   online softmax, write P back over S, and at the end normalise O
+//                   and write the fp32 partial row and its log2-LSE.
+// The MMA warp runs its waits as a whole warp with one lane issuing (measured on
+// GB300: a completed mbarrier costs 100-200 cycles to poll, more from one lane
+// than from a whole warp, and one lane issuing while the rest of its warp polls
+// another barrier is slowed several-fold), and one barrier covers V_j and
+// K_{j+1}, so each issue step has a single wait for its operands.
+// The online softmax rescales lazily: the running max only moves when it grows
+// by more than 2^8, and O is then rescaled in tensor memory.
 // fp8-e4m3 caches use kind::f8f6f4: the e4m3 K/V tiles are loaded as stored,
 // each query row is quantised to e4m3 with its own scale amax/448 (folded, with
 // the per-head key scale, into the softmax scale), and P is written to tensor
 // memory as e4m3 (P <= 2^8 under the lazy bound, inside the e4m3 range); the
 // value scale is applied to the normalised output.
-// Every mbarrier wait is bounded; on timeout the kernel records the site in the
-// device status word and unwinds (draining its own TMA copies, freeing its
-// tensor memory) instead of hanging.
+// Every mbarrier wait is bounded and also watches a CTA-wide abort flag: on a
+// timeout the kernel records the site in the device status word, raises the flag
+// so that every other role stops waiting, and unwinds (draining its own TMA
+// copies and tensor-core products, freeing its tensor memory) instead of hanging.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -49,11 +54,13 @@ namespace {
 using namespace dev;
 using namespace sm100;
 
-constexpr int kRows = 128;                 // UMMA M (stacked query rows per tile)
-constexpr int kTok = 128;                  // tokens per K/V tile (N of S, K of PV)
-constexpr int kD = 128;                    // head dim (K of S, N of PV)
-constexpr int kThreads = 352;              // warps 0-7 softmax, 8 K producer, 9 V producer, 10 MMA
-constexpr uint32_t kTmemCols = 512;        // S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512)
+constexpr int kRows = 128;                   // UMMA M (stacked query rows per tile)
+constexpr int kTok = 128;                    // tokens per K/V tile (N of S, K of PV)
+constexpr int kD = 128;                      // head dim (K of S, N of PV)
+constexpr int kGroup = 128;                  // threads of one softmax group (one per tile row)
+constexpr int kWarpP = 8, kWarpM = 9;        // producer and MMA warps
+constexpr int kThreads = 2 * kGroup + 64;
+constexpr uint32_t kTmemCols = 512;          // S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512)
 constexpr float kRescaleLog2 = 8.f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -65,7 +72,7 @@ __device__ __forceinline__ float ex2(float x) {
 template <bool FP8>
 struct DenseCfg {
   static constexpr uint32_t kElem = FP8 ? 1 : 2;
-  static constexpr int kStages = FP8 ? 4 : 2;                // K and V ring depth
+  static constexpr int kStages = FP8 ? 5 : 2;                // ring depth, stages of (V_j, K_{j+1})
   static constexpr uint32_t kTileBytes = kTok * kD * kElem;  // one K or V tile
   static constexpr uint32_t kQBytes = kRows * kD * kElem;    // one query tile
   static constexpr uint32_t kHalves = FP8 ? 1 : 2;           // 128-byte column blocks of a row
@@ -73,21 +80,51 @@ struct DenseCfg {
   static constexpr uint32_t kQHalf = kQBytes / kHalves;
   static constexpr int kBoxElems = 128 / kElem;              // d elements per TMA box row
   static constexpr int kKStep = 32 / kElem;                  // K elements per MMA instruction
-  static constexpr uint32_t kOffQ = 0;                       // Q_A, Q_B
-  static constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
-  static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // barriers: q_ready, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], pv_done[2], o_full, final
-  static constexpr int kBarQ = 0, kBarKFull = 1, kBarKEmpty = 1 + kStages, kBarVFull = 1 + 2 * kStages,
-                       kBarVEmpty = 1 + 3 * kStages, kBarSFull = 1 + 4 * kStages, kBarPFull = 3 + 4 * kStages,
-                       kBarPvDone = 5 + 4 * kStages, kBarOFull = 7 + 4 * kStages, kBarFinal = 8 + 4 * kStages,
-                       kNumBars = 9 + 4 * kStages;
+  static constexpr uint32_t kOffQ = 0;                       // Q_A, Q_B (each reused as its tile's epilogue staging)
+  static constexpr uint32_t kOffK0 = kOffQ + 2 * kQBytes;   // K_0
+  static constexpr uint32_t kOffRing = kOffK0 + kTileBytes;  // stage s: V at +0, K at +kTileBytes
+  static constexpr uint32_t kStageBytes = 2 * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffRing + kStages * kStageBytes;
+  // barriers: k0_full, full[S], empty[S], q_full[2], s_full[2], p_full[2], o_full[2], drain
+  static constexpr int kBarK0 = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarQFull = 1 + 2 * kStages,
+                       kBarSFull = kBarQFull + 2, kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2,
+                       kBarDrain = kBarOFull + 2, kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffTmem = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kOffFlag = kOffTmem + 8;
-  static constexpr uint32_t kSmemBytes = kOffFlag + 8 + 1024;  // + alignment slack
+  static constexpr uint32_t kOffAbort = kOffTmem + 8;       // int: a role gave up (CTA-wide)
+  static constexpr uint32_t kOffAny = kOffAbort + 8;        // int: some member must arrive
+  static constexpr uint32_t kOffFlags = kOffAny + 8;        // int flags[2 * kRows]: member must arrive
+  static constexpr uint32_t kSmemBytes = kOffFlags + 2 * kRows * 4 + 1024;  // + alignment slack
   static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(kRows, kTok, false) : idesc_f16(kRows, kTok, 1, false);
   static constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3(kRows, kD, true) : idesc_f16(kRows, kD, 1, true);
+  static_assert(4 * 32 * 32 * 4 <= kQBytes, "epilogue staging (4 warps x 32 x 32 fp32) must fit in one Q tile");
 };
+
+// TMA loads of one 128-token tile (tile j of the chunk [t0, t1)) into dst, completing on bar.
+template <uint32_t kHalf, uint32_t kHalves, int kBoxElems>
+__device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, uint32_t bar, const int32_t* list,
+                                          int shift, int h, int t0, int t1, int j, int num_slots) {
+  const int mask = (1 << shift) - 1;
+  const int br = min(1 << shift, 64);  // rows per TMA box; boxes never straddle a page
+  for (int r = 0; r < kTok; r += br) {
+    const int tok = t0 + j * kTok + r;
+    const int slot = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
+#pragma unroll
+    for (uint32_t hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * kHalf + r * 128, map, hf * kBoxElems, h, slot, bar);
+  }
+}
+
+// Bounded wait that also gives up as soon as another role of the CTA has given up.
+// On its own timeout it records the site and raises the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status,
+                                              int site) {
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 31 && *abort) return false;
+  }
+  atomicCAS(status, 0, kDevTimeout | (site << 8));
+  *abort = 1;
+  return false;
+}
 
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -95,14 +132,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap vmap, int num_slots) {
   using C = DenseCfg<FP8>;
   constexpr int NS = C::kStages;
-  constexpr uint32_t kTileBytes = C::kTileBytes;
-  constexpr uint32_t kHalf = C::kHalf;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   auto bar = [&](int i) { return base + C::kOffBar + 8u * i; };
-  volatile int* failed = reinterpret_cast<volatile int*>(gbase + C::kOffFlag);
+  volatile int* abort = reinterpret_cast<volatile int*>(gbase + C::kOffAbort);
+  volatile int* any_arrive = reinterpret_cast<volatile int*>(gbase + C::kOffAny);
+  int* flags = reinterpret_cast<int*>(gbase + C::kOffFlags);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -116,29 +153,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.group;
   const int m_eff = p.group_m_eff[g];
   const int row_base = rb * 2 * kRows;
-  const bool tile_b = row_base + kRows < m_eff;  // tile B holds live rows
+  const int n_rows = min(2 * kRows, m_eff - row_base);
+  const bool tile_b = n_rows > kRows;  // tile B holds live rows
   const int32_t* members = p.group_members + p.group_member_indptr[g];
   int32_t* status = p.status;
 
   if (threadIdx.x == 0) {
-    *failed = 0;
-    mbar_init(bar(C::kBarQ), tile_b ? 256 : 128);
+    *abort = n_tiles > 0 ? 0 : 1;
+    *any_arrive = 0;
+    if (n_tiles <= 0) atomicCAS(status, 0, kDevTimeout | (12 << 8));  // never planned: empty chunk
+    mbar_init(bar(C::kBarK0), 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(bar(C::kBarKFull + s), 1);
-      mbar_init(bar(C::kBarKEmpty + s), 1);
-      mbar_init(bar(C::kBarVFull + s), 1);
-      mbar_init(bar(C::kBarVEmpty + s), 1);
+      mbar_init(bar(C::kBarFull + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarQFull + t), kGroup / 32);  // one arrival per warp
       mbar_init(bar(C::kBarSFull + t), 1);
-      mbar_init(bar(C::kBarPFull + t), 128);
-      mbar_init(bar(C::kBarPvDone + t), 1);
+      mbar_init(bar(C::kBarPFull + t), kGroup / 32);
+      mbar_init(bar(C::kBarOFull + t), 1);
     }
-    mbar_init(bar(C::kBarOFull), 1);
-    mbar_init(bar(C::kBarFinal), 1);
+    mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
   }
-  if (warp == 10) {
+  if (warp == kWarpP) {
     tmem_alloc(base + C::kOffTmem, kTmemCols);
     tmem_relinquish();
   }
@@ -146,16 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kOffTmem);
+  const bool run = !*abort;
 
-  if (warp == 8 || warp == 9) {
-    // ------------------------------------------------- producers: warp 8 keys, warp 9 values
-    if (lane == 0) {
-      const bool is_v = warp == 9;
-      const CUtensorMap* map = is_v ? &vmap : &kmap;
-      prefetch_tmap(map);
-      const int full0 = is_v ? C::kBarVFull : C::kBarKFull;
-      const int empty0 = is_v ? C::kBarVEmpty : C::kBarKEmpty;
-      const uint32_t ring = base + (is_v ? C::kOffV : C::kOffK);
+  if (warp == kWarpP) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && run) {
       const int32_t* list;
       int shift;
       if (p.token_flat) {
@@ -165,111 +198,122 @@ __global__ void __launch_bounds__(kThreads, 1)
         list = p.group_page_indices + p.group_page_indptr[g];
         shift = p.page_shift;
       }
-      const int mask = (1 << shift) - 1;
-      const int br = min(1 << shift, 64);  // rows per TMA box; boxes never straddle a page
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
+      mbar_arrive_tx(bar(C::kBarK0), C::kTileBytes);
+      load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&kmap, base + C::kOffK0, bar(C::kBarK0), list, shift, h, t0, t1,
+                                                    0, num_slots);
       int issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % NS;
-        if (j >= NS && !mbar_wait(bar(empty0 + s), ((j / NS) - 1) & 1, status, is_v ? 2 : 1)) break;
-        mbar_arrive_tx(bar(full0 + s), kTileBytes);
-        const uint32_t dst = ring + s * kTileBytes;
-        for (int r = 0; r < kTok; r += br) {
-          const int tok = t0 + j * kTok + r;
-          const int slot = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
-#pragma unroll
-          for (uint32_t hf = 0; hf < C::kHalves; ++hf)
-            tma_load_3d(dst + hf * kHalf + r * 128, map, hf * C::kBoxElems, h, slot, bar(full0 + s));
-        }
+        const int st = j % NS;
+        if (j >= NS && !wait_or_abort(bar(C::kBarEmpty + st), ((j / NS) - 1) & 1, abort, status, 1)) break;
+        const bool more = j + 1 < n_tiles;
+        const uint32_t full = bar(C::kBarFull + st), dst = base + C::kOffRing + st * C::kStageBytes;
+        mbar_arrive_tx(full, more ? 2 * C::kTileBytes : C::kTileBytes);
+        load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&vmap, dst, full, list, shift, h, t0, t1, j, num_slots);
+        if (more)
+          load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&kmap, dst + C::kTileBytes, full, list, shift, h, t0, t1,
+                                                        j + 1, num_slots);
         issued = j + 1;
       }
-      // drain: the last load issued on each stage must have landed before the CTA may exit
-      for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(bar(full0 + j % NS), (j / NS) & 1, status, 3);
+      // drain: every load issued must have landed before the CTA may exit (plain bounded waits)
+      mbar_wait(bar(C::kBarK0), 0, status, 3);
+      for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(bar(C::kBarFull + j % NS), (j / NS) & 1, status, 3);
     }
-  } else if (warp == 10) {
-    // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
-      bool ok = mbar_wait(bar(C::kBarQ), 0, status, 4);
-      tc_fence_after();
-      // S_t = Q_t K_j^T into the S columns of tile t
-      auto issue_s = [&](int t, int j) {
-        const uint32_t kbase = base + C::kOffK + (j % NS) * kTileBytes;
+  } else if (warp == kWarpM) {
+    // -------------------------------------------------------------------- MMA
+    // The whole warp runs the loop and its waits; lane 0 issues.
+    if (run) {
+      // S_t = Q_t K^T (K tile at kbase) into the S columns of tile t
+      auto issue_s = [&](int t, uint32_t kbase) {
         const uint32_t qbase = base + C::kOffQ + t * C::kQBytes;
 #pragma unroll
         for (int ks = 0; ks < kD / C::kKStep; ++ks) {
           // K-major operands: 32 bytes of K per instruction inside a 128-byte swizzled row
           const uint32_t off = (ks & 3) * 32;
           const uint64_t adesc = sw128_desc(qbase + (ks >> 2) * C::kQHalf + off, 16, 1024);
-          const uint64_t bdesc = sw128_desc(kbase + (ks >> 2) * kHalf + off, 16, 1024);
+          const uint64_t bdesc = sw128_desc(kbase + (ks >> 2) * C::kHalf + off, 16, 1024);
           if constexpr (FP8) {
             mma_ss_f8(tmem + t * kTok, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
           } else {
             mma_ss(tmem + t * kTok, adesc, bdesc, C::kIdescS, ks > 0 ? 1u : 0u);
           }
         }
-        mma_commit(bar(C::kBarSFull + t));
       };
-      // O_t += P_t V_j (P from the S columns of tile t)
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t vbase = base + C::kOffV + (j % NS) * kTileBytes;
+      // O_t += P_t V (V tile at vbase; P from the S columns of tile t)
+      auto issue_pv = [&](int t, uint32_t vbase, bool accumulate) {
 #pragma unroll
         for (int ks = 0; ks < kTok / C::kKStep; ++ks) {
           // V is the MN-major B operand: K (tokens) advances by whole 128-byte rows
-          const uint64_t bdesc = sw128_desc(vbase + ks * C::kKStep * 128, kHalf, 1024);
-          const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+          const uint64_t bdesc = sw128_desc(vbase + ks * C::kKStep * 128, C::kHalf, 1024);
+          const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
           if constexpr (FP8) {
             mma_ts_f8(tmem + 256 + t * kD, tmem + t * kTok + ks * 8, bdesc, C::kIdescPV, acc);
           } else {
             mma_ts(tmem + 256 + t * kD, tmem + t * kTok + ks * 8, bdesc, C::kIdescPV, acc);
           }
         }
-        mma_commit(bar(C::kBarPvDone + t));
       };
-      if (ok && n_tiles > 0) {
-        ok = mbar_wait(bar(C::kBarKFull), 0, status, 7);
+      auto all = [](bool v) { return __all_sync(0xffffffffu, v); };
+      bool ok = all(wait_or_abort(bar(C::kBarQFull), 0, abort, status, 4)) &&
+                (!tile_b || all(wait_or_abort(bar(C::kBarQFull + 1), 0, abort, status, 4))) &&
+                all(wait_or_abort(bar(C::kBarK0), 0, abort, status, 7));
+      if (ok && lane == 0) {
         tc_fence_after();
-        if (ok) {
-          issue_s(0, 0);
-          if (tile_b) issue_s(1, 0);
-          mma_commit(bar(C::kBarKEmpty));
+        issue_s(0, base + C::kOffK0);
+        mma_commit(bar(C::kBarSFull));
+        if (tile_b) {
+          issue_s(1, base + C::kOffK0);
+          mma_commit(bar(C::kBarSFull + 1));
         }
       }
+      __syncwarp();
       for (int j = 0; j < n_tiles && ok; ++j) {
         const bool more = j + 1 < n_tiles;
-        ok = mbar_wait(bar(C::kBarPFull + 0), j & 1, status, 5) &&
-             mbar_wait(bar(C::kBarVFull + j % NS), (j / NS) & 1, status, 6);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(0, j);
-        if (more) {
-          ok = mbar_wait(bar(C::kBarKFull + (j + 1) % NS), ((j + 1) / NS) & 1, status, 7);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(0, j + 1);  // S_A's columns are reused only after PV_A(j) (issued above) has read P_A(j)
+        const int st = j % NS;
+        const uint32_t sb = base + C::kOffRing + st * C::kStageBytes;
+        for (int t = 0; t < (tile_b ? 2 : 1) && ok; ++t) {
+          ok = all(wait_or_abort(bar(C::kBarPFull + t), j & 1, abort, status, 5)) &&
+               (t > 0 || all(wait_or_abort(bar(C::kBarFull + st), (j / NS) & 1, abort, status, 6)));
+          if (ok && lane == 0) {
+            tc_fence_after();
+            issue_pv(t, sb, j > 0);
+            // S_t's columns are overwritten only after PV_t(j) (issued first) has read P_t(j)
+            if (more) issue_s(t, sb + C::kTileBytes);
+            mma_commit(bar((more ? C::kBarSFull : C::kBarOFull) + t));
+          }
+          __syncwarp();
         }
-        if (tile_b) {
-          ok = mbar_wait(bar(C::kBarPFull + 1), j & 1, status, 5);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(1, j);
-          if (more) issue_s(1, j + 1);
-        }
-        mma_commit(bar(C::kBarVEmpty + j % NS));
-        if (more) mma_commit(bar(C::kBarKEmpty + (j + 1) % NS));
+        if (ok && lane == 0) mma_commit(bar(C::kBarEmpty + st));
+        __syncwarp();
       }
-      mma_commit(bar(C::kBarOFull));
-      mma_commit(bar(C::kBarFinal));
-      mbar_wait(bar(C::kBarFinal), 0, status, 8);  // every MMA of this CTA has completed
+    }
+    if (lane == 0) {
+      // every product of the CTA has completed before the tensor memory is freed
+      mma_commit(bar(C::kBarDrain));
+      mbar_wait(bar(C::kBarDrain), 0, status, 8);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------- softmax warps
+  } else if (run && (warp < 4 || tile_b)) {
+    // ------------------------------------------------------- softmax warps (A: 0-3, B: 4-7)
     const int t = warp >> 2;                   // query tile (0 = A, 1 = B)
     const int r = threadIdx.x & 127;           // row of the tile = TMEM lane
     const int R = row_base + t * kRows + r;
     const bool live = R < m_eff;
-    const bool active = t == 0 || tile_b;
-    float q_scale = 1.f;  // fp8: this row's quantisation scale
-    if (active) {
+
+    // members of the block that must arrive on their (b, h) counter after the partials
+    // are written; looked up now, so the loads are off the kernel's tail
+    if (t == 0) {
+      for (int m = r; m < n_rows / G; m += kGroup) {
+        const int f = prefix_member_arrives(p, members[row_base / G + m]) ? 1 : 0;
+        flags[m] = f;
+        if (f) *any_arrive = 1;
+      }
+    }
+
+    // ---- Q tile t into shared memory (K-major, 128-byte swizzle), e4m3 per-row scaled for fp8
+    float q_scale = 1.f;
+    {
       const uint4* qrow = nullptr;
       if (live) {
         const int mem = R / G, jq = R - mem * G;
@@ -313,8 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(gbase + qoff + (c >> 3) * C::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v[c];
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar(C::kBarQ));
     }
+
+      // one arrival per warp: 32 arrivals on one barrier word serialise (measured ~500 cycles
+      // for a 128-thread group), one per warp after a warp sync does not
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kBarQFull + t));
+
+    const uint32_t s_full = bar(C::kBarSFull + t), o_full = bar(C::kBarOFull + t);
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = t * kTok, o_col = 256 + t * kD;
     float scale = p.scale_log2;  // > 0, so max(x) * scale = max(x * scale)
@@ -324,9 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       out_scale = __ldg(p.v_scale + h);
     }
     float m_used = neg_inf(), l = 0.f;
-    bool ok = active;
+    bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarSFull + t), j & 1, status, 9));
+      // S_t(j) complete, and with it every earlier product (one issuing thread), so O_t
+      // holds exactly the tiles < j.  __all_sync: the warp leaves the poll loop together
+      // before its aligned tcgen05 loads.
+      ok = __all_sync(0xffffffffu, wait_or_abort(s_full, j & 1, abort, status, 9));
       if (!ok) break;
       tc_fence_after();
       float x[kTok];
@@ -388,63 +441,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O_t holds the products of tiles < j; wait for the last of them, then rescale this row
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarPvDone + t), (j - 1) & 1, status, 10));
-        if (ok) {
-          tc_fence_after();
+        // rescale this warp's rows of O_t
 #pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
-            uint32_t u[32];
-            tmem_ld32(lane_addr + o_col + c * 32, u);
-            tmem_wait_ld();
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(lane_addr + o_col + c * 32, u);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-            tmem_st32(lane_addr + o_col + c * 32, u);
-          }
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(lane_addr + o_col + c * 32, u);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarPFull + t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kBarPFull + t));
     }
-    // epilogue: O / l -> fp32 partial row, log2-LSE
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarOFull), 0, status, 11));
+    if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(o_full, 0, abort, status, 11));
     if (ok) {
+      // ---- epilogue: O / l -> fp32 partial rows, log2-LSE.  Each warp transposes its 32 rows
+      // through 4 KB of its tile's Q area (free: every product of the group has completed) so
+      // that the global stores are whole 128-byte row segments.
       tc_fence_after();
-      const int64_t row = p.chunk_row_offset[ci] + static_cast<int64_t>(h) * m_eff + R;
-      float4* dst = live ? reinterpret_cast<float4*>(p.o_pre + row * kD) : nullptr;
+      const int wq = warp & 3;
+      float* stage = reinterpret_cast<float*>(gbase + C::kOffQ + t * C::kQBytes + wq * 4096);  // [32][32]
+      const int row0 = row_base + t * kRows + wq * 32;  // block row of lane 0
+      const int live_rows = min(32, m_eff - row0);
+      const int64_t grow0 = p.chunk_row_offset[ci] + static_cast<int64_t>(h) * m_eff + row0;
       const float inv = out_scale / l;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t u[32];
         tmem_ld32(lane_addr + o_col + c * 32, u);
         tmem_wait_ld();
-        if (live) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[c * 8 + i] = make_float4(__uint_as_float(u[4 * i]) * inv, __uint_as_float(u[4 * i + 1]) * inv,
-                                         __uint_as_float(u[4 * i + 2]) * inv, __uint_as_float(u[4 * i + 3]) * inv);
+        for (int q = 0; q < 8; ++q)  // 16-byte chunk q of this lane's row, XOR-swizzled by row
+          *reinterpret_cast<float4*>(stage + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+              make_float4(__uint_as_float(u[4 * q]) * inv, __uint_as_float(u[4 * q + 1]) * inv,
+                          __uint_as_float(u[4 * q + 2]) * inv, __uint_as_float(u[4 * q + 3]) * inv);
+        __syncwarp();
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 4) {  // four rows per instruction, eight lanes per row
+          const int row = k0 + (lane >> 3);
+          if (row < live_rows) {
+            const float4 val = *reinterpret_cast<const float4*>(stage + row * 32 + (((lane & 7) ^ (row & 7)) << 2));
+            *reinterpret_cast<float4*>(p.o_pre + (grow0 + row) * kD + c * 32 + (lane & 7) * 4) = val;
+          }
         }
+        __syncwarp();
       }
-      if (live) p.lse_pre[row] = m_used + __log2f(l);
+      if (live) p.lse_pre[grow0 + lane] = m_used + __log2f(l);
       __threadfence();
     }
-    if (active && !ok) *failed = 1;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 10) {
+  if (warp == kWarpP) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // arrive for every member of this row block (shared memory is free now: every MMA and
-  // TMA copy of this CTA has completed); the arrival that completes a member merges it
-  if (!*failed) {
-    const int n_rows = min(2 * kRows, m_eff - row_base);
-    __syncthreads();
-    prefix_arrive_and_merge<kD>(p, members, h, row_base, n_rows, reinterpret_cast<int*>(gbase));
-  }
+  // arrivals of the block's members whose (b, h) counters need them; the arrival that
+  // completes a member merges it (shared memory is free: every product and copy is done)
+  if (!*abort && *any_arrive) prefix_arrive_and_merge_flagged<kD>(p, members, h, row_base, n_rows, flags);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -119,6 +119,13 @@ __device__ __forceinline__ void store_final(const StepParams& p, int64_t row, in
   }
 }
 
+// Whether member b of a prefix row block must arrive on its (b, h) counter: every
+// request does, unless it has exactly one suffix split and the prefix kernels run
+// before the suffix kernel (that split then merges the prefix partials itself).
+__device__ __forceinline__ bool prefix_member_arrives(const StepParams& p, int b) {
+  return p.concurrent || p.split_indptr[b + 1] - p.split_indptr[b] != 1;
+}
+
 // Prefix kernels: after this CTA's partial rows [row0, row0 + n) of head h are
 // written by the calling warp group, arrive once per member whose G rows all lie
 // in the range and merge the members that this arrival completes.  Members with
@@ -133,8 +140,7 @@ __device__ __forceinline__ void prefix_arrive_and_merge(const StepParams& p, con
   const int n_members = n / G;  // row blocks hold whole members (G divides the block)
   for (int m = threadIdx.x; m < n_members; m += blockDim.x) {
     const int b = members[(row0 / G) + m];
-    const bool solo = !p.concurrent && p.split_indptr[b + 1] - p.split_indptr[b] == 1;
-    flags[m] = (!solo && arrive_is_last(p, b, h)) ? 1 : 0;
+    flags[m] = (prefix_member_arrives(p, b) && arrive_is_last(p, b, h)) ? 1 : 0;
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
@@ -144,6 +150,28 @@ __device__ __forceinline__ void prefix_arrive_and_merge(const StepParams& p, con
       const int R = row0 + rr;
       const int b = members[R / G];
       merge_row<D>(p, b, h * G + (R - (R / G) * G), lane);
+    }
+  }
+}
+
+// As prefix_arrive_and_merge, with flags[m] (m < n / G) already holding
+// prefix_member_arrives() for each member of the block, computed early so that
+// the loads are off the kernel's tail.  Called by every thread after a
+// __syncthreads() that follows the partial writes (each writer fenced its own).
+template <int D>
+__device__ __forceinline__ void prefix_arrive_and_merge_flagged(const StepParams& p, const int32_t* members, int h,
+                                                                int row0, int n, int* flags) {
+  const int G = p.group;
+  const int n_members = n / G;
+  for (int m = threadIdx.x; m < n_members; m += blockDim.x)
+    if (flags[m]) flags[m] = arrive_is_last(p, members[(row0 / G) + m], h) ? 1 : 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int rr = warp; rr < n; rr += nwarps) {
+    const int m = rr / G;
+    if (flags[m]) {
+      const int R = row0 + rr;
+      merge_row<D>(p, members[R / G], h * G + (R - (R / G) * G), lane);
     }
   }
 }

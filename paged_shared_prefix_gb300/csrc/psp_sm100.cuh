@@ -57,6 +57,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
   return mbar_wait_polls(bar, parity, status, site, 1u << 24);  // each poll may suspend briefly
 }
 
+// Named barrier over `nthreads` threads (whole warps) that also ORs a predicate
+// across them: every participant gets the same answer, so a warp group can agree
+// on giving up without any thread waiting for one that has left.
+__device__ __forceinline__ bool group_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "setp.ne.u32 p, %1, 0;\n"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n"
+      "selp.u32 %0, 1, 0, q;\n"
+      "}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// Named barrier `id` completing when `nthreads` threads have arrived: sync waits for
+// it, arrive only counts (a producer/consumer hand-off between warp groups).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("barrier.cta.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("barrier.cta.arrive %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
