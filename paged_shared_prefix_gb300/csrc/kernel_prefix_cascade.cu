@@ -46,10 +46,11 @@ __global__ void __launch_bounds__(NW * 32) prefix_cascade_kernel(const StepParam
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // an item's row block may span several CTAs of NW * 16 rows each
-  const int item = blockIdx.x / ctas_per_item;
+  const int h = blockIdx.x % p.hkv;  // KV head fastest (neighbouring heads' rows are adjacent)
+  const int cta = blockIdx.x / p.hkv;
+  const int item = cta / ctas_per_item;
   const int ci = item_chunk[item];
-  const int rb = item_rb[item] * ctas_per_item + (blockIdx.x - item * ctas_per_item);
-  const int h = blockIdx.y;
+  const int rb = item_rb[item] * ctas_per_item + (cta - item * ctas_per_item);
   const int g = p.chunk_group[ci];
   const int t0 = p.chunk_begin[ci];
   const int t1 = p.chunk_end[ci];
@@ -308,7 +309,7 @@ cudaError_t launch_t(const StepParams& p, const int32_t* chunks, const int32_t* 
   auto kern = prefix_cascade_kernel<KV, D, NW, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(n * per_item, p.hkv);
+  const int grid = n * per_item * p.hkv;
   kern<<<grid, NW * 32, bytes, s>>>(p, chunks, rbs, per_item);
   return cudaGetLastError();
 }

@@ -143,9 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ci = p.item_chunk_dense[blockIdx.x];
-  const int rb = p.item_rb_dense[blockIdx.x];  // 256-row block
-  const int h = blockIdx.y;
+  const int h = blockIdx.x % p.hkv;  // KV head fastest (neighbouring heads' rows are adjacent)
+  const int item = blockIdx.x / p.hkv;
+  const int ci = p.item_chunk_dense[item];
+  const int rb = p.item_rb_dense[item];  // 256-row block
   const int g = p.chunk_group[ci];
   const int t0 = p.chunk_begin[ci];
   const int t1 = p.chunk_end[ci];
@@ -549,7 +550,7 @@ cudaError_t launch_t(const StepParams& p, int num_items, cudaStream_t s) {
   static_assert(bytes <= 232448, "dense prefix CTA exceeds the shared memory of one SM");
   e = cudaFuncSetAttribute(prefix_dense_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(num_items, p.hkv);
+  const int grid = num_items * p.hkv;
   prefix_dense_kernel<FP8><<<grid, kThreads, bytes, s>>>(p, kmap, vmap, static_cast<int>(slots));
   return cudaGetLastError();
 }

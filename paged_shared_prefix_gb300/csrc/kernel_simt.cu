@@ -29,7 +29,8 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
   __shared__ float vs[kTok][D];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
+  const int h = blockIdx.x % p.hkv;  // KV head fastest (neighbouring heads' rows are adjacent)
+  const int item = blockIdx.x / p.hkv;
   const int G = p.group;
   const float* kpool = static_cast<const float*>(p.k_pool);
   const float* vpool = static_cast<const float*>(p.v_pool);
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
   const int32_t* members = nullptr;
   int row0 = 0;
   if (mode == 0) {  // suffix split
-    const int split = blockIdx.x;
+    const int split = item;
     b_suffix = p.split_req[split];
     t0 = p.split_begin[split];
     t1 = p.split_end[split];
@@ -56,7 +57,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
     n_rows = G;
     out_base = (static_cast<int64_t>(split) * p.hkv + h) * G;
   } else {  // prefix chunk x row block
-    const int ci = item_chunk[blockIdx.x];
+    const int ci = item_chunk[item];
     const int g = p.chunk_group[ci];
     t0 = p.chunk_begin[ci];
     t1 = p.chunk_end[ci];
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
       list = p.group_page_indices + p.group_page_indptr[g];
       shift = p.page_shift;
     }
-    row0 = item_rb[blockIdx.x] * rows_per_block;
+    row0 = item_rb[item] * rows_per_block;
     n_rows = min(rows_per_block, m_eff - row0);
     out_base = p.chunk_row_offset[ci] + static_cast<int64_t>(h) * m_eff + row0;
   }
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
 
 cudaError_t launch_simt(const StepParams& p, int mode, int n, const int32_t* chunks, const int32_t* rbs, int rows,
                         cudaStream_t s) {
-  dim3 grid(n, p.hkv);
+  const int grid = n * p.hkv;
   if (p.head_dim == 128) {
     simt_kernel<128><<<grid, kWarps * 32, 0, s>>>(p, mode, chunks, rbs, rows);
   } else {

@@ -49,8 +49,10 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
-  const int h = blockIdx.y;
+  // one-dimensional grid, KV head fastest: the Hkv CTAs of a split run side by side, so
+  // the heads' rows of each token (adjacent in the pool) are read at about the same time
+  const int h = blockIdx.x % p.hkv;
+  const int split = blockIdx.x / p.hkv;
   const int b = p.split_req[split];
   const int t0 = p.split_begin[split];
   const int t1 = p.split_end[split];
@@ -131,18 +133,32 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     out_scale = __ldg(p.v_scale + h);
   }
 
-  // -------- asynchronous gather of one 16-token sub-tile (K and V) into ring stage i % NST
-  auto issue = [&](int i) {
+  // -------- asynchronous gather of one 16-token sub-tile (K and V) into ring stage i % NST.
+  // The block-table entries of a sub-tile's rows are loaded one sub-tile ahead of its
+  // copies (load_pages), so no copy waits on a dependent table load: the copies are
+  // asm statements with a memory clobber, which keeps the compiler from hoisting the
+  // next row's table load above the previous row's copy.
+  constexpr int kRowsPerPass = 32 / C::kChunks;
+  constexpr int kRowIters = 16 / kRowsPerPass;
+  const int mask = (1 << shift) - 1;
+  auto load_pages = [&](int i, int32_t (&pg)[kRowIters]) {
+    const int tb = t0 + (warp + i * NW) * 16;
+#pragma unroll
+    for (int k = 0; k < kRowIters; ++k) {
+      const int t = tb + lane / C::kChunks + k * kRowsPerPass;
+      pg[k] = t < t1 ? __ldg(list + (t >> shift)) : -1;
+    }
+  };
+  auto issue = [&](int i, const int32_t (&pg)[kRowIters]) {
     const int tb = t0 + (warp + i * NW) * 16;
     unsigned char* kdst = ring + (i % NST) * C::kStageBytes;
-    constexpr int kRowsPerPass = 32 / C::kChunks;
     const int c = lane % C::kChunks;
 #pragma unroll
-    for (int k = 0; k < 16 / kRowsPerPass; ++k) {
+    for (int k = 0; k < kRowIters; ++k) {
       const int r = lane / C::kChunks + k * kRowsPerPass;
-      const int t = tb + r;
-      const bool valid = t < t1;
-      const int64_t off = valid ? slot_of(list, t, shift) * row_stride + c * 16 : 0;
+      const bool valid = pg[k] >= 0;
+      const int64_t slot = (static_cast<int64_t>(pg[k]) << shift) | ((tb + r) & mask);
+      const int64_t off = valid ? slot * row_stride + c * 16 : 0;
       const uint32_t d = smem_u32(kdst + r * C::kRowBytes + swz<C::kChunks>(r, c) * 16);
       cp_async_16(d, kbase + off, valid);
       cp_async_16(d + C::kTileBytes, vbase + off, valid);
@@ -155,45 +171,63 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   float m0 = neg_inf(), m1 = neg_inf();  // running max of query heads 2c, 2c+1 (log2 domain)
   float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
 
+  int32_t pages[kRowIters];
 #pragma unroll
   for (int i = 0; i < NST - 1; ++i) {
-    if (i < my_n) issue(i);
+    if (i < my_n) {
+      load_pages(i, pages);
+      issue(i, pages);
+    }
     cp_async_commit();
   }
 
   for (int i = 0; i < my_n; ++i) {
+    const int nx = i + NST - 1;
+    if (nx < my_n) load_pages(nx, pages);  // in flight while this sub-tile is computed
     cp_async_wait<NST - 2>();
     __syncwarp();
     const unsigned char* kt = ring + (i % NST) * C::kStageBytes;
     const unsigned char* vt = kt + C::kTileBytes;
 
-    // ---- S^T (16 tokens x 8 query heads)
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- fragment loads of K (A operand of S^T) and V (A operand of O^T) for the whole
+    // sub-tile first, so their shared-memory latencies overlap each other and the softmax
+    // (the loads are volatile asm: the compiler keeps them in source order)
+    constexpr int kKFrag = (KV == PSP_KV_BF16) ? D / 16 : D / 32;
+    constexpr int kVFrag = (KV == PSP_KV_BF16) ? C::kMTiles : D / 32;
+    uint32_t kf[kKFrag][4], vf[kVFrag][4];
     {
       const int j = lane >> 3;
-      const int row = (lane & 7) + (j & 1) * 8;
+      const int krow = (lane & 7) + (j & 1) * 8;
+      const int vrow = (lane & 7) + (j >> 1) * 8;
+#pragma unroll
+      for (int f = 0; f < kKFrag; ++f)
+        ldsm_x4(kf[f], smem_u32(kt + krow * C::kRowBytes + swz<C::kChunks>(krow, 2 * f + (j >> 1)) * 16));
+#pragma unroll
+      for (int f = 0; f < kVFrag; ++f)
+        ldsm_x4_t(vf[f], smem_u32(vt + vrow * C::kRowBytes + swz<C::kChunks>(vrow, 2 * f + (j & 1)) * 16));
+    }
+
+    // ---- S^T (16 tokens x 8 query heads); two accumulators halve the dependent mma chain
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      float s2[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (KV == PSP_KV_BF16) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          uint32_t a[4];
-          const int ch = 2 * ks + (j >> 1);
-          ldsm_x4(a, smem_u32(kt + row * C::kRowBytes + swz<C::kChunks>(row, ch) * 16));
-          mma_bf16(s, a, qf[ks][0], qf[ks][1]);
-        }
+        for (int ks = 0; ks < D / 16; ++ks) mma_bf16((ks & 1) ? s2 : s, kf[ks], qf[ks][0], qf[ks][1]);
       } else {
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk) {
-          uint32_t r[4];
-          const int ch = 2 * kk + (j >> 1);
-          ldsm_x4(r, smem_u32(kt + row * C::kRowBytes + swz<C::kChunks>(row, ch) * 16));
+          const uint32_t* r = kf[kk];
           const uint32_t a0[4] = {e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[1]), e4m3x2_to_f16x2(r[0] >> 16),
                                   e4m3x2_to_f16x2(r[1] >> 16)};
           const uint32_t a1[4] = {e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[3]), e4m3x2_to_f16x2(r[2] >> 16),
                                   e4m3x2_to_f16x2(r[3] >> 16)};
           mma_f16(s, a0, qf[2 * kk][0], qf[2 * kk][1]);
-          mma_f16(s, a1, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
+          mma_f16(s2, a1, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
         }
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[e] += s2[e];
     }
 
     // ---- online softmax on the fragments: rows = tokens (lane>>2, +8), cols = heads (2c, 2c+1)
@@ -231,40 +265,24 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     }
 
     // ---- O^T += V^T P^T
-    {
-      const int j = lane >> 3;
-      const int row = (lane & 7) + (j >> 1) * 8;
-      if constexpr (KV == PSP_KV_BF16) {
+    if constexpr (KV == PSP_KV_BF16) {
 #pragma unroll
-        for (int mt = 0; mt < C::kMTiles; ++mt) {
-          uint32_t a[4];
-          const int ch = 2 * mt + (j & 1);
-          ldsm_x4_t(a, smem_u32(vt + row * C::kRowBytes + swz<C::kChunks>(row, ch) * 16));
-          mma_bf16(o[mt], a, pb0, pb1);
-        }
-      } else {
+      for (int mt = 0; mt < C::kMTiles; ++mt) mma_bf16(o[mt], vf[mt], pb0, pb1);
+    } else {
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[4];
-          const int ch = 2 * cc + (j & 1);
-          ldsm_x4_t(r, smem_u32(vt + row * C::kRowBytes + swz<C::kChunks>(row, ch) * 16));
-          // each register: (token 2c: d 2p, 2p+1), (token 2c+1: d 2p, 2p+1); split even / odd d
-          const uint32_t ax[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, 0x20)),
-                                  e4m3x2_to_f16x2(__byte_perm(r[1], 0, 0x20)),
-                                  e4m3x2_to_f16x2(__byte_perm(r[2], 0, 0x20)),
-                                  e4m3x2_to_f16x2(__byte_perm(r[3], 0, 0x20))};
-          const uint32_t ay[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, 0x31)),
-                                  e4m3x2_to_f16x2(__byte_perm(r[1], 0, 0x31)),
-                                  e4m3x2_to_f16x2(__byte_perm(r[2], 0, 0x31)),
-                                  e4m3x2_to_f16x2(__byte_perm(r[3], 0, 0x31))};
-          mma_f16(o[2 * cc], ax, pb0, pb1);
-          mma_f16(o[2 * cc + 1], ay, pb0, pb1);
-        }
+      for (int cc = 0; cc < D / 32; ++cc) {
+        const uint32_t* r = vf[cc];
+        // each register: (token 2c: d 2p, 2p+1), (token 2c+1: d 2p, 2p+1); split even / odd d
+        const uint32_t ax[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, 0x20)), e4m3x2_to_f16x2(__byte_perm(r[1], 0, 0x20)),
+                                e4m3x2_to_f16x2(__byte_perm(r[2], 0, 0x20)), e4m3x2_to_f16x2(__byte_perm(r[3], 0, 0x20))};
+        const uint32_t ay[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, 0x31)), e4m3x2_to_f16x2(__byte_perm(r[1], 0, 0x31)),
+                                e4m3x2_to_f16x2(__byte_perm(r[2], 0, 0x31)), e4m3x2_to_f16x2(__byte_perm(r[3], 0, 0x31))};
+        mma_f16(o[2 * cc], ax, pb0, pb1);
+        mma_f16(o[2 * cc + 1], ay, pb0, pb1);
       }
     }
     __syncwarp();
-    const int nx = i + NST - 1;
-    if (nx < my_n) issue(nx);
+    if (nx < my_n) issue(nx, pages);
     cp_async_commit();
   }
   cp_async_wait<0>();
@@ -366,8 +384,7 @@ cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
   auto kern = suffix_kernel<KV, D, NW, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(num_splits, p.hkv);
-  kern<<<grid, NW * 32, bytes, s>>>(p);
+  kern<<<num_splits * p.hkv, NW * 32, bytes, s>>>(p);
   return cudaGetLastError();
 }
 
