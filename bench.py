@@ -5,19 +5,24 @@
                     [--impl reference]
 
 A step is one call of psp_run over the whole synthetic batch: the prefix
-kernel of the shared-prefix group (dense or cascade branch), the split-KV
-suffix kernel and the log-sum-exp merge, with the K/V pool, the queries and
-the uploaded plan resident in HBM.  The metric is device time per step and
-the achieved HBM bandwidth on the step's unique K/V bytes (a shared prefix
-page counts once).  L2 is flushed (a buffer of twice the L2 size is written and read back)
-between timed steps, outside the timed events.
+kernel of the shared-prefix group (dense or cascade branch, chosen by the
+dispatcher) and the split-KV suffix kernel, whose last arriving CTA per
+(request, KV head) performs the log-sum-exp merge, with the K/V pool, the
+queries and the uploaded plan resident in HBM.  The metric is device time per
+step and the achieved HBM bandwidth on the step's unique K/V bytes (a shared
+prefix page counts once).  L2 is flushed (a buffer of twice the L2 size is
+written and read back) between timed steps, outside the timed events.  The
+default workload is the Llama-3.1-8B-shaped layer without sharing (B=32,
+32/8 heads, bf16, contexts U[2048,4096], page size 16); --workload selects
+the shared-prefix batches.
 
 Printed (rank 0, one JSON line): value = unique-KV GB/s over all ranks,
 us_per_step, the dominant kernel's roofline, the oracle's CPU baseline, the
 end-to-end figure through psp_step_host with host buffers (plan, plan upload,
 query copy in, output copy out, every step), sampled SM clocks, the launch
-count, and for shared-prefix workloads the per-request paged comparator
-(every request reading the prefix through its own block table).
+count, a bare read of the same byte count for context (read_ceiling), and for
+shared-prefix workloads the per-request paged comparator (every request
+reading the prefix through its own block table).
 
 --impl reference times the fp64 CPU oracle (the reference arm of this path)
 on a bounded sample of the same workload, in the same metric and unit.
@@ -59,7 +64,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="agent", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="llama8b_noshare", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--page-size", type=int, default=None)
     ap.add_argument("--impl", default="psp", choices=["psp", "reference"])
     ap.add_argument("--seed", type=int, default=0)
@@ -71,6 +76,7 @@ def parse():
     ap.add_argument("--no-comparator", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-read-ceiling", action="store_true", help="skip the bare-read ceiling measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle CPU time for the baseline")
     ap.add_argument("--sweep-threshold", action="store_true",
                     help="time the dense and cascade prefix kernels over an M_eff sweep and report the refit threshold")
@@ -385,6 +391,25 @@ def main():
     ms, value = aggregate_replicas(statistics.mean(step_ms), ub, world, dev)
     launches = sum(len(v) for v in kern.values())
 
+    # ---- single-launch read ceiling: a bare read of as many bytes as the step's unique K/V
+    # (torch's sum kernel, L2 flushed the same way), for context beside the roofline peak
+    ceil = None
+    if not args.no_read_ceiling:
+        buf = torch.empty(ub // 4, dtype=torch.float32, device=dev).fill_(1.0)
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(8)]
+        for i in range(10):
+            flush_l2()
+            if i >= 2:
+                cev[i - 2][0].record(stream)
+            torch.sum(buf, dim=0, out=sink)
+            if i >= 2:
+                cev[i - 2][1].record(stream)
+        torch.cuda.synchronize()
+        cms = statistics.mean(a.elapsed_time(b) for a, b in cev)
+        ceil = {"gbs": buf.numel() * 4 / (cms * 1e-3) / 1e9, "bytes": int(buf.numel() * 4),
+                "how": "torch.sum over a float32 buffer of the unique K/V size, one launch, L2 flushed as for the step"}
+        del buf
+
     # ---- roofline of the dominant kernel
     pk, pk_src = peaks()
     kmean = {k: statistics.mean(v) for k, v in kern.items()}
@@ -425,7 +450,7 @@ def main():
         "unique_kv_bytes": ub, "paged_kv_bytes": paged_b,
         "hbm_frac_of_8tbs": value / world / 8000.0,
         "kernels_ms": kmean, "plan_us": statistics.median(t_plan) * 1e6,
-        "roofline": roof, "clocks": clk, "gpu_launches": launches, "wall_s": wall,
+        "roofline": roof, "read_ceiling": ceil, "clocks": clk, "gpu_launches": launches, "wall_s": wall,
         "plan": {k: info[k] for k in ("num_splits", "num_chunks", "suffix_ctas", "prefix_dense_ctas",
                                        "prefix_cascade_ctas", "dense_threshold", "num_sms")},
     }

@@ -23,9 +23,12 @@ using psp::PlanLayout;
 using psp::StepParams;
 
 // Dense/cascade threshold used when the configuration passes 0.  The pages fit
-// 1024 on A100 and ask for a refit per GPU ("GraniKV", section 3); this value
-// is the GB300 refit from the M_eff sweep of the benchmark.
-constexpr int32_t kDefaultDenseThreshold = 1024;
+// 1024 on A100 and ask for a refit per GPU ("GraniKV", section 3).  This value
+// is the GB300 refit: over a 4096-token prefix, 8 KV heads, GQA groups 1-8 and
+// M_eff from 16 to 4096, the tcgen05 dense kernel was never slower than the
+// cascade kernel (17.0 vs 18.4 us at M_eff 16, 86 vs 301 us at 4096), so the
+// smallest swept M_eff is the threshold.
+constexpr int32_t kDefaultDenseThreshold = 16;
 
 constexpr int32_t kSplitMinTiles = 4;
 constexpr int32_t kSplitCtasPerSm = 8;  // measured: 8 (split, head) CTAs per SM balance best
