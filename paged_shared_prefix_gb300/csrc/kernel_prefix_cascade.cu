@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(NW * 32) prefix_cascade_kernel(const StepParam
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // an item's row block may span several CTAs of NW * 16 rows each
+  pdl_launch_dependents();  // the step's suffix kernel may start filling free SMs
   const int h = blockIdx.x % p.hkv;  // KV head fastest (neighbouring heads' rows are adjacent)
   const int cta = blockIdx.x / p.hkv;
   const int item = cta / ctas_per_item;

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  dev::pdl_launch_dependents();  // the step's suffix kernel may start filling free SMs
   const int h = blockIdx.x % p.hkv;  // KV head fastest (neighbouring heads' rows are adjacent)
   const int item = blockIdx.x / p.hkv;
   const int ci = p.item_chunk_dense[item];

@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
   __shared__ float vs[kTok][D];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if (mode == 1) pdl_launch_dependents();  // prefix items: the suffix kernel may start early
   const int h = blockIdx.x % p.hkv;  // KV head fastest (neighbouring heads' rows are adjacent)
   const int item = blockIdx.x / p.hkv;
   const int G = p.group;

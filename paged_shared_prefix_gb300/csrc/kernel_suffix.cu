@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   const bool pre_smem = solo && n_chunks > 0 && n_chunks * G <= kPreRows;
   float* pre_o = reinterpret_cast<float*>(smem + NW * NST * C::kStageBytes);   // [chunk * G + j][D]
   float* pre_l = pre_o + kPreRows * D;                                           // [chunk * G + j]
-  if (pre_smem) {
+  auto prefetch_prefix = [&]() {
     const int m_eff = p.group_m_eff[g_req];
     const int prow = p.req_member[b] * G;
     constexpr int kRowChunks = D * 4 / 16;
@@ -101,7 +101,10 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
         cp_async_4(smem_u32(pre_l + c * G + j), p.lse_pre + row);
       }
     }
-  }
+  };
+  // launched as a dependent of the prefix kernel, the prefix partials are read only
+  // after that grid has completed (below, after this CTA's own stream)
+  if (pre_smem && !p.pdl) prefetch_prefix();
 
   // -------- query fragments: B operand of S^T = K Q^T (k = head dim, n = query head)
   const int qg = lane >> 2;  // query head within the group (B fragment column)
@@ -286,6 +289,14 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     cp_async_commit();
   }
   cp_async_wait<0>();
+  if (p.pdl) {
+    pdl_wait_primary();  // every prefix partial and prefix arrival of this step is complete
+    if (pre_smem) {
+      prefetch_prefix();
+      cp_async_commit();
+      cp_async_wait<0>();
+    }
+  }
 
   // -------- combine the warps' partial states through shared memory
   l0 = xor_sum<4, 16>(l0);
@@ -384,7 +395,18 @@ cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
   auto kern = suffix_kernel<KV, D, NW, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  kern<<<num_splits * p.hkv, NW * 32, bytes, s>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_splits * p.hkv);
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -737,17 +737,22 @@ psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
   const HostPlan& P = h->plan;
   if (P.B == 0) return PSP_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const StepParams p = make_params(h, t);
+  StepParams p = make_params(h, t);
   int slot = 0;
   h->recorded = 0;
   psp_status st;
+  const int nd = static_cast<int>(P.item_chunk_dense.size());
+  const int nc = static_cast<int>(P.item_chunk_cascade.size());
+  const bool fork = p.concurrent && (nd > 0 || nc > 0) && P.NS > 0;
+  // The suffix kernel follows the prefix kernel as a programmatic dependent: it streams
+  // its own K/V while the prefix kernel finishes and waits for it only before reading
+  // prefix partials.  Not with per-kernel timing (events between the launches) nor when
+  // the prefix runs on its own stream.
+  p.pdl = (!fork && !h->timing && (nd > 0 || nc > 0) && P.NS > 0) ? 1 : 0;
   if (p.token_flat) {
     st = timed_launch(h, s, "expand_kv_indices", slot, expand_entry, p, 0);
     if (st) return st;
   }
-  const int nd = static_cast<int>(P.item_chunk_dense.size());
-  const int nc = static_cast<int>(P.item_chunk_cascade.size());
-  const bool fork = p.concurrent && (nd > 0 || nc > 0) && P.NS > 0;
   cudaStream_t ps = s;  // stream of the prefix kernels
   cudaError_t e;
   if (fork) {

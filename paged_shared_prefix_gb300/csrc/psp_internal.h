@@ -36,6 +36,7 @@ struct StepParams {
   int32_t num_pages;
   int32_t token_flat;                // read K/V through kv_indices (page size 1 view)
   int32_t concurrent;                // prefix and suffix kernels may run at the same time
+  int32_t pdl;                       // the suffix kernel is a programmatic dependent of the prefix kernel
   float scale_log2;                  // log2(e) / sqrt(head_dim)
 
   // caller tensors (device)
