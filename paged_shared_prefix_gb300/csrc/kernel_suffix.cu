@@ -109,31 +109,63 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   // -------- query fragments: B operand of S^T = K Q^T (k = head dim, n = query head)
   const int qg = lane >> 2;  // query head within the group (B fragment column)
   const int qc = lane & 3;
-  uint32_t qf[D / 16][2];
+  // bf16: m16n8k16 fragments (two bf16 per register).  fp8: m16n8k32 e4m3 fragments (four
+  // codes per register: d = 32kk + 4c .. 4c+3 and 32kk + 16 + 4c .. +3), the query row
+  // quantised to e4m3 with its own scale amax/448, folded into the score scale below.
+  constexpr int kQFrag = (KV == PSP_KV_BF16) ? D / 16 : D / 32;
+  uint32_t qf[kQFrag][2];
+  float q_scale = 1.f;  // fp8: this lane's query head's scale
   {
     const bool live = qg < G;
     const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
                                 (static_cast<int64_t>(b) * p.hq + h * G + (live ? qg : 0)) * D;
+    if constexpr (KV == PSP_KV_BF16) {
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      if constexpr (KV == PSP_KV_BF16) {
+      for (int ks = 0; ks < D / 16; ++ks) {
         const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow + ks * 16);
         qf[ks][0] = live ? __ldg(q32 + qc) : 0u;
         qf[ks][1] = live ? __ldg(q32 + 4 + qc) : 0u;
-      } else {
-        // k-slots (2c, 2c+1) <- d = 4c, 4c+1 and (2c+8, 2c+9) <- d = 4c+2, 4c+3 (matches the
-        // byte order the fp8 key fragments arrive in)
-        const uint2 v = live ? __ldg(reinterpret_cast<const uint2*>(qrow + ks * 16 + 4 * qc)) : make_uint2(0u, 0u);
-        qf[ks][0] = pack_f16(bf16_bits_to_float(v.x & 0xffff), bf16_bits_to_float(v.x >> 16));
-        qf[ks][1] = pack_f16(bf16_bits_to_float(v.y & 0xffff), bf16_bits_to_float(v.y >> 16));
       }
+    } else {
+      uint2 v[kQFrag][2];
+#pragma unroll
+      for (int kk = 0; kk < kQFrag; ++kk)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+          v[kk][hf] = live ? __ldg(reinterpret_cast<const uint2*>(qrow + kk * 32 + hf * 16 + 4 * qc)) : make_uint2(0u, 0u);
+      float amax = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < kQFrag; ++kk)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint32_t w[2] = {v[kk][hf].x, v[kk][hf].y};
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_bits_to_float(w[e] & 0xffff)), fabsf(bf16_bits_to_float(w[e] >> 16))));
+        }
+      amax = xor_max<1, 2>(amax);  // the four lanes of this query head
+      q_scale = amax > 0.f ? amax / 448.f : 1.f;
+      const float inv = 1.f / q_scale;
+#pragma unroll
+      for (int kk = 0; kk < kQFrag; ++kk)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint2 w = v[kk][hf];
+          qf[kk][hf] = e4m3x4_from_floats(bf16_bits_to_float(w.x & 0xffff) * inv, bf16_bits_to_float(w.x >> 16) * inv,
+                                          bf16_bits_to_float(w.y & 0xffff) * inv, bf16_bits_to_float(w.y >> 16) * inv);
+        }
     }
   }
-  float score_scale = p.scale_log2;
+  float score_scale = p.scale_log2;  // per accumulator column below (sc0: head 2c, sc1: head 2c+1)
   float out_scale = 1.f;
   if constexpr (KV == PSP_KV_FP8) {
     score_scale *= __ldg(p.k_scale + h);
     out_scale = __ldg(p.v_scale + h);
+  }
+  float sc0 = score_scale, sc1 = score_scale;
+  if constexpr (KV == PSP_KV_FP8) {
+    sc0 *= __shfl_sync(0xffffffffu, q_scale, 8 * qc);      // lanes 4n.. hold query head n
+    sc1 *= __shfl_sync(0xffffffffu, q_scale, 8 * qc + 4);
   }
 
   // -------- asynchronous gather of one 16-token sub-tile (K and V) into ring stage i % NST.
@@ -174,119 +206,165 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   float m0 = neg_inf(), m1 = neg_inf();  // running max of query heads 2c, 2c+1 (log2 domain)
   float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
 
-  int32_t pages[kRowIters];
+  // Sub-tiles per iteration: bf16 takes one; fp8 takes two, so that the value product runs
+  // on e4m3 tensor cores with k = 32 tokens (m16n8k32) and the fp8 codes need no conversion.
+  constexpr int U = (KV == PSP_KV_FP8) ? 2 : 1;
+  static_assert(NST >= 2 * U, "the ring must hold the sub-tiles of one iteration plus those in flight");
+  // fp8: the running max is kept 8 below the true max, so P <= 2^8 (inside e4m3's range and
+  // clear of its subnormals); l carries the same factor, so O / l and m + log2(l) are exact.
+  constexpr float kPShift = (KV == PSP_KV_FP8) ? 8.f : 0.f;
+
+  int32_t pages[U][kRowIters];
 #pragma unroll
-  for (int i = 0; i < NST - 1; ++i) {
+  for (int i = 0; i < NST - U; ++i) {
     if (i < my_n) {
-      load_pages(i, pages);
-      issue(i, pages);
+      load_pages(i, pages[0]);
+      issue(i, pages[0]);
     }
     cp_async_commit();
   }
 
-  for (int i = 0; i < my_n; ++i) {
-    const int nx = i + NST - 1;
-    if (nx < my_n) load_pages(nx, pages);  // in flight while this sub-tile is computed
-    cp_async_wait<NST - 2>();
+  for (int i0 = 0; i0 < my_n; i0 += U) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int nx = i0 + NST - U + u;
+      if (nx < my_n) load_pages(nx, pages[u]);  // in flight while this iteration computes
+    }
+    cp_async_wait<NST - 2 * U>();
     __syncwarp();
-    const unsigned char* kt = ring + (i % NST) * C::kStageBytes;
-    const unsigned char* vt = kt + C::kTileBytes;
 
     // ---- fragment loads of K (A operand of S^T) and V (A operand of O^T) for the whole
-    // sub-tile first, so their shared-memory latencies overlap each other and the softmax
+    // iteration first, so their shared-memory latencies overlap each other and the softmax
     // (the loads are volatile asm: the compiler keeps them in source order)
     constexpr int kKFrag = (KV == PSP_KV_BF16) ? D / 16 : D / 32;
     constexpr int kVFrag = (KV == PSP_KV_BF16) ? C::kMTiles : D / 32;
-    uint32_t kf[kKFrag][4], vf[kVFrag][4];
-    {
+    uint32_t kf[U][kKFrag][4], vf[U][kVFrag][4];
+    const bool second = (U == 1) || (i0 + 1 < my_n);  // fp8: the iteration's second sub-tile exists
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const unsigned char* kt = ring + ((i0 + u) % NST) * C::kStageBytes;
+      const unsigned char* vt = kt + C::kTileBytes;
       const int j = lane >> 3;
       const int krow = (lane & 7) + (j & 1) * 8;
       const int vrow = (lane & 7) + (j >> 1) * 8;
 #pragma unroll
       for (int f = 0; f < kKFrag; ++f)
-        ldsm_x4(kf[f], smem_u32(kt + krow * C::kRowBytes + swz<C::kChunks>(krow, 2 * f + (j >> 1)) * 16));
+        ldsm_x4(kf[u][f], smem_u32(kt + krow * C::kRowBytes + swz<C::kChunks>(krow, 2 * f + (j >> 1)) * 16));
 #pragma unroll
       for (int f = 0; f < kVFrag; ++f)
-        ldsm_x4_t(vf[f], smem_u32(vt + vrow * C::kRowBytes + swz<C::kChunks>(vrow, 2 * f + (j & 1)) * 16));
+        ldsm_x4_t(vf[u][f], smem_u32(vt + vrow * C::kRowBytes + swz<C::kChunks>(vrow, 2 * f + (j & 1)) * 16));
+    }
+    if (!second) {
+      // no second sub-tile: its stage holds stale codes (possibly NaN), so its value
+      // fragments are zero and its scores are masked below
+#pragma unroll
+      for (int f = 0; f < kVFrag; ++f) vf[U - 1][f][0] = vf[U - 1][f][1] = vf[U - 1][f][2] = vf[U - 1][f][3] = 0u;
     }
 
-    // ---- S^T (16 tokens x 8 query heads); two accumulators halve the dependent mma chain
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-      float s2[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S^T (16 tokens x 8 query heads) per sub-tile; two accumulators halve the mma chain
+    float x[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (KV == PSP_KV_BF16) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) mma_bf16((ks & 1) ? s2 : s, kf[ks], qf[ks][0], qf[ks][1]);
+        for (int ks = 0; ks < D / 16; ++ks) mma_bf16((ks & 1) ? sb : sa, kf[u][ks], qf[ks][0], qf[ks][1]);
       } else {
+        // the ldmatrix fragments of 16 rows x 32 codes are the e4m3 A operand as they stand
 #pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk) {
-          const uint32_t* r = kf[kk];
-          const uint32_t a0[4] = {e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[1]), e4m3x2_to_f16x2(r[0] >> 16),
-                                  e4m3x2_to_f16x2(r[1] >> 16)};
-          const uint32_t a1[4] = {e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[3]), e4m3x2_to_f16x2(r[2] >> 16),
-                                  e4m3x2_to_f16x2(r[3] >> 16)};
-          mma_f16(s, a0, qf[2 * kk][0], qf[2 * kk][1]);
-          mma_f16(s2, a1, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
-        }
+        for (int kk = 0; kk < D / 32; ++kk) mma_e4m3((kk & 1) ? sb : sa, kf[u][kk], qf[kk][0], qf[kk][1]);
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[e] += s2[e];
+      // rows = tokens (lane>>2, +8), cols = heads (2c, 2c+1)
+      const int tb = t0 + (warp + (i0 + u) * NW) * 16;
+      const bool live = (u == 0) || second;
+      const bool v_lo = live && tb + (lane >> 2) < t1;
+      const bool v_hi = live && tb + (lane >> 2) + 8 < t1;
+      x[u][0] = v_lo ? (sa[0] + sb[0]) * sc0 : neg_inf();
+      x[u][1] = v_lo ? (sa[1] + sb[1]) * sc1 : neg_inf();
+      x[u][2] = v_hi ? (sa[2] + sb[2]) * sc0 : neg_inf();
+      x[u][3] = v_hi ? (sa[3] + sb[3]) * sc1 : neg_inf();
     }
 
-    // ---- online softmax on the fragments: rows = tokens (lane>>2, +8), cols = heads (2c, 2c+1)
-    const int tb = t0 + (warp + i * NW) * 16;
-    const bool v_lo = tb + (lane >> 2) < t1;
-    const bool v_hi = tb + (lane >> 2) + 8 < t1;
-    const float s0 = v_lo ? s[0] * score_scale : neg_inf();
-    const float s1 = v_lo ? s[1] * score_scale : neg_inf();
-    const float s2 = v_hi ? s[2] * score_scale : neg_inf();
-    const float s3 = v_hi ? s[3] * score_scale : neg_inf();
-    const float mx0 = xor_max<4, 16>(fmaxf(s0, s2));
-    const float mx1 = xor_max<4, 16>(fmaxf(s1, s3));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
-    const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
-    const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
-    l0 = l0 * a0 + p0 + p2;
-    l1 = l1 * a1 + p1 + p3;
-    m0 = mn0;
-    m1 = mn1;
+    // ---- online softmax over the iteration's tokens
+    float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
-    for (int mt = 0; mt < C::kMTiles; ++mt) {
-      o[mt][0] *= a0;
-      o[mt][1] *= a1;
-      o[mt][2] *= a0;
-      o[mt][3] *= a1;
+    for (int u = 1; u < U; ++u) {
+      mx0 = fmaxf(mx0, fmaxf(x[u][0], x[u][2]));
+      mx1 = fmaxf(mx1, fmaxf(x[u][1], x[u][3]));
     }
-    uint32_t pb0, pb1;  // P^T as the B operand (k = token, n = query head)
-    if constexpr (KV == PSP_KV_BF16) {
-      pb0 = movmatrix_t(pack_bf16(p0, p1));
-      pb1 = movmatrix_t(pack_bf16(p2, p3));
-    } else {
-      pb0 = movmatrix_t(pack_f16(p0, p1));
-      pb1 = movmatrix_t(pack_f16(p2, p3));
+    mx0 = xor_max<4, 16>(mx0) - kPShift;
+    mx1 = xor_max<4, 16>(mx1) - kPShift;
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    float pr[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      pr[u][0] = exp2f(x[u][0] - mn0);
+      pr[u][1] = exp2f(x[u][1] - mn1);
+      pr[u][2] = exp2f(x[u][2] - mn0);
+      pr[u][3] = exp2f(x[u][3] - mn1);
+    }
+    // fp8 (bound by its instruction count): rescale only when some running max moved,
+    // which stops once the maxima settle; bf16 (bound by memory) rescales every sub-tile
+    if (KV != PSP_KV_FP8 || __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+      l0 *= a0;
+      l1 *= a1;
+#pragma unroll
+      for (int mt = 0; mt < C::kMTiles; ++mt) {
+        o[mt][0] *= a0;
+        o[mt][1] *= a1;
+        o[mt][2] *= a0;
+        o[mt][3] *= a1;
+      }
+      m0 = mn0;
+      m1 = mn1;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      l0 += pr[u][0] + pr[u][2];
+      l1 += pr[u][1] + pr[u][3];
     }
 
     // ---- O^T += V^T P^T
     if constexpr (KV == PSP_KV_BF16) {
+      // P^T as the B operand (k = token, n = query head) by an in-register 8x8 transpose
+      const uint32_t pb0 = movmatrix_t(pack_bf16(pr[0][0], pr[0][1]));
+      const uint32_t pb1 = movmatrix_t(pack_bf16(pr[0][2], pr[0][3]));
 #pragma unroll
-      for (int mt = 0; mt < C::kMTiles; ++mt) mma_bf16(o[mt], vf[mt], pb0, pb1);
+      for (int mt = 0; mt < C::kMTiles; ++mt) mma_bf16(o[mt], vf[0][mt], pb0, pb1);
     } else {
+      // k = 32 tokens per product, ordered (2c, 2c+1, 2c+8, 2c+9) of sub-tile 0 at k = 4c..4c+3
+      // and the same tokens of sub-tile 1 at k = 16+4c..: the transposed f16 probabilities of
+      // head g become four e4m3 codes per register, and the value fragments are regrouped
+      // to the same token order by byte permutes (even and odd d separately)
+      uint32_t pb[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t lo = movmatrix_t(pack_f16(pr[u][0], pr[u][1]));  // tokens 2c, 2c+1 of head g
+        const uint32_t hi = movmatrix_t(pack_f16(pr[u][2], pr[u][3]));  // tokens 2c+8, 2c+9
+        pb[u] = e4m3x2_from_f16x2(lo) | (e4m3x2_from_f16x2(hi) << 16);
+      }
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
-        const uint32_t* r = vf[cc];
-        // each register: (token 2c: d 2p, 2p+1), (token 2c+1: d 2p, 2p+1); split even / odd d
-        const uint32_t ax[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, 0x20)), e4m3x2_to_f16x2(__byte_perm(r[1], 0, 0x20)),
-                                e4m3x2_to_f16x2(__byte_perm(r[2], 0, 0x20)), e4m3x2_to_f16x2(__byte_perm(r[3], 0, 0x20))};
-        const uint32_t ay[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, 0x31)), e4m3x2_to_f16x2(__byte_perm(r[1], 0, 0x31)),
-                                e4m3x2_to_f16x2(__byte_perm(r[2], 0, 0x31)), e4m3x2_to_f16x2(__byte_perm(r[3], 0, 0x31))};
-        mma_f16(o[2 * cc], ax, pb0, pb1);
-        mma_f16(o[2 * cc + 1], ay, pb0, pb1);
+        // vf[u][cc][0]: (token 2c: d 32cc+2g, +1), (token 2c+1: same d); [2]: tokens 2c+8, 2c+9;
+        // [1], [3]: the same for d 32cc+16+2g, +1
+        const uint32_t ae[4] = {__byte_perm(vf[0][cc][0], vf[0][cc][2], 0x6420), __byte_perm(vf[0][cc][1], vf[0][cc][3], 0x6420),
+                                __byte_perm(vf[U - 1][cc][0], vf[U - 1][cc][2], 0x6420),
+                                __byte_perm(vf[U - 1][cc][1], vf[U - 1][cc][3], 0x6420)};
+        const uint32_t ao[4] = {__byte_perm(vf[0][cc][0], vf[0][cc][2], 0x7531), __byte_perm(vf[0][cc][1], vf[0][cc][3], 0x7531),
+                                __byte_perm(vf[U - 1][cc][0], vf[U - 1][cc][2], 0x7531),
+                                __byte_perm(vf[U - 1][cc][1], vf[U - 1][cc][3], 0x7531)};
+        mma_e4m3(o[2 * cc], ae, pb[0], pb[U - 1]);
+        mma_e4m3(o[2 * cc + 1], ao, pb[0], pb[U - 1]);
       }
     }
     __syncwarp();
-    if (nx < my_n) issue(nx, pages);
-    cp_async_commit();
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int nx = i0 + NST - U + u;
+      if (nx < my_n) issue(nx, pages[u]);
+      cp_async_commit();
+    }
   }
   cp_async_wait<0>();
   if (p.pdl) {
@@ -434,10 +512,10 @@ cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
   }
   if (p.kv_dtype == PSP_KV_FP8) {
     if (p.head_dim != 128) return launch_t<PSP_KV_FP8, 64, 4, 6>(p, num_splits, s);
-    switch (suffix_stages(3)) {
-      case 2: return launch_t<PSP_KV_FP8, 128, 4, 2>(p, num_splits, s);
-      case 3: return launch_t<PSP_KV_FP8, 128, 4, 3>(p, num_splits, s);
-      default: return launch_t<PSP_KV_FP8, 128, 4, 5>(p, num_splits, s);
+    switch (suffix_stages(4)) {  // fp8 consumes two sub-tiles per iteration: at least 4 stages
+      case 5: return launch_t<PSP_KV_FP8, 128, 4, 5>(p, num_splits, s);
+      case 6: return launch_t<PSP_KV_FP8, 128, 4, 6>(p, num_splits, s);
+      default: return launch_t<PSP_KV_FP8, 128, 4, 4>(p, num_splits, s);
     }
   }
   return launch_suffix_simt(p, num_splits, s);

@@ -68,6 +68,15 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A(16x32, row) * B(32x8, col) + D on e4m3 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Transposes an 8x8 matrix of 16-bit elements held in the warp's fragment layout.
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;
@@ -88,6 +97,15 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x & 0xffffu), __NV_E4M3);
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Two halves (an f16x2 word, first element in the low half) -> two e4m3 codes in the low
+// 16 bits, first in the low byte (round to nearest even, saturating).
+__device__ __forceinline__ uint32_t e4m3x2_from_f16x2(uint32_t h) {
+  __half2_raw r;
+  r.x = static_cast<unsigned short>(h & 0xffffu);
+  r.y = static_cast<unsigned short>(h >> 16);
+  return static_cast<uint32_t>(__nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3));
 }
 
 // Four floats -> four e4m3 codes (round to nearest even, saturating), a in byte 0.
