@@ -302,3 +302,30 @@ def test_concurrent_prefix_matches_oracle(spec):
     assert max_err(o2.float().cpu().double().numpy(), ref_o) <= tol
     assert max_err(l2.cpu().double().numpy(), ref_lse) <= tol
     step.close()
+
+
+def _multi_group_full_case():
+    """Three prefix groups (160, 37 and 512 tokens; 8, 6 and 6 members) plus ungrouped
+    requests in one pool, with every slot of the pool holding finite random K/V."""
+    from test_abi_host import _multi_group_case
+    tables = _multi_group_case()
+    full = workloads.make_case("agent", 3, batch=tables.batch)
+    w = full.workload
+    shape = (tables.num_pages, tables.page_size, w.num_kv_heads, w.head_dim)
+    k = workloads.bf16_bits_from_f32(workloads.normal_f32(shape, 21, 1))
+    v = workloads.bf16_bits_from_f32(workloads.normal_f32(shape, 21, 2))
+    return dataclasses.replace(tables, q=full.q, k_pool=k, v_pool=v, k_scale=None, v_scale=None)
+
+
+@pytest.mark.gpu
+def test_multi_group_mixed_branches_match_oracle():
+    # M_eff = 32, 24, 24 (G = 4): threshold 30 sends group 0 to the dense kernel and
+    # groups 1 and 2 to the cascade kernel in the same step, then the suffix kernel
+    case = _multi_group_full_case()
+    ref_o, ref_lse = oracle.attend_all(case)
+    tol = TOL[case.workload.kv_dtype]
+    tens = device_tensors(case)
+    for thr, kw in ((30, {}), (1, {}), (1 << 20, {}), (30, dict(concurrent=True)), (30, dict(token_flat=True))):
+        o, lse = run_case(case, threshold=thr, tensors=tens, **kw)
+        assert np.isfinite(o).all() and np.isfinite(lse).all(), (thr, kw)
+        assert max_err(o, ref_o) <= tol and max_err(lse, ref_lse) <= tol, (thr, kw, max_err(o, ref_o))
