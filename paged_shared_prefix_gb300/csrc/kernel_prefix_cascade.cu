@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(NW * 32) prefix_cascade_kernel(const StepParam
   __syncthreads();
   const int row0 = rb * NW * 16;
   prefix_arrive_and_merge<D>(p, members, h, row0, min(NW * 16, m_eff - row0), reinterpret_cast<int*>(smem));
+  prefix_rows_done(p, min(NW * 16, m_eff - row0));
 }
 
 template <int KV, int D, int NW, int NST>

@@ -506,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // arrivals of the block's members whose (b, h) counters need them; the arrival that
   // completes a member merges it (shared memory is free: every product and copy is done)
   if (!*abort && *any_arrive) prefix_arrive_and_merge_flagged<kD>(p, members, h, row_base, n_rows, flags);
+  if (!*abort) prefix_rows_done(p, n_rows);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

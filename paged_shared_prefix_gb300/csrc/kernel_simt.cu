@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
       for (int rr = warp; rr < G; rr += kWarps) merge_row<D>(p, b_suffix, h * G + rr, lane);
   } else {
     prefix_arrive_and_merge<D>(p, members, h, row0, n_rows, flags);
+    prefix_rows_done(p, n_rows);
   }
 }
 

@@ -102,9 +102,10 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
       }
     }
   };
-  // launched as a dependent of the prefix kernel, the prefix partials are read only
-  // after that grid has completed (below, after this CTA's own stream)
-  if (pre_smem && !p.pdl) prefetch_prefix();
+  // a dependent launch that keeps the sequential protocol reads the prefix partials only
+  // after the prefix grid has completed (below, after this CTA's own stream)
+  const bool wait_prefix = p.pdl && !p.concurrent;
+  if (pre_smem && !wait_prefix) prefetch_prefix();
 
   // -------- query fragments: B operand of S^T = K Q^T (k = head dim, n = query head)
   const int qg = lane >> 2;  // query head within the group (B fragment column)
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     }
   }
   cp_async_wait<0>();
-  if (p.pdl) {
+  if (wait_prefix) {
     pdl_wait_primary();  // every prefix partial and prefix arrival of this step is complete
     if (pre_smem) {
       prefetch_prefix();
@@ -411,9 +412,21 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   // A single-split request writes its final output here: its own result merged with the
   // prefetched prefix partials (none without a shared prefix).  Otherwise write the partial
   // and let the last arrival of (b, h) merge.
-  const bool only_part = p.split_indptr[b + 1] - p.split_indptr[b] == 1 && n_chunks == 0;
+  const bool one_split = p.split_indptr[b + 1] - p.split_indptr[b] == 1;
+  const bool only_part = one_split && n_chunks == 0;
   const bool direct = only_part || (solo && pre_smem);
-  const bool solo_global = solo && !direct;   // too many prefix chunks to prefetch: read them here
+  // Launched as a dependent of a still running prefix kernel: a one-split request whose
+  // prefix partials are all complete (every prefix row counted done) merges them here like
+  // a solo request; otherwise its part goes through the (request, KV head) counter.
+  bool ready = false;
+  if (p.pdl && p.concurrent && one_split && n_chunks > 0) {
+    __shared__ int prefix_ready;
+    if (threadIdx.x == 0) prefix_ready = *reinterpret_cast<volatile int32_t*>(p.prefix_done) == p.prefix_rows_total;
+    __syncthreads();
+    ready = prefix_ready != 0;
+    if (ready) __threadfence();  // the prefix partials were fenced before their rows were counted
+  }
+  const bool solo_global = (solo && !direct) || ready;  // read the prefix partials from global memory
   const int64_t row0 = (static_cast<int64_t>(split) * p.hkv + h) * G;
   const int64_t orow0 = static_cast<int64_t>(b) * p.hq + h * G;
   for (int e = threadIdx.x; e < G * D; e += NW * 32) {
@@ -450,18 +463,32 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
       if (d == 0) p.lse_suf[row0 + g] = mmax + log2f(sum);
     }
   }
-  if (direct) return;
-  __threadfence();
-  __syncthreads();
-  if (solo_global) {  // every other part of (b, h) is already complete
-    for (int rr = warp; rr < G; rr += NW) merge_row<D>(p, b, h * G + rr, lane);
-    return;
+  if (!direct) {
+    __threadfence();
+    __syncthreads();
+    if (solo_global) {  // every other part of (b, h) is already complete
+      for (int rr = warp; rr < G; rr += NW) merge_row<D>(p, b, h * G + rr, lane);
+      // every prefix arrival on (b, h) was made and nothing else arrives: clear it for the next step
+      if (ready && threadIdx.x == 0) p.counters[static_cast<int64_t>(b) * p.hkv + h] = 0;
+    } else {
+      __shared__ int last;
+      if (threadIdx.x == 0) last = arrive_is_last(p, b, h) ? 1 : 0;
+      __syncthreads();
+      if (last)
+        for (int rr = warp; rr < G; rr += NW) merge_row<D>(p, b, h * G + rr, lane);
+    }
   }
-  __shared__ int last;
-  if (threadIdx.x == 0) last = arrive_is_last(p, b, h) ? 1 : 0;
-  __syncthreads();
-  if (last)
-    for (int rr = warp; rr < G; rr += NW) merge_row<D>(p, b, h * G + rr, lane);
+  if (p.pdl && p.concurrent) {
+    // launched as a dependent of the prefix kernel and never waiting for it: the grid's
+    // last CTA waits for the prefix grid, so this grid (and the stream after it) completes
+    // only after the prefix kernel (in the other form every CTA has waited already)
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(p.done_ctas, 1) == static_cast<int>(gridDim.x) - 1) {
+      *p.done_ctas = 0;  // ready for the next step (stream-ordered)
+      pdl_wait_primary();
+      *p.prefix_done = 0;  // every prefix CTA has counted its rows
+    }
+  }
 }
 
 template <int KV, int D, int NW, int NST>

@@ -491,6 +491,13 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.o_pre = F(L.o_pre);
   p.lse_pre = F(L.lse_pre);
   p.status = I(L.status);
+  p.done_ctas = I(L.status + 32);    // inside the status block, cleared with it at upload
+  p.prefix_done = I(L.status + 48);
+  {
+    int64_t rows = 0;  // sum over prefix chunks of M_eff of the chunk's group, for every KV head
+    for (size_t ci = 0; ci < P.chunk_group.size(); ++ci) rows += P.group_m_eff[P.chunk_group[ci]];
+    p.prefix_rows_total = static_cast<int32_t>(rows * c.num_kv_heads);
+  }
   p.counters = I(L.counters);
   return p;
 }
@@ -744,11 +751,17 @@ psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
   const int nd = static_cast<int>(P.item_chunk_dense.size());
   const int nc = static_cast<int>(P.item_chunk_cascade.size());
   const bool fork = p.concurrent && (nd > 0 || nc > 0) && P.NS > 0;
-  // The suffix kernel follows the prefix kernel as a programmatic dependent: it streams
-  // its own K/V while the prefix kernel finishes and waits for it only before reading
-  // prefix partials.  Not with per-kernel timing (events between the launches) nor when
-  // the prefix runs on its own stream.
+  // The suffix kernel follows the prefix kernel as a programmatic dependent: its CTAs start
+  // on the SMs the prefix kernel leaves free and never wait for it.  The two kernels then
+  // run at the same time, so every part of a (request, KV head) arrives on its counter and
+  // the last arrival merges (the concurrent protocol).  Not with per-kernel timing (events
+  // between the launches) nor when the prefix runs on its own stream.
   p.pdl = (!fork && !h->timing && (nd > 0 || nc > 0) && P.NS > 0) ? 1 : 0;
+  // Two forms (measured on GB300): when the prefix grid leaves at least half of the SMs free,
+  // the suffix kernel never waits and uses the concurrent merge protocol (short prefixes:
+  // 76 vs 81 us); when the prefix grid fills the GPU, the suffix CTAs wait for it before
+  // reading prefix partials and keep the sequential protocol (agent batch: 148 vs 163 us).
+  if (p.pdl && static_cast<int64_t>(nd + nc) * p.hkv * 2 <= h->num_sms_resolved) p.concurrent = 1;
   if (p.token_flat) {
     st = timed_launch(h, s, "expand_kv_indices", slot, expand_entry, p, 0);
     if (st) return st;

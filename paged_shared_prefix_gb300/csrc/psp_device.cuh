@@ -22,10 +22,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 // 16-byte asynchronous global->shared copy; src_bytes 0 zero-fills the destination.
 // Programmatic dependent launch: a prefix kernel lets the suffix kernel of the same
-// step start early (its CTAs stream their own K/V while the prefix kernel runs);
-// the suffix kernel waits for the prefix grid (completion and memory) before it
-// touches anything the prefix kernel writes.  Both are no-ops outside such a pair.
+// step start as soon as every prefix CTA is running (the suffix CTAs then fill the
+// SMs the prefix kernel leaves free).  A no-op when no dependent is launched.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+// Waits until the grids this one depends on have completed and their writes are visible.
 __device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool valid) {

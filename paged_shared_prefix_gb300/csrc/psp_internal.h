@@ -84,6 +84,9 @@ struct StepParams {
   float* lse_pre;
   int32_t* status;                     // device status word
   int32_t* counters;                   // [B * Hkv] arrivals of partial results (zero between steps)
+  int32_t* done_ctas;                  // suffix CTAs finished this step (zero between steps)
+  int32_t* prefix_done;                // prefix rows (x heads) whose partials and arrivals are done
+  int32_t prefix_rows_total;           // its value once the whole prefix kernel has finished
 };
 
 // Byte offsets of every array inside the workspace (256-byte aligned each).

@@ -119,6 +119,19 @@ __device__ __forceinline__ void store_final(const StepParams& p, int64_t row, in
   }
 }
 
+// Prefix kernels launched ahead of a dependent suffix kernel that does not wait for them
+// (the concurrent form): after this CTA's partials and arrivals are complete, count its
+// rows as done, so that suffix CTAs can see that the whole prefix is finished.  Called by
+// every thread of the CTA.
+__device__ __forceinline__ void prefix_rows_done(const StepParams& p, int n_rows) {
+  if (!p.pdl || !p.concurrent) return;  // only the concurrent form reads the count
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(p.prefix_done, n_rows);
+  }
+}
+
 // Whether member b of a prefix row block must arrive on its (b, h) counter: every
 // request does, unless it has exactly one suffix split and the prefix kernels run
 // before the suffix kernel (that split then merges the prefix partials itself).
