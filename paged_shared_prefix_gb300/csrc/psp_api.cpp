@@ -139,6 +139,10 @@ psp_status validate_batch(psp_handle* h, const psp_batch* bt) {
   if (B > 0 && bt->page_indptr[0] != 0) return fail(h, PSP_ERR_INVALID_ARGUMENT, "page_indptr[0] != 0");
   const int64_t ps = c.page_size;
   int64_t total = 0;
+  // The shared pages of a group member after the first are compared with the first
+  // member's (build_plan), whose pages are range-checked in full here, so they are not
+  // range-checked a second time.
+  std::vector<int32_t> first_member(std::max(bt->num_groups, 0), -1);
   for (int b = 0; b < B; ++b) {
     const int64_t L = bt->kv_len[b];
     if (L < 1) return fail(h, PSP_ERR_LENGTH, "kv_len[" + std::to_string(b) + "] < 1");
@@ -146,17 +150,46 @@ psp_status validate_batch(psp_handle* h, const psp_batch* bt) {
     if (n != cdiv(L, ps))
       return fail(h, PSP_ERR_LENGTH, "request " + std::to_string(b) + " has " + std::to_string(n) +
                                          " pages for kv_len " + std::to_string(L));
-    for (int64_t i = bt->page_indptr[b]; i < bt->page_indptr[b + 1]; ++i) {
-      const int32_t pg = bt->page_indices[i];
-      if (pg < 0 || pg >= c.num_pages)
-        return fail(h, PSP_ERR_PAGE_OUT_OF_RANGE,
-                    "page id " + std::to_string(pg) + " of request " + std::to_string(b) + " outside [0, num_pages)");
+    // range check as a branch-free min / max pass (it vectorises); the offending id is
+    // searched for only to word the error
+    int64_t skip = 0;
+    const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
+    if (g >= 0 && g < bt->num_groups && bt->group_prefix_len[g] >= 0) {
+      if (first_member[g] < 0) {
+        first_member[g] = b;
+      } else {
+        skip = std::min<int64_t>(n, bt->group_prefix_len[g] / ps);
+      }
+    }
+    const int32_t* pg = bt->page_indices + bt->page_indptr[b];
+    int32_t lo = INT32_MAX, hi = INT32_MIN;
+    for (int64_t i = skip; i < n; ++i) {
+      lo = std::min(lo, pg[i]);
+      hi = std::max(hi, pg[i]);
+    }
+    if (n > skip && (lo < 0 || hi >= c.num_pages)) {
+      const int32_t bad = lo < 0 ? lo : hi;
+      return fail(h, PSP_ERR_PAGE_OUT_OF_RANGE,
+                  "page id " + std::to_string(bad) + " of request " + std::to_string(b) + " outside [0, num_pages)");
     }
     total += L;
     if (total > INT32_MAX) return fail(h, PSP_ERR_INVALID_ARGUMENT, "sum of kv_len exceeds int32");
   }
   for (int g = 0; g < bt->num_groups; ++g)
     if (bt->group_prefix_len[g] < 0) return fail(h, PSP_ERR_INVALID_ARGUMENT, "negative group prefix length");
+  return PSP_OK;
+}
+
+// Range check of every page id in request order (the slow path behind a failed group
+// comparison: an out-of-range id takes precedence over a prefix mismatch).
+psp_status full_range_check(psp_handle* h, const psp_batch* bt) {
+  for (int b = 0; b < bt->batch_size; ++b)
+    for (int64_t i = bt->page_indptr[b]; i < bt->page_indptr[b + 1]; ++i) {
+      const int32_t pg = bt->page_indices[i];
+      if (pg < 0 || pg >= h->cfg.num_pages)
+        return fail(h, PSP_ERR_PAGE_OUT_OF_RANGE,
+                    "page id " + std::to_string(pg) + " of request " + std::to_string(b) + " outside [0, num_pages)");
+    }
   return PSP_OK;
 }
 
@@ -188,9 +221,12 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
     } else {
       const int32_t* mine = bt->page_indices + bt->page_indptr[b];
       const int32_t* ref = bt->page_indices + bt->page_indptr[first[g]];
-      if (!std::equal(mine, mine + n_sh, ref))
+      if (n_sh > 0 && std::memcmp(mine, ref, static_cast<size_t>(n_sh) * sizeof(int32_t)) != 0) {
+        const psp_status range = full_range_check(h, bt);
+        if (range) return range;
         return fail(h, PSP_ERR_PREFIX_MISMATCH,
                     "request " + std::to_string(b) + " does not share the prefix pages of its group");
+      }
     }
     P.req_member[b] = count[g]++;
   }
@@ -347,7 +383,8 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   L.total = off;
 
   // host image of the integer region
-  P.image.assign(L.plan_bytes, 0);
+  // (through zero_end: the status word and the merge counters upload as zeros with the plan)
+  P.image.assign(L.zero_end, 0);
   auto put = [&](size_t off, const std::vector<int32_t>& v) {
     if (!v.empty()) std::memcpy(P.image.data() + off, v.data(), v.size() * sizeof(int32_t));
   };
@@ -659,22 +696,21 @@ psp_status psp_upload(psp_handle* h, void* workspace, size_t workspace_bytes, vo
     e = cudaEventCreateWithFlags(&h->staging_done, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventCreate");
   }
-  if (h->staging_bytes < L.plan_bytes) {
+  if (h->staging_bytes < L.zero_end) {
     if (h->staging) cudaFreeHost(h->staging);
     h->staging = nullptr;
     h->staging_bytes = 0;
-    const size_t want = std::max<size_t>(L.plan_bytes, 1 << 16) * 5 / 4;
+    const size_t want = std::max<size_t>(L.zero_end, 1 << 16) * 5 / 4;
     e = cudaHostAlloc(reinterpret_cast<void**>(&h->staging), want, cudaHostAllocDefault);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaHostAlloc (plan staging)");
     h->staging_bytes = want;
   }
-  std::memcpy(h->staging, P.image.data(), L.plan_bytes);
-  e = cudaMemcpyAsync(workspace, h->staging, L.plan_bytes, cudaMemcpyHostToDevice, s);
+  // one copy: the plan's integer arrays, then the zeroed status word and merge counters
+  std::memcpy(h->staging, P.image.data(), L.zero_end);
+  e = cudaMemcpyAsync(workspace, h->staging, L.zero_end, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "plan upload");
   e = cudaEventRecord(h->staging_done, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventRecord");
-  e = cudaMemsetAsync(static_cast<unsigned char*>(workspace) + L.status, 0, L.zero_end - L.status, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "clearing the device status word and merge counters");
   h->workspace = static_cast<unsigned char*>(workspace);
   h->workspace_bytes = workspace_bytes;
   h->uploaded = true;
@@ -881,10 +917,9 @@ psp_status bind_image_and_run(psp_handle* h, unsigned char* ws, size_t cap, cons
                     std::to_string(cap) + " bytes; plan a smaller batch or use psp_upload with a workspace");
   if (!t || !t->q || !t->k_pool || !t->v_pool || !t->o)
     return fail(h, PSP_ERR_INVALID_ARGUMENT, "q, k_pool, v_pool and o must be set");
-  cudaError_t e = cudaMemcpyAsync(ws, h->plan.image.data(), L.plan_bytes, cudaMemcpyHostToDevice, s);
+  // the image runs through zero_end: the status word and merge counters arrive as zeros
+  cudaError_t e = cudaMemcpyAsync(ws, h->plan.image.data(), L.zero_end, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "plan copy into the static scratch");
-  e = cudaMemsetAsync(ws + L.status, 0, L.zero_end - L.status, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "clearing the device status word and merge counters");
   h->workspace = ws;
   h->workspace_bytes = cap;
   h->uploaded = true;

@@ -223,6 +223,14 @@ def test_invalid_batches_rejected_like_the_oracle():
     bad_cases.append(("group id out of range", dataclasses.replace(c, prefix_group=pg), -1))
     bad_cases.append(("prefix longer than a context",
                       dataclasses.replace(c, group_prefix_len=np.array([int(c.kv_len.min()) + 1], np.int32)), -5))
+    # out of range inside a later member's shared pages: reported as out of range, not as a
+    # prefix mismatch (the library compares those pages instead of range-checking them twice)
+    pi = c.page_indices.copy()
+    pi[c.page_indptr[2]] = c.num_pages + 7
+    bad_cases.append(("out of range in a shared page of the third member", dataclasses.replace(c, page_indices=pi), -3))
+    pi = c.page_indices.copy()
+    pi[c.page_indptr[2]] = -2
+    bad_cases.append(("negative id in a shared page of the third member", dataclasses.replace(c, page_indices=pi), -3))
     for label, case, code in bad_cases:
         assert _status_of_plan(case) == code, label
         assert _oracle_status(case) == code, label
