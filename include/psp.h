@@ -283,11 +283,13 @@ PSP_API psp_status psp_upload(psp_handle* h, void* workspace, size_t workspace_b
  * batch and configuration.  Errors: NO_PLAN, INVALID_ARGUMENT, CUDA. */
 PSP_API psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream);
 
-/* Host-buffer variant of one whole step, synchronous: psp_plan(batch), upload
- * into `workspace`, copy q_host (pinned, [B, Hq, d] q_dtype) to dev->q, psp_run,
- * copy dev->o and dev->lse back to o_host and lse_host (lse_host may be NULL),
- * then wait for the stream.  dev->q/o/lse are device staging buffers, dev's
- * pools and scales are the resident cache.  Errors: as the calls it makes. */
+/* Host-buffer variant of one whole step, synchronous: enqueue the copy of q_host
+ * (pinned, [B, Hq, d] q_dtype) to dev->q, psp_plan(batch) on the host while that
+ * copy runs, upload into `workspace`, psp_run, copy dev->o and dev->lse back to
+ * o_host and lse_host (lse_host may be NULL), then wait for the stream.
+ * dev->q/o/lse are device staging buffers, dev's pools and scales are the
+ * resident cache.  Errors: as the calls it makes (a planning error returns with
+ * the query copy already enqueued on the stream). */
 PSP_API psp_status psp_step_host(psp_handle* h, const psp_batch* batch, const void* q_host,
                          void* o_host, float* lse_host, const psp_tensors* dev,
                          void* workspace, size_t workspace_bytes, void* stream);

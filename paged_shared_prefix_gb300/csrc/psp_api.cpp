@@ -841,16 +841,18 @@ psp_status psp_step_host(psp_handle* h, const psp_batch* batch, const void* q_ho
   if (!h) return PSP_ERR_INVALID_ARGUMENT;
   if (!q_host || !o_host || !dev || !dev->q || !dev->o || (lse_host && !dev->lse))
     return fail(h, PSP_ERR_INVALID_ARGUMENT, "host and device staging buffers must be set");
+  if (!batch || batch->batch_size < 0) return fail(h, PSP_ERR_INVALID_ARGUMENT, "batch is NULL or negative");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const psp_config& c = h->cfg;
+  const size_t rows = static_cast<size_t>(batch->batch_size) * c.num_q_heads;
+  // the query copy does not depend on the plan: it runs while the host plans
+  cudaError_t e = cudaMemcpyAsync(const_cast<void*>(dev->q), q_host, rows * c.head_dim * dtype_bytes(c.q_dtype),
+                                  cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "copying q to the device");
   psp_status st = psp_plan(h, batch);
   if (st) return st;
   st = psp_upload(h, workspace, workspace_bytes, stream);
   if (st) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const psp_config& c = h->cfg;
-  const size_t rows = static_cast<size_t>(batch->batch_size) * c.num_q_heads;
-  cudaError_t e = cudaMemcpyAsync(const_cast<void*>(dev->q), q_host, rows * c.head_dim * dtype_bytes(c.q_dtype),
-                                  cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "copying q to the device");
   st = psp_run(h, dev, stream);
   if (st) return st;
   e = cudaMemcpyAsync(o_host, dev->o, rows * c.head_dim * dtype_bytes(c.o_dtype), cudaMemcpyDeviceToHost, s);
