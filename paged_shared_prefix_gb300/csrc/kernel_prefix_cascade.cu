@@ -119,16 +119,27 @@ __global__ void __launch_bounds__(NW * 32) prefix_cascade_kernel(const StepParam
     const int tb = t0 + i * kTile;
     unsigned char* kdst = smem + (i % NST) * C::kStageBytes;
     constexpr int kChunksTotal = kTile * C::kChunks;
+    constexpr int kIters = (kChunksTotal + NW * 32 - 1) / (NW * 32);
+    // all block-table lookups first (independent loads in flight together), then the
+    // copies: a lookup issued between copies (asm with a memory clobber) would wait alone
+    int64_t off[kIters];
 #pragma unroll
-    for (int e = threadIdx.x; e < kChunksTotal; e += NW * 32) {
+    for (int it = 0; it < kIters; ++it) {
+      const int e = threadIdx.x + it * NW * 32;
+      const int r = e / C::kChunks;
+      const int t = tb + r;
+      off[it] = (e < kChunksTotal && t < t1) ? slot_of(list, t, shift) * row_stride + (e - r * C::kChunks) * 16 : -1;
+    }
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+      const int e = threadIdx.x + it * NW * 32;
+      if (e >= kChunksTotal) break;
       const int r = e / C::kChunks;
       const int c = e - r * C::kChunks;
-      const int t = tb + r;
-      const bool valid = t < t1;
-      const int64_t off = valid ? slot_of(list, t, shift) * row_stride + c * 16 : 0;
+      const bool valid = off[it] >= 0;
       const uint32_t d = smem_u32(kdst + r * C::kRowBytes + swz<C::kChunks>(r, c) * 16);
-      cp_async_16(d, kbase + off, valid);
-      cp_async_16(d + C::kTileBytes, vbase + off, valid);
+      cp_async_16(d, kbase + (valid ? off[it] : 0), valid);
+      cp_async_16(d + C::kTileBytes, vbase + (valid ? off[it] : 0), valid);
     }
   };
 

@@ -100,12 +100,16 @@ struct DenseCfg {
 };
 
 // TMA loads of one 128-token tile (tile j of the chunk [t0, t1)) into dst, completing on bar.
+// Called by all lanes of the producer warp: lane l takes boxes l, l + 32, ..., so the
+// block-table lookups of a tile are independent loads in flight together (one lane
+// issuing every box would wait for each lookup in turn: 8 round trips per tile at
+// page size 16).
 template <uint32_t kHalf, uint32_t kHalves, int kBoxElems>
 __device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, uint32_t bar, const int32_t* list,
-                                          int shift, int h, int t0, int t1, int j, int num_slots) {
+                                          int shift, int h, int t0, int t1, int j, int num_slots, int lane) {
   const int mask = (1 << shift) - 1;
   const int br = min(1 << shift, 64);  // rows per TMA box; boxes never straddle a page
-  for (int r = 0; r < kTok; r += br) {
+  for (int r = lane * br; r < kTok; r += 32 * br) {
     const int tok = t0 + j * kTok + r;
     const int slot = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
 #pragma unroll
@@ -190,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpP) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0 && run) {
+    // the whole warp: lane 0 waits and sets the expected bytes, every lane issues boxes
+    if (run) {
       const int32_t* list;
       int shift;
       if (p.token_flat) {
@@ -200,27 +205,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         list = p.group_page_indices + p.group_page_indptr[g];
         shift = p.page_shift;
       }
-      prefetch_tmap(&kmap);
-      prefetch_tmap(&vmap);
-      mbar_arrive_tx(bar(C::kBarK0), C::kTileBytes);
+      if (lane == 0) {
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&vmap);
+        mbar_arrive_tx(bar(C::kBarK0), C::kTileBytes);
+      }
+      __syncwarp();
       load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&kmap, base + C::kOffK0, bar(C::kBarK0), list, shift, h, t0, t1,
-                                                    0, num_slots);
+                                                    0, num_slots, lane);
       int issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % NS;
-        if (j >= NS && !wait_or_abort(bar(C::kBarEmpty + st), ((j / NS) - 1) & 1, abort, status, 1)) break;
+        if (j >= NS) {
+          int ok = 0;
+          if (lane == 0) ok = wait_or_abort(bar(C::kBarEmpty + st), ((j / NS) - 1) & 1, abort, status, 1) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        }
         const bool more = j + 1 < n_tiles;
         const uint32_t full = bar(C::kBarFull + st), dst = base + C::kOffRing + st * C::kStageBytes;
-        mbar_arrive_tx(full, more ? 2 * C::kTileBytes : C::kTileBytes);
-        load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&vmap, dst, full, list, shift, h, t0, t1, j, num_slots);
+        if (lane == 0) mbar_arrive_tx(full, more ? 2 * C::kTileBytes : C::kTileBytes);
+        __syncwarp();
+        load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&vmap, dst, full, list, shift, h, t0, t1, j, num_slots, lane);
         if (more)
           load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&kmap, dst + C::kTileBytes, full, list, shift, h, t0, t1,
-                                                        j + 1, num_slots);
+                                                        j + 1, num_slots, lane);
         issued = j + 1;
       }
       // drain: every load issued must have landed before the CTA may exit (plain bounded waits)
-      mbar_wait(bar(C::kBarK0), 0, status, 3);
-      for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(bar(C::kBarFull + j % NS), (j / NS) & 1, status, 3);
+      if (lane == 0) {
+        mbar_wait(bar(C::kBarK0), 0, status, 3);
+        for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(bar(C::kBarFull + j % NS), (j / NS) & 1, status, 3);
+      }
+      __syncwarp();
     }
   } else if (warp == kWarpM) {
     // -------------------------------------------------------------------- MMA
