@@ -99,37 +99,6 @@ struct DenseCfg {
   static_assert(4 * 32 * 32 * 4 <= kQBytes, "epilogue staging (4 warps x 32 x 32 fp32) must fit in one Q tile");
 };
 
-// TMA loads of one 128-token tile (tile j of the chunk [t0, t1)) into dst, completing on bar.
-// Called by all lanes of the producer warp: lane l takes boxes l, l + 32, ..., so the
-// block-table lookups of a tile are independent loads in flight together (one lane
-// issuing every box would wait for each lookup in turn: 8 round trips per tile at
-// page size 16).
-template <uint32_t kHalf, uint32_t kHalves, int kBoxElems>
-__device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, uint32_t bar, const int32_t* list,
-                                          int shift, int h, int t0, int t1, int j, int num_slots, int lane) {
-  const int mask = (1 << shift) - 1;
-  const int br = min(1 << shift, 64);  // rows per TMA box; boxes never straddle a page
-  for (int r = lane * br; r < kTok; r += 32 * br) {
-    const int tok = t0 + j * kTok + r;
-    const int slot = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
-#pragma unroll
-    for (uint32_t hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * kHalf + r * 128, map, hf * kBoxElems, h, slot, bar);
-  }
-}
-
-// Bounded wait that also gives up as soon as another role of the CTA has given up.
-// On its own timeout it records the site and raises the abort flag.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status,
-                                              int site) {
-  for (uint32_t i = 0; i < (1u << 24); ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31) == 31 && *abort) return false;
-  }
-  atomicCAS(status, 0, kDevTimeout | (site << 8));
-  *abort = 1;
-  return false;
-}
-
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_dense_kernel(const StepParams p, const __grid_constant__ CUtensorMap kmap,
@@ -211,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_tx(bar(C::kBarK0), C::kTileBytes);
       }
       __syncwarp();
-      load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&kmap, base + C::kOffK0, bar(C::kBarK0), list, shift, h, t0, t1,
+      load_tile<kTok, C::kHalf, C::kHalves, C::kBoxElems>(&kmap, base + C::kOffK0, bar(C::kBarK0), list, shift, h, t0, t1,
                                                     0, num_slots, lane);
       int issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
@@ -225,9 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t full = bar(C::kBarFull + st), dst = base + C::kOffRing + st * C::kStageBytes;
         if (lane == 0) mbar_arrive_tx(full, more ? 2 * C::kTileBytes : C::kTileBytes);
         __syncwarp();
-        load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&vmap, dst, full, list, shift, h, t0, t1, j, num_slots, lane);
+        load_tile<kTok, C::kHalf, C::kHalves, C::kBoxElems>(&vmap, dst, full, list, shift, h, t0, t1, j, num_slots, lane);
         if (more)
-          load_tile<C::kHalf, C::kHalves, C::kBoxElems>(&kmap, dst + C::kTileBytes, full, list, shift, h, t0, t1,
+          load_tile<kTok, C::kHalf, C::kHalves, C::kBoxElems>(&kmap, dst + C::kTileBytes, full, list, shift, h, t0, t1,
                                                         j + 1, num_slots, lane);
         issued = j + 1;
       }
@@ -525,7 +494,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!*abort) prefix_rows_done(p, n_rows);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+template <bool FP8>
+cudaError_t launch_t(const StepParams& p, int num_items, cudaStream_t s) {
+  const int64_t slots = static_cast<int64_t>(p.num_pages) * p.page_size;
+  if (slots >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  const int rows = p.token_flat ? 1 : (p.page_size < 64 ? p.page_size : 64);
+  CUtensorMap kmap, vmap;
+  cudaError_t e = make_pool_map(&kmap, p.k_pool, slots, p.hkv, rows, FP8);
+  if (e != cudaSuccess) return e;
+  e = make_pool_map(&vmap, p.v_pool, slots, p.hkv, rows, FP8);
+  if (e != cudaSuccess) return e;
+  constexpr uint32_t bytes = DenseCfg<FP8>::kSmemBytes;
+  static_assert(bytes <= 232448, "dense prefix CTA exceeds the shared memory of one SM");
+  e = cudaFuncSetAttribute(prefix_dense_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  const int grid = num_items * p.hkv;
+  prefix_dense_kernel<FP8><<<grid, kThreads, bytes, s>>>(p, kmap, vmap, static_cast<int>(slots));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -553,27 +543,6 @@ cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int64_t slots, int
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-
-template <bool FP8>
-cudaError_t launch_t(const StepParams& p, int num_items, cudaStream_t s) {
-  const int64_t slots = static_cast<int64_t>(p.num_pages) * p.page_size;
-  if (slots >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
-  const int rows = p.token_flat ? 1 : (p.page_size < 64 ? p.page_size : 64);
-  CUtensorMap kmap, vmap;
-  cudaError_t e = make_pool_map(&kmap, p.k_pool, slots, p.hkv, rows, FP8);
-  if (e != cudaSuccess) return e;
-  e = make_pool_map(&vmap, p.v_pool, slots, p.hkv, rows, FP8);
-  if (e != cudaSuccess) return e;
-  constexpr uint32_t bytes = DenseCfg<FP8>::kSmemBytes;
-  static_assert(bytes <= 232448, "dense prefix CTA exceeds the shared memory of one SM");
-  e = cudaFuncSetAttribute(prefix_dense_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) return e;
-  const int grid = num_items * p.hkv;
-  prefix_dense_kernel<FP8><<<grid, kThreads, bytes, s>>>(p, kmap, vmap, static_cast<int>(slots));
-  return cudaGetLastError();
-}
-
-}  // namespace
 
 // True when the tcgen05 dense kernel serves this configuration (bf16 or e4m3 K/V, d = 128).
 bool dense_tc_supported(const StepParams& p) {

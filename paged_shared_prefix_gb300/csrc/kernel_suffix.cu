@@ -14,9 +14,10 @@
 // heads on N), the online softmax runs on the accumulator fragments with a
 // three-step shuffle max per tile, P^T is turned into the B operand of the
 // second product by an in-register 8x8 transpose (movmatrix), and the value
-// product is O^T = V^T P^T.  fp8-e4m3 keys/values are converted to f16 in
-// registers (exact); the per-head scales fold into the score and output
-// scalars.  The warps' partial states are combined through shared memory and
+// product is O^T = V^T P^T.  fp8-e4m3 keys/values enter both products as
+// e4m3 mma.sync operands (m16n8k32, two sub-tiles per iteration, the query
+// rows and P quantised to e4m3); the per-head scales fold into the score and
+// output scalars.  The warps' partial states are combined through shared memory and
 // written as one normalised fp32 partial (O, log2-LSE) per (split, head, q).
 #include <cuda_runtime.h>
 
@@ -25,13 +26,12 @@
 #include "psp_device.cuh"
 #include "psp_internal.h"
 #include "psp_merge.cuh"
+#include "psp_suffix_epi.cuh"
 
 namespace psp {
 namespace {
 
 using namespace dev;
-
-constexpr int kPreRows = 16;  // prefix partial rows (chunks x query heads) prefetched per single-split request
 
 template <int KV, int D>
 struct SufCfg {
@@ -77,35 +77,13 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
 
   // A request with one suffix split merges its shared-prefix partials here: the prefix
   // kernel ran earlier on the stream, so its rows are complete.  They are prefetched into
-  // a shared-memory area of their own, in the first cp.async group of every thread.
-  const int g_req = p.req_group[b];
-  const bool solo = !p.concurrent && p.split_indptr[b + 1] - p.split_indptr[b] == 1;
-  const int c0 = g_req >= 0 ? p.group_chunk_indptr[g_req] : 0;
-  const int n_chunks = g_req >= 0 ? p.group_chunk_indptr[g_req + 1] - c0 : 0;
-  const bool pre_smem = solo && n_chunks > 0 && n_chunks * G <= kPreRows;
+  // a shared-memory area of their own, in the first cp.async group of every thread (a
+  // dependent launch that keeps the sequential protocol reads them only after the prefix
+  // grid has completed, below, after this CTA's own stream).
+  const SuffixCta cta = suffix_cta(p, split, h);
   float* pre_o = reinterpret_cast<float*>(smem + NW * NST * C::kStageBytes);   // [chunk * G + j][D]
   float* pre_l = pre_o + kPreRows * D;                                           // [chunk * G + j]
-  auto prefetch_prefix = [&]() {
-    const int m_eff = p.group_m_eff[g_req];
-    const int prow = p.req_member[b] * G;
-    constexpr int kRowChunks = D * 4 / 16;
-    for (int e = threadIdx.x; e < n_chunks * G * (kRowChunks + 1); e += NW * 32) {
-      const int c = e / (G * (kRowChunks + 1));
-      const int rem = e - c * G * (kRowChunks + 1);
-      const int j = rem / (kRowChunks + 1);
-      const int q = rem - j * (kRowChunks + 1);
-      const int64_t row = p.chunk_row_offset[c0 + c] + static_cast<int64_t>(h) * m_eff + prow + j;
-      if (q < kRowChunks) {
-        cp_async_16(smem_u32(pre_o + (c * G + j) * D + q * 4), p.o_pre + row * D + q * 4, true);
-      } else {
-        cp_async_4(smem_u32(pre_l + c * G + j), p.lse_pre + row);
-      }
-    }
-  };
-  // a dependent launch that keeps the sequential protocol reads the prefix partials only
-  // after the prefix grid has completed (below, after this CTA's own stream)
-  const bool wait_prefix = p.pdl && !p.concurrent;
-  if (pre_smem && !wait_prefix) prefetch_prefix();
+  if (cta.pre_smem && !cta.wait_prefix) prefetch_prefix_rows<D, NW * 32>(p, cta, pre_o, pre_l);
 
   // -------- query fragments: B operand of S^T = K Q^T (k = head dim, n = query head)
   const int qg = lane >> 2;  // query head within the group (B fragment column)
@@ -208,7 +186,8 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
 
   // Sub-tiles per iteration: bf16 takes one; fp8 takes two, so that the value product runs
-  // on e4m3 tensor cores with k = 32 tokens (m16n8k32) and the fp8 codes need no conversion.
+  // as e4m3 mma.sync with k = 32 tokens (m16n8k32) and the code needs no conversion of its own
+  // (on sm_103a the instruction itself unpacks the codes to f16 for the tensor cores).
   constexpr int U = (KV == PSP_KV_FP8) ? 2 : 1;
   static_assert(NST >= 2 * U, "the ring must hold the sub-tiles of one iteration plus those in flight");
   // fp8: the running max is kept 8 below the true max, so P <= 2^8 (inside e4m3's range and
@@ -368,10 +347,10 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     }
   }
   cp_async_wait<0>();
-  if (wait_prefix) {
+  if (cta.wait_prefix) {
     pdl_wait_primary();  // every prefix partial and prefix arrival of this step is complete
-    if (pre_smem) {
-      prefetch_prefix();
+    if (cta.pre_smem) {
+      prefetch_prefix_rows<D, NW * 32>(p, cta, pre_o, pre_l);
       cp_async_commit();
       cp_async_wait<0>();
     }
@@ -409,86 +388,8 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     }
   }
   __syncthreads();
-  // A single-split request writes its final output here: its own result merged with the
-  // prefetched prefix partials (none without a shared prefix).  Otherwise write the partial
-  // and let the last arrival of (b, h) merge.
-  const bool one_split = p.split_indptr[b + 1] - p.split_indptr[b] == 1;
-  const bool only_part = one_split && n_chunks == 0;
-  const bool direct = only_part || (solo && pre_smem);
-  // Launched as a dependent of a still running prefix kernel: a one-split request whose
-  // prefix partials are all complete (every prefix row counted done) merges them here like
-  // a solo request; otherwise its part goes through the (request, KV head) counter.
-  bool ready = false;
-  if (p.pdl && p.concurrent && one_split && n_chunks > 0) {
-    __shared__ int prefix_ready;
-    if (threadIdx.x == 0) prefix_ready = *reinterpret_cast<volatile int32_t*>(p.prefix_done) == p.prefix_rows_total;
-    __syncthreads();
-    ready = prefix_ready != 0;
-    if (ready) __threadfence();  // the prefix partials were fenced before their rows were counted
-  }
-  const bool solo_global = (solo && !direct) || ready;  // read the prefix partials from global memory
-  const int64_t row0 = (static_cast<int64_t>(split) * p.hkv + h) * G;
-  const int64_t orow0 = static_cast<int64_t>(b) * p.hq + h * G;
-  for (int e = threadIdx.x; e < G * D; e += NW * 32) {
-    const int g = e / D;
-    const int d = e - g * D;
-    float mmax = neg_inf();
-#pragma unroll
-    for (int w = 0; w < NW; ++w) mmax = fmaxf(mmax, ms[w * 8 + g]);
-    float acc = 0.f, sum = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float sc = exp2f(ms[w * 8 + g] - mmax);
-      sum += ls[w * 8 + g] * sc;
-      acc += red[(w * 8 + g) * D + d] * sc;
-    }
-    if (direct) {
-      // own part: O_s = acc / sum * out_scale with log2-LSE mmax + log2(sum); prefix chunks first
-      float lse_own = mmax + log2f(sum);
-      float big = lse_own;
-      for (int c = 0; c < n_chunks; ++c) big = fmaxf(big, pre_l[c * G + g]);
-      float wsum = 0.f, out = 0.f;
-      for (int c = 0; c < n_chunks; ++c) {
-        const float w = exp2f(pre_l[c * G + g] - big);
-        wsum += w;
-        out = fmaf(w, pre_o[(c * G + g) * D + d], out);
-      }
-      const float w_own = exp2f(lse_own - big);
-      wsum += w_own;
-      out = fmaf(w_own, acc / sum * out_scale, out);
-      store_final(p, orow0 + g, d, out / wsum);
-      if (d == 0 && p.lse) p.lse[orow0 + g] = (big + log2f(wsum)) * 0.6931471805599453f;
-    } else {
-      p.o_suf[(row0 + g) * D + d] = acc / sum * out_scale;
-      if (d == 0) p.lse_suf[row0 + g] = mmax + log2f(sum);
-    }
-  }
-  if (!direct) {
-    __threadfence();
-    __syncthreads();
-    if (solo_global) {  // every other part of (b, h) is already complete
-      for (int rr = warp; rr < G; rr += NW) merge_row<D>(p, b, h * G + rr, lane);
-      // every prefix arrival on (b, h) was made and nothing else arrives: clear it for the next step
-      if (ready && threadIdx.x == 0) p.counters[static_cast<int64_t>(b) * p.hkv + h] = 0;
-    } else {
-      __shared__ int last;
-      if (threadIdx.x == 0) last = arrive_is_last(p, b, h) ? 1 : 0;
-      __syncthreads();
-      if (last)
-        for (int rr = warp; rr < G; rr += NW) merge_row<D>(p, b, h * G + rr, lane);
-    }
-  }
-  if (p.pdl && p.concurrent) {
-    // launched as a dependent of the prefix kernel and never waiting for it: the grid's
-    // last CTA waits for the prefix grid, so this grid (and the stream after it) completes
-    // only after the prefix kernel (in the other form every CTA has waited already)
-    __syncthreads();
-    if (threadIdx.x == 0 && atomicAdd(p.done_ctas, 1) == static_cast<int>(gridDim.x) - 1) {
-      *p.done_ctas = 0;  // ready for the next step (stream-ordered)
-      pdl_wait_primary();
-      *p.prefix_done = 0;  // every prefix CTA has counted its rows
-    }
-  }
+  suffix_finish<D, NW, NW * 32>(p, cta, red, ms, ls, pre_o, pre_l, out_scale);
+  suffix_grid_tail(p);
 }
 
 template <int KV, int D, int NW, int NST>
@@ -527,6 +428,17 @@ int suffix_stages(int fallback) {
   return env > 0 ? env : fallback;
 }
 
+// e4m3 K/V at d = 128 run on the mma.sync kernel here; PSP_SUFFIX_TC=1 selects the
+// persistent tensor-core suffix kernel (kernel_suffix_tc.cu), which is exact but slower on
+// GB300 as measured (497 us against 260 us on the large-prefix fp8 batch).
+static bool suffix_tc_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("PSP_SUFFIX_TC");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
 cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
   if (num_splits <= 0) return cudaSuccess;
   if (p.kv_dtype == PSP_KV_BF16) {
@@ -539,6 +451,7 @@ cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
   }
   if (p.kv_dtype == PSP_KV_FP8) {
     if (p.head_dim != 128) return launch_t<PSP_KV_FP8, 64, 4, 6>(p, num_splits, s);
+    if (suffix_tc_enabled()) return launch_suffix_tc(p, num_splits, s);
     switch (suffix_stages(4)) {  // fp8 consumes two sub-tiles per iteration: at least 4 stages
       case 5: return launch_t<PSP_KV_FP8, 128, 4, 5>(p, num_splits, s);
       case 6: return launch_t<PSP_KV_FP8, 128, 4, 6>(p, num_splits, s);

@@ -478,6 +478,7 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.head_dim = c.head_dim;
   p.page_size = c.page_size;
   p.page_shift = h->page_shift;
+  p.num_sms = h->num_sms_resolved;
   p.kv_dtype = c.kv_dtype;
   p.q_dtype = c.q_dtype;
   p.o_dtype = c.o_dtype;
@@ -530,6 +531,8 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.status = I(L.status);
   p.done_ctas = I(L.status + 32);    // inside the status block, cleared with it at upload
   p.prefix_done = I(L.status + 48);
+  p.work_next = I(L.status + 8);
+  p.work_done = I(L.status + 12);
   {
     int64_t rows = 0;  // sum over prefix chunks of M_eff of the chunk's group, for every KV head
     for (size_t ci = 0; ci < P.chunk_group.size(); ++ci) rows += P.group_m_eff[P.chunk_group[ci]];

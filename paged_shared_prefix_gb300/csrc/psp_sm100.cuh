@@ -1,5 +1,5 @@
 // psp_sm100.cuh -- inline-PTX wrappers for the Blackwell (sm_100 family)
-// features used by the dense prefix kernel: mbarriers with bounded waits,
+// features used by the tcgen05 kernels: mbarriers with bounded waits,
 // TMA tensor loads, tensor-memory allocation, tcgen05.mma / commit / ld / st
 // and the shared-memory matrix and instruction descriptors.
 #pragma once
@@ -34,6 +34,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "{\n"
       ".reg .pred p;\n"
       "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Same test with an explicit suspend-time hint: a thread whose phase has not completed
+// is suspended (not eligible to issue) until it completes or about `ns` nanoseconds
+// pass, so a waiting warp leaves the issue slots of its sub-partition to working warps.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of the same condition (never suspends the thread): for a warp that
+// alternates between several barriers.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
       "selp.u32 %0, 1, 0, p;\n"
       "}\n"
       : "=r"(ok)
@@ -99,6 +132,54 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// TMA loads of one kTok-token tile (tile j of the token range [t0, t1) of a block table)
+// into dst, completing on bar.  The pool map is [slot][kv head][d] (make_pool_map), its
+// box min(page size, 64) tokens x 128 bytes of d; boxes start page-aligned relative to
+// t0 (callers keep t0 a multiple of the box height), so no box straddles a page.  Rows
+// at or past t1 are read from slot num_slots, out of the map: the copy fills them with
+// zeros.  Called by all lanes of a warp: lane l takes boxes l, l + 32, ..., so the
+// block-table lookups of a tile are independent loads in flight together (one lane
+// issuing every box would wait for each lookup in turn: 8 round trips per tile at page
+// size 16).
+template <int kTok, uint32_t kHalf, uint32_t kHalves, int kBoxElems>
+__device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, uint32_t bar, const int32_t* list,
+                                          int shift, int h, int t0, int t1, int j, int num_slots, int lane) {
+  const int mask = (1 << shift) - 1;
+  const int br = min(1 << shift, 64);  // rows per TMA box
+  for (int r = lane * br; r < kTok; r += 32 * br) {
+    const int tok = t0 + j * kTok + r;
+    const int slot = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
+#pragma unroll
+    for (uint32_t hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * kHalf + r * 128, map, hf * kBoxElems, h, slot, bar);
+  }
+}
+
+// Bounded wait with suspension between polls (mbar_try_wait_hint, 128 ns): at most
+// 2^23 polls, about a second; gives up as soon as another role has given up.
+__device__ __forceinline__ bool wait_or_abort_sleep(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                    int32_t* status, int site) {
+  for (uint32_t i = 0; i < (1u << 23); ++i) {
+    if (mbar_try_wait_hint(bar, parity, 128)) return true;
+    if ((i & 7) == 7 && *abort) return false;
+  }
+  atomicCAS(status, 0, kDevTimeout | (site << 8));
+  *abort = 1;
+  return false;
+}
+
+// Bounded wait that also gives up as soon as another role of the CTA has given up.
+// On its own timeout it records the site and raises the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status,
+                                              int site) {
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 31 && *abort) return false;
+  }
+  atomicCAS(status, 0, kDevTimeout | (site << 8));
+  *abort = 1;
+  return false;
 }
 
 // ------------------------------------------------------------------- TMEM
@@ -202,6 +283,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
@@ -222,10 +314,25 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t lbo,
   return d;
 }
 
+// Shared-memory matrix descriptor without swizzling: core matrices of 8 rows x 16
+// bytes stored as 128 contiguous bytes.  An MN-major operand whose MN extent is 16
+// bytes (one core matrix wide) steps along K by 8-row groups; both offsets are given
+// that stride, so the layout does not depend on which of the two the unit reads as the
+// K stride.
+__device__ __forceinline__ uint64_t plain_desc(uint32_t smem_addr, uint32_t k_group_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((k_group_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((k_group_stride >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version; layout type 0 = no swizzle
+  return d;
+}
+
 // Instruction descriptor, kind::f8f6f4 with e4m3 A and B and fp32 accumulation.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n, bool b_mn_major) {
-  return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
+// a_mn_major / b_mn_major: the operand is stored MN-major (transposed).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n, bool b_mn_major, bool a_mn_major = false) {
+  return (1u << 4) | (a_mn_major ? (1u << 15) : 0u) | (b_mn_major ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // Instruction descriptor, kind::f16 with fp32 accumulation.
@@ -240,4 +347,9 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, int ab_type, bool
 }
 
 }  // namespace sm100
+
+// Tensor map of a K or V pool [slots][Hkv][d] (d = 128), 128-byte swizzle, box = 128
+// bytes of d x 1 head x `rows` tokens; defined with the dense prefix kernel.
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int64_t slots, int hkv, int rows, bool fp8);
+
 }  // namespace psp

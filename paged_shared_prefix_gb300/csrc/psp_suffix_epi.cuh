@@ -1,0 +1,165 @@
+// psp_suffix_epi.cuh -- the end of one suffix (split, KV head) CTA, shared by the
+// suffix kernels: the prefetch of a single-split request's shared-prefix
+// partial rows, and the combination of the CTA's partial softmax states into
+// either the request's final output (merged with those prefix rows) or a
+// normalised partial (O, log2-LSE) that goes through the (request, KV head)
+// counter ("GraniKV", section 3: the prefix result is merged with each
+// request's suffix attention; the merge itself is in psp_merge.cuh).
+#pragma once
+
+#include "psp_device.cuh"
+#include "psp_internal.h"
+#include "psp_merge.cuh"
+
+namespace psp {
+namespace dev {
+
+constexpr int kPreRows = 16;  // prefix partial rows (chunks x query heads) prefetched per single-split request
+
+// What the end of a suffix CTA needs to know about its request.
+struct SuffixCta {
+  int split, h, b;
+  int c0, n_chunks;  // b's shared-prefix chunks [c0, c0 + n_chunks)
+  bool solo;         // one suffix split and the prefix kernels complete before its rows are read
+  bool pre_smem;     // solo, and the prefix rows fit the shared-memory prefetch area
+  bool wait_prefix;  // dependent launch, sequential form: prefix rows only after the prefix grid
+};
+
+__device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, int split, int h) {
+  SuffixCta c;
+  c.split = split;
+  c.h = h;
+  c.b = p.split_req[split];
+  const int g_req = p.req_group[c.b];
+  c.solo = !p.concurrent && p.split_indptr[c.b + 1] - p.split_indptr[c.b] == 1;
+  c.c0 = g_req >= 0 ? p.group_chunk_indptr[g_req] : 0;
+  c.n_chunks = g_req >= 0 ? p.group_chunk_indptr[g_req + 1] - c.c0 : 0;
+  c.pre_smem = c.solo && c.n_chunks > 0 && c.n_chunks * p.group <= kPreRows;
+  c.wait_prefix = p.pdl && !p.concurrent;
+  return c;
+}
+
+// cp.async of b's prefix partial rows of head h into pre_o [chunk * G + j][D] and
+// pre_l [chunk * G + j], by NT threads numbered tid = 0 .. NT - 1 (the caller commits
+// and waits).
+template <int D, int NT>
+__device__ __forceinline__ void prefetch_prefix_rows(const StepParams& p, const SuffixCta& c, float* pre_o,
+                                                     float* pre_l, int tid = threadIdx.x) {
+  const int G = p.group;
+  const int m_eff = p.group_m_eff[p.req_group[c.b]];
+  const int prow = p.req_member[c.b] * G;
+  constexpr int kRowChunks = D * 4 / 16;
+  for (int e = tid; e < c.n_chunks * G * (kRowChunks + 1); e += NT) {
+    const int ch = e / (G * (kRowChunks + 1));
+    const int rem = e - ch * G * (kRowChunks + 1);
+    const int j = rem / (kRowChunks + 1);
+    const int q = rem - j * (kRowChunks + 1);
+    const int64_t row = p.chunk_row_offset[c.c0 + ch] + static_cast<int64_t>(c.h) * m_eff + prow + j;
+    if (q < kRowChunks) {
+      cp_async_16(smem_u32(pre_o + (ch * G + j) * D + q * 4), p.o_pre + row * D + q * 4, true);
+    } else {
+      cp_async_4(smem_u32(pre_l + ch * G + j), p.lse_pre + row);
+    }
+  }
+}
+
+// Combines NSTATE partial softmax states of the CTA's G query heads (red [state][8][D]
+// unnormalised outputs, ms [state][8] log2-domain maxima, ls [state][8] sums, all in
+// shared memory and complete) and delivers the result.  A single-split request writes
+// its final output, merged with its prefix rows when they are in pre_o / pre_l; any
+// other writes its normalised partial and arrives on the (b, h) counter, and the
+// arrival that completes (b, h) merges it.  Called by all NT threads of the CTA, after
+// a __syncthreads() that follows the writes of red / ms / ls (and, for pre_smem, of
+// the prefetched rows).
+template <int D, int NSTATE, int NT>
+__device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixCta& c, const float* red,
+                                              const float* ms, const float* ls, const float* pre_o,
+                                              const float* pre_l, float out_scale) {
+  constexpr int kWarps = NT / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int b = c.b, h = c.h;
+  const bool one_split = p.split_indptr[b + 1] - p.split_indptr[b] == 1;
+  const bool only_part = one_split && c.n_chunks == 0;
+  const bool direct = only_part || (c.solo && c.pre_smem);
+  // Launched as a dependent of a still running prefix kernel: a one-split request whose
+  // prefix partials are all complete (every prefix row counted done) merges them here like
+  // a solo request; otherwise its part goes through the (request, KV head) counter.
+  bool ready = false;
+  if (p.pdl && p.concurrent && one_split && c.n_chunks > 0) {
+    __shared__ int prefix_ready;
+    if (threadIdx.x == 0) prefix_ready = *reinterpret_cast<volatile int32_t*>(p.prefix_done) == p.prefix_rows_total;
+    __syncthreads();
+    ready = prefix_ready != 0;
+    if (ready) __threadfence();  // the prefix partials were fenced before their rows were counted
+  }
+  const bool solo_global = (c.solo && !direct) || ready;  // read the prefix partials from global memory
+  const int64_t row0 = (static_cast<int64_t>(c.split) * p.hkv + h) * G;
+  const int64_t orow0 = static_cast<int64_t>(b) * p.hq + h * G;
+  for (int e = threadIdx.x; e < G * D; e += NT) {
+    const int g = e / D;
+    const int d = e - g * D;
+    float mmax = neg_inf();
+#pragma unroll
+    for (int w = 0; w < NSTATE; ++w) mmax = fmaxf(mmax, ms[w * 8 + g]);
+    float acc = 0.f, sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < NSTATE; ++w) {
+      const float sc = exp2f(ms[w * 8 + g] - mmax);
+      sum += ls[w * 8 + g] * sc;
+      acc += red[(w * 8 + g) * D + d] * sc;
+    }
+    if (direct) {
+      // own part: O_s = acc / sum * out_scale with log2-LSE mmax + log2(sum); prefix chunks first
+      float lse_own = mmax + log2f(sum);
+      float big = lse_own;
+      for (int ch = 0; ch < c.n_chunks; ++ch) big = fmaxf(big, pre_l[ch * G + g]);
+      float wsum = 0.f, out = 0.f;
+      for (int ch = 0; ch < c.n_chunks; ++ch) {
+        const float w = exp2f(pre_l[ch * G + g] - big);
+        wsum += w;
+        out = fmaf(w, pre_o[(ch * G + g) * D + d], out);
+      }
+      const float w_own = exp2f(lse_own - big);
+      wsum += w_own;
+      out = fmaf(w_own, acc / sum * out_scale, out);
+      store_final(p, orow0 + g, d, out / wsum);
+      if (d == 0 && p.lse) p.lse[orow0 + g] = (big + log2f(wsum)) * 0.6931471805599453f;
+    } else {
+      p.o_suf[(row0 + g) * D + d] = acc / sum * out_scale;
+      if (d == 0) p.lse_suf[row0 + g] = mmax + log2f(sum);
+    }
+  }
+  if (!direct) {
+    __threadfence();
+    __syncthreads();
+    if (solo_global) {  // every other part of (b, h) is already complete
+      for (int rr = warp; rr < G; rr += kWarps) merge_row<D>(p, b, h * G + rr, lane);
+      // every prefix arrival on (b, h) was made and nothing else arrives: clear it for the next step
+      if (ready && threadIdx.x == 0) p.counters[static_cast<int64_t>(b) * p.hkv + h] = 0;
+    } else {
+      __shared__ int last;
+      if (threadIdx.x == 0) last = arrive_is_last(p, b, h) ? 1 : 0;
+      __syncthreads();
+      if (last)
+        for (int rr = warp; rr < G; rr += kWarps) merge_row<D>(p, b, h * G + rr, lane);
+    }
+  }
+}
+
+// End of every suffix CTA.  Launched as a dependent of the prefix kernel and never
+// waiting for it (the concurrent form), the grid's last CTA waits for the prefix grid,
+// so this grid (and the stream after it) completes only after the prefix kernel; in the
+// sequential form every CTA has waited already.  Called by every thread of the CTA.
+__device__ __forceinline__ void suffix_grid_tail(const StepParams& p) {
+  if (!p.pdl || !p.concurrent) return;
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(p.done_ctas, 1) == static_cast<int>(gridDim.x) - 1) {
+    *p.done_ctas = 0;  // ready for the next step (stream-ordered)
+    pdl_wait_primary();
+    *p.prefix_done = 0;  // every prefix CTA has counted its rows
+  }
+}
+
+}  // namespace dev
+}  // namespace psp

@@ -329,3 +329,65 @@ def test_multi_group_mixed_branches_match_oracle():
         o, lse = run_case(case, threshold=thr, tensors=tens, **kw)
         assert np.isfinite(o).all() and np.isfinite(lse).all(), (thr, kw)
         assert max_err(o, ref_o) <= tol and max_err(lse, ref_lse) <= tol, (thr, kw, max_err(o, ref_o))
+
+
+def _fp8_growing_scores_case():
+    """e4m3 suffixes whose first 128 keys per request are zero: the first tile's scores are
+    all 0, so a later tile's maximum exceeds the first reference by more than 2^8 and the
+    tensor-core suffix kernel must move its reference max and rescale O^T mid-sequence.
+    Lengths give 1-11 tiles (ragged tails; more tiles than ring stages)."""
+    case = workloads.make_case("fp8_large", 11, batch=4, prefix_len=0, private_lengths=[700, 130, 1300, 257])
+    ps = case.page_size
+    k = case.k_pool.reshape(-1, case.workload.num_kv_heads, case.workload.head_dim)
+    for b in range(case.batch):
+        pages = case.page_indices[case.page_indptr[b]:case.page_indptr[b + 1]]
+        t = np.arange(min(128, int(case.kv_len[b])))
+        k[pages[t // ps] * ps + t % ps] = 0  # e4m3 code 0 is +0
+    return case
+
+
+@pytest.mark.gpu
+def test_fp8_suffix_rescale_and_long_splits(monkeypatch):
+    case = _fp8_growing_scores_case()
+    ref_o, ref_lse = oracle.attend_all(case)
+    tol = TOL["fp8_e4m3"]
+    tens = device_tensors(case)
+    # default partition (256-token splits here: every request is merged through its
+    # counter), then one split per request (direct merge, up to 11 tiles per CTA)
+    for min_tiles in (None, "64"):
+        if min_tiles:
+            monkeypatch.setenv("PSP_SPLIT_MIN_TILES", min_tiles)
+        o, lse = run_case(case, tensors=tens)
+        assert np.isfinite(o).all() and np.isfinite(lse).all(), min_tiles
+        assert max_err(o, ref_o) <= tol and max_err(lse, ref_lse) <= tol, (min_tiles, max_err(o, ref_o))
+
+
+@pytest.mark.gpu
+def test_fp8_suffix_tensor_core_kernel_matches_oracle():
+    # the persistent tcgen05 suffix kernel is opt-in (PSP_SUFFIX_TC=1, read once per
+    # process): a child process runs it on a prefix batch and on the growing-scores case
+    # (mid-sequence rescale; default and one-split partitions)
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import os, sys; sys.path[:0] = [%r, %r]\n"
+        "import numpy as np, oracle, workloads\n"
+        "from gpu_util import TOL, max_err, run_case\n"
+        "from test_gpu_parity import _fp8_growing_scores_case\n"
+        "tol = TOL['fp8_e4m3']\n"
+        "case = workloads.make_case('fp8_large', 3, batch=6, prefix_len=256, private_range=(1, 400))\n"
+        "o, lse = run_case(case)\n"
+        "ro, rl = oracle.attend_all(case)\n"
+        "assert max_err(o, ro) <= tol and max_err(lse, rl) <= tol, max_err(o, ro)\n"
+        "case = _fp8_growing_scores_case()\n"
+        "ro, rl = oracle.attend_all(case)\n"
+        "for mt in (None, '64'):\n"
+        "    if mt: os.environ['PSP_SPLIT_MIN_TILES'] = mt\n"
+        "    o, lse = run_case(case)\n"
+        "    assert np.isfinite(o).all() and max_err(o, ro) <= tol and max_err(lse, rl) <= tol, (mt, max_err(o, ro))\n"
+        "print('ok')\n" % (here, os.path.dirname(here)))
+    env = dict(os.environ, PSP_SUFFIX_TC="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
