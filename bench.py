@@ -202,10 +202,19 @@ def oracle_timing(case, target_s: float, seed: int = 0) -> dict:
     t = time.perf_counter()
     oracle.attend(case, rows // Hq, rows % Hq)
     dt = time.perf_counter() - t
+    reps = 1
+    if n2 == len(order) and dt < 0.5 * target_s:
+        # the whole step is shorter than the target: repeat it and average
+        reps = 0
+        t = time.perf_counter()
+        while reps < 10000 and (reps == 0 or time.perf_counter() - t < target_s):
+            oracle.attend(case, rows // Hq, rows % Hq)
+            reps += 1
+        dt = (time.perf_counter() - t) / reps
     tok = float(case.kv_len[rows // Hq].astype(np.int64).sum())
     step_s = dt * total_tok / tok
     return {"step_s": step_s, "rows": int(n2), "total_rows": int(B * Hq), "cores": oracle.num_threads(),
-            "sample_s": dt}
+            "sample_s": dt * reps, "reps": reps}
 
 
 # ------------------------------------------------------------------ replicas
@@ -518,8 +527,10 @@ def main():
         ot = oracle_timing(case, args.cpu_seconds)
         result["cpu_baseline"] = {"value": ub / ot["step_s"] / 1e9, "unit": UNIT, "cores": ot["cores"],
                                   "kind": "oracle", "us_per_step": ot["step_s"] * 1e6,
-                                  "sample": f"{ot['rows']} of {ot['total_rows']} (request, head) rows, "
-                                            f"{ot['sample_s']:.1f} s of fp64 work, scaled by context tokens"}
+                                  "sample": f"{ot['rows']} of {ot['total_rows']} (request, head) rows"
+                                            + (f", the whole step {ot['reps']} times" if ot["reps"] > 1 else "")
+                                            + f", {ot['sample_s']:.1f} s of fp64 work on {ot['cores']} threads, "
+                                            "scaled by context tokens"}
     step.close()
     if world > 1:
         dist.barrier()
