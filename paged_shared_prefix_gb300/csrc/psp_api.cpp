@@ -101,6 +101,7 @@ struct psp_handle {
   cudaStream_t side = nullptr;
   cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
   bool allow_concurrent = true;   // false on the workspace-free path (no object creation)
+  int32_t pdl_form = 0;           // dependent-launch form: 0 by grid size, 1 sequential, 2 concurrent
 
   // per-kernel timing
   bool timing = false;
@@ -605,6 +606,7 @@ psp_status psp_create(const psp_config* cfg, psp_handle** out) {
   h->split_ctas_per_sm = env_int("PSP_SPLIT_CTAS_PER_SM", kSplitCtasPerSm);
   h->prefix_min_tiles = env_int("PSP_PREFIX_MIN_TILES", kPrefixMinTiles);
   h->prefix_ctas_per_sm = env_int("PSP_PREFIX_CTAS_PER_SM", kPrefixCtasPerSm);
+  h->pdl_form = env_int("PSP_PDL_FORM", 0);
   if (c.dense_threshold == 0) {
     const int t = env_int("PSP_DENSE_THRESHOLD", 0);
     if (t > 0) h->cfg.dense_threshold = t;
@@ -801,6 +803,9 @@ psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
   // 76 vs 81 us); when the prefix grid fills the GPU, the suffix CTAs wait for it before
   // reading prefix partials and keep the sequential protocol (agent batch: 148 vs 163 us).
   if (p.pdl && static_cast<int64_t>(nd + nc) * p.hkv * 2 <= h->num_sms_resolved) p.concurrent = 1;
+  // PSP_PDL_FORM overrides the choice for measurements: 1 sequential, 2 concurrent
+  if (p.pdl && h->pdl_form == 1) p.concurrent = 0;
+  if (p.pdl && h->pdl_form == 2) p.concurrent = 1;
   if (p.token_flat) {
     st = timed_launch(h, s, "expand_kv_indices", slot, expand_entry, p, 0);
     if (st) return st;
