@@ -72,6 +72,23 @@ struct HostPlan {
   PlanLayout layout{};
   psp_plan_info info{};
   std::vector<unsigned char> image;  // the uploaded integer region, laid out as in the workspace
+
+  // Empties the plan for the next step, keeping every array's allocation (a decode loop
+  // plans every step with arrays of about the same sizes).
+  void clear() {
+    B = NG = NS = NC = 0;
+    for (std::vector<int32_t>* v :
+         {&suffix_page_indptr, &suffix_page_indices, &suffix_start, &suffix_len, &split_indptr, &split_req,
+          &split_begin, &split_end, &req_group, &req_member, &group_page_indptr, &group_page_indices,
+          &group_m_eff, &group_shared_len, &group_branch, &group_row_blocks, &group_member_indptr, &group_members,
+          &group_chunk_indptr, &chunk_group, &chunk_begin, &chunk_end, &chunk_row_offset, &item_chunk_dense,
+          &item_rb_dense, &item_chunk_cascade, &item_rb_cascade, &kv_indptr})
+      v->clear();
+    kv_indices_len = suffix_tokens = shared_tokens = pre_rows = 0;
+    layout = PlanLayout{};
+    info = psp_plan_info{};
+    image.clear();
+  }
 };
 
 }  // namespace
@@ -201,7 +218,7 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   const int64_t tile = psp::kTileTokens;
   const int32_t threshold = c.dense_threshold > 0 ? c.dense_threshold : kDefaultDenseThreshold;
   const int64_t sms = h->num_sms_resolved;
-  P = HostPlan();
+  P.clear();
   P.B = B;
   P.NG = NG;
 
