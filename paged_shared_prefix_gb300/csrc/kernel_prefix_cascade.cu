@@ -320,7 +320,7 @@ cudaError_t launch_t(const StepParams& p, const int32_t* chunks, const int32_t* 
   using C = PreCfg<KV, D>;
   const int bytes = NST * C::kStageBytes;
   auto kern = prefix_cascade_kernel<KV, D, NW, NST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = ensure_smem_limit<prefix_cascade_kernel<KV, D, NW, NST>>(bytes);
   if (e != cudaSuccess) return e;
   const int grid = n * per_item * p.hkv;
   kern<<<grid, NW * 32, bytes, s>>>(p, chunks, rbs, per_item);

@@ -506,7 +506,7 @@ cudaError_t launch_t(const StepParams& p, int num_items, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   constexpr uint32_t bytes = DenseCfg<FP8>::kSmemBytes;
   static_assert(bytes <= 232448, "dense prefix CTA exceeds the shared memory of one SM");
-  e = cudaFuncSetAttribute(prefix_dense_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  e = ensure_smem_limit<prefix_dense_kernel<FP8>>(bytes);
   if (e != cudaSuccess) return e;
   const int grid = num_items * p.hkv;
   prefix_dense_kernel<FP8><<<grid, kThreads, bytes, s>>>(p, kmap, vmap, static_cast<int>(slots));

@@ -399,7 +399,7 @@ cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
   const int epi = (NW * 8 * D + 2 * NW * 8) * 4;
   const int bytes = (ring > epi ? ring : epi) + kPreRows * (D + 1) * 4;
   auto kern = suffix_kernel<KV, D, NW, NST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = ensure_smem_limit<suffix_kernel<KV, D, NW, NST>>(bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_splits * p.hkv);

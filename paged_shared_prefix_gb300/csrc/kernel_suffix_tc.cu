@@ -782,7 +782,7 @@ cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
   constexpr uint32_t bytes = TcCfg<NS>::kSmemBytes;
   static_assert(bytes <= 232448, "suffix CTA exceeds the shared memory of one SM");
   auto kern = suffix_tc_kernel<NS>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  e = ensure_smem_limit<suffix_tc_kernel<NS>>(bytes);
   if (e != cudaSuccess) return e;
   const int total = num_splits * p.hkv;
   const int grid = total < p.num_sms ? total : (p.num_sms > 0 ? p.num_sms : 1);

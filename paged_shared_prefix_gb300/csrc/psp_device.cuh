@@ -12,6 +12,21 @@
 #include "psp_internal.h"
 
 namespace psp {
+
+// Raises the dynamic shared-memory limit of kernel Kern to `bytes` once per device
+// (the driver call would otherwise cost host time on every step's launch).
+template <auto Kern>
+inline cudaError_t ensure_smem_limit(int bytes) {
+  static int done_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (done_dev == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done_dev = dev;
+  return e;
+}
+
 namespace dev {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
