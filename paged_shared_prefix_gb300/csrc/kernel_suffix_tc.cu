@@ -1,6 +1,9 @@
 // kernel_suffix_tc.cu -- split-KV paged decode over each request's private
 // suffix for fp8-e4m3 K/V at d = 128, on the 5th-generation tensor cores, as
-// one persistent CTA per SM.
+// one persistent CTA per SM.  Selected with PSP_SUFFIX_TC=1: it is exact, but on
+// GB300 it measured slower than the mma.sync kernel in kernel_suffix.cu, which
+// stays the default (its per-item epilogue throttles the stream; see the design
+// notes for the measurements).
 //
 // Same work as the suffix kernel in kernel_suffix.cu (one item = one (split, KV
 // head); all G <= 8 query heads of the KV head are served from one read of each
@@ -18,11 +21,12 @@
 //                        with the block-table entries of the next tile already loaded;
 //   warp 10 (queries)    quantises the next item's query rows to e4m3 (per-row scale
 //                        amax/448) into one of two query buffers;
-//   warp 9 (MMA)         one lane issues S^T = K Q^T (M = 128 tokens, N = 16: the
-//                        query heads padded, K = 128) into one of two TMEM score
-//                        buffers, and O^T += V^T P^T (M = 128 = d, N = 16, K = 128
-//                        tokens) into one of two TMEM output buffers, with V read
-//                        MN-major straight from its tile and P^T from shared memory;
+//   warp 9 (MMA)         one lane issues, whichever is ready first, S^T = K Q^T
+//                        (M = 128 tokens, N = 16: the query heads padded, K = 128)
+//                        into one of two TMEM score buffers, and O^T += V^T P^T
+//                        (M = 128 = d, N = 16, K = 128 tokens) into one of two TMEM
+//                        output buffers, with V read MN-major straight from its tile
+//                        and P^T from shared memory;
 //   warps 0-3 (softmax)  one thread per token row of a tile (= TMEM lane): scores of
 //                        its 8 heads, exp2 against a reference max per head, the P^T
 //                        row as 8 e4m3 codes;
@@ -34,9 +38,9 @@
 // 2^8 (near e4m3's largest finite value) starts an exchange of the tile's maxima among
 // the softmax warps, after which that tile's max maps to 2^4 (small probabilities stay
 // clear of e4m3's subnormals) and O^T is rescaled in tensor memory; otherwise a tile
-// costs the softmax warps one barrier.  The key scale folds into the score scale and
-// the value scale into the output ("GraniKV", section 2: each request's private suffix
-// is read through its block table; the pages' fp8 caches keep per-head scales).
+// costs the softmax warps one barrier.  The per-KV-head key scale folds into the score
+// scale and the value scale into the output ("GraniKV", section 2: each request's
+// private suffix is read through its block table).
 // Every mbarrier wait is bounded and watches a CTA-wide abort flag; each warp group
 // takes its decisions to leave through barrier reductions, so no warp waits at a
 // barrier for one that has left.
