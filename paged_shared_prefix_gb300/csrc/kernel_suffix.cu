@@ -33,6 +33,8 @@ namespace {
 
 using namespace dev;
 
+constexpr int kTablePrefetch = 8;  // sub-tiles (per warp) between a table prefetch and its use
+
 template <int KV, int D>
 struct SufCfg {
   static constexpr int kElem = (KV == PSP_KV_BF16) ? 2 : 1;
@@ -209,6 +211,11 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     for (int u = 0; u < U; ++u) {
       const int nx = i0 + NST - U + u;
       if (nx < my_n) load_pages(nx, pages[u]);  // in flight while this iteration computes
+      // the block-table entries of a sub-tile kTablePrefetch iterations later, pulled into L2
+      // now: at small page sizes every sub-tile reads its own 64 bytes of the table, and a
+      // DRAM round trip taken only one sub-tile ahead of the copies would stall them
+      const int pf = nx + kTablePrefetch;
+      if (lane == 0 && pf < my_n) prefetch_l2(list + ((t0 + (warp + pf * NW) * 16) >> shift));
     }
     cp_async_wait<NST - 2 * U>();
     __syncwarp();

@@ -41,6 +41,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // SMs the prefix kernel leaves free).  A no-op when no dependent is launched.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 // Waits until the grids this one depends on have completed and their writes are visible.
+// Pulls the line holding ptr into L2 (no register result, so nothing waits for it).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(ptr));
+}
 __device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool valid) {
