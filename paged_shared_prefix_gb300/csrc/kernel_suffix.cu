@@ -450,10 +450,10 @@ cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
   if (num_splits <= 0) return cudaSuccess;
   if (p.kv_dtype == PSP_KV_BF16) {
     if (p.head_dim != 128) return launch_t<PSP_KV_BF16, 64, 4, 4>(p, num_splits, s);
-    switch (suffix_stages(3)) {
-      case 2: return launch_t<PSP_KV_BF16, 128, 4, 2>(p, num_splits, s);
+    switch (suffix_stages(2)) {  // 2 stages: three CTAs per SM (measured best with 5 split CTAs per SM)
+      case 3: return launch_t<PSP_KV_BF16, 128, 4, 3>(p, num_splits, s);
       case 4: return launch_t<PSP_KV_BF16, 128, 4, 4>(p, num_splits, s);
-      default: return launch_t<PSP_KV_BF16, 128, 4, 3>(p, num_splits, s);
+      default: return launch_t<PSP_KV_BF16, 128, 4, 2>(p, num_splits, s);
     }
   }
   if (p.kv_dtype == PSP_KV_FP8) {

@@ -31,7 +31,7 @@ using psp::StepParams;
 constexpr int32_t kDefaultDenseThreshold = 16;
 
 constexpr int32_t kSplitMinTiles = 4;
-constexpr int32_t kSplitCtasPerSm = 8;  // measured: 8 (split, head) CTAs per SM balance best
+constexpr int32_t kSplitCtasPerSm = 5;  // measured on GB300 with 2-stage bf16 rings: 5 (split, head) CTAs per SM
 constexpr int32_t kPrefixMinTiles = 4;
 constexpr int32_t kPrefixCtasPerSm = 1;  // a dense prefix CTA fills an SM (all of tensor memory)
 
