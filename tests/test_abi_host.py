@@ -259,3 +259,59 @@ def test_plan_query_capacity_and_empty_batch():
     step.plan(np.zeros(0, np.int32), np.zeros(1, np.int32), np.zeros(0, np.int32))
     assert step.plan_info()["num_splits"] == 0
     step.close()
+
+
+def _random_batch(rng, ps, n_pages, max_b=24):
+    """A seeded random batch: 0-3 prefix groups (unaligned prefix lengths, some shorter
+    than a page), ungrouped requests, suffixes of 1-700 tokens, pages drawn without
+    replacement from a pool of n_pages."""
+    import dataclasses
+    B = int(rng.integers(1, max_b + 1))
+    ng = int(rng.integers(0, 4))
+    gl = rng.integers(0, 900, ng).astype(np.int32)
+    groups = rng.integers(-1, ng, B).astype(np.int32) if ng else np.full(B, -1, np.int32)
+    priv = rng.integers(1, 701, B)
+    if rng.random() < 0.2:
+        priv[:] = 1
+    pre_len = gl[np.maximum(groups, 0)] if ng else np.zeros(B, np.int32)
+    kv_len = (np.where(groups >= 0, pre_len, 0) + priv).astype(np.int32)
+    perm = rng.permutation(n_pages)
+    pos = 0
+    shared = []
+    for g in range(ng):
+        n = int(gl[g]) // ps
+        shared.append(perm[pos:pos + n])
+        pos += n
+    tables = []
+    for b in range(B):
+        g = int(groups[b])
+        pre = shared[g] if g >= 0 else np.zeros(0, np.int64)
+        need = -(-int(kv_len[b]) // ps) - len(pre)
+        tables.append(np.concatenate([pre, perm[pos:pos + need]]))
+        pos += need
+    assert pos <= n_pages
+    indptr = np.concatenate([[0], np.cumsum([len(t) for t in tables])]).astype(np.int32)
+    base = workloads.make_case("agent", 0, batch=B, page_size=ps, tables_only=True)
+    return dataclasses.replace(base, num_pages=n_pages, kv_len=kv_len, page_indptr=indptr,
+                               page_indices=np.concatenate(tables).astype(np.int32), prefix_group=groups,
+                               group_prefix_len=gl)
+
+
+@pytest.mark.parametrize("ps", [1, 16, 128])
+def test_replans_on_one_handle_match_oracle(ps):
+    # one handle plans a sequence of random batches that grow and shrink; every plan must
+    # match the oracle's exactly (nothing of an earlier plan may leak into a later one)
+    rng = np.random.default_rng([11, ps])
+    n_pages = 40000 // ps + 64
+    first = _random_batch(rng, ps, n_pages)
+    step = psp.DecodeStep.for_case(first, num_sms=NUM_SMS)
+    for i in range(12):
+        case = first if i == 0 else _random_batch(rng, ps, n_pages)
+        step.plan_case(case)
+        info = step.plan_info()
+        ref = oracle.plan(case, {k: info[k] for k, _ in oracle.PlanParams._fields_})
+        for f in PLAN_FIELDS:
+            assert np.array_equal(step.plan_query(f), np.asarray(ref[f], np.int32)), (ps, i, f)
+        assert info["num_splits"] == len(ref["split_begin"]) and info["num_chunks"] == len(ref["chunk_begin"])
+        assert info["num_groups"] == case.num_groups
+    step.close()
