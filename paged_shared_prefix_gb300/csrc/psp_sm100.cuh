@@ -108,13 +108,9 @@ __device__ __forceinline__ bool group_bar_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
-// Named barrier `id` completing when `nthreads` threads have arrived: sync waits for
-// it, arrive only counts (a producer/consumer hand-off between warp groups).
+// Named barrier `id` over `nthreads` threads (whole warps): waits until all have arrived.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("barrier.cta.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
-}
-__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
-  asm volatile("barrier.cta.arrive %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------------------- TMA
@@ -273,14 +269,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
       "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
       "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 // 8 consecutive 32-bit columns of this thread's TMEM lane.
