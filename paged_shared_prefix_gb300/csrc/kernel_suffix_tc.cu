@@ -696,27 +696,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // direct delivery the weights of the prefix chunks' rows and of the own part, all
       // divided by their sum (prefix chunks first, then the own part)
       if (d < G) {
+        // SFU approximations and one reciprocal: this runs as one dependent chain per head
+        // on a few lanes of one warp, between the item's end and its delivery
         const int hd = d;
         float lse_own = 0.f, l_own = 1.f;
 #pragma unroll
         for (int h8 = 0; h8 < 8; ++h8)
           if (h8 == hd) {
-            lse_own = Mx[h8] + log2f(Ls[h8]);
+            lse_own = Mx[h8] + __log2f(Ls[h8]);
             l_own = Ls[h8];
           }
         float* w = hw + hd * kHw;
         if (direct) {
           float big = lse_own;
           for (int ch = 0; ch < cta.n_chunks; ++ch) big = fmaxf(big, pre_l[ch * G + hd]);
-          float wsum = exp2f(lse_own - big);
-          for (int ch = 0; ch < cta.n_chunks; ++ch) wsum += exp2f(pre_l[ch * G + hd] - big);
-          const float inv = 1.f / wsum;
-          for (int ch = 0; ch < cta.n_chunks; ++ch) w[1 + ch] = exp2f(pre_l[ch * G + hd] - big) * inv;
-          w[0] = exp2f(lse_own - big) * inv * vs / l_own;
-          w[kHw - 1] = big + log2f(wsum);
-          if (p.lse) p.lse[orow0 + hd] = (big + log2f(wsum)) * 0.6931471805599453f;
+          const float w_own = ex2(lse_own - big);
+          float wsum = w_own;
+          for (int ch = 0; ch < cta.n_chunks; ++ch) {
+            const float wc = ex2(pre_l[ch * G + hd] - big);
+            w[1 + ch] = wc;
+            wsum += wc;
+          }
+          const float inv = __frcp_rn(wsum);
+          for (int ch = 0; ch < cta.n_chunks; ++ch) w[1 + ch] *= inv;
+          w[0] = w_own * inv * vs * __frcp_rn(l_own);
+          w[kHw - 1] = big + __log2f(wsum);
+          if (p.lse) p.lse[orow0 + hd] = w[kHw - 1] * 0.6931471805599453f;
         } else {
-          w[0] = vs / l_own;
+          w[0] = vs * __frcp_rn(l_own);
           w[kHw - 1] = lse_own;
         }
       }
