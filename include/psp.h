@@ -41,6 +41,25 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Launches and copies are asynchronous on it.
  *   - A handle serves one stream at a time and is not thread-safe.
+ *
+ * Environment overrides, for measurements and tuning sweeps (read when a
+ * handle is created, or once per process where marked; the defaults are the
+ * values measured best on GB300):
+ *   PSP_DENSE_THRESHOLD     dispatcher threshold T when psp_config.dense_threshold
+ *                           is 0 (default 16)
+ *   PSP_SPLIT_MIN_TILES     smallest split in 64-token granules (default 4)
+ *   PSP_SPLIT_CTAS_PER_SM   split-KV target, (split, KV head) items per SM (default 5)
+ *   PSP_PREFIX_MIN_TILES,   prefix-chunk partition: smallest chunk in 64-token granules
+ *   PSP_PREFIX_CTAS_PER_SM  (default 4) and prefix CTAs per SM (default 1)
+ *   PSP_PDL_FORM            prefix -> suffix dependent launch: 0 chosen by the prefix
+ *                           grid's size (default), 1 sequential, 2 concurrent
+ *   PSP_SUFFIX_STAGES       suffix ring depth per warp at d = 128 (default 2 for bf16,
+ *                           4 for e4m3; once per process)
+ *   PSP_SUFFIX_TC           1: e4m3 K/V at d = 128 use the persistent tcgen05 suffix
+ *                           kernel (exact, slower as measured; once per process)
+ *   PSP_SUFFIX_TC_STAGES    its ring depth (default 6; once per process)
+ * The plan outputs depend on the partition constants; psp_plan_info_get reports
+ * the values a plan was built with.
  */
 #ifndef PSP_H_
 #define PSP_H_
