@@ -29,6 +29,17 @@ def test_library_exports_every_declared_function():
     assert set(names) == set(psp.EXPORTED), "binding and header disagree"
 
 
+def test_header_documents_every_environment_override():
+    import glob
+    header = open(os.path.join(ROOT, "include", "psp.h")).read()
+    section = header[header.index("Environment overrides"):header.index("#ifndef PSP_H_")]
+    documented = set(re.findall(r"\bPSP_[A-Z_]+[A-Z]\b", section))
+    read = set()
+    for path in glob.glob(os.path.join(ROOT, "paged_shared_prefix_gb300", "csrc", "*.c*")):
+        read |= set(re.findall(r'(?:getenv|env_int)\("(PSP_[A-Z_]+)"', open(path).read()))
+    assert read and read == documented, (sorted(read - documented), sorted(documented - read))
+
+
 def test_version_and_status_strings():
     assert "sm_103a" in psp.version()
     for code in psp.STATUS_NAMES:
