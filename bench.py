@@ -2,27 +2,31 @@
 """Benchmark of one paged shared-prefix decode-attention step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--page-size P]
-                    [--impl reference]
+                    [--layout scatter|contiguous|block128] [--impl reference]
 
 A step is one call of psp_run over the whole synthetic batch: the prefix
-kernel of the shared-prefix group (dense or cascade branch, chosen by the
+kernel of each shared-prefix group (dense or cascade branch, chosen by the
 dispatcher) and the split-KV suffix kernel, whose last arriving CTA per
 (request, KV head) performs the log-sum-exp merge, with the K/V pool, the
 queries and the uploaded plan resident in HBM.  The metric is device time per
 step and the achieved HBM bandwidth on the step's unique K/V bytes (a shared
 prefix page counts once).  L2 is flushed (a buffer of twice the L2 size is
-written and read back) between timed steps, outside the timed events.  The
-default workload is the Llama-3.1-8B-shaped layer without sharing (B=32,
-32/8 heads, bf16, contexts U[2048,4096], page size 16); --workload selects
-the shared-prefix batches.
+written and read back) between timed steps, outside the timed events.
+
+The default workload is the largest single-GPU batch: 512 requests sharing a
+16,384-token prefix stored once (64 q / 8 KV heads, M_eff 4096, e4m3 K/V
+with per-head scales, suffixes U[1,2048], page size 16).  The Llama-shaped
+layer without sharing, the 256-request agent batch and the short-prefix batch
+are measured in the same process (per_config).
 
 Printed (rank 0, one JSON line): value = unique-KV GB/s over all ranks,
-us_per_step, the dominant kernel's roofline, the oracle's CPU baseline, the
-end-to-end figure through psp_step_host with host buffers (plan, plan upload,
-query copy in, output copy out, every step), sampled SM clocks, the launch
-count, a bare read of the same byte count for context (read_ceiling), and for
-shared-prefix workloads the per-request paged comparator (every request
-reading the prefix through its own block table).
+us_per_step, per-kernel times, the dominant kernel's roofline (roofline) and
+the other kernels' (roofline_other), the per-request paged comparator (every
+request reading the prefix through its own block table) and the read-once
+speedup over it, the oracle's CPU baseline, the end-to-end figure through
+psp_step_host with host buffers (plan, plan upload, query copy in, output copy
+out, every step), sampled SM clocks, the launch count, a bare read of the same
+byte count for context (read_ceiling) and per_config.
 
 --impl reference times the fp64 CPU oracle (the reference arm of this path)
 on a bounded sample of the same workload, in the same metric and unit.
@@ -51,6 +55,10 @@ import workloads  # noqa: E402
 METRIC = "decode-attn µs/step and achieved HBM GB/s (unique KV bytes) vs GB300 peak"
 UNIT = "GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# the headline workload: the largest single-GPU shared-prefix batch (16,384-token prefix read once,
+# M_eff 4096, e4m3 cache); the other workloads are measured beside it in the same process
+HEADLINE = "fp8_large"
+PER_CONFIG = ("llama8b_noshare", "agent", "short_prefix")
 KERNEL_SOURCES = {
     "suffix_splitkv": "paged_shared_prefix_gb300/csrc/kernel_suffix.cu",
     "prefix_cascade": "paged_shared_prefix_gb300/csrc/kernel_prefix_cascade.cu",
@@ -64,7 +72,9 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="llama8b_noshare", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--layout", default="scatter", choices=["scatter", "contiguous", "block128"],
+                    help="physical page layout of the pool (the generator's layouts)")
     ap.add_argument("--page-size", type=int, default=None)
     ap.add_argument("--impl", default="psp", choices=["psp", "reference"])
     ap.add_argument("--seed", type=int, default=0)
@@ -75,6 +85,8 @@ def parse():
                          "(default: the library default for the workload)")
     ap.add_argument("--no-comparator", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads measured beside the headline one")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-read-ceiling", action="store_true", help="skip the bare-read ceiling measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle CPU time for the baseline")
@@ -238,7 +250,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    case = workloads.make_case(args.workload, args.seed, page_size=args.page_size)
+    case = workloads.make_case(args.workload, args.seed, page_size=args.page_size, layout=args.layout)
     ub = workloads.unique_kv_bytes(case)
     per_step_target = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -308,6 +320,174 @@ def sweep_threshold(args):
     return 0
 
 
+def to_device(case, dev):
+    import torch
+
+    def t(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    return dict(q=t(case.q), k=t(case.k_pool), v=t(case.v_pool), ks=t(case.k_scale), vs=t(case.v_scale))
+
+
+def make_outputs(case, dev):
+    import torch
+    w = case.workload
+    odt = torch.float32 if w.o_dtype == "f32" else torch.bfloat16
+    o = torch.empty((case.batch, w.num_q_heads, w.head_dim), dtype=odt, device=dev)
+    lse = torch.empty((case.batch, w.num_q_heads), dtype=torch.float32, device=dev)
+    return o, lse
+
+
+def kernel_roofline(name, ms, case, info, pk, pk_src):
+    """Roofline entry of one kernel: algorithmic work per launch / its mean event time."""
+    w = case.workload
+    Hkv, d = w.num_kv_heads, w.head_dim
+    tok_bytes = 2 * Hkv * d * workloads.elem_bytes(w.kv_dtype)
+    if name in ("prefix_dense", "prefix_cascade"):
+        m_eff = int(case.batch * (w.num_q_heads // Hkv))
+        flops = 4.0 * m_eff * info["shared_tokens"] * d * Hkv
+        achieved = flops / (ms * 1e-3) / 1e12
+        peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        note = f"{pk_src} bf16 burst"
+        if w.kv_dtype == "fp8_e4m3" and name == "prefix_dense":
+            # e4m3 products: the measured bf16 peak times the nominal e4m3 / bf16 ratio (4.5 / 2.25)
+            peak *= 2.0
+            note = f"{pk_src} bf16 burst x 2 (nominal e4m3 / bf16 ratio)"
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": recorded_traffic(name, w.name), "kernel": name, "us": ms * 1e3,
+                "algorithmic": f"{flops:.4g} FLOP per launch = 4 x M_eff {m_eff} x {info['shared_tokens']} shared "
+                               f"tokens x d {d} x Hkv {Hkv}",
+                "peak_source": note}
+    if name == "suffix_splitkv":
+        alg = info["suffix_tokens"] * tok_bytes
+        desc = f"{alg} B per launch = {info['suffix_tokens']} suffix tokens x {tok_bytes} B (K+V, all KV heads)"
+    else:
+        alg = info["kv_indices_len"] * 4
+        desc = f"{alg} B per launch = {info['kv_indices_len']} indices x 4 B written"
+    achieved = alg / (ms * 1e-3) / 1e9
+    peak = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": recorded_traffic(name, w.name), "kernel": name, "us": ms * 1e3, "algorithmic": desc,
+            "peak_source": pk_src}
+
+
+class Runner:
+    """Device state shared by every measurement of one bench process."""
+
+    def __init__(self, dev, stream):
+        import torch
+        self.dev, self.stream = dev, stream
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20)
+        self.flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2(self):
+        import torch
+        # write a buffer of twice the L2 size (evicts the step's data), then read it back so
+        # no dirty line is left whose write-back would land inside the next timed step
+        self.flush.fill_(1.0)
+        torch.sum(self.flush, dim=0, out=self.sink)
+
+    def time_steps(self, fn, steps, warmup, clocks=None):
+        """Mean ms of `steps` calls of fn() (each after an untimed L2 flush), CUDA events on the
+        launching stream; returns (ms list, wall seconds of the timed loop)."""
+        import torch
+        for _ in range(max(3, warmup)):
+            self.flush_l2()
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if clocks:
+            clocks.start()
+        wall0 = time.perf_counter()
+        for a, b in evs:
+            self.flush_l2()
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        return [a.elapsed_time(b) for a, b in evs], wall
+
+    def kernel_times(self, step, run, n):
+        """Per-kernel mean ms from psp's own events around each launch (a separate pass: the
+        events sit between the kernels and disable the dependent launch)."""
+        import torch
+        step.set_kernel_timing(True)
+        kern = {}
+        for _ in range(n):
+            self.flush_l2()
+            run()
+            torch.cuda.synchronize()
+            for name, kms in step.kernel_times():
+                kern.setdefault(name, []).append(kms)
+        step.set_kernel_timing(False)
+        return {k: statistics.mean(v) for k, v in kern.items()}
+
+
+def measure_case(psp, runner, case, steps, warmup, *, threshold=0, token_flat=False, concurrent=False,
+                 comparator=True, clocks=None, tensors=None):
+    """One workload: whole-step times, per-kernel times, plan facts and the per-request paged
+    comparator (the same batch with every request reading its prefix through its own table)."""
+    import torch
+    dev, stream = runner.dev, runner.stream
+    tens = tensors or to_device(case, dev)
+    o, lse = make_outputs(case, dev)
+    step = psp.DecodeStep.for_case(case, dense_threshold=threshold, token_flat=token_flat, concurrent=concurrent)
+    t_plan = []
+    for _ in range(5):
+        t0 = time.perf_counter()
+        step.plan_case(case)
+        t_plan.append(time.perf_counter() - t0)
+    info = step.plan_info()
+    ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device=dev)
+    step.upload(ws, stream)
+
+    def run():
+        step.run(tens["q"], tens["k"], tens["v"], o, lse, tens["ks"], tens["vs"], stream)
+
+    ms_list, wall = runner.time_steps(run, steps, warmup, clocks)
+    n_kernel_steps = max(3, min(steps, 20))
+    kern = runner.kernel_times(step, run, n_kernel_steps)
+    ub = workloads.unique_kv_bytes(case)
+    ms = statistics.mean(ms_list)
+    res = {"case": case, "step": step, "ws": ws, "tens": tens, "o": o, "lse": lse, "info": info,
+           "ms": ms, "ms_list": ms_list, "wall": wall, "kernels_ms": kern, "plan_us": statistics.median(t_plan) * 1e6,
+           "unique_bytes": ub, "paged_bytes": workloads.paged_kv_bytes(case),
+           "launches_per_step": len(kern)}
+    if comparator and case.num_groups > 0:
+        nc = case.without_sharing()
+        cstep = psp.DecodeStep.for_case(nc, token_flat=token_flat)
+        cstep.plan_case(nc)
+        cws = torch.empty(cstep.workspace_size(), dtype=torch.uint8, device=dev)
+        cstep.upload(cws, stream)
+        cms, _ = runner.time_steps(
+            lambda: cstep.run(tens["q"], tens["k"], tens["v"], o, lse, tens["ks"], tens["vs"], stream),
+            max(5, min(steps, 20)), 3)
+        cmean = statistics.mean(cms)
+        res["paged_comparator"] = {"us_per_step": cmean * 1e3, "speedup_read_once": cmean / ms,
+                                   "bytes_per_step": workloads.paged_kv_bytes(case),
+                                   "what": "the same batch planned without prefix groups: every request reads "
+                                           "the shared prefix through its own block table (suffix kernel only)"}
+        cstep.close()
+        del cws
+    return res
+
+
+def config_summary(res, pk, pk_src):
+    case, info = res["case"], res["info"]
+    ub, ms = res["unique_bytes"], res["ms"]
+    gbs = ub / (ms * 1e-3) / 1e9
+    out = {"workload": describe(case), "us_per_step": ms * 1e3, "unique_kv_bytes": ub, "value": gbs, "unit": UNIT,
+           "hbm_frac_of_8tbs": gbs / 8000.0, "frac_of_measured_hbm": gbs / pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
+           "kernels_us": {k: v * 1e3 for k, v in res["kernels_ms"].items()},
+           "kernel_rooflines": {k: kernel_roofline(k, v, case, info, pk, pk_src) for k, v in res["kernels_ms"].items()},
+           "plan": {k: info[k] for k in ("num_splits", "num_chunks", "suffix_ctas", "prefix_dense_ctas",
+                                          "prefix_cascade_ctas", "dense_threshold")}}
+    if "paged_comparator" in res:
+        out["paged_comparator"] = {k: v for k, v in res["paged_comparator"].items() if k != "what"}
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -328,136 +508,41 @@ def main():
         dist.init_process_group("nccl")
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-
-    case = workloads.make_case(args.workload, args.seed + rank, page_size=args.page_size)
-    w = case.workload
-    ub = workloads.unique_kv_bytes(case)
-    paged_b = workloads.paged_kv_bytes(case)
-
-    def t(a):
-        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    q, kp, vp, ks, vs = t(case.q), t(case.k_pool), t(case.v_pool), t(case.k_scale), t(case.v_scale)
-    odt = torch.float32 if w.o_dtype == "f32" else torch.bfloat16
-    o = torch.empty((case.batch, w.num_q_heads, w.head_dim), dtype=odt, device=dev)
-    lse = torch.empty((case.batch, w.num_q_heads), dtype=torch.float32, device=dev)
-
-    concurrent = bool(args.concurrent) if args.concurrent is not None else False
-    step = psp.DecodeStep.for_case(case, dense_threshold=args.threshold, token_flat=args.token_flat,
-                                   concurrent=concurrent)
-    t_plan = []
-    for _ in range(5):
-        t0 = time.perf_counter()
-        step.plan_case(case)
-        t_plan.append(time.perf_counter() - t0)
-    info = step.plan_info()
-    ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    step.upload(ws, stream)
-    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20)
-    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
-    sink = torch.empty((), dtype=torch.float32, device=dev)
+    runner = Runner(dev, stream)
+    pk, pk_src = peaks()
 
-    def flush_l2():
-        # write a buffer of twice the L2 size (evicts the step's data), then read it back so
-        # no dirty line is left whose write-back would land inside the next timed step
-        flush.fill_(1.0)
-        torch.sum(flush, dim=0, out=sink)
-
-    def one(timed_events=None):
-        flush_l2()
-        if timed_events:
-            timed_events[0].record(stream)
-        step.run(q, kp, vp, o, lse, ks, vs, stream)
-        if timed_events:
-            timed_events[1].record(stream)
-
-    for _ in range(max(3, args.warmup)):
-        one()
-    torch.cuda.synchronize()
-
-    # ---- timed region: whole steps, no per-kernel events (they would sit between the prefix
-    # and suffix kernels and stop the suffix kernel from starting early)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    case = workloads.make_case(args.workload, args.seed + rank, page_size=args.page_size, layout=args.layout)
+    w = case.workload
+    concurrent = bool(args.concurrent) if args.concurrent is not None else False
     clocks = ClockSampler(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    wall0 = time.perf_counter()
-    for i in range(args.steps):
-        one(evs[i])
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
+    head = measure_case(psp, runner, case, args.steps, args.warmup, threshold=args.threshold,
+                        token_flat=args.token_flat, concurrent=concurrent, comparator=not args.no_comparator,
+                        clocks=clocks)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    ms, value = aggregate_replicas(statistics.mean(step_ms), ub, world, dev)
-
-    # ---- per-kernel times (events on the launching stream around each kernel), a separate pass
-    step.set_kernel_timing(True)
-    kern = {}
-    n_kernel_steps = max(3, min(args.steps, 20))
-    for i in range(n_kernel_steps):
-        one()
-        torch.cuda.synchronize()
-        for name, kms in step.kernel_times():
-            kern.setdefault(name, []).append(kms)
-    step.set_kernel_timing(False)
-    launches = args.steps * sum(len(v) for v in kern.values()) // n_kernel_steps
+    ub = head["unique_bytes"]
+    ms, value = aggregate_replicas(head["ms"], ub, world, dev)
+    info, kmean = head["info"], head["kernels_ms"]
+    step, ws, tens, o, lse = head["step"], head["ws"], head["tens"], head["o"], head["lse"]
 
     # ---- single-launch read ceiling: a bare read of as many bytes as the step's unique K/V
     # (torch's sum kernel, L2 flushed the same way), for context beside the roofline peak
     ceil = None
     if not args.no_read_ceiling:
         buf = torch.empty(ub // 4, dtype=torch.float32, device=dev).fill_(1.0)
-        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(8)]
-        for i in range(10):
-            flush_l2()
-            if i >= 2:
-                cev[i - 2][0].record(stream)
-            torch.sum(buf, dim=0, out=sink)
-            if i >= 2:
-                cev[i - 2][1].record(stream)
-        torch.cuda.synchronize()
-        cms = statistics.mean(a.elapsed_time(b) for a, b in cev)
-        ceil = {"gbs": buf.numel() * 4 / (cms * 1e-3) / 1e9, "bytes": int(buf.numel() * 4),
+        cms, _ = runner.time_steps(lambda: torch.sum(buf, dim=0, out=runner.sink), 8, 2)
+        ceil = {"gbs": buf.numel() * 4 / (statistics.mean(cms) * 1e-3) / 1e9, "bytes": int(buf.numel() * 4),
                 "how": "torch.sum over a float32 buffer of the unique K/V size, one launch, L2 flushed as for the step"}
         del buf
 
-    # ---- roofline of the dominant kernel
-    pk, pk_src = peaks()
-    kmean = {k: statistics.mean(v) for k, v in kern.items()}
-    dom = max(kmean, key=kmean.get)
-    Hkv, d = w.num_kv_heads, w.head_dim
-    elem = workloads.elem_bytes(w.kv_dtype)
-    tok_bytes = 2 * Hkv * d * elem
-    if dom in ("prefix_dense", "prefix_cascade"):
-        m_eff = int(case.batch * (w.num_q_heads // Hkv))
-        flops = 4.0 * m_eff * info["shared_tokens"] * d * Hkv
-        achieved = flops / (kmean[dom] * 1e-3) / 1e12
-        peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        peak_note = pk_src
-        if w.kv_dtype == "fp8_e4m3" and dom == "prefix_dense":
-            # e4m3 products: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
-            peak *= 2.0
-            peak_note = f"{pk_src} bf16 x 2 (nominal e4m3 / bf16 ratio)"
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": recorded_traffic(dom, w.name), "kernel": dom,
-                "algorithmic": f"{flops:.4g} FLOP per launch (4*M_eff*P*d*Hkv)", "peak_source": peak_note}
-    else:
-        if dom == "suffix_splitkv":
-            alg = info["suffix_tokens"] * tok_bytes
-            desc = f"{alg} B per launch = {info['suffix_tokens']} suffix tokens x {tok_bytes} B (K+V, all KV heads)"
-        else:
-            alg = ub
-            desc = f"{alg} unique K/V bytes"
-        achieved = alg / (kmean[dom] * 1e-3) / 1e9
-        peak = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": recorded_traffic(dom, w.name), "kernel": dom, "algorithmic": desc,
-                "peak_source": pk_src}
-
+    rooflines = {k: kernel_roofline(k, v, case, info, pk, pk_src) for k, v in kmean.items()}
+    order = sorted(kmean, key=kmean.get, reverse=True)
+    dom = order[0]
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
@@ -467,34 +552,18 @@ def main():
         "config": {"workload": describe(case), "l2": "flushed between steps (2x L2 buffer written then read back, untimed)",
                    "parallelism": f"replicas x{world}", "token_flat": bool(args.token_flat),
                    "concurrent_prefix": concurrent},
-        "unique_kv_bytes": ub, "paged_kv_bytes": paged_b,
+        "unique_kv_bytes": ub, "paged_kv_bytes": head["paged_bytes"],
         "hbm_frac_of_8tbs": value / world / 8000.0,
-        "kernels_ms": kmean, "plan_us": statistics.median(t_plan) * 1e6,
-        "roofline": roof, "read_ceiling": ceil, "clocks": clk, "gpu_launches": launches, "wall_s": wall,
+        "kernels_ms": kmean, "plan_us": head["plan_us"],
+        "roofline": rooflines[dom],
+        "roofline_other": [rooflines[k] for k in order[1:]],
+        "read_ceiling": ceil, "clocks": clk, "gpu_launches": args.steps * head["launches_per_step"],
+        "wall_s": head["wall"],
         "plan": {k: info[k] for k in ("num_splits", "num_chunks", "suffix_ctas", "prefix_dense_ctas",
                                        "prefix_cascade_ctas", "dense_threshold", "num_sms")},
     }
-
-    # ---- per-request paged comparator (prefix read through every block table)
-    if not args.no_comparator and case.num_groups > 0:
-        nc = case.without_sharing()
-        cstep = psp.DecodeStep.for_case(nc, token_flat=args.token_flat)
-        cstep.plan_case(nc)
-        cws = torch.empty(cstep.workspace_size(), dtype=torch.uint8, device=dev)
-        cstep.upload(cws, stream)
-        ce = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
-        for i in range(13):
-            flush_l2()
-            if i >= 3:
-                ce[i - 3][0].record(stream)
-            cstep.run(q, kp, vp, o, lse, ks, vs, stream)
-            if i >= 3:
-                ce[i - 3][1].record(stream)
-        torch.cuda.synchronize()
-        cms = statistics.mean(a.elapsed_time(b) for a, b in ce)
-        result["paged_comparator"] = {"us_per_step": cms * 1e3, "speedup_read_once": cms / ms,
-                                      "bytes_per_step": paged_b}
-        cstep.close()
+    if "paged_comparator" in head:
+        result["paged_comparator"] = head["paged_comparator"]
 
     # ---- end to end through the C ABI with host buffers
     if not args.no_e2e:
@@ -502,13 +571,13 @@ def main():
         qh = qh.pin_memory()
         oh = torch.empty(o.shape, dtype=torch.int16 if w.o_dtype == "bf16" else torch.float32).pin_memory()
         lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-        qd = torch.empty_like(q)
+        qd = torch.empty_like(tens["q"])
         batch, keep = step.make_batch(case.kv_len, case.page_indptr, case.page_indices, case.prefix_group,
                                       case.group_prefix_len)
-        devt = step.tensors(qd, kp, vp, o, lse, ks, vs)
+        devt = step.tensors(qd, tens["k"], tens["v"], o, lse, tens["ks"], tens["vs"])
         e2e = []
         for i in range(3 + args.steps):
-            flush_l2()
+            runner.flush_l2()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             step.step_host(batch, qh, oh, lh, devt, ws, stream)
@@ -521,6 +590,22 @@ def main():
                          "d2h_bytes_per_step": int(oh.numel() * oh.element_size() + lh.numel() * 4),
                          "path": "psp_step_host: plan + plan upload + q H2D + run + o/lse D2H, synchronous; "
                                  "the K/V cache stays resident in HBM"}
+    step.close()
+    del head, ws, tens
+
+    # ---- the other workloads, measured in the same process (context for the headline line)
+    if not args.no_per_config and rank == 0:
+        per = {}
+        for name in PER_CONFIG:
+            if name == args.workload:
+                continue
+            c = workloads.make_case(name, args.seed)
+            r = measure_case(psp, runner, c, max(5, min(args.steps, 30)), 3)
+            per[name] = config_summary(r, pk, pk_src)
+            r["step"].close()
+            del r
+            torch.cuda.empty_cache()
+        result["per_config"] = per
 
     # ---- CPU baseline: the oracle as it stands
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -531,7 +616,6 @@ def main():
                                             + (f", the whole step {ot['reps']} times" if ot["reps"] > 1 else "")
                                             + f", {ot['sample_s']:.1f} s of fp64 work on {ot['cores']} threads, "
                                             "scaled by context tokens"}
-    step.close()
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
