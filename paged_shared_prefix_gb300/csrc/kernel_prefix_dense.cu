@@ -386,33 +386,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kTok; ++i) x[i] = i < valid ? x[i] : neg_inf();
       }
       // tile max with eight independent accumulators (short dependency chains)
-      float mx[8];
+      auto tile_max = [&]() {
+        float mx[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) mx[a] = x[a];
+        for (int a = 0; a < 8; ++a) mx[a] = x[a];
 #pragma unroll
-      for (int i = 8; i < kTok; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * scale;
-      const bool need = mt > m_used + kRescaleLog2;
+        for (int i = 8; i < kTok; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+        return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+               scale;
+      };
+      bool need = false;
       float alpha = 1.f;
-      if (need) {
-        alpha = ex2(m_used - mt);
-        m_used = mt;
-        l *= alpha;
-      }
-      const float neg_m = -m_used;
-      float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if constexpr (FP8) {
+        // The probabilities of a tile must stay <= 2^8 (inside e4m3).  After the first tile
+        // the max pass is skipped: they are computed against the current reference, and since
+        // all are >= 0 their sum bounds each of them, so a tile sum <= 2^8 proves the bound.
+        // Only a larger sum (rare: the scores rose) takes the max and, if it moved by more
+        // than 2^8, rebases and recomputes the tile.
         uint32_t u[kTok / 4];  // four e4m3 probabilities per column
+        const float2 scale2 = make_float2(scale, scale);
+        auto make_p = [&](float m) {
+          const float2 neg_m2 = make_float2(-m, -m);
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int i = 0; i < kTok / 4; ++i) {
-          const float a = ex2(fmaf(x[4 * i], scale, neg_m)), b = ex2(fmaf(x[4 * i + 1], scale, neg_m));
-          const float c2 = ex2(fmaf(x[4 * i + 2], scale, neg_m)), d2 = ex2(fmaf(x[4 * i + 3], scale, neg_m));
-          sm[i & 7] += (a + b) + (c2 + d2);
-          u[i] = e4m3x4_from_floats(a, b, c2, d2);
+          for (int i = 0; i < kTok / 4; ++i) {
+            const float2 y0 = __ffma2_rn(make_float2(x[4 * i], x[4 * i + 1]), scale2, neg_m2);
+            const float2 y1 = __ffma2_rn(make_float2(x[4 * i + 2], x[4 * i + 3]), scale2, neg_m2);
+            const float2 p0 = make_float2(ex2(y0.x), ex2(y0.y)), p1 = make_float2(ex2(y1.x), ex2(y1.y));
+            acc[i & 3] = __fadd2_rn(acc[i & 3], __fadd2_rn(p0, p1));
+            u[i] = e4m3x4_from_floats(p0.x, p0.y, p1.x, p1.y);
+          }
+          const float2 s = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+          return s.x + s.y;
+        };
+        float tile_sum;
+        if (j == 0) {
+          need = true;
+          m_used = tile_max();
+          tile_sum = make_p(m_used);
+        } else {
+          tile_sum = make_p(m_used);
+          if (!(tile_sum <= 256.f)) {  // also catches an infinite sum
+            const float mt = tile_max();
+            if (mt > m_used + kRescaleLog2) {
+              need = true;
+              alpha = ex2(m_used - mt);
+              m_used = mt;
+              l *= alpha;
+              tile_sum = make_p(m_used);
+            }
+          }
         }
+        l += tile_sum;
         tmem_st32(lane_addr + s_col, u);
       } else {
+        const float mt = tile_max();
+        need = mt > m_used + kRescaleLog2;
+        if (need) {
+          alpha = ex2(m_used - mt);
+          m_used = mt;
+          l *= alpha;
+        }
+        const float neg_m = -m_used;
+        float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t u[32];  // two bf16 probabilities per column
@@ -425,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st32(lane_addr + s_col + c * 32, u);
         }
+        l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       }
-      l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // rescale this warp's rows of O_t
 #pragma unroll
