@@ -55,9 +55,12 @@
  *                           grid's size (default), 1 sequential, 2 concurrent
  *   PSP_SUFFIX_STAGES       suffix ring depth per warp at d = 128 (default 2 for bf16,
  *                           4 for e4m3; once per process)
- *   PSP_SUFFIX_TC           1: e4m3 K/V at d = 128 use the persistent tcgen05 suffix
- *                           kernel (exact, slower as measured; once per process)
- *   PSP_SUFFIX_TC_STAGES    its ring depth (default 6; once per process)
+ *   PSP_LOG                 1: psp_plan writes one line per planned step to stderr,
+ *                           "psp_step " and a JSON object: shapes and dtypes, page size,
+ *                           block-table and kv_indices lengths, suffix and shared tokens,
+ *                           splits, chunks and CTAs, per group its members, M_eff,
+ *                           shared tokens, branch and chunks, and "coerced": false
+ *                           (nothing is ever coerced); default 0
  * The plan outputs depend on the partition constants; psp_plan_info_get reports
  * the values a plan was built with.
  */
@@ -358,7 +361,14 @@ PSP_API psp_status psp_device_status(psp_handle* h, int32_t* code);
  * array, which keeps the last call's contents: calls whose work overlaps on
  * the GPU race with each other, so serialise them (one stream, or events).
  * A plan whose workspace (psp_workspace_size) exceeds 64 MiB is rejected with
- * PSP_ERR_WORKSPACE before anything is copied or launched.
+ * PSP_ERR_WORKSPACE before anything is copied or launched; so is any call that
+ * psp_run's own argument checks would reject (the call then leaves the array and
+ * the handle's workspace binding untouched, and a call that fails after the copy
+ * restores the binding).  After a successful call the handle stays bound to the
+ * shared array: psp_device_status reads its status word, and psp_run or
+ * psp_expand_kv_indices on the handle use it as their workspace, until the next
+ * psp_upload binds one of the caller's; calls from other handles may overwrite
+ * the array in between.
  * Errors: INVALID_ARGUMENT, NO_PLAN, WORKSPACE, UNSUPPORTED (device ordinal >
  * 63), CUDA. */
 PSP_API psp_status psp_run_noalloc(psp_handle* h, const psp_tensors* t, void* stream);

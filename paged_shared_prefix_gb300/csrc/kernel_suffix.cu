@@ -435,17 +435,6 @@ int suffix_stages(int fallback) {
   return env > 0 ? env : fallback;
 }
 
-// e4m3 K/V at d = 128 run on the mma.sync kernel here; PSP_SUFFIX_TC=1 selects the
-// persistent tensor-core suffix kernel (kernel_suffix_tc.cu), which is exact but slower on
-// GB300 as measured (497 us against 260 us on the large-prefix fp8 batch).
-static bool suffix_tc_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("PSP_SUFFIX_TC");
-    return v && v[0] == '1';
-  }();
-  return on;
-}
-
 cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
   if (num_splits <= 0) return cudaSuccess;
   if (p.kv_dtype == PSP_KV_BF16) {
@@ -458,7 +447,6 @@ cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
   }
   if (p.kv_dtype == PSP_KV_FP8) {
     if (p.head_dim != 128) return launch_t<PSP_KV_FP8, 64, 4, 6>(p, num_splits, s);
-    if (suffix_tc_enabled()) return launch_suffix_tc(p, num_splits, s);
     switch (suffix_stages(4)) {  // fp8 consumes two sub-tiles per iteration: at least 4 stages
       case 5: return launch_t<PSP_KV_FP8, 128, 4, 5>(p, num_splits, s);
       case 6: return launch_t<PSP_KV_FP8, 128, 4, 6>(p, num_splits, s);

@@ -119,6 +119,7 @@ struct psp_handle {
   cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
   bool allow_concurrent = true;   // false on the workspace-free path (no object creation)
   int32_t pdl_form = 0;           // dependent-launch form: 0 by grid size, 1 sequential, 2 concurrent
+  bool log = false;               // PSP_LOG: one structured line per plan on stderr
 
   // per-kernel timing
   bool timing = false;
@@ -496,7 +497,6 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.head_dim = c.head_dim;
   p.page_size = c.page_size;
   p.page_shift = h->page_shift;
-  p.num_sms = h->num_sms_resolved;
   p.kv_dtype = c.kv_dtype;
   p.q_dtype = c.q_dtype;
   p.o_dtype = c.o_dtype;
@@ -549,8 +549,6 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.status = I(L.status);
   p.done_ctas = I(L.status + 32);    // inside the status block, cleared with it at upload
   p.prefix_done = I(L.status + 48);
-  p.work_next = I(L.status + 8);
-  p.work_done = I(L.status + 12);
   {
     int64_t rows = 0;  // sum over prefix chunks of M_eff of the chunk's group, for every KV head
     for (size_t ci = 0; ci < P.chunk_group.size(); ++ci) rows += P.group_m_eff[P.chunk_group[ci]];
@@ -561,6 +559,17 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The argument checks of a step, made before anything is copied or launched.
+psp_status check_tensors(psp_handle* h, const psp_tensors* t) {
+  if (!t || !t->q || !t->k_pool || !t->v_pool || !t->o)
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "q, k_pool, v_pool and o must be set");
+  if (h->cfg.kv_dtype == PSP_DTYPE_FP8_E4M3 && (!t->k_scale || !t->v_scale))
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "fp8 KV needs k_scale and v_scale");
+  if (!aligned16(t->q) || !aligned16(t->k_pool) || !aligned16(t->v_pool) || !aligned16(t->o))
+    return fail(h, PSP_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  return PSP_OK;
+}
 
 }  // namespace
 
@@ -624,6 +633,7 @@ psp_status psp_create(const psp_config* cfg, psp_handle** out) {
   h->prefix_min_tiles = env_int("PSP_PREFIX_MIN_TILES", kPrefixMinTiles);
   h->prefix_ctas_per_sm = env_int("PSP_PREFIX_CTAS_PER_SM", kPrefixCtasPerSm);
   h->pdl_form = env_int("PSP_PDL_FORM", 0);
+  h->log = env_int("PSP_LOG", 0) > 0;
   if (c.dense_threshold == 0) {
     const int t = env_int("PSP_DENSE_THRESHOLD", 0);
     if (t > 0) h->cfg.dense_threshold = t;
@@ -646,6 +656,55 @@ void psp_destroy(psp_handle* h) {
 const char* psp_last_error(const psp_handle* h) {
   return h ? h->last_error.c_str() : g_create_error.c_str();
 }
+
+}  // extern "C"
+
+namespace {
+
+// The record of one planned step ("The 25% Page-Size Slowdown That Wasn't", "The
+// workflow": log the shapes, the index and page-table lengths and what the dispatcher
+// chose, per step, before reading any timing): one JSON object on one stderr line.
+void log_plan(const psp_handle* h, const psp_batch* bt) {
+  const psp_config& c = h->cfg;
+  const HostPlan& P = h->plan;
+  const psp_plan_info& I = P.info;
+  static const char* kDtype[] = {"f32", "bf16", "fp8_e4m3"};
+  static const char* kBranch[] = {"none", "cascade", "dense"};
+  int64_t page_entries = bt->batch_size > 0 ? bt->page_indptr[bt->batch_size] : 0;
+  std::string s;
+  s.reserve(512 + 96 * static_cast<size_t>(P.NG));
+  char buf[512];
+  std::snprintf(buf, sizeof buf,
+                "psp_step {\"batch\": %d, \"num_q_heads\": %d, \"num_kv_heads\": %d, \"head_dim\": %d, "
+                "\"q_dtype\": \"%s\", \"kv_dtype\": \"%s\", \"o_dtype\": \"%s\", \"page_size\": %d, "
+                "\"num_pages\": %d, \"token_flat\": %s, \"page_table_len\": %lld, \"kv_indices_len\": %lld, "
+                "\"suffix_tokens\": %lld, \"shared_tokens\": %lld, \"num_splits\": %d, \"num_chunks\": %d, "
+                "\"suffix_ctas\": %d, \"prefix_dense_ctas\": %d, \"prefix_cascade_ctas\": %d, "
+                "\"dense_threshold\": %d, \"num_sms\": %d, \"workspace_bytes\": %lld, \"coerced\": false, "
+                "\"groups\": [",
+                P.B, c.num_q_heads, c.num_kv_heads, c.head_dim, kDtype[c.q_dtype], kDtype[c.kv_dtype],
+                kDtype[c.o_dtype], c.page_size, c.num_pages, (c.flags & PSP_FLAG_TOKEN_FLAT) ? "true" : "false",
+                static_cast<long long>(page_entries), static_cast<long long>(I.kv_indices_len),
+                static_cast<long long>(I.suffix_tokens), static_cast<long long>(I.shared_tokens), I.num_splits,
+                I.num_chunks, I.suffix_ctas, I.prefix_dense_ctas, I.prefix_cascade_ctas, I.dense_threshold,
+                I.num_sms, static_cast<long long>(I.workspace_bytes));
+  s += buf;
+  for (int g = 0; g < P.NG; ++g) {
+    std::snprintf(buf, sizeof buf,
+                  "%s{\"group\": %d, \"members\": %d, \"m_eff\": %d, \"shared_tokens\": %d, "
+                  "\"branch\": \"%s\", \"chunks\": %d}",
+                  g ? ", " : "", g, P.group_member_indptr[g + 1] - P.group_member_indptr[g], P.group_m_eff[g],
+                  P.group_shared_len[g], kBranch[P.group_branch[g]],
+                  P.group_chunk_indptr[g + 1] - P.group_chunk_indptr[g]);
+    s += buf;
+  }
+  s += "]}\n";
+  std::fputs(s.c_str(), stderr);
+}
+
+}  // namespace
+
+extern "C" {
 
 psp_status psp_plan(psp_handle* h, const psp_batch* batch) {
   if (!h) return PSP_ERR_INVALID_ARGUMENT;
@@ -672,6 +731,7 @@ psp_status psp_plan(psp_handle* h, const psp_batch* batch) {
   if (st) return st;
   h->planned = true;
   h->last_error.clear();
+  if (h->log) log_plan(h, batch);
   return PSP_OK;
 }
 
@@ -793,12 +853,8 @@ static cudaError_t expand_entry(const StepParams& p, int, cudaStream_t s) {
 psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
   if (!h) return PSP_ERR_INVALID_ARGUMENT;
   if (!h->planned || !h->uploaded) return fail(h, PSP_ERR_NO_PLAN, "psp_run needs psp_plan and psp_upload first");
-  if (!t || !t->q || !t->k_pool || !t->v_pool || !t->o)
-    return fail(h, PSP_ERR_INVALID_ARGUMENT, "q, k_pool, v_pool and o must be set");
-  if (h->cfg.kv_dtype == PSP_DTYPE_FP8_E4M3 && (!t->k_scale || !t->v_scale))
-    return fail(h, PSP_ERR_INVALID_ARGUMENT, "fp8 KV needs k_scale and v_scale");
-  if (!aligned16(t->q) || !aligned16(t->k_pool) || !aligned16(t->v_pool) || !aligned16(t->o))
-    return fail(h, PSP_ERR_INVALID_ARGUMENT, "tensors must be 16-byte aligned");
+  const psp_status bad = check_tensors(h, t);
+  if (bad) return bad;
   const HostPlan& P = h->plan;
   if (P.B == 0) return PSP_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -931,8 +987,11 @@ psp_status set_error(psp_handle* h, psp_status code, const char* msg) { return f
 
 // Copies the plan's host image into caller-provided device scratch without any
 // allocation (pageable source, no pinned staging), clears the status word, binds
-// the scratch as the handle's workspace and launches the step.  Kernel timing
-// events are not recorded on this path (creating them would allocate).
+// the scratch as the handle's workspace and launches the step.  Every argument check
+// of psp_run comes first, so a rejected call has written nothing into the scratch (which
+// every handle shares) and leaves the handle's binding as it was; a call that fails after
+// the copy restores the previous binding too.  Kernel timing events are not recorded on
+// this path (creating them would allocate).
 psp_status bind_image_and_run(psp_handle* h, unsigned char* ws, size_t cap, const psp_tensors* t,
                               cudaStream_t s) {
   if (!h) return PSP_ERR_INVALID_ARGUMENT;
@@ -942,8 +1001,11 @@ psp_status bind_image_and_run(psp_handle* h, unsigned char* ws, size_t cap, cons
     return fail(h, PSP_ERR_WORKSPACE,
                 "the plan needs " + std::to_string(L.total) + " bytes of scratch but the static scratch holds " +
                     std::to_string(cap) + " bytes; plan a smaller batch or use psp_upload with a workspace");
-  if (!t || !t->q || !t->k_pool || !t->v_pool || !t->o)
-    return fail(h, PSP_ERR_INVALID_ARGUMENT, "q, k_pool, v_pool and o must be set");
+  const psp_status bad = check_tensors(h, t);
+  if (bad) return bad;
+  unsigned char* const prev_ws = h->workspace;
+  const size_t prev_bytes = h->workspace_bytes;
+  const bool prev_uploaded = h->uploaded;
   // the image runs through zero_end: the status word and merge counters arrive as zeros
   cudaError_t e = cudaMemcpyAsync(ws, h->plan.image.data(), L.zero_end, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "plan copy into the static scratch");
@@ -956,6 +1018,11 @@ psp_status bind_image_and_run(psp_handle* h, unsigned char* ws, size_t cap, cons
   const psp_status st = psp_run(h, t, s);
   h->allow_concurrent = true;
   h->timing = timing;
+  if (st != PSP_OK) {
+    h->workspace = prev_ws;
+    h->workspace_bytes = prev_bytes;
+    h->uploaded = prev_uploaded;
+  }
   return st;
 }
 

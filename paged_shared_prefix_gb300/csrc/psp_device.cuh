@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "psp_internal.h"
@@ -14,16 +15,20 @@
 namespace psp {
 
 // Raises the dynamic shared-memory limit of kernel Kern to `bytes` once per device
-// (the driver call would otherwise cost host time on every step's launch).
+// (the driver call would otherwise cost host time on every step's launch).  One flag per
+// device ordinal and kernel, atomic, so host threads driving different devices neither
+// race nor undo each other's record; ordinals past the table set the attribute every time.
 template <auto Kern>
 inline cudaError_t ensure_smem_limit(int bytes) {
-  static int done_dev = -1;
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> done[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (done_dev == dev) return cudaSuccess;
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  if (tracked && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done_dev = dev;
+  if (e == cudaSuccess && tracked) done[dev].store(true, std::memory_order_release);
   return e;
 }
 

@@ -87,9 +87,6 @@ struct StepParams {
   int32_t* done_ctas;                  // suffix CTAs finished this step (zero between steps)
   int32_t* prefix_done;                // prefix rows (x heads) whose partials and arrivals are done
   int32_t prefix_rows_total;           // its value once the whole prefix kernel has finished
-  int32_t* work_next;                  // next (split, KV head) item of a persistent suffix grid (zero between steps)
-  int32_t* work_done;                  // persistent suffix CTAs finished this step (zero between steps)
-  int32_t num_sms;                     // SMs a persistent grid is sized for
 };
 
 // Byte offsets of every array inside the workspace (256-byte aligned each).
@@ -117,7 +114,6 @@ cudaError_t launch_prefix_cascade(const StepParams& p, int num_items, cudaStream
 cudaError_t launch_prefix_dense(const StepParams& p, int num_items, cudaStream_t s);
 cudaError_t launch_expand_kv_indices(const StepParams& p, int32_t* out, cudaStream_t s);
 cudaError_t launch_suffix_simt(const StepParams& p, int num_splits, cudaStream_t s);
-cudaError_t launch_suffix_tc(const StepParams& p, int num_splits, cudaStream_t s);
 cudaError_t launch_prefix_simt(const StepParams& p, int num_items, bool dense, cudaStream_t s);
 cudaError_t launch_prefix_dense_mma(const StepParams& p, int num_items, cudaStream_t s);
 cudaError_t launch_prefix_dense_tc(const StepParams& p, int num_items, cudaStream_t s);

@@ -42,39 +42,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Same test with an explicit suspend-time hint: a thread whose phase has not completed
-// is suspended (not eligible to issue) until it completes or about `ns` nanoseconds
-// pass, so a waiting warp leaves the issue slots of its sub-partition to working warps.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
-      "selp.u32 %0, 1, 0, p;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
-// Non-blocking test of the same condition (never suspends the thread): for a warp that
-// alternates between several barriers.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits for the phase of the given parity to complete, giving up after a
 // bounded number of polls: on timeout the status word records kDevTimeout
 // (plus the site in the upper bits) and false is returned, so the kernel can
@@ -88,29 +55,6 @@ __device__ __forceinline__ bool mbar_wait_polls(uint32_t bar, uint32_t parity, i
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status, int site) {
   return mbar_wait_polls(bar, parity, status, site, 1u << 24);  // each poll may suspend briefly
-}
-
-// Named barrier over `nthreads` threads (whole warps) that also ORs a predicate
-// across them: every participant gets the same answer, so a warp group can agree
-// on giving up without any thread waiting for one that has left.
-__device__ __forceinline__ bool group_bar_or(int id, int nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n"
-      ".reg .pred p, q;\n"
-      "setp.ne.u32 p, %1, 0;\n"
-      "barrier.cta.red.or.pred q, %2, %3, p;\n"
-      "selp.u32 %0, 1, 0, q;\n"
-      "}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
-// Named barrier `id` over `nthreads` threads (whole warps): waits until all have arrived.
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("barrier.cta.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------------------- TMA
@@ -152,106 +96,12 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, 
   }
 }
 
-// TMA boxes of one kTok-token tile (tile j of the token range [t0, t1) of a block
-// table).  The pool map is [slot][kv head][d] (make_pool_map), its box
-// br = min(page size, 64) tokens x 128 bytes of d; boxes start page-aligned relative
-// to t0 (callers keep t0 a multiple of the box height), so no box straddles a page.
-// Lane l takes boxes l, l + 32, ..., l + 32 (kBoxes - 1) (rows (l + 32k) * br), so the
-// block-table lookups of a tile are independent loads spread over the warp.
-//
-// tile_slots: the pool slots of this lane's boxes (-1: no box; rows at or past t1
-// read slot num_slots, out of the map, which the copy fills with zeros).  Issued
-// ahead of the copies that use them, so no copy waits on a table lookup.
-template <int kTok>
-struct TileSlots {
-  static constexpr int kBoxes = (kTok + 31) / 32;  // boxes per lane at one token per box
-  int s[kBoxes];
-};
-template <int kTok>
-__device__ __forceinline__ TileSlots<kTok> tile_slots(const int32_t* list, int shift, int t0, int t1, int j,
-                                                      int num_slots, int lane) {
-  const int br = min(1 << shift, 64);
-  const int mask = (1 << shift) - 1;
-  TileSlots<kTok> out;
-#pragma unroll
-  for (int k = 0; k < TileSlots<kTok>::kBoxes; ++k) {
-    const int r = (lane + 32 * k) * br;
-    out.s[k] = -1;
-    if (r < kTok) {
-      const int tok = t0 + j * kTok + r;
-      out.s[k] = tok < t1 ? ((__ldg(list + (tok >> shift)) << shift) | (tok & mask)) : num_slots;
-    }
-  }
-  return out;
-}
-template <int kTok>
-__device__ __forceinline__ TileSlots<kTok> no_slots() {
-  TileSlots<kTok> out;
-#pragma unroll
-  for (int k = 0; k < TileSlots<kTok>::kBoxes; ++k) out.s[k] = -1;
-  return out;
-}
-
-// tile_boxes: the copies of one tile into dst (rows of 128 bytes per column block,
-// blocks kHalf apart), completing on bar, from the slots tile_slots returned.
-template <int kTok, uint32_t kHalf, uint32_t kHalves, int kBoxElems>
-__device__ __forceinline__ void tile_boxes(const CUtensorMap* map, uint32_t dst, uint32_t bar,
-                                           const TileSlots<kTok>& slots, int shift, int h, int lane) {
-  const int br = min(1 << shift, 64);
-#pragma unroll
-  for (int k = 0; k < TileSlots<kTok>::kBoxes; ++k) {
-    if (slots.s[k] < 0) continue;
-    const uint32_t r = static_cast<uint32_t>((lane + 32 * k) * br);
-#pragma unroll
-    for (uint32_t hf = 0; hf < kHalves; ++hf)
-      tma_load_3d(dst + hf * kHalf + r * 128, map, hf * kBoxElems, h, slots.s[k], bar);
-  }
-}
-
-// Bounded wait with suspension between polls (mbar_try_wait_hint, 128 ns): at most
-// 2^23 polls, about a second; gives up as soon as another role has given up.
-__device__ __forceinline__ bool wait_or_abort_sleep(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                    int32_t* status, int site) {
-  for (uint32_t i = 0; i < (1u << 23); ++i) {
-    if (mbar_try_wait_hint(bar, parity, 128)) return true;
-    if ((i & 7) == 7 && *abort) return false;
-  }
-  atomicCAS(status, 0, kDevTimeout | (site << 8));
-  *abort = 1;
-  return false;
-}
-
 // Bounded wait that also gives up as soon as another role of the CTA has given up.
 // On its own timeout it records the site and raises the abort flag.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status,
                                               int site) {
   for (uint32_t i = 0; i < (1u << 24); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31) == 31 && *abort) return false;
-  }
-  atomicCAS(status, 0, kDevTimeout | (site << 8));
-  *abort = 1;
-  return false;
-}
-
-// Waits for two barrier phases at once: both tests are issued together, so their
-// latencies overlap.  Bounded like wait_or_abort and watching the same abort flag.
-__device__ __forceinline__ bool wait2_or_abort(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2,
-                                               volatile int* abort, int32_t* status, int site) {
-  for (uint32_t i = 0; i < (1u << 24); ++i) {
-    uint32_t both;
-    asm volatile(
-        "{\n"
-        ".reg .pred p, q;\n"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 q, [%3], %4;\n"
-        "and.pred p, p, q;\n"
-        "selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(both)
-        : "r"(b1), "r"(p1), "r"(b2), "r"(p2)
-        : "memory");
-    if (both) return true;
     if ((i & 31) == 31 && *abort) return false;
   }
   atomicCAS(status, 0, kDevTimeout | (site << 8));
@@ -352,25 +202,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-// 8 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
@@ -388,20 +219,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t lbo,
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;  // descriptor version
   d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
-  return d;
-}
-
-// Shared-memory matrix descriptor without swizzling: core matrices of 8 rows x 16
-// bytes stored as 128 contiguous bytes.  An MN-major operand whose MN extent is 16
-// bytes (one core matrix wide) steps along K by 8-row groups; both offsets are given
-// that stride, so the layout does not depend on which of the two the unit reads as the
-// K stride.
-__device__ __forceinline__ uint64_t plain_desc(uint32_t smem_addr, uint32_t k_group_stride) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((k_group_stride >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((k_group_stride >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;  // descriptor version; layout type 0 = no swizzle
   return d;
 }
 

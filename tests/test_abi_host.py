@@ -326,3 +326,44 @@ def test_replans_on_one_handle_match_oracle(ps):
         assert info["num_splits"] == len(ref["split_begin"]) and info["num_chunks"] == len(ref["chunk_begin"])
         assert info["num_groups"] == case.num_groups
     step.close()
+
+
+def test_plan_log_line_records_the_step():
+    # PSP_LOG=1 (read at psp_create): one "psp_step {json}" line per plan on stderr with the
+    # shapes, index and block-table lengths and the dispatcher's choice per group
+    import json
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path[:0] = [%r, %r]\n"
+        "import json, workloads, paged_shared_prefix_gb300 as psp\n"
+        "from test_abi_host import _multi_group_case\n"
+        "case = _multi_group_case()\n"
+        "step = psp.DecodeStep.for_case(case, num_sms=152, dense_threshold=26)\n"
+        "step.plan_case(case)\n"
+        "info = step.plan_info()\n"
+        "print(json.dumps({'info': info, 'm_eff': step.plan_query('group_m_eff').tolist(),\n"
+        "                  'branch': step.plan_query('group_branch').tolist(),\n"
+        "                  'pages': int(case.page_indptr[-1])}))\n" % (here, os.path.dirname(here)))
+    env = dict(os.environ, PSP_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("psp_step ")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0][len("psp_step "):])
+    want = json.loads(r.stdout.strip().splitlines()[-1])
+    info = want["info"]
+    for k in ("kv_indices_len", "suffix_tokens", "shared_tokens", "num_splits", "num_chunks", "suffix_ctas",
+              "prefix_dense_ctas", "prefix_cascade_ctas", "dense_threshold", "num_sms", "workspace_bytes"):
+        assert rec[k] == info[k], k
+    assert rec["batch"] == info["batch_size"] and rec["page_table_len"] == want["pages"]
+    assert rec["coerced"] is False and rec["kv_dtype"] == "bf16" and rec["page_size"] == 16
+    names = {0: "none", 1: "cascade", 2: "dense"}
+    assert [g["m_eff"] for g in rec["groups"]] == want["m_eff"]
+    assert [g["branch"] for g in rec["groups"]] == [names[b] for b in want["branch"]]
+    assert {g["branch"] for g in rec["groups"]} == {"dense", "cascade"}
+    # without the variable nothing is written
+    r = subprocess.run([sys.executable, "-c", code], env={k: v for k, v in os.environ.items() if k != "PSP_LOG"},
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "psp_step" not in r.stderr

@@ -28,16 +28,24 @@ def _fresh_outputs(case):
     return o, lse
 
 
-@pytest.mark.parametrize("name,kw", [
-    ("agent", dict(batch=24, prefix_len=512, private_range=(1, 300))),
-    ("fp8_large", dict(batch=10, prefix_len=384, private_range=(1, 200))),
-    ("tiny", dict()),
-])
-def test_noalloc_matches_workspace_run_twice(name, kw):
+NOALLOC_CASES = [
+    ("agent", dict(batch=24, prefix_len=512, private_range=(1, 300)), {}),
+    ("fp8_large", dict(batch=10, prefix_len=384, private_range=(1, 200)), {}),
+    ("tiny", dict(), {}),
+    # the token-flat indices lie past the zeroed region of the scratch
+    ("agent", dict(batch=12, prefix_len=256, private_range=(1, 300)), dict(token_flat=True)),
+    # the concurrent flag is ignored on this path (one stream, no side stream to create)
+    ("fp8_large", dict(batch=8, prefix_len=320, private_range=(1, 200)), dict(token_flat=True, concurrent=True)),
+]
+
+
+@pytest.mark.parametrize("name,kw,flags", NOALLOC_CASES,
+                         ids=["agent", "fp8", "tiny", "agent-token-flat", "fp8-concurrent-token-flat"])
+def test_noalloc_matches_workspace_run_twice(name, kw, flags):
     case = workloads.make_case(name, 3, **kw)
-    ref_o, ref_lse = run_case(case)                # psp_run with a caller workspace
+    ref_o, ref_lse = run_case(case, **flags)        # psp_run with a caller workspace
     tens = device_tensors(case)
-    step = psp.DecodeStep.for_case(case)
+    step = psp.DecodeStep.for_case(case, **flags)
     step.plan_case(case)
     tol = TOL[case.workload.kv_dtype]
     for _ in range(2):                             # the second call reuses the scratch as left
@@ -50,6 +58,22 @@ def test_noalloc_matches_workspace_run_twice(name, kw):
         assert max_err(got_o, ref_o) <= tol and max_err(got_lse, ref_lse) <= tol
     o_ref, _ = oracle.attend_all(case)
     assert max_err(got_o, o_ref) <= tol
+    step.close()
+
+
+def test_noalloc_rejected_call_leaves_the_binding():
+    # an fp8 call without scales is rejected before anything is copied; the handle's own
+    # workspace stays bound, so psp_run on it still gives the workspace result
+    case = workloads.make_case("fp8_large", 4, batch=6, prefix_len=256, private_range=(1, 120))
+    (ref_o, ref_lse), step, ws = run_case(case, return_step=True)
+    tens = device_tensors(case)
+    o, lse = _fresh_outputs(case)
+    t = step.tensors(tens["q"], tens["k_pool"], tens["v_pool"], o, lse, None, None)
+    assert psp.psp_run_noalloc(step.handle, ctypes.byref(t), None) == -1   # PSP_ERR_INVALID_ARGUMENT
+    step.run(tens["q"], tens["k_pool"], tens["v_pool"], o, lse, tens["k_scale"], tens["v_scale"])
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    assert np.array_equal(o.float().cpu().double().numpy(), ref_o)
     step.close()
 
 
