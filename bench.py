@@ -90,6 +90,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-read-ceiling", action="store_true", help="skip the bare-read ceiling measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle CPU time for the baseline")
+    ap.add_argument("--sweep-read-once", action="store_true",
+                    help="time the read-once step against the per-request paged step over prefix length x "
+                         "members x dtype and report the refit minimum of saved bytes")
     ap.add_argument("--sweep-threshold", action="store_true",
                     help="time the dense and cascade prefix kernels over an M_eff sweep and report the refit threshold")
     return ap.parse_args()
@@ -295,7 +298,8 @@ def sweep_threshold(args):
             o = torch.empty((B, 8 * G, 128), dtype=torch.bfloat16, device=dev)
             res = {}
             for branch, thr in (("dense", 1), ("cascade", 1 << 30)):
-                step = psp.DecodeStep.for_case(case, dense_threshold=thr)
+                step = psp.DecodeStep.for_case(case, dense_threshold=thr, read_once_min_tokens=-1,
+                                               read_once_min_mib=-1)
                 step.plan_case(case)
                 ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device=dev)
                 step.upload(ws)
@@ -450,6 +454,8 @@ def measure_case(psp, runner, case, steps, warmup, *, threshold=0, token_flat=Fa
     kern = runner.kernel_times(step, run, n_kernel_steps)
     ub = workloads.unique_kv_bytes(case)
     ms = statistics.mean(ms_list)
+    names = {0: "none", 1: "cascade", 2: "dense", 3: "paged"}
+    info["branches"] = [names[int(b)] for b in step.plan_query("group_branch")] if case.num_groups else []
     res = {"case": case, "step": step, "ws": ws, "tens": tens, "o": o, "lse": lse, "info": info,
            "ms": ms, "ms_list": ms_list, "wall": wall, "kernels_ms": kern, "plan_us": statistics.median(t_plan) * 1e6,
            "unique_bytes": ub, "paged_bytes": workloads.paged_kv_bytes(case),
@@ -482,10 +488,46 @@ def config_summary(res, pk, pk_src):
            "kernels_us": {k: v * 1e3 for k, v in res["kernels_ms"].items()},
            "kernel_rooflines": {k: kernel_roofline(k, v, case, info, pk, pk_src) for k, v in res["kernels_ms"].items()},
            "plan": {k: info[k] for k in ("num_splits", "num_chunks", "suffix_ctas", "prefix_dense_ctas",
-                                          "prefix_cascade_ctas", "dense_threshold")}}
+                                          "prefix_cascade_ctas", "dense_threshold", "branches")}}
     if "paged_comparator" in res:
         out["paged_comparator"] = {k: v for k, v in res["paged_comparator"].items() if k != "what"}
     return out
+
+
+def sweep_read_once(args):
+    """Dispatcher refit of the read-once choice: for prefix lengths x members x cache dtype,
+    the step with the prefix read once (prefix kernel + suffix kernel) against the same batch
+    planned without groups (every member reads the prefix through its own block table).
+    Reports the bytes that reading once saves, (members - 1) x shared tokens x bytes per
+    token, and the speedup; the refit minimum is the smallest saved size from which reading
+    once is never slower."""
+    import torch
+
+    import paged_shared_prefix_gb300 as psp
+    dev = torch.device("cuda:0")
+    runner = Runner(dev, torch.cuda.current_stream(dev))
+    rows = []
+    for name, heads in (("short_prefix", 16), ("agent", 32), ("fp8_large", 64)):
+        for P in (128, 256, 512, 1024, 2048, 4096):
+            for B in (8, 32, 128, 256):
+                case = workloads.make_case(name, 13, batch=B, prefix_len=P, private_range=(256, 2048),
+                                           num_q_heads=heads, num_kv_heads=8)
+                r = measure_case(psp, runner, case, 10, 3)
+                tb = case.kv_token_bytes()
+                rows.append({"workload": name, "kv_dtype": case.workload.kv_dtype, "prefix": P, "members": B,
+                             "m_eff": B * heads // 8, "saved_bytes": (B - 1) * P * tb,
+                             "read_once_us": r["ms"] * 1e3, "paged_us": r["paged_comparator"]["us_per_step"],
+                             "speedup": r["paged_comparator"]["speedup_read_once"]})
+                r["step"].close()
+                del r
+    rows.sort(key=lambda x: x["saved_bytes"])
+    floor = None
+    for i, x in enumerate(rows):
+        if all(y["speedup"] >= 1.0 for y in rows[i:]):
+            floor = x["saved_bytes"]
+            break
+    print(json.dumps({"sweep": rows, "refit_min_saved_bytes": floor, "gpu": torch.cuda.get_device_name(0)}))
+    return 0
 
 
 def main():
@@ -494,6 +536,8 @@ def main():
         return run_reference(args)
     if args.sweep_threshold:
         return sweep_threshold(args)
+    if args.sweep_read_once:
+        return sweep_read_once(args)
 
     import torch
     import torch.distributed as dist
@@ -560,7 +604,8 @@ def main():
         "read_ceiling": ceil, "clocks": clk, "gpu_launches": args.steps * head["launches_per_step"],
         "wall_s": head["wall"],
         "plan": {k: info[k] for k in ("num_splits", "num_chunks", "suffix_ctas", "prefix_dense_ctas",
-                                       "prefix_cascade_ctas", "dense_threshold", "num_sms")},
+                                       "prefix_cascade_ctas", "dense_threshold", "num_sms", "branches",
+                                       "read_once_min_tokens", "read_once_min_mib")},
     }
     if "paged_comparator" in head:
         result["paged_comparator"] = head["paged_comparator"]

@@ -74,7 +74,7 @@
 extern "C" {
 #endif
 
-#define PSP_ABI_VERSION 1
+#define PSP_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define PSP_API __attribute__((visibility("default")))
@@ -106,6 +106,9 @@ typedef int32_t psp_status;
 #define PSP_BRANCH_NONE 0    /* no member, or the prefix is shorter than one page */
 #define PSP_BRANCH_CASCADE 1 /* small-M tiled loop over the stacked queries */
 #define PSP_BRANCH_DENSE 2   /* 128-row tensor-core tiles over the stacked queries */
+#define PSP_BRANCH_PAGED 3   /* reading the prefix once does not pay at this size: every member
+                                reads its whole context, prefix included, through its own block
+                                table (the group's plan equals the plan without the group) */
 
 /* Flags for psp_config.flags. */
 #define PSP_FLAG_TOKEN_FLAT 1 /* lower block tables to per-token kv_indices on the device
@@ -136,6 +139,11 @@ typedef struct psp_config {
   int32_t dense_threshold; /* M_eff at or above which a group takes the dense branch;
                               0 = the built-in value measured on GB300 */
   int32_t flags;           /* PSP_FLAG_* */
+  int32_t read_once_min_tokens; /* a group's prefix is read once only if its shared tokens
+                                   reach this; 0 = the built-in GB300 value, < 0 = no minimum */
+  int32_t read_once_min_mib;    /* ... and only if reading once saves at least this many MiB,
+                                   (members - 1) x shared tokens x 2 x Hkv x d x element size;
+                                   0 = the built-in GB300 value, < 0 = no minimum */
 } psp_config;
 
 /*
@@ -208,6 +216,9 @@ typedef struct psp_plan_info {
   int32_t prefix_rows_cascade;
   int32_t prefix_min_tiles;
   int32_t prefix_ctas_per_sm;
+  int32_t read_once_min_tokens; /* as resolved (-1: no minimum) */
+  int32_t read_once_min_mib;    /* as resolved (-1: no minimum) */
+  int32_t token_bytes;          /* K + V bytes of one token over all KV heads */
 } psp_plan_info;
 
 /* Plan arrays readable with psp_plan_query (all int32). */
@@ -254,12 +265,19 @@ PSP_API const char* psp_last_error(const psp_handle* h);
  * queries the current device's SM count once).  Validates the batch (see
  * psp_batch) and builds, in token units independent of the page size:
  *  - per request: shared pages n_sh = floor(P_g / page_size) for a member of
- *    group g (0 otherwise), suffix_start = n_sh * page_size, suffix_len =
+ *    a group g whose prefix is read once (0 otherwise, PAGED groups included),
+ *    suffix_start = n_sh * page_size, suffix_len =
  *    kv_len - suffix_start, the suffix page list = pages[n_sh:] ("Track C
  *    Document 10", block-aligned prefix matching);
- *  - per group: the shared page list, M_eff = members x (Hq / Hkv) and the
- *    branch DENSE if M_eff >= dense_threshold else CASCADE ("GraniKV", section
- *    3 Per-step dispatcher; NONE without members or full pages);
+ *  - per group: M_eff = members x (Hq / Hkv) and the branch ("GraniKV",
+ *    section 3 Per-step dispatcher): NONE without members or full pages; PAGED
+ *    when reading the prefix once does not pay (shared tokens below
+ *    read_once_min_tokens, or (members - 1) x shared tokens x token_bytes below
+ *    read_once_min_mib MiB; the built-in values 1024 tokens and 64 MiB are the
+ *    GB300 refit); else DENSE if M_eff >= dense_threshold, else CASCADE.  A
+ *    DENSE or CASCADE group's shared page list is read once; a PAGED group
+ *    shares nothing (shared length 0, no chunks) and its members' suffixes are
+ *    their whole contexts;
  *  - the split-KV partition: with granule tile_tokens, T_b = ceil(S_b / tile)
  *    granules per suffix, W = Hkv * sum T_b, C = max(split_min_tiles,
  *    ceil(W / (split_ctas_per_sm * num_sms))) granules per split, and split s

@@ -8,8 +8,9 @@ single C file ``oracle.c`` with gcc (``build()``).
 Functions (each cites the passage it follows in ``oracle.c``):
   decode_bf16 / decode_fp8     element decoders (format definitions)
   expand_kv_indices(case)      token-flat kv_indices lowering
-  plan(case, params)           block-aligned prefix split, M_eff, branch,
-                               split-KV and prefix-chunk partition
+  plan(case, params)           block-aligned prefix split, M_eff, branch (dense,
+                               cascade, or paged when reading once does not
+                               pay), split-KV and prefix-chunk partition
   attend(case, rows, t0, t1)   softmax(q K^T / sqrt(d)) V in fp64 per row
   merge(o1, lse1, o2, lse2)    log-sum-exp merge (self-check only)
 
@@ -36,7 +37,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 
 DTYPE_CODE = {"f32": 0, "bf16": 1, "fp8_e4m3": 2}
-BRANCH_NONE, BRANCH_CASCADE, BRANCH_DENSE = 0, 1, 2
+BRANCH_NONE, BRANCH_CASCADE, BRANCH_DENSE, BRANCH_PAGED = 0, 1, 2, 3
 ERRORS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "page id out of range",
           -4: "length/page-count mismatch", -5: "prefix mismatch", -6: "capacity", -7: "no memory"}
 
@@ -72,7 +73,8 @@ def _i32(a) -> np.ndarray:
 class PlanParams(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_sms", "dense_threshold", "tile_tokens", "split_min_tiles", "split_ctas_per_sm",
-        "prefix_rows_dense", "prefix_rows_cascade", "prefix_min_tiles", "prefix_ctas_per_sm")]
+        "prefix_rows_dense", "prefix_rows_cascade", "prefix_min_tiles", "prefix_ctas_per_sm",
+        "read_once_min_tokens", "read_once_min_mib", "token_bytes")]
 
 
 class _PlanOut(ctypes.Structure):
@@ -157,6 +159,10 @@ class Oracle:
         out.split_cap = split_cap
         out.group_page_cap = arrs["group_page_indices"].shape[0]
         out.chunk_cap = prefix_tiles
+        # the read-once minimums default to none (every group with full pages reads its prefix
+        # once) and the bytes per token to the case's own
+        params = dict({"read_once_min_tokens": -1, "read_once_min_mib": -1,
+                       "token_bytes": case.kv_token_bytes()}, **params)
         pp = PlanParams(**{k: int(params[k]) for k, _ in PlanParams._fields_})
         kv_len, pind, pidx = _i32(case.kv_len), _i32(case.page_indptr), _i32(case.page_indices)
         pg = _i32(case.prefix_group)

@@ -47,7 +47,7 @@
 enum { OR_F32 = 0, OR_BF16 = 1, OR_FP8_E4M3 = 2 };
 enum { OR_OK = 0, OR_EARG = -1, OR_EUNSUP = -2, OR_ERANGE = -3, OR_ELEN = -4,
        OR_EPREFIX = -5, OR_ECAP = -6, OR_ENOMEM = -7 };
-enum { OR_BRANCH_NONE = 0, OR_BRANCH_CASCADE = 1, OR_BRANCH_DENSE = 2 };
+enum { OR_BRANCH_NONE = 0, OR_BRANCH_CASCADE = 1, OR_BRANCH_DENSE = 2, OR_BRANCH_PAGED = 3 };
 
 /* ---------------------------------------------------------------- decode */
 
@@ -144,6 +144,9 @@ typedef struct {
   int32_t prefix_rows_cascade;
   int32_t prefix_min_tiles;   /* smallest prefix chunk, in granules */
   int32_t prefix_ctas_per_sm; /* prefix target: at most this many items per SM */
+  int32_t read_once_min_tokens; /* shared tokens below this -> paged branch (< 0: no minimum) */
+  int32_t read_once_min_mib;    /* bytes saved by reading once below this many MiB -> paged (< 0: none) */
+  int32_t token_bytes;          /* K + V bytes of one token, all KV heads */
 } oracle_plan_params;
 
 /* Plan outputs; capacities in elements are given by the *_cap fields. */
@@ -209,13 +212,34 @@ int oracle_plan(int B, int Hq, int Hkv, int ps, int num_pages,
     members[g] += 1;
   }
 
-  /* per request: block-aligned split of the block table */
+  /* per group: the dispatcher's branch (GraniKV section 3: M_eff = members x G against the
+     dense threshold), after the read-once test: a prefix is read once only if it has at least
+     read_once_min_tokens shared tokens and reading it once saves (members - 1) x shared
+     tokens x token_bytes >= read_once_min_mib MiB; otherwise every member reads it through
+     its own block table (the paged branch, nothing shared) */
+  for (int g = 0; g < num_groups; ++g) {
+    int64_t n_sh = (members[g] > 0) ? group_prefix_len[g] / ps : 0;
+    int64_t m_eff = (int64_t)members[g] * G;
+    out->group_m_eff[g] = (int32_t)m_eff;
+    int branch = OR_BRANCH_NONE;
+    if (m_eff > 0 && n_sh > 0) {
+      int64_t shared = n_sh * ps;
+      int64_t saved = (int64_t)(members[g] - 1) * shared * pp->token_bytes;
+      int too_short = pp->read_once_min_tokens > 0 && shared < pp->read_once_min_tokens;
+      int too_little = pp->read_once_min_mib > 0 && saved < ((int64_t)pp->read_once_min_mib << 20);
+      if (too_short || too_little) branch = OR_BRANCH_PAGED;
+      else branch = (m_eff >= pp->dense_threshold) ? OR_BRANCH_DENSE : OR_BRANCH_CASCADE;
+    }
+    out->group_branch[g] = branch;
+  }
+
+  /* per request: block-aligned split of the block table (members of a paged group share nothing) */
   {
     int64_t np_out = 0;
     out->suffix_page_indptr[0] = 0;
     for (int b = 0; b < B; ++b) {
       int g = prefix_group ? prefix_group[b] : -1;
-      int64_t n_sh = (g >= 0) ? group_prefix_len[g] / ps : 0;
+      int64_t n_sh = (g >= 0 && out->group_branch[g] != OR_BRANCH_PAGED) ? group_prefix_len[g] / ps : 0;
       out->suffix_start[b] = (int32_t)(n_sh * ps);
       out->suffix_len[b] = (int32_t)(kv_len[b] - n_sh * ps);
       for (int64_t i = page_indptr[b] + n_sh; i < page_indptr[b + 1]; ++i) {
@@ -257,21 +281,17 @@ int oracle_plan(int B, int Hq, int Hkv, int ps, int num_pages,
     out->group_page_indptr[0] = 0;
     out->group_chunk_indptr[0] = 0;
     for (int g = 0; g < num_groups; ++g) {
-      int64_t n_sh = (members[g] > 0) ? group_prefix_len[g] / ps : 0;
+      int branch = out->group_branch[g];
+      int64_t n_sh = (members[g] > 0 && branch != OR_BRANCH_PAGED) ? group_prefix_len[g] / ps : 0;
       out->group_shared_len[g] = (int32_t)(n_sh * ps);
       for (int64_t i = 0; i < n_sh; ++i) {
         if (gp >= out->group_page_cap) { rc = OR_ECAP; goto done; }
         out->group_page_indices[gp++] = page_indices[page_indptr[first_member[g]] + i];
       }
       out->group_page_indptr[g + 1] = (int32_t)gp;
-      int64_t m_eff = (int64_t)members[g] * G;
-      out->group_m_eff[g] = (int32_t)m_eff;
-      int branch = OR_BRANCH_NONE;
-      if (m_eff > 0 && n_sh > 0)
-        branch = (m_eff >= pp->dense_threshold) ? OR_BRANCH_DENSE : OR_BRANCH_CASCADE;
-      out->group_branch[g] = branch;
+      int64_t m_eff = out->group_m_eff[g];
       int64_t rows = 0, n_chunks = 0, per_chunk = 0;
-      if (branch != OR_BRANCH_NONE) {
+      if (branch == OR_BRANCH_DENSE || branch == OR_BRANCH_CASCADE) {
         int64_t rows_per = (branch == OR_BRANCH_DENSE) ? pp->prefix_rows_dense : pp->prefix_rows_cascade;
         rows = ceil_div(m_eff, rows_per);
         int64_t tiles = ceil_div(out->group_shared_len[g], tile);

@@ -35,7 +35,7 @@ STATUS_NAMES = {0: "PSP_OK", -1: "PSP_ERR_INVALID_ARGUMENT", -2: "PSP_ERR_UNSUPP
                 -6: "PSP_ERR_NO_PLAN", -7: "PSP_ERR_WORKSPACE", -8: "PSP_ERR_CUDA",
                 -9: "PSP_ERR_DEVICE_TIMEOUT", -10: "PSP_ERR_HOST_ALLOC", -11: "PSP_ERR_CAPACITY"}
 DTYPES = {"f32": 0, "bf16": 1, "fp8_e4m3": 2}
-BRANCH_NONE, BRANCH_CASCADE, BRANCH_DENSE = 0, 1, 2
+BRANCH_NONE, BRANCH_CASCADE, BRANCH_DENSE, BRANCH_PAGED = 0, 1, 2, 3
 FLAG_TOKEN_FLAT = 1
 FLAG_CONCURRENT = 2
 FIELDS = {
@@ -50,7 +50,7 @@ FIELDS = {
 class psp_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_q_heads", "num_kv_heads", "head_dim", "q_dtype", "kv_dtype", "o_dtype", "page_size",
-        "num_pages", "num_sms", "dense_threshold", "flags")]
+        "num_pages", "num_sms", "dense_threshold", "flags", "read_once_min_tokens", "read_once_min_mib")]
 
 
 class psp_batch(ctypes.Structure):
@@ -74,7 +74,8 @@ class psp_plan_info(ctypes.Structure):
                 ("prefix_cascade_ctas", ctypes.c_int32), ("merge_rows", ctypes.c_int32)] + [
         (n, ctypes.c_int32) for n in (
             "num_sms", "dense_threshold", "tile_tokens", "split_min_tiles", "split_ctas_per_sm",
-            "prefix_rows_dense", "prefix_rows_cascade", "prefix_min_tiles", "prefix_ctas_per_sm")]
+            "prefix_rows_dense", "prefix_rows_cascade", "prefix_min_tiles", "prefix_ctas_per_sm",
+            "read_once_min_tokens", "read_once_min_mib", "token_bytes")]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -151,10 +152,12 @@ class DecodeStep:
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int, q_dtype: str,
                  kv_dtype: str, o_dtype: str, page_size: int, num_pages: int, num_sms: int = 0,
-                 dense_threshold: int = 0, token_flat: bool = False, concurrent: bool = False):
+                 dense_threshold: int = 0, token_flat: bool = False, concurrent: bool = False,
+                 read_once_min_tokens: int = 0, read_once_min_mib: int = 0):
         flags = (FLAG_TOKEN_FLAT if token_flat else 0) | (FLAG_CONCURRENT if concurrent else 0)
         self.cfg = psp_config(num_q_heads, num_kv_heads, head_dim, DTYPES[q_dtype], DTYPES[kv_dtype],
-                              DTYPES[o_dtype], page_size, num_pages, num_sms, dense_threshold, flags)
+                              DTYPES[o_dtype], page_size, num_pages, num_sms, dense_threshold, flags,
+                              read_once_min_tokens, read_once_min_mib)
         h = _H()
         st = psp_create(ctypes.byref(self.cfg), ctypes.byref(h))
         if st != PSP_OK:
@@ -164,10 +167,11 @@ class DecodeStep:
 
     @classmethod
     def for_case(cls, case, num_sms: int = 0, dense_threshold: int = 0, token_flat: bool = False,
-                 concurrent: bool = False):
+                 concurrent: bool = False, read_once_min_tokens: int = 0, read_once_min_mib: int = 0):
         w = case.workload
         return cls(w.num_q_heads, w.num_kv_heads, w.head_dim, w.q_dtype, w.kv_dtype, w.o_dtype,
-                   case.page_size, case.num_pages, num_sms, dense_threshold, token_flat, concurrent)
+                   case.page_size, case.num_pages, num_sms, dense_threshold, token_flat, concurrent,
+                   read_once_min_tokens, read_once_min_mib)
 
     def close(self):
         if getattr(self, "handle", None):

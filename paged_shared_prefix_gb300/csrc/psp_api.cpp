@@ -30,6 +30,15 @@ using psp::StepParams;
 // smallest swept M_eff is the threshold.
 constexpr int32_t kDefaultDenseThreshold = 16;
 
+// Minimums for reading a group's prefix once (else the group takes the paged branch): at
+// least this many shared tokens, and at least this much HBM traffic saved, (members - 1) x
+// shared tokens x bytes per token.  GB300 refit: a sweep over prefix lengths 128-4096,
+// 8-256 members and bf16 / e4m3 caches, read-once step against the same batch planned
+// without groups; these minimums gave the least total loss against the faster choice per
+// point (0.20 in summed log time ratios, against 5.06 for always reading once).
+constexpr int32_t kReadOnceMinTokens = 1024;
+constexpr int32_t kReadOnceMinMiB = 64;
+
 constexpr int32_t kSplitMinTiles = 4;
 constexpr int32_t kSplitCtasPerSm = 5;  // measured on GB300 with 2-stage bf16 rings: 5 (split, head) CTAs per SM
 constexpr int32_t kPrefixMinTiles = 4;
@@ -218,6 +227,10 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   const int64_t ps = c.page_size;
   const int64_t tile = psp::kTileTokens;
   const int32_t threshold = c.dense_threshold > 0 ? c.dense_threshold : kDefaultDenseThreshold;
+  const int32_t min_tokens = c.read_once_min_tokens > 0 ? c.read_once_min_tokens
+                             : c.read_once_min_tokens == 0 ? kReadOnceMinTokens : -1;
+  const int32_t min_mib = c.read_once_min_mib > 0 ? c.read_once_min_mib : c.read_once_min_mib == 0 ? kReadOnceMinMiB : -1;
+  const int64_t token_bytes = 2LL * Hkv * c.head_dim * dtype_bytes(c.kv_dtype);
   const int64_t sms = h->num_sms_resolved;
   P.clear();
   P.B = B;
@@ -265,9 +278,18 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   P.group_page_indptr.assign(NG + 1, 0);
   P.group_chunk_indptr.assign(NG + 1, 0);
   for (int g = 0; g < NG; ++g) {
-    const int64_t n_sh = count[g] > 0 ? bt->group_prefix_len[g] / ps : 0;
-    const int64_t shared = n_sh * ps;
+    int64_t n_sh = count[g] > 0 ? bt->group_prefix_len[g] / ps : 0;
     const int64_t m_eff = static_cast<int64_t>(count[g]) * G;
+    int branch = PSP_BRANCH_NONE;
+    if (m_eff > 0 && n_sh > 0) {
+      const int64_t saved = static_cast<int64_t>(count[g] - 1) * n_sh * ps * token_bytes;
+      if ((min_tokens > 0 && n_sh * ps < min_tokens) || (min_mib > 0 && saved < (static_cast<int64_t>(min_mib) << 20)))
+        branch = PSP_BRANCH_PAGED;
+      else
+        branch = m_eff >= threshold ? PSP_BRANCH_DENSE : PSP_BRANCH_CASCADE;
+    }
+    if (branch == PSP_BRANCH_PAGED) n_sh = 0;  // nothing is read once
+    const int64_t shared = n_sh * ps;
     P.group_shared_len[g] = static_cast<int32_t>(shared);
     P.group_m_eff[g] = static_cast<int32_t>(m_eff);
     if (n_sh > 0) {
@@ -275,10 +297,8 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
       P.group_page_indices.insert(P.group_page_indices.end(), src, src + n_sh);
     }
     P.group_page_indptr[g + 1] = static_cast<int32_t>(P.group_page_indices.size());
-    int branch = PSP_BRANCH_NONE;
-    if (m_eff > 0 && n_sh > 0) branch = m_eff >= threshold ? PSP_BRANCH_DENSE : PSP_BRANCH_CASCADE;
     P.group_branch[g] = branch;
-    if (branch != PSP_BRANCH_NONE) {
+    if (branch == PSP_BRANCH_DENSE || branch == PSP_BRANCH_CASCADE) {
       const int64_t rows = branch == PSP_BRANCH_DENSE ? psp::kDenseRows : psp::kCascadeRows;
       const int64_t rb = cdiv(m_eff, rows);
       const int64_t tiles = cdiv(shared, tile);
@@ -314,8 +334,10 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   // requests whose group runs no prefix kernel read everything as suffix
   for (int b = 0; b < B; ++b) {
     const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
-    if (g >= 0 && P.group_branch[g] == PSP_BRANCH_NONE) P.req_group[b] = -1;
-    else P.req_group[b] = g;
+    if (g >= 0 && (P.group_branch[g] == PSP_BRANCH_NONE || P.group_branch[g] == PSP_BRANCH_PAGED))
+      P.req_group[b] = -1;
+    else
+      P.req_group[b] = g;
   }
 
   // --- per request: suffix after the group's shared pages
@@ -325,7 +347,7 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   P.kv_indptr.assign(B + 1, 0);
   for (int b = 0; b < B; ++b) {
     const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
-    const int64_t n_sh = g >= 0 ? bt->group_prefix_len[g] / ps : 0;
+    const int64_t n_sh = (g >= 0 && P.group_branch[g] != PSP_BRANCH_PAGED) ? bt->group_prefix_len[g] / ps : 0;
     P.suffix_start[b] = static_cast<int32_t>(n_sh * ps);
     P.suffix_len[b] = static_cast<int32_t>(bt->kv_len[b] - n_sh * ps);
     const int32_t* pages = bt->page_indices + bt->page_indptr[b];
@@ -458,6 +480,9 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   I.prefix_rows_cascade = psp::kCascadeRows;
   I.prefix_min_tiles = h->prefix_min_tiles;
   I.prefix_ctas_per_sm = h->prefix_ctas_per_sm;
+  I.read_once_min_tokens = min_tokens;
+  I.read_once_min_mib = min_mib;
+  I.token_bytes = static_cast<int32_t>(token_bytes);
   return PSP_OK;
 }
 
@@ -669,7 +694,7 @@ void log_plan(const psp_handle* h, const psp_batch* bt) {
   const HostPlan& P = h->plan;
   const psp_plan_info& I = P.info;
   static const char* kDtype[] = {"f32", "bf16", "fp8_e4m3"};
-  static const char* kBranch[] = {"none", "cascade", "dense"};
+  static const char* kBranch[] = {"none", "cascade", "dense", "paged"};
   int64_t page_entries = bt->batch_size > 0 ? bt->page_indptr[bt->batch_size] : 0;
   std::string s;
   s.reserve(512 + 96 * static_cast<size_t>(P.NG));

@@ -9,6 +9,11 @@ import paged_shared_prefix_gb300 as psp
 
 TOL = {"f32": 2e-3, "bf16": 1.5e-2, "fp8_e4m3": 6e-2}
 
+# The kernel parity tests read every shared prefix once, whatever its size, so that the prefix
+# kernels run on their small cases; the dispatcher's built-in read-once minimums have tests of
+# their own (read_once=None keeps them).
+READ_ONCE_ALWAYS = dict(read_once_min_tokens=-1, read_once_min_mib=-1)
+
 
 def device_tensors(case, dev="cuda:0"):
     def t(a):
@@ -18,13 +23,13 @@ def device_tensors(case, dev="cuda:0"):
 
 
 def run_case(case, *, threshold=0, token_flat=False, tensors=None, num_sms=0, return_step=False,
-             concurrent=False):
+             concurrent=False, read_once=READ_ONCE_ALWAYS):
     """One step on cuda:0; returns (O float64 [B, Hq, d], LSE float64 [B, Hq])."""
     w = case.workload
     dev = torch.device("cuda:0")
     tens = tensors or device_tensors(case)
     step = psp.DecodeStep.for_case(case, num_sms=num_sms, dense_threshold=threshold, token_flat=token_flat,
-                                   concurrent=concurrent)
+                                   concurrent=concurrent, **(read_once or {}))
     step.plan_case(case)
     ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device=dev)
     step.upload(ws)

@@ -285,6 +285,36 @@ def pin_dispatcher(orc):
         assert p["group_branch"][0] == want
 
 
+def pin_paged_branch(orc):
+    """A prefix too short, or saving too few bytes, to be read once is planned as not shared:
+    every per-request array equals the plan of the same batch without the group and the group
+    shares nothing.  Hand-computed boundaries of the read-once test ((members - 1) x shared
+    tokens x bytes per token against the minimum; 4096 bytes per token here: 8 KV heads x
+    d = 128 x 2 bytes x K and V): at either minimum exactly the prefix is read once."""
+    arrays = ("suffix_start", "suffix_len", "suffix_page_indptr", "suffix_page_indices", "split_indptr",
+              "split_begin", "split_end")
+    base = dict(PLAN_PARAMS, dense_threshold=1)
+    c = workloads.make_case("agent", 4, batch=40, prefix_len=1024, tables_only=True)
+    assert c.kv_token_bytes() == 4096
+    alone = orc.plan(c.without_sharing(), base)
+    paged = orc.plan(c, dict(base, read_once_min_tokens=1025))
+    assert paged["group_branch"][0] == 3 and paged["group_shared_len"][0] == 0
+    assert len(paged["chunk_begin"]) == 0
+    for f in arrays:
+        assert np.array_equal(paged[f], alone[f]), f
+    once = orc.plan(c, dict(base, read_once_min_tokens=1024))
+    assert once["group_branch"][0] == 2 and once["group_shared_len"][0] == 1024
+    assert np.all(once["suffix_start"] == 1024)
+    # 257 members x 64 shared tokens: 256 x 64 x 4096 B = 64 MiB saved, exactly the minimum
+    c = workloads.make_case("agent", 4, batch=257, prefix_len=64, private_range=(1, 20), tables_only=True)
+    assert orc.plan(c, dict(base, read_once_min_mib=64))["group_branch"][0] == 2
+    assert orc.plan(c, dict(base, read_once_min_mib=65))["group_branch"][0] == 3
+    # 2 members x 8192 tokens: the one other member's re-read, 8192 x 4096 B = 32 MiB, is saved
+    c = workloads.make_case("agent", 4, batch=2, prefix_len=8192, private_range=(1, 20), tables_only=True)
+    assert orc.plan(c, dict(base, read_once_min_mib=32))["group_branch"][0] == 2
+    assert orc.plan(c, dict(base, read_once_min_mib=33))["group_branch"][0] == 3
+
+
 def pin_partition(orc):
     """Splits tile each suffix exactly, in order, in equal tile-aligned chunks except the
     last; prefix chunks tile the shared prefix; the partition is the same at every page
@@ -351,6 +381,6 @@ def pin_validation(orc):
     rejects(dataclasses.replace(c, group_prefix_len=gl), -5)
 
 
-ALL_PINS = [pin_fp8_decode_all_codes, pin_bf16_decode_all_patterns, pin_sdpa_fp64,
+ALL_PINS = [pin_paged_branch, pin_fp8_decode_all_codes, pin_bf16_decode_all_patterns, pin_sdpa_fp64,
             pin_closed_forms, pin_paging_invariance, pin_merge_identity, pin_kv_indices,
             pin_block_aligned_prefix, pin_dispatcher, pin_partition, pin_validation]

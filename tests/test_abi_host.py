@@ -80,8 +80,11 @@ def test_create_validation(over, expect):
     assert _create_status(**over) == expect
 
 
-def _lib_plan(case, threshold=0, num_sms=NUM_SMS):
-    step = psp.DecodeStep.for_case(case, num_sms=num_sms, dense_threshold=threshold)
+NO_MINIMUM = dict(read_once_min_tokens=-1, read_once_min_mib=-1)  # every shared prefix read once
+
+
+def _lib_plan(case, threshold=0, num_sms=NUM_SMS, **read_once):
+    step = psp.DecodeStep.for_case(case, num_sms=num_sms, dense_threshold=threshold, **read_once)
     step.plan_case(case)
     return step
 
@@ -92,8 +95,8 @@ PLAN_FIELDS = ["suffix_start", "suffix_len", "suffix_page_indptr", "suffix_page_
                "group_chunk_indptr", "chunk_begin", "chunk_end"]
 
 
-def _check_plan_matches_oracle(case, threshold=0, num_sms=NUM_SMS):
-    step = _lib_plan(case, threshold, num_sms)
+def _check_plan_matches_oracle(case, threshold=0, num_sms=NUM_SMS, **read_once):
+    step = _lib_plan(case, threshold, num_sms, **read_once)
     info = step.plan_info()
     params = {k: info[k] for k, _ in oracle.PlanParams._fields_}
     ref = oracle.plan(case, params)
@@ -136,11 +139,12 @@ def test_plan_matches_oracle(label, kw):
     kw = dict(kw)
     name = kw.pop("name")
     case = workloads.make_case(name, 3, tables_only=True, **kw)
-    _check_plan_matches_oracle(case)
+    _check_plan_matches_oracle(case)                       # built-in read-once minimums
     _check_plan_matches_oracle(case.without_sharing())
-    _check_plan_matches_oracle(case, threshold=1)          # every group dense
-    _check_plan_matches_oracle(case, threshold=1 << 20)    # every group cascade
+    _check_plan_matches_oracle(case, threshold=1, **NO_MINIMUM)        # every group dense
+    _check_plan_matches_oracle(case, threshold=1 << 20, **NO_MINIMUM)  # every group cascade
     _check_plan_matches_oracle(case, num_sms=7)
+    _check_plan_matches_oracle(case, num_sms=7, **NO_MINIMUM)
 
 
 def test_plan_identical_across_page_sizes():
@@ -186,8 +190,11 @@ def _multi_group_case():
 def test_plan_multi_group_matches_oracle():
     case = _multi_group_case()
     for thr in (0, 1, 40, 1 << 20):
-        info, ref = _check_plan_matches_oracle(case, threshold=thr)
+        for ro in ({}, NO_MINIMUM, dict(read_once_min_tokens=100, read_once_min_mib=-1)):
+            info, ref = _check_plan_matches_oracle(case, threshold=thr, **ro)
     assert info["num_groups"] == 3
+    # a 100-token minimum: the 37-token group (two full pages, 32 shared tokens) takes the paged branch
+    assert list(ref["group_branch"]) == [2 if thr <= 28 else 1, 3, 2 if thr <= 24 else 1]
 
 
 def _status_of_plan(case):
@@ -340,7 +347,8 @@ def test_plan_log_line_records_the_step():
         "import json, workloads, paged_shared_prefix_gb300 as psp\n"
         "from test_abi_host import _multi_group_case\n"
         "case = _multi_group_case()\n"
-        "step = psp.DecodeStep.for_case(case, num_sms=152, dense_threshold=26)\n"
+        "step = psp.DecodeStep.for_case(case, num_sms=152, dense_threshold=26, read_once_min_tokens=-1,\n"
+        "                               read_once_min_mib=-1)\n"
         "step.plan_case(case)\n"
         "info = step.plan_info()\n"
         "print(json.dumps({'info': info, 'm_eff': step.plan_query('group_m_eff').tolist(),\n"
@@ -359,7 +367,7 @@ def test_plan_log_line_records_the_step():
         assert rec[k] == info[k], k
     assert rec["batch"] == info["batch_size"] and rec["page_table_len"] == want["pages"]
     assert rec["coerced"] is False and rec["kv_dtype"] == "bf16" and rec["page_size"] == 16
-    names = {0: "none", 1: "cascade", 2: "dense"}
+    names = {0: "none", 1: "cascade", 2: "dense", 3: "paged"}
     assert [g["m_eff"] for g in rec["groups"]] == want["m_eff"]
     assert [g["branch"] for g in rec["groups"]] == [names[b] for b in want["branch"]]
     assert {g["branch"] for g in rec["groups"]} == {"dense", "cascade"}
@@ -367,3 +375,57 @@ def test_plan_log_line_records_the_step():
     r = subprocess.run([sys.executable, "-c", code], env={k: v for k, v in os.environ.items() if k != "PSP_LOG"},
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and "psp_step" not in r.stderr
+
+
+SUFFIX_FIELDS = ["suffix_start", "suffix_len", "suffix_page_indptr", "suffix_page_indices", "split_indptr",
+                 "split_begin", "split_end"]
+
+
+def test_paged_branch_shares_nothing():
+    # a group whose prefix is too short, or saves too little, to be read once takes the paged
+    # branch: nothing is shared and every per-request array is the plan without the group
+    cases = [
+        (workloads.make_case("short_prefix", 2, tables_only=True), {}),           # 512 tokens < 1024
+        (workloads.make_case("agent", 2, batch=8, prefix_len=2048, tables_only=True), {}),  # 7 x 2048 x 4 KiB < 64 MiB
+        (workloads.make_case("agent", 2, batch=40, prefix_len=1024, tables_only=True),
+         dict(read_once_min_tokens=1025, read_once_min_mib=-1)),
+    ]
+    for case, ro in cases:
+        step = _lib_plan(case, **ro)
+        alone = _lib_plan(case.without_sharing())
+        for f in SUFFIX_FIELDS:
+            assert np.array_equal(step.plan_query(f), alone.plan_query(f)), f
+        assert list(step.plan_query("group_branch")) == [psp.BRANCH_PAGED]
+        assert list(step.plan_query("group_shared_len")) == [0]
+        assert list(step.plan_query("group_chunk_indptr")) == [0, 0]
+        G = case.workload.num_q_heads // case.workload.num_kv_heads
+        assert list(step.plan_query("group_m_eff")) == [case.batch * G]
+        info = step.plan_info()
+        assert info["shared_tokens"] == 0 and info["prefix_dense_ctas"] == 0 and info["prefix_cascade_ctas"] == 0
+        _check_plan_matches_oracle(case, **ro)
+        step.close()
+        alone.close()
+
+
+def test_read_once_minimums_at_their_boundaries():
+    # shared tokens equal to the minimum are read once, one token more is the paged branch
+    case = workloads.make_case("agent", 4, batch=40, prefix_len=1024, tables_only=True)
+    for min_tokens, want in ((1024, psp.BRANCH_DENSE), (1025, psp.BRANCH_PAGED)):
+        step = _lib_plan(case, read_once_min_tokens=min_tokens, read_once_min_mib=-1)
+        assert list(step.plan_query("group_branch")) == [want]
+        step.close()
+    # 257 members sharing 64 tokens of 4 KiB save 256 x 64 x 4096 bytes = exactly 64 MiB
+    case = workloads.make_case("agent", 4, batch=257, prefix_len=64, private_range=(1, 20), tables_only=True)
+    assert case.kv_token_bytes() == 4096
+    for min_mib, want in ((64, psp.BRANCH_DENSE), (65, psp.BRANCH_PAGED)):
+        step = _lib_plan(case, read_once_min_tokens=-1, read_once_min_mib=min_mib)
+        assert list(step.plan_query("group_branch")) == [want]
+        info = step.plan_info()
+        assert info["read_once_min_mib"] == min_mib and info["token_bytes"] == 4096
+        _check_plan_matches_oracle(case, read_once_min_tokens=-1, read_once_min_mib=min_mib)
+        step.close()
+    # the built-in minimums as reported
+    step = _lib_plan(case)
+    info = step.plan_info()
+    assert (info["read_once_min_tokens"], info["read_once_min_mib"]) == (1024, 64)
+    step.close()

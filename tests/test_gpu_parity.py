@@ -17,7 +17,7 @@ import torch
 import oracle
 import paged_shared_prefix_gb300 as psp
 import workloads
-from gpu_util import TOL, device_tensors, max_err, run_case
+from gpu_util import READ_ONCE_ALWAYS, TOL, device_tensors, max_err, run_case
 
 pytestmark = pytest.mark.gpu
 
@@ -158,7 +158,7 @@ def test_step_host_matches_run():
 def test_kernel_timing_reports_launches():
     case = workloads.make_case("agent", 9, batch=8, prefix_len=256, private_range=(1, 200))
     tens = device_tensors(case)
-    step = psp.DecodeStep.for_case(case, dense_threshold=1)
+    step = psp.DecodeStep.for_case(case, dense_threshold=1, **READ_ONCE_ALWAYS)
     step.plan_case(case)
     ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device="cuda:0")
     step.upload(ws)
@@ -368,3 +368,25 @@ def test_fp8_suffix_rescale_and_long_splits(monkeypatch):
         o, lse = run_case(case, tensors=tens)
         assert np.isfinite(o).all() and np.isfinite(lse).all(), min_tiles
         assert max_err(o, ref_o) <= tol and max_err(lse, ref_lse) <= tol, (min_tiles, max_err(o, ref_o))
+
+
+
+def test_paged_branch_equals_the_plan_without_the_group():
+    # the built-in read-once minimums send the short-prefix batch (512 shared tokens) down the
+    # paged branch: its step is the step of the same batch without the group, bit for bit
+    case = workloads.make_case("short_prefix", 0)
+    (o, lse), step, ws = run_case(case, read_once=None, return_step=True)
+    assert list(step.plan_query("group_branch")) == [psp.BRANCH_PAGED]
+    assert step.plan_info()["prefix_dense_ctas"] == 0
+    step.close()
+    o2, lse2 = run_case(case.without_sharing(), read_once=None)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    ro, rl = oracle.attend_all(case)
+    assert max_err(o, ro) <= TOL["bf16"] and max_err(lse, rl) <= TOL["bf16"]
+    # and the headline batches read their prefixes once under the same minimums
+    for name in ("agent", "fp8_large"):
+        c = workloads.make_case(name, 0, tables_only=True)
+        s = psp.DecodeStep.for_case(c)
+        s.plan_case(c)
+        assert list(s.plan_query("group_branch")) == [psp.BRANCH_DENSE]
+        s.close()

@@ -21,8 +21,15 @@ MUTATIONS = [
     ("fp8_subnormal_exponent", "ldexp((double)mantissa / 8.0, 1 - 7)", "ldexp((double)mantissa / 8.0, -7)"),
     ("bf16_shift", "((uint32_t)bits) << 16;", "((uint32_t)bits) << 15;"),
     ("merge_weight_swapped", "w2 * o2[(int64_t)r * d + i];", "w1 * o2[(int64_t)r * d + i];"),
-    ("prefix_pages_rounded_up", "int64_t n_sh = (g >= 0) ? group_prefix_len[g] / ps : 0;",
-     "int64_t n_sh = (g >= 0) ? (group_prefix_len[g] + ps - 1) / ps : 0;"),
+    ("prefix_pages_rounded_up",
+     "int64_t n_sh = (g >= 0 && out->group_branch[g] != OR_BRANCH_PAGED) ? group_prefix_len[g] / ps : 0;",
+     "int64_t n_sh = (g >= 0 && out->group_branch[g] != OR_BRANCH_PAGED) ? (group_prefix_len[g] + ps - 1) / ps : 0;"),
+    ("paged_saving_counts_every_member", "int64_t saved = (int64_t)(members[g] - 1) * shared * pp->token_bytes;",
+     "int64_t saved = (int64_t)members[g] * shared * pp->token_bytes;"),
+    ("paged_minimum_tokens_inclusive", "shared < pp->read_once_min_tokens;", "shared <= pp->read_once_min_tokens;"),
+    ("paged_members_keep_their_prefix",
+     "int64_t n_sh = (g >= 0 && out->group_branch[g] != OR_BRANCH_PAGED) ? group_prefix_len[g] / ps : 0;",
+     "int64_t n_sh = (g >= 0) ? group_prefix_len[g] / ps : 0;"),
     ("v_from_k_pool", "out[i] += w * (elem(v_pool, base + i, kv_dtype) * vs);",
      "out[i] += w * (elem(k_pool, base + i, kv_dtype) * vs);"),
     ("q_row_transposed", "qv[i] = elem(q, ((int64_t)b * Hq + hq) * d + i, q_dtype);",

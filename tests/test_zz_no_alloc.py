@@ -15,7 +15,7 @@ import torch
 import oracle
 import paged_shared_prefix_gb300 as psp
 import workloads
-from gpu_util import TOL, device_tensors, max_err, run_case
+from gpu_util import READ_ONCE_ALWAYS, TOL, device_tensors, max_err, run_case
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +45,7 @@ def test_noalloc_matches_workspace_run_twice(name, kw, flags):
     case = workloads.make_case(name, 3, **kw)
     ref_o, ref_lse = run_case(case, **flags)        # psp_run with a caller workspace
     tens = device_tensors(case)
-    step = psp.DecodeStep.for_case(case, **flags)
+    step = psp.DecodeStep.for_case(case, **flags, **READ_ONCE_ALWAYS)
     step.plan_case(case)
     tol = TOL[case.workload.kv_dtype]
     for _ in range(2):                             # the second call reuses the scratch as left
