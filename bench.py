@@ -84,12 +84,17 @@ def parse():
                     help="1: prefix kernels on a side stream concurrent with the suffix kernel, 0: one stream "
                          "(default: the library default for the workload)")
     ap.add_argument("--no-comparator", action="store_true")
+    ap.add_argument("--no-sharing", action="store_true",
+                    help="plan the workload without prefix groups (every request reads its whole context "
+                         "through its own block table) and measure that step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the other workloads measured beside the headline one")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-read-ceiling", action="store_true", help="skip the bare-read ceiling measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle CPU time for the baseline")
+    ap.add_argument("--sweep-control", action="store_true",
+                    help="page size x index layout x footprint control study of the suffix kernel")
     ap.add_argument("--sweep-read-once", action="store_true",
                     help="time the read-once step against the per-request paged step over prefix length x "
                          "members x dtype and report the refit minimum of saved bytes")
@@ -530,6 +535,52 @@ def sweep_read_once(args):
     return 0
 
 
+def sweep_control(args):
+    """Control study of page size and index contiguity on the suffix kernel ("The 25% Page-Size
+    Slowdown That Wasn't", "When source beats intuition": FlashInfer decode moved -1.0..+1.3%
+    between contiguous and scattered indices over 0.03-8.59 GB).  Llama-shaped layers (32 / 8
+    heads, d = 128, bf16, contexts U[2048, 4096]) of 2 to 680 requests, at page sizes 1 and 16,
+    with the pages laid out contiguously, in 128-token blocks or scattered; block tables from
+    the seeded generator, K/V filled on the device with N(0, 1) bf16 values (the step's time
+    does not depend on the values; the host never holds the larger pools)."""
+    import torch
+
+    import paged_shared_prefix_gb300 as psp
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream(dev)
+    runner = Runner(dev, stream)
+    rows = []
+    for B in (2, 6, 24, 96, 384, 680):
+        for ps in (1, 16):
+            for layout in ("contiguous", "block128", "scatter"):
+                case = workloads.make_case("llama8b_noshare", 17, batch=B, page_size=ps, layout=layout,
+                                           tables_only=True)
+                w = case.workload
+                shape = (case.num_pages, ps, w.num_kv_heads, w.head_dim)
+                kp = torch.randn(shape, dtype=torch.bfloat16, device=dev)
+                vp = torch.randn(shape, dtype=torch.bfloat16, device=dev)
+                q = torch.randn((B, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+                o = torch.empty_like(q)
+                step = psp.DecodeStep.for_case(case)
+                step.plan_case(case)
+                ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device=dev)
+                step.upload(ws, stream)
+                ms, _ = runner.time_steps(lambda: step.run(q, kp, vp, o, None, None, None, stream), 10, 3)
+                ub = workloads.unique_kv_bytes(case)
+                us = statistics.median(ms) * 1e3
+                rows.append({"requests": B, "page_size": ps, "layout": layout, "kv_bytes": ub,
+                             "us_per_step": us, "gbs": ub / (us * 1e-6) / 1e9})
+                step.close()
+                del kp, vp, ws
+                torch.cuda.empty_cache()
+    for r in rows:
+        base = next(x for x in rows if x["requests"] == r["requests"] and x["page_size"] == r["page_size"]
+                    and x["layout"] == "contiguous")
+        r["vs_contiguous_pct"] = 100.0 * (r["us_per_step"] / base["us_per_step"] - 1.0)
+    print(json.dumps({"control": rows, "gpu": torch.cuda.get_device_name(0)}))
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -538,6 +589,8 @@ def main():
         return sweep_threshold(args)
     if args.sweep_read_once:
         return sweep_read_once(args)
+    if args.sweep_control:
+        return sweep_control(args)
 
     import torch
     import torch.distributed as dist
@@ -557,6 +610,8 @@ def main():
     pk, pk_src = peaks()
 
     case = workloads.make_case(args.workload, args.seed + rank, page_size=args.page_size, layout=args.layout)
+    if args.no_sharing:
+        case = case.without_sharing()
     w = case.workload
     concurrent = bool(args.concurrent) if args.concurrent is not None else False
     clocks = ClockSampler(local)
