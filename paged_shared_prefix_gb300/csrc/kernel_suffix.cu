@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   }
 
   // -------- asynchronous gather of one 16-token sub-tile (K and V) into ring stage i % NST.
-  // The block-table entries of a sub-tile's rows are loaded one sub-tile ahead of its
+  // The block-table entries of a sub-tile's rows are loaded one iteration ahead of its
   // copies (load_pages), so no copy waits on a dependent table load: the copies are
   // asm statements with a memory clobber, which keeps the compiler from hoisting the
   // next row's table load above the previous row's copy.
@@ -196,6 +196,11 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   // clear of its subnormals); l carries the same factor, so O / l and m + log2(l) are exact.
   constexpr float kPShift = (KV == PSP_KV_FP8) ? 8.f : 0.f;
 
+  // Ring schedule: sub-tiles 0 .. NST-U-1 are issued before the loop (one cp.async group
+  // each).  Every iteration first refills the U stages its predecessor consumed with the
+  // sub-tiles NST-U further on, then waits for its own U, so NST-U sub-tiles stay in flight
+  // while it computes.  The block-table entries of a sub-tile are loaded one iteration
+  // before its copies, so no copy waits on a dependent table load.
   int32_t pages[U][kRowIters];
 #pragma unroll
   for (int i = 0; i < NST - U; ++i) {
@@ -205,19 +210,24 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     }
     cp_async_commit();
   }
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (NST - U + u < my_n) load_pages(NST - U + u, pages[u]);
 
   for (int i0 = 0; i0 < my_n; i0 += U) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int nx = i0 + NST - U + u;
-      if (nx < my_n) load_pages(nx, pages[u]);  // in flight while this iteration computes
+      if (nx < my_n) issue(nx, pages[u]);
+      cp_async_commit();
+      if (nx + U < my_n) load_pages(nx + U, pages[u]);  // in flight while this iteration computes
       // the block-table entries of a sub-tile kTablePrefetch iterations later, pulled into L2
       // now: at small page sizes every sub-tile reads its own 64 bytes of the table, and a
-      // DRAM round trip taken only one sub-tile ahead of the copies would stall them
-      const int pf = nx + kTablePrefetch;
+      // DRAM round trip taken only one iteration ahead of the copies would stall them
+      const int pf = nx + U + kTablePrefetch;
       if (lane == 0 && pf < my_n) prefetch_l2(list + ((t0 + (warp + pf * NW) * 16) >> shift));
     }
-    cp_async_wait<NST - 2 * U>();
+    cp_async_wait<NST - U>();
     __syncwarp();
 
     // ---- fragment loads of K (A operand of S^T) and V (A operand of O^T) for the whole
@@ -345,13 +355,7 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
         mma_e4m3(o[2 * cc + 1], ao, pb[0], pb[U - 1]);
       }
     }
-    __syncwarp();
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int nx = i0 + NST - U + u;
-      if (nx < my_n) issue(nx, pages[u]);
-      cp_async_commit();
-    }
+    __syncwarp();  // every lane's fragment loads are done before the next refill of these stages
   }
   cp_async_wait<0>();
   if (cta.wait_prefix) {
