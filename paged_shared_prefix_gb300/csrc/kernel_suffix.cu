@@ -43,6 +43,10 @@ struct SufCfg {
   static constexpr int kTileBytes = 16 * kRowBytes;   // one 16-token sub-tile of K (or V)
   static constexpr int kStageBytes = 2 * kTileBytes;  // K + V
   static constexpr int kMTiles = D / 16;              // m16 tiles of the value product
+  // prefix-row prefetch area: kPreRows rows, or one prefix chunk of <= 8 heads where the
+  // 16-row area would keep a 3-stage e4m3 ring (48 KB) from four resident CTAs per SM
+  template <int NST>
+  __host__ __device__ static constexpr int pre_rows() { return (KV == PSP_KV_FP8 && D == 128 && NST == 3) ? 8 : kPreRows; }
 };
 
 template <int KV, int D, int NW, int NST>
@@ -82,9 +86,10 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   // a shared-memory area of their own, in the first cp.async group of every thread (a
   // dependent launch that keeps the sequential protocol reads them only after the prefix
   // grid has completed, below, after this CTA's own stream).
-  const SuffixCta cta = suffix_cta(p, split, h);
+  constexpr int kPre = C::template pre_rows<NST>();
+  const SuffixCta cta = suffix_cta(p, split, h, kPre);
   float* pre_o = reinterpret_cast<float*>(smem + NW * NST * C::kStageBytes);   // [chunk * G + j][D]
-  float* pre_l = pre_o + kPreRows * D;                                           // [chunk * G + j]
+  float* pre_l = pre_o + kPre * D;                                               // [chunk * G + j]
   if (cta.pre_smem && !cta.wait_prefix) prefetch_prefix_rows<D, NW * 32>(p, cta, pre_o, pre_l);
 
   // -------- query fragments: B operand of S^T = K Q^T (k = head dim, n = query head)
@@ -191,7 +196,7 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   // as e4m3 mma.sync with k = 32 tokens (m16n8k32) and the code needs no conversion of its own
   // (on sm_103a the instruction itself unpacks the codes to f16 for the tensor cores).
   constexpr int U = (KV == PSP_KV_FP8) ? 2 : 1;
-  static_assert(NST >= 2 * U, "the ring must hold the sub-tiles of one iteration plus those in flight");
+  static_assert(NST >= U + 1, "the ring holds the sub-tiles of one iteration and at least one in flight");
   // fp8: the running max is kept 8 below the true max, so P <= 2^8 (inside e4m3's range and
   // clear of its subnormals); l carries the same factor, so O / l and m + log2(l) are exact.
   constexpr float kPShift = (KV == PSP_KV_FP8) ? 8.f : 0.f;
@@ -230,33 +235,41 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     cp_async_wait<NST - U>();
     __syncwarp();
 
-    // ---- fragment loads of K (A operand of S^T) and V (A operand of O^T) for the whole
-    // iteration first, so their shared-memory latencies overlap each other and the softmax
-    // (the loads are volatile asm: the compiler keeps them in source order)
+    // ---- fragment loads of K (A operand of S^T) and V (A operand of O^T).  bf16 loads
+    // both for the whole iteration first, so their shared-memory latencies overlap each
+    // other and the softmax; fp8 loads V once the score products have consumed K, so the
+    // two sets of fragments never hold registers at the same time (the loads are volatile
+    // asm: the compiler keeps them in source order)
     constexpr int kKFrag = (KV == PSP_KV_BF16) ? D / 16 : D / 32;
     constexpr int kVFrag = (KV == PSP_KV_BF16) ? C::kMTiles : D / 32;
     uint32_t kf[U][kKFrag][4], vf[U][kVFrag][4];
     const bool second = (U == 1) || (i0 + 1 < my_n);  // fp8: the iteration's second sub-tile exists
+    const int lj = lane >> 3;
+    const int krow = (lane & 7) + (lj & 1) * 8;
+    const int vrow = (lane & 7) + (lj >> 1) * 8;
+    auto load_v = [&]() {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const unsigned char* vt = ring + ((i0 + u) % NST) * C::kStageBytes + C::kTileBytes;
+#pragma unroll
+        for (int f = 0; f < kVFrag; ++f)
+          ldsm_x4_t(vf[u][f], smem_u32(vt + vrow * C::kRowBytes + swz<C::kChunks>(vrow, 2 * f + (lj & 1)) * 16));
+      }
+      if (!second) {
+        // no second sub-tile: its stage holds stale codes (possibly NaN), so its value
+        // fragments are zero and its scores are masked below
+#pragma unroll
+        for (int f = 0; f < kVFrag; ++f) vf[U - 1][f][0] = vf[U - 1][f][1] = vf[U - 1][f][2] = vf[U - 1][f][3] = 0u;
+      }
+    };
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const unsigned char* kt = ring + ((i0 + u) % NST) * C::kStageBytes;
-      const unsigned char* vt = kt + C::kTileBytes;
-      const int j = lane >> 3;
-      const int krow = (lane & 7) + (j & 1) * 8;
-      const int vrow = (lane & 7) + (j >> 1) * 8;
 #pragma unroll
       for (int f = 0; f < kKFrag; ++f)
-        ldsm_x4(kf[u][f], smem_u32(kt + krow * C::kRowBytes + swz<C::kChunks>(krow, 2 * f + (j >> 1)) * 16));
-#pragma unroll
-      for (int f = 0; f < kVFrag; ++f)
-        ldsm_x4_t(vf[u][f], smem_u32(vt + vrow * C::kRowBytes + swz<C::kChunks>(vrow, 2 * f + (j & 1)) * 16));
+        ldsm_x4(kf[u][f], smem_u32(kt + krow * C::kRowBytes + swz<C::kChunks>(krow, 2 * f + (lj >> 1)) * 16));
     }
-    if (!second) {
-      // no second sub-tile: its stage holds stale codes (possibly NaN), so its value
-      // fragments are zero and its scores are masked below
-#pragma unroll
-      for (int f = 0; f < kVFrag; ++f) vf[U - 1][f][0] = vf[U - 1][f][1] = vf[U - 1][f][2] = vf[U - 1][f][3] = 0u;
-    }
+    if constexpr (KV == PSP_KV_BF16) load_v();
 
     // ---- S^T (16 tokens x 8 query heads) per sub-tile; two accumulators halve the mma chain
     float x[U][4];
@@ -282,6 +295,8 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
       x[u][3] = v_hi ? (sa[3] + sb[3]) * sc1 : neg_inf();
     }
 
+    if constexpr (KV != PSP_KV_BF16) load_v();
+
     // ---- online softmax over the iteration's tokens
     float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
@@ -295,15 +310,15 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     float pr[U][4];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      pr[u][0] = exp2f(x[u][0] - mn0);
-      pr[u][1] = exp2f(x[u][1] - mn1);
-      pr[u][2] = exp2f(x[u][2] - mn0);
-      pr[u][3] = exp2f(x[u][3] - mn1);
+      pr[u][0] = ex2_ftz(x[u][0] - mn0);
+      pr[u][1] = ex2_ftz(x[u][1] - mn1);
+      pr[u][2] = ex2_ftz(x[u][2] - mn0);
+      pr[u][3] = ex2_ftz(x[u][3] - mn1);
     }
     // fp8 (bound by its instruction count): rescale only when some running max moved,
     // which stops once the maxima settle; bf16 (bound by memory) rescales every sub-tile
     if (KV != PSP_KV_FP8 || __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+      const float a0 = ex2_ftz(m0 - mn0), a1 = ex2_ftz(m1 - mn1);
       l0 *= a0;
       l1 *= a1;
 #pragma unroll
@@ -408,7 +423,7 @@ cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
   using C = SufCfg<KV, D>;
   const int ring = NW * NST * C::kStageBytes;
   const int epi = (NW * 8 * D + 2 * NW * 8) * 4;
-  const int bytes = (ring > epi ? ring : epi) + kPreRows * (D + 1) * 4;
+  const int bytes = (ring > epi ? ring : epi) + C::template pre_rows<NST>() * (D + 1) * 4;
   auto kern = suffix_kernel<KV, D, NW, NST>;
   cudaError_t e = ensure_smem_limit<suffix_kernel<KV, D, NW, NST>>(bytes);
   if (e != cudaSuccess) return e;
@@ -451,10 +466,10 @@ cudaError_t launch_suffix(const StepParams& p, int num_splits, cudaStream_t s) {
   }
   if (p.kv_dtype == PSP_KV_FP8) {
     if (p.head_dim != 128) return launch_t<PSP_KV_FP8, 64, 4, 6>(p, num_splits, s);
-    switch (suffix_stages(4)) {  // fp8 consumes two sub-tiles per iteration: at least 4 stages
+    switch (suffix_stages(3)) {  // 3 stages, 128 registers: four CTAs per SM (measured best)
+      case 4: return launch_t<PSP_KV_FP8, 128, 4, 4>(p, num_splits, s);
       case 5: return launch_t<PSP_KV_FP8, 128, 4, 5>(p, num_splits, s);
-      case 6: return launch_t<PSP_KV_FP8, 128, 4, 6>(p, num_splits, s);
-      default: return launch_t<PSP_KV_FP8, 128, 4, 4>(p, num_splits, s);
+      default: return launch_t<PSP_KV_FP8, 128, 4, 3>(p, num_splits, s);
     }
   }
   return launch_suffix_simt(p, num_splits, s);

@@ -159,6 +159,14 @@ __device__ __forceinline__ int64_t slot_of(const int32_t* list, int t, int shift
   return (static_cast<int64_t>(__ldg(list + (t >> shift))) << shift) | (t & ((1 << shift) - 1));
 }
 
+// 2^x on the special-function unit; results below the smallest normal flush to zero
+// (a probability that small adds nothing to a softmax sum of at least 1).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Max / sum over the lanes that differ only in the given xor-mask bits.
 template <int FIRST, int LAST>
 __device__ __forceinline__ float xor_max(float v) {

@@ -25,7 +25,8 @@ struct SuffixCta {
   bool wait_prefix;  // dependent launch, sequential form: prefix rows only after the prefix grid
 };
 
-__device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, int split, int h) {
+// pre_rows: capacity of the caller's prefix-row prefetch area (at most kPreRows).
+__device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, int split, int h, int pre_rows = kPreRows) {
   SuffixCta c;
   c.split = split;
   c.h = h;
@@ -34,7 +35,7 @@ __device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, int split, 
   c.solo = !p.concurrent && p.split_indptr[c.b + 1] - p.split_indptr[c.b] == 1;
   c.c0 = g_req >= 0 ? p.group_chunk_indptr[g_req] : 0;
   c.n_chunks = g_req >= 0 ? p.group_chunk_indptr[g_req + 1] - c.c0 : 0;
-  c.pre_smem = c.solo && c.n_chunks > 0 && c.n_chunks * p.group <= kPreRows;
+  c.pre_smem = c.solo && c.n_chunks > 0 && c.n_chunks * p.group <= pre_rows;
   c.wait_prefix = p.pdl && !p.concurrent;
   return c;
 }
