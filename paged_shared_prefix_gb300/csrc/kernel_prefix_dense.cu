@@ -20,7 +20,13 @@
 //                   softmax works and the other way round;
 //   warps 0-3 / 4-7 (softmax, tiles A / B) one thread per row: read the S row,
 //                   online softmax, write P back over S, and at the end normalise O
-//                   and write the fp32 partial row and its log2-LSE.
+//                   and write the fp32 partial row and its log2-LSE.  With bf16 the
+//                   two groups take turns at the exponentials of a tile (A(j), B(j),
+//                   A(j+1), ..., handed over on two barriers): groups left to
+//                   themselves fall into step, computing at the same time and then
+//                   waiting together for the tensor pipe (measured on GB300: 4% on the
+//                   bf16 agent batch; e4m3 tiles, whose softmax is bound by the latency
+//                   of one warp rather than by the shared units, run 18% slower in turns).
 // The MMA warp runs its waits as a whole warp with one lane issuing (measured on
 // GB300: a completed mbarrier costs 100-200 cycles to poll, more from one lane
 // than from a whole warp, and one lane issuing while the rest of its warp polls
@@ -85,10 +91,10 @@ struct DenseCfg {
   static constexpr uint32_t kOffRing = kOffK0 + kTileBytes;  // stage s: V at +0, K at +kTileBytes
   static constexpr uint32_t kStageBytes = 2 * kTileBytes;
   static constexpr uint32_t kOffBar = kOffRing + kStages * kStageBytes;
-  // barriers: k0_full, full[S], empty[S], q_full[2], s_full[2], p_full[2], o_full[2], drain
+  // barriers: k0_full, full[S], empty[S], q_full[2], s_full[2], p_full[2], o_full[2], drain, turn[2]
   static constexpr int kBarK0 = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarQFull = 1 + 2 * kStages,
                        kBarSFull = kBarQFull + 2, kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2,
-                       kBarDrain = kBarOFull + 2, kNumBars = kBarDrain + 1;
+                       kBarDrain = kBarOFull + 2, kBarTurn = kBarDrain + 1, kNumBars = kBarTurn + 2;
   static constexpr uint32_t kOffTmem = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffAbort = kOffTmem + 8;       // int: a role gave up (CTA-wide)
   static constexpr uint32_t kOffAny = kOffAbort + 8;        // int: some member must arrive
@@ -147,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::kBarSFull + t), 1);
       mbar_init(bar(C::kBarPFull + t), kGroup / 32);
       mbar_init(bar(C::kBarOFull + t), 1);
+      mbar_init(bar(C::kBarTurn + t), kGroup / 32);  // one arrival per warp of the other group
     }
     mbar_init(bar(C::kBarDrain), 1);
     fence_mbar_init();
@@ -362,6 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float m_used = neg_inf(), l = 0.f;
     bool ok = true;
+    constexpr bool kTurns = !FP8;
+    // hands the exponentials over to the other group (one arrival per warp)
+    auto pass_turn = [&]() {
+      if (kTurns && tile_b) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kBarTurn + 1 - t));
+      }
+    };
     for (int j = 0; j < n_tiles && ok; ++j) {
       // S_t(j) complete, and with it every earlier product (one issuing thread), so O_t
       // holds exactly the tiles < j.  __all_sync: the warp leaves the poll loop together
@@ -369,8 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, wait_or_abort(s_full, j & 1, abort, status, 9));
       if (!ok) break;
       tc_fence_after();
+      const int valid = t1 - (t0 + j * kTok);
+      // the whole S row in registers (bf16 tiles; e4m3 tiles only when they need the max)
       float x[kTok];
-      {
+      auto load_row = [&]() {
         uint32_t u[kTok / 32][32];
 #pragma unroll
         for (int c = 0; c < kTok / 32; ++c) tmem_ld32(lane_addr + s_col + c * 32, u[c]);
@@ -379,11 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kTok / 32; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[c][i]);
-      }
-      const int valid = t1 - (t0 + j * kTok);
-      if (valid < kTok) {
+        if (valid < kTok) {
 #pragma unroll
-        for (int i = 0; i < kTok; ++i) x[i] = i < valid ? x[i] : neg_inf();
+          for (int i = 0; i < kTok; ++i) x[i] = i < valid ? x[i] : neg_inf();
+        }
+      };
+      if constexpr (!FP8) load_row();
+      // this group's turn at the exponentials (the other group finished its previous tile)
+      if (kTurns && tile_b && (t == 1 || j > 0)) {
+        ok = __all_sync(0xffffffffu, wait_or_abort(bar(C::kBarTurn + t), (t == 1 ? j : j - 1) & 1, abort, status, 13));
+        if (!ok) break;
       }
       // tile max with eight independent accumulators (short dependency chains)
       auto tile_max = [&]() {
@@ -402,7 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the max pass is skipped: they are computed against the current reference, and since
         // all are >= 0 their sum bounds each of them, so a tile sum <= 2^8 proves the bound.
         // Only a larger sum (rare: the scores rose) takes the max and, if it moved by more
-        // than 2^8, rebases and recomputes the tile.
+        // than 2^8, rebases; that tile, the first and a ragged last tile are computed again
+        // from the whole row.
         uint32_t u[kTok / 4];  // four e4m3 probabilities per column
         const float2 scale2 = make_float2(scale, scale);
         auto make_p = [&](float m) {
@@ -419,25 +442,59 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 s = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
           return s.x + s.y;
         };
-        float tile_sum;
-        if (j == 0) {
-          need = true;
-          m_used = tile_max();
-          tile_sum = make_p(m_used);
-        } else {
-          tile_sum = make_p(m_used);
-          if (!(tile_sum <= 256.f)) {  // also catches an infinite sum
-            const float mt = tile_max();
-            if (mt > m_used + kRescaleLog2) {
-              need = true;
-              alpha = ex2(m_used - mt);
-              m_used = mt;
-              l *= alpha;
-              tile_sum = make_p(m_used);
+        // The S row streamed from tensor memory in 32-column pieces, the next piece loading
+        // while this one computes: a full tile needs neither its max nor a register copy of
+        // the whole row (the row fills most of a thread's registers).
+        auto stream_p = [&](float m) {
+          const float2 neg_m2 = make_float2(-m, -m);
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          uint32_t ra[32], rb[32];
+          tmem_ld32(lane_addr + s_col, ra);
+          tmem_wait_ld_regs(ra);
+#pragma unroll
+          for (int c = 0; c < kTok / 32; ++c) {
+            uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+            uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+            if (c + 1 < kTok / 32) tmem_ld32(lane_addr + s_col + (c + 1) * 32, nxt);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(cur[4 * k]), __uint_as_float(cur[4 * k + 1])),
+                                           scale2, neg_m2);
+              const float2 y1 = __ffma2_rn(
+                  make_float2(__uint_as_float(cur[4 * k + 2]), __uint_as_float(cur[4 * k + 3])), scale2, neg_m2);
+              const float2 p0 = make_float2(ex2(y0.x), ex2(y0.y)), p1 = make_float2(ex2(y1.x), ex2(y1.y));
+              acc[k & 3] = __fadd2_rn(acc[k & 3], __fadd2_rn(p0, p1));
+              u[c * 8 + k] = e4m3x4_from_floats(p0.x, p0.y, p1.x, p1.y);
             }
+            if (c + 1 < kTok / 32) tmem_wait_ld_regs(nxt);
           }
+          const float2 s = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+          return s.x + s.y;
+        };
+        float tile_sum = 0.f;
+        bool whole = j == 0 || valid < kTok;  // first tile (no reference max yet) or ragged
+        if (!whole) {
+          tile_sum = stream_p(m_used);
+          // warp-uniform (the row reload below is a warp-collective tensor-memory load); a
+          // row whose own sum passed recomputes the same probabilities against the same max
+          whole = __any_sync(0xffffffffu, !(tile_sum <= 256.f));  // also catches an infinite sum
+        }
+        if (whole) {
+          load_row();
+          const float mt = tile_max();
+          if (j == 0) {
+            need = true;
+            m_used = mt;
+          } else if (mt > m_used + kRescaleLog2) {
+            need = true;
+            alpha = ex2(m_used - mt);
+            m_used = mt;
+            l *= alpha;
+          }
+          tile_sum = make_p(m_used);
         }
         l += tile_sum;
+        pass_turn();
         tmem_st32(lane_addr + s_col, u);
       } else {
         const float mt = tile_max();
@@ -462,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(lane_addr + s_col + c * 32, u);
         }
         l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+        pass_turn();
       }
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // rescale this warp's rows of O_t
