@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_kernel(const StepParams p, i
     if (threadIdx.x == 0) flags[0] = (solo || arrive_is_last(p, b_suffix, h)) ? 1 : 0;
     __syncthreads();
     if (flags[0])
-      for (int rr = warp; rr < G; rr += kWarps) merge_row<D>(p, b_suffix, h * G + rr, lane);
+      for (int j0 = warp; j0 < G; j0 += kWarps) merge_rows<D, 32>(p, b_suffix, h, j0, lane);
   } else {
     prefix_arrive_and_merge<D>(p, members, h, row0, n_rows, flags);
     prefix_rows_done(p, n_rows);

@@ -47,13 +47,21 @@ __device__ __forceinline__ bool arrive_is_last(const StepParams& p, int b, int h
   return false;
 }
 
-// Warp-cooperative merge of row (b, hq): lane l owns D/32 consecutive elements.
-template <int D>
-__device__ __forceinline__ void merge_row(const StepParams& p, int b, int hq, int lane) {
-  constexpr int kPer = D / 32;
+// Warp-cooperative merge of rows j0 .. j0 + 32/LANES - 1 (those below G) of (b, h): LANES
+// lanes per row, each owning D/LANES consecutive elements, every row at once, and no
+// store before the last load, so that the loads of every part of every row can be in
+// flight together (a merge costs a few dependent global round trips, not a few per row).
+// LANES = 4 merges a whole (request, KV head) in one warp; more lanes per row use fewer
+// registers per lane.
+template <int D, int LANES>
+__device__ __forceinline__ void merge_rows(const StepParams& p, int b, int h, int j0, int lane) {
+  constexpr int kPer = D / LANES;           // elements per lane
+  constexpr int kW = kPer % 4 == 0 ? 4 : 2;  // elements per vector access
+  static_assert(kPer % kW == 0, "whole vectors per lane");
   const int G = p.group;
-  const int h = hq / G;
-  const int j = hq - h * G;
+  const int j = j0 + lane / LANES;
+  const int sub = lane % LANES;
+  if (j >= G) return;
   const int g = p.req_group[b];
   int c0 = 0, c1 = 0, m_eff = 0, prow = 0;
   if (g >= 0) {
@@ -74,40 +82,37 @@ __device__ __forceinline__ void merge_row(const StepParams& p, int b, int hq, in
   auto add = [&](int64_t r, const float* obuf, const float* lbuf) {
     const float w = exp2f(__ldcg(lbuf + r) - mmax);
     sum += w;
-    const float* src = obuf + r * D + lane * kPer;
-    if constexpr (kPer == 4) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-      acc[0] = fmaf(w, v.x, acc[0]);
-      acc[1] = fmaf(w, v.y, acc[1]);
-      acc[2] = fmaf(w, v.z, acc[2]);
-      acc[3] = fmaf(w, v.w, acc[3]);
-    } else {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-      acc[0] = fmaf(w, v.x, acc[0]);
-      acc[1] = fmaf(w, v.y, acc[1]);
+    const float* src = obuf + r * D + sub * kPer;
+#pragma unroll
+    for (int v = 0; v < kPer; v += kW) {
+      if constexpr (kW == 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + v));
+        acc[v] = fmaf(w, x.x, acc[v]);
+        acc[v + 1] = fmaf(w, x.y, acc[v + 1]);
+        acc[v + 2] = fmaf(w, x.z, acc[v + 2]);
+        acc[v + 3] = fmaf(w, x.w, acc[v + 3]);
+      } else {
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(src + v));
+        acc[v] = fmaf(w, x.x, acc[v]);
+        acc[v + 1] = fmaf(w, x.y, acc[v + 1]);
+      }
     }
   };
   for (int c = c0; c < c1; ++c) add(p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow, p.o_pre, p.lse_pre);
   for (int s = s0; s < s1; ++s) add((static_cast<int64_t>(s) * p.hkv + h) * G + j, p.o_suf, p.lse_suf);
   const float inv = 1.f / sum;
-  const int64_t row = static_cast<int64_t>(b) * p.hq + hq;
-  const int64_t obase = row * D + lane * kPer;
+  const int64_t row = static_cast<int64_t>(b) * p.hq + h * G + j;
+  const int64_t obase = row * D + sub * kPer;
   if (p.o_dtype == PSP_KV_BF16) {
-    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o) + obase;
-    if constexpr (kPer == 4) {
-      uint2 v;
-      v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-      v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-      *reinterpret_cast<uint2*>(o) = v;
-    } else {
-      *reinterpret_cast<uint32_t*>(o) = pack_bf16(acc[0] * inv, acc[1] * inv);
-    }
+    uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.o) + obase);
+#pragma unroll
+    for (int v = 0; v < kPer; v += 2) o[v / 2] = pack_bf16(acc[v] * inv, acc[v + 1] * inv);
   } else {
     float* o = static_cast<float*>(p.o) + obase;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) o[k] = acc[k] * inv;
+    for (int v = 0; v < kPer; ++v) o[v] = acc[v] * inv;
   }
-  if (p.lse && lane == 0) p.lse[row] = (mmax + log2f(sum)) * 0.6931471805599453f;
+  if (p.lse && sub == 0) p.lse[row] = (mmax + log2f(sum)) * 0.6931471805599453f;
 }
 
 // Writes one row's final result directly (the row has exactly one partial).
@@ -157,14 +162,8 @@ __device__ __forceinline__ void prefix_arrive_and_merge(const StepParams& p, con
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  for (int rr = warp; rr < n; rr += nwarps) {
-    const int m = rr / G;
-    if (flags[m]) {
-      const int R = row0 + rr;
-      const int b = members[R / G];
-      merge_row<D>(p, b, h * G + (R - (R / G) * G), lane);
-    }
-  }
+  for (int m = warp; m < n_members; m += nwarps)
+    if (flags[m]) merge_rows<D, 32 / kMaxGroupSize>(p, members[(row0 / G) + m], h, 0, lane);
 }
 
 // As prefix_arrive_and_merge, with flags[m] (m < n / G) already holding
@@ -180,13 +179,8 @@ __device__ __forceinline__ void prefix_arrive_and_merge_flagged(const StepParams
     if (flags[m]) flags[m] = arrive_is_last(p, members[(row0 / G) + m], h) ? 1 : 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  for (int rr = warp; rr < n; rr += nwarps) {
-    const int m = rr / G;
-    if (flags[m]) {
-      const int R = row0 + rr;
-      merge_row<D>(p, members[R / G], h * G + (R - (R / G) * G), lane);
-    }
-  }
+  for (int m = warp; m < n_members; m += nwarps)
+    if (flags[m]) merge_rows<D, 32 / kMaxGroupSize>(p, members[(row0 / G) + m], h, 0, lane);
 }
 
 }  // namespace dev

@@ -76,7 +76,6 @@ template <int D, int NSTATE, int NT>
 __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixCta& c, const float* red,
                                               const float* ms, const float* ls, const float* pre_o,
                                               const float* pre_l, float out_scale) {
-  constexpr int kWarps = NT / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int b = c.b, h = c.h;
@@ -95,6 +94,10 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
     if (ready) __threadfence();  // the prefix partials were fenced before their rows were counted
   }
   const bool solo_global = (c.solo && !direct) || ready;  // read the prefix partials from global memory
+  // the G rows of (b, h) over the CTA's warps, two rows per warp at once (16 lanes a row)
+  auto merge_cta_rows = [&](int bb) {
+    for (int j0 = warp; j0 < G; j0 += NT / 32) merge_rows<D, 32>(p, bb, h, j0, lane);
+  };
   const int64_t row0 = (static_cast<int64_t>(c.split) * p.hkv + h) * G;
   const int64_t orow0 = static_cast<int64_t>(b) * p.hq + h * G;
   for (int e = threadIdx.x; e < G * D; e += NT) {
@@ -135,15 +138,14 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
     __threadfence();
     __syncthreads();
     if (solo_global) {  // every other part of (b, h) is already complete
-      for (int rr = warp; rr < G; rr += kWarps) merge_row<D>(p, b, h * G + rr, lane);
+      merge_cta_rows(b);
       // every prefix arrival on (b, h) was made and nothing else arrives: clear it for the next step
       if (ready && threadIdx.x == 0) p.counters[static_cast<int64_t>(b) * p.hkv + h] = 0;
     } else {
       __shared__ int last;
       if (threadIdx.x == 0) last = arrive_is_last(p, b, h) ? 1 : 0;
       __syncthreads();
-      if (last)
-        for (int rr = warp; rr < G; rr += kWarps) merge_row<D>(p, b, h * G + rr, lane);
+      if (last) merge_cta_rows(b);
     }
   }
 }
