@@ -52,7 +52,8 @@
  *   PSP_PREFIX_MIN_TILES,   prefix-chunk partition: smallest chunk in 64-token granules
  *   PSP_PREFIX_CTAS_PER_SM  (default 4) and prefix CTAs per SM (default 1)
  *   PSP_PDL_FORM            prefix -> suffix dependent launch: 0 chosen by the prefix
- *                           grid's size (default), 1 sequential, 2 concurrent
+ *                           grid's size and chunk length (default), 1 sequential,
+ *                           2 concurrent
  *   PSP_SUFFIX_STAGES       suffix ring depth per warp at d = 128 (default 2 for bf16,
  *                           4 for e4m3; once per process)
  *   PSP_LOG                 1: psp_plan writes one line per planned step to stderr,

@@ -40,6 +40,7 @@ constexpr int32_t kReadOnceMinTokens = 1024;
 constexpr int32_t kReadOnceMinMiB = 64;
 
 constexpr int32_t kSplitMinTiles = 4;
+constexpr int32_t kConcurrentChunkTokens = 4096;  // prefix chunk length from which the concurrent form runs
 constexpr int32_t kSplitCtasPerSm = 5;  // measured on GB300 with 2-stage bf16 rings: 5 (split, head) CTAs per SM
 constexpr int32_t kPrefixMinTiles = 4;
 constexpr int32_t kPrefixCtasPerSm = 1;  // a dense prefix CTA fills an SM (all of tensor memory)
@@ -896,11 +897,19 @@ psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
   // the last arrival merges (the concurrent protocol).  Not with per-kernel timing (events
   // between the launches) nor when the prefix runs on its own stream.
   p.pdl = (!fork && !h->timing && (nd > 0 || nc > 0) && P.NS > 0) ? 1 : 0;
-  // Two forms (measured on GB300): when the prefix grid leaves at least half of the SMs free,
-  // the suffix kernel never waits and uses the concurrent merge protocol (short prefixes:
-  // 76 vs 81 us); when the prefix grid fills the GPU, the suffix CTAs wait for it before
-  // reading prefix partials and keep the sequential protocol (agent batch: 148 vs 163 us).
-  if (p.pdl && static_cast<int64_t>(nd + nc) * p.hkv * 2 <= h->num_sms_resolved) p.concurrent = 1;
+  // Two forms (measured on GB300).  Concurrent: the suffix kernel never waits and uses the
+  // concurrent merge protocol.  Sequential: the suffix CTAs wait for the prefix grid before
+  // reading prefix partials.  The concurrent form wins when the prefix grid leaves at least
+  // half of the SMs free (short prefixes: 76 vs 81 us) or when its CTAs run long, so that the
+  // SMs it leaves free do a large share of the suffix meanwhile (16384-token chunks, e4m3
+  // batch: 384 vs 395 us); with short chunks on a full GPU the sequential form is ahead
+  // (1024-token chunks, agent batch: 138 vs 140 us).
+  if (p.pdl) {
+    int32_t longest = 0;
+    for (size_t ci = 0; ci < P.chunk_begin.size(); ++ci) longest = std::max(longest, P.chunk_end[ci] - P.chunk_begin[ci]);
+    if (static_cast<int64_t>(nd + nc) * p.hkv * 2 <= h->num_sms_resolved || longest >= kConcurrentChunkTokens)
+      p.concurrent = 1;
+  }
   // PSP_PDL_FORM overrides the choice for measurements: 1 sequential, 2 concurrent
   if (p.pdl && h->pdl_form == 1) p.concurrent = 0;
   if (p.pdl && h->pdl_form == 2) p.concurrent = 1;

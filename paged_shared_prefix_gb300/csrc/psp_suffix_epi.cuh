@@ -23,6 +23,7 @@ struct SuffixCta {
   bool solo;         // one suffix split and the prefix kernels complete before its rows are read
   bool pre_smem;     // solo, and the prefix rows fit the shared-memory prefetch area
   bool wait_prefix;  // dependent launch, sequential form: prefix rows only after the prefix grid
+  bool late;         // dependent launch, concurrent form, and the prefix was complete at the start
 };
 
 // pre_rows: capacity of the caller's prefix-row prefetch area (at most kPreRows).
@@ -32,9 +33,25 @@ __device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, int split, 
   c.h = h;
   c.b = p.split_req[split];
   const int g_req = p.req_group[c.b];
-  c.solo = !p.concurrent && p.split_indptr[c.b + 1] - p.split_indptr[c.b] == 1;
+  const bool one_split = p.split_indptr[c.b + 1] - p.split_indptr[c.b] == 1;
+  c.solo = !p.concurrent && one_split;
   c.c0 = g_req >= 0 ? p.group_chunk_indptr[g_req] : 0;
   c.n_chunks = g_req >= 0 ? p.group_chunk_indptr[g_req + 1] - c.c0 : 0;
+  // Concurrent form: a one-split request whose CTA starts after every prefix row is done
+  // (the prefix CTAs count their rows after their partials and arrivals) merges like a
+  // solo request of the sequential form, from prefetched rows, without its counter.
+  c.late = false;
+  if (p.pdl && p.concurrent && one_split && c.n_chunks > 0) {
+    __shared__ int prefix_complete;
+    if (threadIdx.x == 0)
+      prefix_complete = *reinterpret_cast<volatile int32_t*>(p.prefix_done) == p.prefix_rows_total;
+    __syncthreads();
+    if (prefix_complete) {
+      __threadfence();  // the prefix partials were fenced before their rows were counted
+      c.late = true;
+      c.solo = true;
+    }
+  }
   c.pre_smem = c.solo && c.n_chunks > 0 && c.n_chunks * p.group <= pre_rows;
   c.wait_prefix = p.pdl && !p.concurrent;
   return c;
@@ -85,8 +102,8 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
   // Launched as a dependent of a still running prefix kernel: a one-split request whose
   // prefix partials are all complete (every prefix row counted done) merges them here like
   // a solo request; otherwise its part goes through the (request, KV head) counter.
-  bool ready = false;
-  if (p.pdl && p.concurrent && one_split && c.n_chunks > 0) {
+  bool ready = c.late;
+  if (!c.late && p.pdl && p.concurrent && one_split && c.n_chunks > 0) {
     __shared__ int prefix_ready;
     if (threadIdx.x == 0) prefix_ready = *reinterpret_cast<volatile int32_t*>(p.prefix_done) == p.prefix_rows_total;
     __syncthreads();
@@ -94,7 +111,7 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
     if (ready) __threadfence();  // the prefix partials were fenced before their rows were counted
   }
   const bool solo_global = (c.solo && !direct) || ready;  // read the prefix partials from global memory
-  // the G rows of (b, h) over the CTA's warps, two rows per warp at once (16 lanes a row)
+  // the G rows of (b, h) over the CTA's warps, one row per warp at a time
   auto merge_cta_rows = [&](int bb) {
     for (int j0 = warp; j0 < G; j0 += NT / 32) merge_rows<D, 32>(p, bb, h, j0, lane);
   };
@@ -129,6 +146,8 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
       out = fmaf(w_own, acc / sum * out_scale, out);
       store_final(p, orow0 + g, d, out / wsum);
       if (d == 0 && p.lse) p.lse[orow0 + g] = (big + log2f(wsum)) * 0.6931471805599453f;
+      // every prefix arrival on (b, h) was made and nothing else arrives: clear it for the next step
+      if (c.late && e == 0) p.counters[static_cast<int64_t>(b) * p.hkv + h] = 0;
     } else {
       p.o_suf[(row0 + g) * D + d] = acc / sum * out_scale;
       if (d == 0) p.lse_suf[row0 + g] = mmax + log2f(sum);
