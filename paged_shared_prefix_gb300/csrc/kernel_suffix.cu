@@ -47,10 +47,14 @@ struct SufCfg {
   // 16-row area would keep a 3-stage e4m3 ring (48 KB) from four resident CTAs per SM
   template <int NST>
   __host__ __device__ static constexpr int pre_rows() { return (KV == PSP_KV_FP8 && D == 128 && NST == 3) ? 8 : kPreRows; }
+  // resident CTAs per SM the register allocation must allow: four for that e4m3 ring (128
+  // registers a thread), otherwise whatever the compiler chooses
+  template <int NST>
+  __host__ __device__ static constexpr int min_ctas() { return (KV == PSP_KV_FP8 && D == 128 && NST == 3) ? 4 : 1; }
 };
 
 template <int KV, int D, int NW, int NST>
-__global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
+__global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>()) suffix_kernel(const StepParams p) {
   using C = SufCfg<KV, D>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
@@ -59,18 +63,19 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   // the heads' rows of each token (adjacent in the pool) are read at about the same time
   const int h = blockIdx.x % p.hkv;
   const int split = blockIdx.x / p.hkv;
-  const int b = p.split_req[split];
-  const int t0 = p.split_begin[split];
-  const int t1 = p.split_end[split];
+  const SplitDesc sd = load_split_desc(p, split);
+  const int b = sd.b;
+  const int t0 = sd.t0;
+  const int t1 = sd.t1;
   const int G = p.group;
 
   const int32_t* list;
   int shift;
   if (p.token_flat) {
-    list = p.kv_indices + p.kv_indptr[b] + p.suffix_start[b];
+    list = p.kv_indices + sd.list_flat;
     shift = 0;
   } else {
-    list = p.suffix_page_indices + p.suffix_page_indptr[b];
+    list = p.suffix_page_indices + sd.list_paged;
     shift = p.page_shift;
   }
   const int64_t row_stride = static_cast<int64_t>(p.hkv) * C::kRowBytes;
@@ -85,9 +90,10 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   // kernel ran earlier on the stream, so its rows are complete.  They are prefetched into
   // a shared-memory area of their own, in the first cp.async group of every thread (a
   // dependent launch that keeps the sequential protocol reads them only after the prefix
-  // grid has completed, below, after this CTA's own stream).
+  // grid has completed, below, after this CTA's own stream; one in the concurrent form
+  // prefetches them once its first copies are in flight if the prefix is complete by then).
   constexpr int kPre = C::template pre_rows<NST>();
-  const SuffixCta cta = suffix_cta(p, split, h, kPre);
+  SuffixCta cta = suffix_cta(p, sd, split, h, kPre);
   float* pre_o = reinterpret_cast<float*>(smem + NW * NST * C::kStageBytes);   // [chunk * G + j][D]
   float* pre_l = pre_o + kPre * D;                                               // [chunk * G + j]
   if (cta.pre_smem && !cta.wait_prefix) prefetch_prefix_rows<D, NW * 32>(p, cta, pre_o, pre_l);
@@ -218,6 +224,7 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
 #pragma unroll
   for (int u = 0; u < U; ++u)
     if (NST - U + u < my_n) load_pages(NST - U + u, pages[u]);
+  if (suffix_cta_late(p, cta, kPre)) prefetch_prefix_rows<D, NW * 32>(p, cta, pre_o, pre_l);
 
   for (int i0 = 0; i0 < my_n; i0 += U) {
 #pragma unroll
@@ -372,6 +379,7 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
     }
     __syncwarp();  // every lane's fragment loads are done before the next refill of these stages
   }
+  const bool grid_last = suffix_grid_arrive(p);
   cp_async_wait<0>();
   if (cta.wait_prefix) {
     pdl_wait_primary();  // every prefix partial and prefix arrival of this step is complete
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(NW * 32) suffix_kernel(const StepParams p) {
   }
   __syncthreads();
   suffix_finish<D, NW, NW * 32>(p, cta, red, ms, ls, pre_o, pre_l, out_scale);
-  suffix_grid_tail(p);
+  suffix_grid_tail(p, grid_last);
 }
 
 template <int KV, int D, int NW, int NST>

@@ -71,6 +71,7 @@ struct HostPlan {
   int32_t B = 0, NG = 0, NS = 0, NC = 0;
   std::vector<int32_t> suffix_page_indptr, suffix_page_indices, suffix_start, suffix_len;
   std::vector<int32_t> split_indptr, split_req, split_begin, split_end;
+  std::vector<int32_t> split_desc;  // kSplitDescInts per split (psp::SplitDesc)
   std::vector<int32_t> req_group, req_member;
   std::vector<int32_t> group_page_indptr, group_page_indices, group_m_eff, group_shared_len;
   std::vector<int32_t> group_branch, group_row_blocks;
@@ -89,7 +90,7 @@ struct HostPlan {
     B = NG = NS = NC = 0;
     for (std::vector<int32_t>* v :
          {&suffix_page_indptr, &suffix_page_indices, &suffix_start, &suffix_len, &split_indptr, &split_req,
-          &split_begin, &split_end, &req_group, &req_member, &group_page_indptr, &group_page_indices,
+          &split_begin, &split_end, &split_desc, &req_group, &req_member, &group_page_indptr, &group_page_indices,
           &group_m_eff, &group_shared_len, &group_branch, &group_row_blocks, &group_member_indptr, &group_members,
           &group_chunk_indptr, &chunk_group, &chunk_begin, &chunk_end, &chunk_row_offset, &item_chunk_dense,
           &item_rb_dense, &item_chunk_cascade, &item_rb_cascade, &kv_indptr})
@@ -376,6 +377,23 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
     P.split_indptr[b + 1] = static_cast<int32_t>(P.split_req.size());
   }
   P.NS = static_cast<int32_t>(P.split_req.size());
+  P.split_desc.assign(static_cast<size_t>(P.NS) * psp::kSplitDescInts, 0);
+  for (int32_t si = 0; si < P.NS; ++si) {
+    psp::SplitDesc d{};
+    const int32_t b = P.split_req[si];
+    const int32_t g = P.req_group[b];
+    d.b = b;
+    d.t0 = P.split_begin[si];
+    d.t1 = P.split_end[si];
+    d.list_paged = P.suffix_page_indptr[b];
+    d.list_flat = P.kv_indptr[b] + P.suffix_start[b];
+    d.c0 = g >= 0 ? P.group_chunk_indptr[g] : 0;
+    d.n_chunks = g >= 0 ? P.group_chunk_indptr[g + 1] - d.c0 : 0;
+    d.one_split = P.split_indptr[b + 1] - P.split_indptr[b] == 1 ? 1 : 0;
+    d.prow = g >= 0 ? P.req_member[b] * G : 0;
+    d.m_eff = g >= 0 ? P.group_m_eff[g] : 0;
+    std::memcpy(P.split_desc.data() + static_cast<size_t>(si) * psp::kSplitDescInts, &d, sizeof(d));
+  }
   if (static_cast<int64_t>(P.NS) * Hkv > INT32_MAX / psp::kMaxGroupSize)
     return fail(h, PSP_ERR_INVALID_ARGUMENT, "too many splits");
 
@@ -392,6 +410,7 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   place(L.split_req, n32(P.split_req));
   place(L.split_begin, n32(P.split_begin));
   place(L.split_end, n32(P.split_end));
+  place(L.split_desc, n32(P.split_desc));
   place(L.req_group, n32(P.req_group));
   place(L.req_member, n32(P.req_member));
   place(L.group_page_indptr, n32(P.group_page_indptr));
@@ -438,6 +457,7 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   put(L.split_req, P.split_req);
   put(L.split_begin, P.split_begin);
   put(L.split_end, P.split_end);
+  put(L.split_desc, P.split_desc);
   put(L.req_group, P.req_group);
   put(L.req_member, P.req_member);
   put(L.group_page_indptr, P.group_page_indptr);
@@ -549,6 +569,7 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.split_req = I(L.split_req);
   p.split_begin = I(L.split_begin);
   p.split_end = I(L.split_end);
+  p.split_desc = reinterpret_cast<const psp::SplitDesc*>(I(L.split_desc));
   p.req_group = I(L.req_group);
   p.req_member = I(L.req_member);
   p.group_page_indptr = I(L.group_page_indptr);

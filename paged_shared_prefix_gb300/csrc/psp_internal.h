@@ -27,6 +27,24 @@ constexpr int32_t kDevBadIndex = 2;
 
 // Everything a kernel of the step reads: configuration, caller tensors, the
 // uploaded plan and the partial-result buffers in the workspace.
+// Everything a suffix CTA needs to know about its split, in one 64-byte record, so that
+// the CTA's first load is not followed by loads that depend on it (each is a DRAM round
+// trip before the first K/V copy can be issued).
+struct SplitDesc {
+  int32_t b;           // request
+  int32_t t0, t1;      // suffix tokens [t0, t1) of b
+  int32_t list_paged;  // b's first entry in suffix_page_indices
+  int32_t list_flat;   // b's first suffix entry in kv_indices (kv_indptr[b] + suffix_start[b])
+  int32_t c0;          // b's shared-prefix chunks [c0, c0 + n_chunks) (none: 0, 0)
+  int32_t n_chunks;
+  int32_t one_split;   // 1: b has exactly one suffix split
+  int32_t prow;        // b's first stacked prefix row (member index x G)
+  int32_t m_eff;       // stacked rows of b's group (0 without a prefix branch)
+  int32_t pad[6];
+};
+static_assert(sizeof(SplitDesc) == 64, "one 64-byte record per split");
+constexpr int kSplitDescInts = static_cast<int>(sizeof(SplitDesc) / sizeof(int32_t));
+
 struct StepParams {
   // configuration
   int32_t batch;
@@ -57,6 +75,7 @@ struct StepParams {
   const int32_t* split_req;            // [S]
   const int32_t* split_begin;          // [S]
   const int32_t* split_end;            // [S]
+  const SplitDesc* split_desc;         // [S]
   const int32_t* req_group;            // [B] group with a prefix branch, else -1
   const int32_t* req_member;           // [B] index of b among its group's members
   const int32_t* group_page_indptr;    // [NG+1]
@@ -92,7 +111,7 @@ struct StepParams {
 // Byte offsets of every array inside the workspace (256-byte aligned each).
 struct PlanLayout {
   size_t suffix_page_indptr, suffix_page_indices, suffix_start, suffix_len;
-  size_t split_indptr, split_req, split_begin, split_end;
+  size_t split_indptr, split_req, split_begin, split_end, split_desc;
   size_t req_group, req_member;
   size_t group_page_indptr, group_page_indices, group_m_eff, group_shared_len;
   size_t group_member_indptr, group_members, group_chunk_indptr;

@@ -16,10 +16,30 @@ namespace dev {
 
 constexpr int kPreRows = 16;  // prefix partial rows (chunks x query heads) prefetched per single-split request
 
+// The split's descriptor: three 16-byte loads, all issued together.
+__device__ __forceinline__ SplitDesc load_split_desc(const StepParams& p, int split) {
+  const int4* src = reinterpret_cast<const int4*>(p.split_desc + split);
+  const int4 a = __ldg(src), b = __ldg(src + 1), c = __ldg(src + 2);
+  SplitDesc d;
+  d.b = a.x;
+  d.t0 = a.y;
+  d.t1 = a.z;
+  d.list_paged = a.w;
+  d.list_flat = b.x;
+  d.c0 = b.y;
+  d.n_chunks = b.z;
+  d.one_split = b.w;
+  d.prow = c.x;
+  d.m_eff = c.y;
+  return d;
+}
+
 // What the end of a suffix CTA needs to know about its request.
 struct SuffixCta {
   int split, h, b;
   int c0, n_chunks;  // b's shared-prefix chunks [c0, c0 + n_chunks)
+  int prow, m_eff;   // b's first stacked prefix row and its group's stacked rows
+  bool one_split;    // b has exactly one suffix split
   bool solo;         // one suffix split and the prefix kernels complete before its rows are read
   bool pre_smem;     // solo, and the prefix rows fit the shared-memory prefetch area
   bool wait_prefix;  // dependent launch, sequential form: prefix rows only after the prefix grid
@@ -27,34 +47,41 @@ struct SuffixCta {
 };
 
 // pre_rows: capacity of the caller's prefix-row prefetch area (at most kPreRows).
-__device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, int split, int h, int pre_rows = kPreRows) {
+__device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, const SplitDesc& d, int split, int h,
+                                                int pre_rows = kPreRows) {
   SuffixCta c;
   c.split = split;
   c.h = h;
-  c.b = p.split_req[split];
-  const int g_req = p.req_group[c.b];
-  const bool one_split = p.split_indptr[c.b + 1] - p.split_indptr[c.b] == 1;
-  c.solo = !p.concurrent && one_split;
-  c.c0 = g_req >= 0 ? p.group_chunk_indptr[g_req] : 0;
-  c.n_chunks = g_req >= 0 ? p.group_chunk_indptr[g_req + 1] - c.c0 : 0;
-  // Concurrent form: a one-split request whose CTA starts after every prefix row is done
-  // (the prefix CTAs count their rows after their partials and arrivals) merges like a
-  // solo request of the sequential form, from prefetched rows, without its counter.
+  c.b = d.b;
+  c.c0 = d.c0;
+  c.n_chunks = d.n_chunks;
+  c.prow = d.prow;
+  c.m_eff = d.m_eff;
+  c.one_split = d.one_split != 0;
+  c.solo = !p.concurrent && c.one_split;
   c.late = false;
-  if (p.pdl && p.concurrent && one_split && c.n_chunks > 0) {
-    __shared__ int prefix_complete;
-    if (threadIdx.x == 0)
-      prefix_complete = *reinterpret_cast<volatile int32_t*>(p.prefix_done) == p.prefix_rows_total;
-    __syncthreads();
-    if (prefix_complete) {
-      __threadfence();  // the prefix partials were fenced before their rows were counted
-      c.late = true;
-      c.solo = true;
-    }
-  }
   c.pre_smem = c.solo && c.n_chunks > 0 && c.n_chunks * p.group <= pre_rows;
   c.wait_prefix = p.pdl && !p.concurrent;
   return c;
+}
+
+// Concurrent form: a one-split request whose CTA finds every prefix row done (the prefix
+// CTAs count their rows after their partials and arrivals) merges like a solo request of
+// the sequential form, from prefetched rows, without its counter.  Called by every thread
+// once the CTA's first copies are in flight (the check is a round trip); returns true when
+// the caller should prefetch the prefix rows now.
+__device__ __forceinline__ bool suffix_cta_late(const StepParams& p, SuffixCta& c, int pre_rows = kPreRows) {
+  if (!(p.pdl && p.concurrent && c.one_split && c.n_chunks > 0)) return false;
+  __shared__ int prefix_complete;
+  if (threadIdx.x == 0)
+    prefix_complete = *reinterpret_cast<volatile int32_t*>(p.prefix_done) == p.prefix_rows_total;
+  __syncthreads();
+  if (!prefix_complete) return false;
+  __threadfence();  // the prefix partials were fenced before their rows were counted
+  c.late = true;
+  c.solo = true;
+  c.pre_smem = c.n_chunks * p.group <= pre_rows;
+  return c.pre_smem;
 }
 
 // cp.async of b's prefix partial rows of head h into pre_o [chunk * G + j][D] and
@@ -64,8 +91,8 @@ template <int D, int NT>
 __device__ __forceinline__ void prefetch_prefix_rows(const StepParams& p, const SuffixCta& c, float* pre_o,
                                                      float* pre_l, int tid = threadIdx.x) {
   const int G = p.group;
-  const int m_eff = p.group_m_eff[p.req_group[c.b]];
-  const int prow = p.req_member[c.b] * G;
+  const int m_eff = c.m_eff;
+  const int prow = c.prow;
   constexpr int kRowChunks = D * 4 / 16;
   for (int e = tid; e < c.n_chunks * G * (kRowChunks + 1); e += NT) {
     const int ch = e / (G * (kRowChunks + 1));
@@ -96,7 +123,7 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int b = c.b, h = c.h;
-  const bool one_split = p.split_indptr[b + 1] - p.split_indptr[b] == 1;
+  const bool one_split = c.one_split;
   const bool only_part = one_split && c.n_chunks == 0;
   const bool direct = only_part || (c.solo && c.pre_smem);
   // Launched as a dependent of a still running prefix kernel: a one-split request whose
@@ -172,15 +199,19 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
 // End of every suffix CTA.  Launched as a dependent of the prefix kernel and never
 // waiting for it (the concurrent form), the grid's last CTA waits for the prefix grid,
 // so this grid (and the stream after it) completes only after the prefix kernel; in the
-// sequential form every CTA has waited already.  Called by every thread of the CTA.
-__device__ __forceinline__ void suffix_grid_tail(const StepParams& p) {
-  if (!p.pdl || !p.concurrent) return;
-  __syncthreads();
-  if (threadIdx.x == 0 && atomicAdd(p.done_ctas, 1) == static_cast<int>(gridDim.x) - 1) {
-    *p.done_ctas = 0;  // ready for the next step (stream-ordered)
-    pdl_wait_primary();
-    *p.prefix_done = 0;  // every prefix CTA has counted its rows
-  }
+// sequential form every CTA has waited already.  suffix_grid_arrive counts the CTA (thread
+// 0, right after its main loop, so that the atomic's round trip overlaps the epilogue) and
+// returns whether it was the last; suffix_grid_tail, at the very end, does the last CTA's
+// waiting.  A reset of the prefix-row count while other CTAs finish only sends their
+// one-split merges through the counter, which is always correct.
+__device__ __forceinline__ bool suffix_grid_arrive(const StepParams& p) {
+  return p.pdl && p.concurrent && threadIdx.x == 0 && atomicAdd(p.done_ctas, 1) == static_cast<int>(gridDim.x) - 1;
+}
+__device__ __forceinline__ void suffix_grid_tail(const StepParams& p, bool last) {
+  if (!last) return;
+  *p.done_ctas = 0;  // ready for the next step (stream-ordered)
+  pdl_wait_primary();
+  *p.prefix_done = 0;  // every prefix CTA has counted its rows
 }
 
 }  // namespace dev
