@@ -124,6 +124,16 @@ __device__ __forceinline__ void store_final(const StepParams& p, int64_t row, in
   }
 }
 
+// Writes four consecutive elements (d a multiple of 4) of one row's final result.
+__device__ __forceinline__ void store_final4(const StepParams& p, int64_t row, int d, float4 v) {
+  const int64_t off = row * p.head_dim + d;
+  if (p.o_dtype == PSP_KV_BF16) {
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + off) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.o) + off) = v;
+  }
+}
+
 // Prefix kernels launched ahead of a dependent suffix kernel that does not wait for them
 // (the concurrent form): after this CTA's partials and arrivals are complete, count its
 // rows as done, so that suffix CTAs can see that the whole prefix is finished.  Called by

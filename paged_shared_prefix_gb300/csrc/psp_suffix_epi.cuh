@@ -144,40 +144,73 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
   };
   const int64_t row0 = (static_cast<int64_t>(c.split) * p.hkv + h) * G;
   const int64_t orow0 = static_cast<int64_t>(b) * p.hq + h * G;
-  for (int e = threadIdx.x; e < G * D; e += NT) {
-    const int g = e / D;
-    const int d = e - g * D;
+  // Per row (one thread per query head): the weight of each warp's state and of each
+  // prefix chunk in the row's result, and the row's log2-LSE.  The own part is
+  // O_s = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w, times the value scale, with
+  // log2-LSE M + log2(sum); a direct merge weighs it against the prefix chunks first.
+  __shared__ float s_coef[NSTATE * 8];  // [warp state][row]
+  __shared__ float s_cpre[kPreRows];    // [chunk * G + row]
+  __shared__ float s_lse[8];
+  if (threadIdx.x < G) {
+    const int g = threadIdx.x;
     float mmax = neg_inf();
 #pragma unroll
     for (int w = 0; w < NSTATE; ++w) mmax = fmaxf(mmax, ms[w * 8 + g]);
-    float acc = 0.f, sum = 0.f;
+    float sc[NSTATE];
+    float sum = 0.f;
 #pragma unroll
     for (int w = 0; w < NSTATE; ++w) {
-      const float sc = exp2f(ms[w * 8 + g] - mmax);
-      sum += ls[w * 8 + g] * sc;
-      acc += red[(w * 8 + g) * D + d] * sc;
+      sc[w] = exp2f(ms[w * 8 + g] - mmax);
+      sum += ls[w * 8 + g] * sc[w];
     }
+    const float lse_own = mmax + log2f(sum);
+    float f = out_scale / sum;
+    float lse_row = lse_own;
     if (direct) {
-      // own part: O_s = acc / sum * out_scale with log2-LSE mmax + log2(sum); prefix chunks first
-      float lse_own = mmax + log2f(sum);
       float big = lse_own;
       for (int ch = 0; ch < c.n_chunks; ++ch) big = fmaxf(big, pre_l[ch * G + g]);
-      float wsum = 0.f, out = 0.f;
+      float wsum = 0.f;
       for (int ch = 0; ch < c.n_chunks; ++ch) {
         const float w = exp2f(pre_l[ch * G + g] - big);
+        s_cpre[ch * G + g] = w;
         wsum += w;
-        out = fmaf(w, pre_o[(ch * G + g) * D + d], out);
       }
       const float w_own = exp2f(lse_own - big);
       wsum += w_own;
-      out = fmaf(w_own, acc / sum * out_scale, out);
-      store_final(p, orow0 + g, d, out / wsum);
-      if (d == 0 && p.lse) p.lse[orow0 + g] = (big + log2f(wsum)) * 0.6931471805599453f;
+      const float inv = 1.f / wsum;
+      for (int ch = 0; ch < c.n_chunks; ++ch) s_cpre[ch * G + g] *= inv;
+      f *= w_own * inv;
+      lse_row = big + log2f(wsum);
+    }
+#pragma unroll
+    for (int w = 0; w < NSTATE; ++w) s_coef[w * 8 + g] = sc[w] * f;
+    s_lse[g] = lse_row;
+  }
+  __syncthreads();
+  // every element: a few FMAs over four consecutive d, one vector store
+  constexpr int kQuads = D / 4;
+  for (int e = threadIdx.x; e < G * kQuads; e += NT) {
+    const int g = e / kQuads;
+    const int d = (e - g * kQuads) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float cf, const float* src) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc.x = fmaf(cf, v.x, acc.x);
+      acc.y = fmaf(cf, v.y, acc.y);
+      acc.z = fmaf(cf, v.z, acc.z);
+      acc.w = fmaf(cf, v.w, acc.w);
+    };
+#pragma unroll
+    for (int w = 0; w < NSTATE; ++w) add(s_coef[w * 8 + g], red + (w * 8 + g) * D + d);
+    if (direct) {
+      for (int ch = 0; ch < c.n_chunks; ++ch) add(s_cpre[ch * G + g], pre_o + (ch * G + g) * D + d);
+      store_final4(p, orow0 + g, d, acc);
+      if (d == 0 && p.lse) p.lse[orow0 + g] = s_lse[g] * 0.6931471805599453f;
       // every prefix arrival on (b, h) was made and nothing else arrives: clear it for the next step
       if (c.late && e == 0) p.counters[static_cast<int64_t>(b) * p.hkv + h] = 0;
     } else {
-      p.o_suf[(row0 + g) * D + d] = acc / sum * out_scale;
-      if (d == 0) p.lse_suf[row0 + g] = mmax + log2f(sum);
+      *reinterpret_cast<float4*>(p.o_suf + (row0 + g) * D + d) = acc;
+      if (d == 0) p.lse_suf[row0 + g] = s_lse[g];
     }
   }
   if (!direct) {
