@@ -64,6 +64,16 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   const int h = blockIdx.x % p.hkv;
   const int split = blockIdx.x / p.hkv;
   const SplitDesc sd = load_split_desc(p, split);
+  // page size >= 16: a 16-token sub-tile lies in one page, and the pages of the split's first
+  // sub-tiles sit in its descriptor, loaded beside it, so the ring's first copies wait for no
+  // block-table load
+  const bool desc_pages = !p.token_flat && p.page_shift >= 4;
+  int32_t first_pg[NST];
+#pragma unroll
+  for (int i = 0; i < NST; ++i) {
+    const int st = warp + i * NW;
+    first_pg[i] = (desc_pages && st < kDescPages) ? __ldg(p.split_desc[split].first_page + st) : -1;
+  }
   const int b = sd.b;
   const int t0 = sd.t0;
   const int t1 = sd.t1;
@@ -176,6 +186,16 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
       pg[k] = t < t1 ? __ldg(list + (t >> shift)) : -1;
     }
   };
+  // the same for the ring's first NST sub-tiles, from the descriptor where it holds them
+  auto load_first_pages = [&](int i, int32_t (&pg)[kRowIters]) {
+    if (desc_pages && warp + i * NW < kDescPages) {
+      const int tb = t0 + (warp + i * NW) * 16;
+#pragma unroll
+      for (int k = 0; k < kRowIters; ++k) pg[k] = tb + lane / C::kChunks + k * kRowsPerPass < t1 ? first_pg[i] : -1;
+    } else {
+      load_pages(i, pg);
+    }
+  };
   auto issue = [&](int i, const int32_t (&pg)[kRowIters]) {
     const int tb = t0 + (warp + i * NW) * 16;
     unsigned char* kdst = ring + (i % NST) * C::kStageBytes;
@@ -207,37 +227,42 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   // clear of its subnormals); l carries the same factor, so O / l and m + log2(l) are exact.
   constexpr float kPShift = (KV == PSP_KV_FP8) ? 8.f : 0.f;
 
-  // Ring schedule: sub-tiles 0 .. NST-U-1 are issued before the loop (one cp.async group
-  // each).  Every iteration first refills the U stages its predecessor consumed with the
+  // Ring schedule: sub-tiles 0 .. NST-1 are issued before the loop (one cp.async group each).
+  // Every later iteration first refills the U stages its predecessor consumed with the
   // sub-tiles NST-U further on, then waits for its own U, so NST-U sub-tiles stay in flight
   // while it computes.  The block-table entries of a sub-tile are loaded one iteration
   // before its copies, so no copy waits on a dependent table load.
   int32_t pages[U][kRowIters];
 #pragma unroll
-  for (int i = 0; i < NST - U; ++i) {
+  for (int i = 0; i < NST; ++i) {
     if (i < my_n) {
-      load_pages(i, pages[0]);
+      load_first_pages(i, pages[0]);
       issue(i, pages[0]);
     }
     cp_async_commit();
   }
 #pragma unroll
   for (int u = 0; u < U; ++u)
-    if (NST - U + u < my_n) load_pages(NST - U + u, pages[u]);
+    if (NST + u < my_n) load_pages(NST + u, pages[u]);
+  // Concurrent form: the check of the prefix rows (a round trip and a CTA barrier) comes
+  // after every first copy is in flight; a late CTA's prefix rows join the next cp.async
+  // group, which the loop waits for one iteration later than its first sub-tiles.
   if (suffix_cta_late(p, cta, kPre)) prefetch_prefix_rows<D, NW * 32>(p, cta, pre_o, pre_l);
 
   for (int i0 = 0; i0 < my_n; i0 += U) {
+    if (i0 > 0) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int nx = i0 + NST - U + u;
-      if (nx < my_n) issue(nx, pages[u]);
-      cp_async_commit();
-      if (nx + U < my_n) load_pages(nx + U, pages[u]);  // in flight while this iteration computes
-      // the block-table entries of a sub-tile kTablePrefetch iterations later, pulled into L2
-      // now: at small page sizes every sub-tile reads its own 64 bytes of the table, and a
-      // DRAM round trip taken only one iteration ahead of the copies would stall them
-      const int pf = nx + U + kTablePrefetch;
-      if (lane == 0 && pf < my_n) prefetch_l2(list + ((t0 + (warp + pf * NW) * 16) >> shift));
+      for (int u = 0; u < U; ++u) {
+        const int nx = i0 + NST - U + u;
+        if (nx < my_n) issue(nx, pages[u]);
+        cp_async_commit();
+        if (nx + U < my_n) load_pages(nx + U, pages[u]);  // in flight while this iteration computes
+        // the block-table entries of a sub-tile kTablePrefetch iterations later, pulled into L2
+        // now: at small page sizes every sub-tile reads its own 64 bytes of the table, and a
+        // DRAM round trip taken only one iteration ahead of the copies would stall them
+        const int pf = nx + U + kTablePrefetch;
+        if (lane == 0 && pf < my_n) prefetch_l2(list + ((t0 + (warp + pf * NW) * 16) >> shift));
+      }
     }
     cp_async_wait<NST - U>();
     __syncwarp();
@@ -380,6 +405,7 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
     __syncwarp();  // every lane's fragment loads are done before the next refill of these stages
   }
   const bool grid_last = suffix_grid_arrive(p);
+  cp_async_commit();  // copies issued after the loop's last commit (a warp without refills)
   cp_async_wait<0>();
   if (cta.wait_prefix) {
     pdl_wait_primary();  // every prefix partial and prefix arrival of this step is complete

@@ -392,6 +392,10 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
     d.one_split = P.split_indptr[b + 1] - P.split_indptr[b] == 1 ? 1 : 0;
     d.prow = g >= 0 ? P.req_member[b] * G : 0;
     d.m_eff = g >= 0 ? P.group_m_eff[g] : 0;
+    for (int k = 0; k < psp::kDescPages; ++k) {
+      const int64_t t = static_cast<int64_t>(d.t0) + 16 * k;
+      d.first_page[k] = (ps >= 16 && t < d.t1) ? P.suffix_page_indices[d.list_paged + (t / ps)] : -1;
+    }
     std::memcpy(P.split_desc.data() + static_cast<size_t>(si) * psp::kSplitDescInts, &d, sizeof(d));
   }
   if (static_cast<int64_t>(P.NS) * Hkv > INT32_MAX / psp::kMaxGroupSize)

@@ -41,8 +41,12 @@ struct SplitDesc {
   int32_t prow;        // b's first stacked prefix row (member index x G)
   int32_t m_eff;       // stacked rows of b's group (0 without a prefix branch)
   int32_t pad[6];
+  // page size >= 16: the page of 16-token sub-tile s (tokens t0 + 16s ..) for s < kDescPages,
+  // -1 past t1, so that a CTA's first copies need no block-table load; unused below 16
+  int32_t first_page[16];
 };
-static_assert(sizeof(SplitDesc) == 64, "one 64-byte record per split");
+constexpr int kDescPages = 16;
+static_assert(sizeof(SplitDesc) == 128, "one 128-byte record per split");
 constexpr int kSplitDescInts = static_cast<int>(sizeof(SplitDesc) / sizeof(int32_t));
 
 struct StepParams {
