@@ -38,6 +38,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -283,49 +284,59 @@ def run_reference(args):
 
 
 def sweep_threshold(args):
-    """Dispatcher refit: for a 4096-token prefix and 8 KV heads, time the prefix kernel of
-    both branches over batch x GQA group; the threshold is the smallest swept M_eff from
-    which the dense branch is never slower than the cascade branch."""
+    """Dispatcher refit: with 8 KV heads, time the prefix kernel of both branches over
+    prefix length x cache type x batch x GQA group; the refit threshold T (dense iff
+    M_eff >= T) is the swept M_eff with the least summed log(time / faster time), reported
+    per (cache, prefix) cell and over all points."""
     import torch
 
     import paged_shared_prefix_gb300 as psp
     dev = torch.device("cuda:0")
     rows = []
-    for G in (1, 2, 4, 8):
-        for B in (4, 8, 16, 32, 64, 128, 256, 512):
-            m_eff = B * G
-            if m_eff < 16 or m_eff > 4096:
-                continue
-            case = workloads.make_case("agent", 11, batch=B, prefix_len=4096, private_range=(1, 16),
-                                       num_q_heads=8 * G, num_kv_heads=8)
-            tens = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev))
-                    for k, v in dict(q=case.q, k=case.k_pool, v=case.v_pool).items()}
-            o = torch.empty((B, 8 * G, 128), dtype=torch.bfloat16, device=dev)
-            res = {}
-            for branch, thr in (("dense", 1), ("cascade", 1 << 30)):
-                step = psp.DecodeStep.for_case(case, dense_threshold=thr, read_once_min_tokens=-1,
-                                               read_once_min_mib=-1)
-                step.plan_case(case)
-                ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device=dev)
-                step.upload(ws)
-                step.set_kernel_timing(True)
-                times = []
-                for i in range(8):
-                    step.run(tens["q"], tens["k"], tens["v"], o)
-                    torch.cuda.synchronize()
-                    if i >= 3:
-                        times += [ms for n, ms in step.kernel_times() if n.startswith("prefix")]
-                res[branch] = statistics.median(times) * 1e3
-                step.close()
-            rows.append({"G": G, "B": B, "m_eff": m_eff, "dense_us": res["dense"], "cascade_us": res["cascade"]})
-    rows.sort(key=lambda r: r["m_eff"])
-    thr = None
-    for i, r in enumerate(rows):
-        if all(x["dense_us"] <= x["cascade_us"] for x in rows[i:]):
-            thr = r["m_eff"]
-            break
-    print(json.dumps({"sweep": rows, "refit_threshold": thr,
-                      "gpu": torch.cuda.get_device_name(0), "prefix_tokens": 4096, "kv_heads": 8}))
+    cells = [("bf16", "agent", P) for P in (1024, 4096, 16384)] + [("fp8_e4m3", "fp8_large", P) for P in (1024, 4096, 16384)]
+    for cache, base, P in cells:
+        for G in (1, 2, 4, 8):
+            for B in (4, 8, 16, 32, 64, 128, 256, 512):
+                m_eff = B * G
+                if m_eff < 16 or m_eff > 4096:
+                    continue
+                case = workloads.make_case(base, 11, batch=B, prefix_len=P, private_range=(1, 16),
+                                           num_q_heads=8 * G, num_kv_heads=8)
+                tens = to_device(case, dev)
+                o = torch.empty((B, 8 * G, 128), dtype=torch.bfloat16, device=dev)
+                res = {}
+                for branch, thr in (("dense", 1), ("cascade", 1 << 30)):
+                    step = psp.DecodeStep.for_case(case, dense_threshold=thr, read_once_min_tokens=-1,
+                                                   read_once_min_mib=-1)
+                    step.plan_case(case)
+                    ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device=dev)
+                    step.upload(ws)
+                    step.set_kernel_timing(True)
+                    times = []
+                    for i in range(8):
+                        step.run(tens["q"], tens["k"], tens["v"], o, None, tens["ks"], tens["vs"])
+                        torch.cuda.synchronize()
+                        if i >= 3:
+                            times += [ms for n, ms in step.kernel_times() if n.startswith("prefix")]
+                    res[branch] = statistics.median(times) * 1e3
+                    step.close()
+                rows.append({"cache": cache, "prefix_tokens": P, "G": G, "B": B, "m_eff": m_eff,
+                             "dense_us": res["dense"], "cascade_us": res["cascade"]})
+    # refit: the swept M_eff whose rule (dense iff M_eff >= T) has the least summed
+    # log(time / faster time), per (cache, prefix) cell and over every point
+    cands = sorted({r["m_eff"] for r in rows})
+
+    def regret(pts, T):
+        return sum(math.log((r["dense_us"] if r["m_eff"] >= T else r["cascade_us"]) /
+                            min(r["dense_us"], r["cascade_us"])) for r in pts)
+    cell_thr = {}
+    for cache, _, P in cells:
+        pts = [r for r in rows if r["cache"] == cache and r["prefix_tokens"] == P]
+        cell_thr[f"{cache}@{P}"] = min(cands, key=lambda T: (regret(pts, T), T))
+    best = min(cands, key=lambda T: (regret(rows, T), T))
+    known = {"refit_regret": regret(rows, best), "regret_by_threshold": {T: regret(rows, T) for T in cands}}
+    print(json.dumps({"sweep": rows, "cell_thresholds": cell_thr, "refit_threshold": best, **known,
+                      "gpu": torch.cuda.get_device_name(0), "kv_heads": 8}))
     return 0
 
 
