@@ -375,8 +375,7 @@ PSP_API psp_status psp_device_status(psp_handle* h, int32_t* code);
  * It calls no cudaMalloc, cudaFree or other allocating routine and records no
  * kernel timing events.
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call, from any handle, shares the one
+ * (cudaGetSymbolAddress) with that device current.  Every call, from any handle, shares the one
  * array, which keeps the last call's contents: calls whose work overlaps on
  * the GPU race with each other, so serialise them (one stream, or events).
  * A plan whose workspace (psp_workspace_size) exceeds 64 MiB is rejected with
