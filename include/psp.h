@@ -55,7 +55,7 @@
  *                           grid's size and chunk length (default), 1 sequential,
  *                           2 concurrent
  *   PSP_SUFFIX_STAGES       suffix ring depth per warp at d = 128 (default 2 for bf16,
- *                           4 for e4m3; once per process)
+ *                           3 for e4m3; once per process)
  *   PSP_LOG                 1: psp_plan writes one line per planned step to stderr,
  *                           "psp_step " and a JSON object: shapes and dtypes, page size,
  *                           block-table and kv_indices lengths, suffix and shared tokens,

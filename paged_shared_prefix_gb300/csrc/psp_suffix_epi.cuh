@@ -144,13 +144,15 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
   };
   const int64_t row0 = (static_cast<int64_t>(c.split) * p.hkv + h) * G;
   const int64_t orow0 = static_cast<int64_t>(b) * p.hq + h * G;
-  // Per row (one thread per query head): the weight of each warp's state and of each
-  // prefix chunk in the row's result, and the row's log2-LSE.  The own part is
-  // O_s = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w, times the value scale, with
-  // log2-LSE M + log2(sum); a direct merge weighs it against the prefix chunks first.
+  // Per row (one thread per query head): the weight of each warp's state in the CTA's own
+  // part O_s = sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w (times the value scale, log2-LSE
+  // M + log2(sum)), and for a direct merge the weights of the prefix chunks and of O_s.
+  // The direct merge repeats merge_rows' arithmetic in its order (the own part as it would
+  // be written, then the parts weighted by 2^(lse - max), summed by fmaf in the fixed order,
+  // times 1 / sum), so a row's result does not depend on which CTA merges it.
   __shared__ float s_coef[NSTATE * 8];  // [warp state][row]
-  __shared__ float s_cpre[kPreRows];    // [chunk * G + row]
-  __shared__ float s_lse[8];
+  __shared__ float s_cpre[kPreRows];    // [chunk * G + row]: 2^(lse_chunk - max)
+  __shared__ float s_own[8], s_inv[8], s_lse[8];
   if (threadIdx.x < G) {
     const int g = threadIdx.x;
     float mmax = neg_inf();
@@ -163,12 +165,14 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
       sc[w] = exp2f(ms[w * 8 + g] - mmax);
       sum += ls[w * 8 + g] * sc[w];
     }
+    const float f = out_scale / sum;
+#pragma unroll
+    for (int w = 0; w < NSTATE; ++w) s_coef[w * 8 + g] = sc[w] * f;
     const float lse_own = mmax + log2f(sum);
-    float f = out_scale / sum;
-    float lse_row = lse_own;
     if (direct) {
-      float big = lse_own;
+      float big = neg_inf();
       for (int ch = 0; ch < c.n_chunks; ++ch) big = fmaxf(big, pre_l[ch * G + g]);
+      big = fmaxf(big, lse_own);
       float wsum = 0.f;
       for (int ch = 0; ch < c.n_chunks; ++ch) {
         const float w = exp2f(pre_l[ch * G + g] - big);
@@ -177,14 +181,12 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
       }
       const float w_own = exp2f(lse_own - big);
       wsum += w_own;
-      const float inv = 1.f / wsum;
-      for (int ch = 0; ch < c.n_chunks; ++ch) s_cpre[ch * G + g] *= inv;
-      f *= w_own * inv;
-      lse_row = big + log2f(wsum);
+      s_own[g] = w_own;
+      s_inv[g] = 1.f / wsum;
+      s_lse[g] = big + log2f(wsum);
+    } else {
+      s_lse[g] = lse_own;
     }
-#pragma unroll
-    for (int w = 0; w < NSTATE; ++w) s_coef[w * 8 + g] = sc[w] * f;
-    s_lse[g] = lse_row;
   }
   __syncthreads();
   // every element: a few FMAs over four consecutive d, one vector store
@@ -192,24 +194,28 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
   for (int e = threadIdx.x; e < G * kQuads; e += NT) {
     const int g = e / kQuads;
     const int d = (e - g * kQuads) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto add = [&](float cf, const float* src) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
+    float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float4& acc, float cf, float4 v) {
       acc.x = fmaf(cf, v.x, acc.x);
       acc.y = fmaf(cf, v.y, acc.y);
       acc.z = fmaf(cf, v.z, acc.z);
       acc.w = fmaf(cf, v.w, acc.w);
     };
 #pragma unroll
-    for (int w = 0; w < NSTATE; ++w) add(s_coef[w * 8 + g], red + (w * 8 + g) * D + d);
+    for (int w = 0; w < NSTATE; ++w)
+      add(os, s_coef[w * 8 + g], *reinterpret_cast<const float4*>(red + (w * 8 + g) * D + d));
     if (direct) {
-      for (int ch = 0; ch < c.n_chunks; ++ch) add(s_cpre[ch * G + g], pre_o + (ch * G + g) * D + d);
-      store_final4(p, orow0 + g, d, acc);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int ch = 0; ch < c.n_chunks; ++ch)
+        add(acc, s_cpre[ch * G + g], *reinterpret_cast<const float4*>(pre_o + (ch * G + g) * D + d));
+      add(acc, s_own[g], os);
+      const float inv = s_inv[g];
+      store_final4(p, orow0 + g, d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
       if (d == 0 && p.lse) p.lse[orow0 + g] = s_lse[g] * 0.6931471805599453f;
       // every prefix arrival on (b, h) was made and nothing else arrives: clear it for the next step
       if (c.late && e == 0) p.counters[static_cast<int64_t>(b) * p.hkv + h] = 0;
     } else {
-      *reinterpret_cast<float4*>(p.o_suf + (row0 + g) * D + d) = acc;
+      *reinterpret_cast<float4*>(p.o_suf + (row0 + g) * D + d) = os;
       if (d == 0) p.lse_suf[row0 + g] = s_lse[g];
     }
   }

@@ -85,6 +85,24 @@ def test_token_flat_lowering_bit_identical():
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), name
 
 
+def test_launch_forms_bit_identical(monkeypatch):
+    """The sequential and the concurrent dependent-launch forms merge a one-split request's
+    row on different paths (in its suffix CTA, or through its counter by whichever part
+    arrives last, at a moment set by timing); the result must not depend on the path."""
+    for name, kw in (("agent", dict(batch=24, prefix_len=1024, private_range=(1, 300))),
+                     ("fp8_large", dict(batch=16, prefix_len=512, private_range=(1, 400)))):
+        case = workloads.make_case(name, 5, **kw)
+        outs = []
+        for form in ("1", "2", "2"):
+            monkeypatch.setenv("PSP_PDL_FORM", form)
+            outs.append(run_case(case))
+        for o, l in outs[1:]:
+            assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1]), name
+        ref_o, ref_lse = oracle.attend_all(case)
+        tol = TOL[case.workload.kv_dtype]
+        assert max_err(outs[0][0], ref_o) <= tol and max_err(outs[0][1], ref_lse) <= tol
+
+
 def test_expand_kv_indices_bit_exact():
     for ps in (1, 16, 128):
         case = workloads.make_case("agent", 1, batch=9, prefix_len=300, private_range=(1, 500), page_size=ps)
