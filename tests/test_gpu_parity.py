@@ -85,6 +85,23 @@ def test_token_flat_lowering_bit_identical():
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), name
 
 
+def test_contiguous_prefix_bit_identical():
+    """A prefix whose pages are physically consecutive is fetched in whole-tile boxes; the
+    results must equal, bit for bit, those of the same batch with its pages scattered."""
+    for name, kw in (("agent", dict(batch=20, prefix_len=1000, private_range=(1, 200))),
+                     ("fp8_large", dict(batch=12, prefix_len=700, private_range=(1, 300)))):
+        for ps in (16, 64):
+            outs = []
+            for layout in ("scatter", "contiguous", "block128"):
+                case = workloads.make_case(name, 6, page_size=ps, layout=layout, **kw)
+                outs.append(run_case(case))
+            for o, l in outs[1:]:
+                assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1]), (name, ps)
+            ref_o, ref_lse = oracle.attend_all(case)
+            tol = TOL[case.workload.kv_dtype]
+            assert max_err(outs[0][0], ref_o) <= tol and max_err(outs[0][1], ref_lse) <= tol
+
+
 def test_launch_forms_bit_identical(monkeypatch):
     """The sequential and the concurrent dependent-launch forms merge a one-split request's
     row on different paths (in its suffix CTA, or through its counter by whichever part
