@@ -10,7 +10,8 @@ Functions (each cites the passage it follows in ``oracle.c``):
   expand_kv_indices(case)      token-flat kv_indices lowering
   plan(case, params)           block-aligned prefix split, M_eff, branch (dense,
                                cascade, or paged when reading once does not
-                               pay), split-KV and prefix-chunk partition
+                               pay), nested groups, split-KV and prefix-chunk
+                               partition
   attend(case, rows, t0, t1)   softmax(q K^T / sqrt(d)) V in fp64 per row
   merge(o1, lse1, o2, lse2)    log-sum-exp merge (self-check only)
 
@@ -89,7 +90,9 @@ class _PlanOut(ctypes.Structure):
         ("group_m_eff", ctypes.c_void_p), ("group_branch", ctypes.c_void_p),
         ("group_row_blocks", ctypes.c_void_p), ("group_chunk_indptr", ctypes.c_void_p),
         ("chunk_begin", ctypes.c_void_p), ("chunk_end", ctypes.c_void_p),
-        ("chunk_cap", ctypes.c_int64)]
+        ("chunk_cap", ctypes.c_int64),
+        ("req_level_indptr", ctypes.c_void_p), ("req_level_group", ctypes.c_void_p),
+        ("req_level_cap", ctypes.c_int64)]
 
 
 class Oracle:
@@ -151,6 +154,8 @@ class Oracle:
             "group_chunk_indptr": np.zeros(ng + 1, np.int32),
             "chunk_begin": np.zeros(prefix_tiles, np.int32),
             "chunk_end": np.zeros(prefix_tiles, np.int32),
+            "req_level_indptr": np.zeros(B + 1, np.int32),
+            "req_level_group": np.zeros(max(B * ng, 1), np.int32),
         }
         out = _PlanOut()
         for k, a in arrs.items():
@@ -159,6 +164,7 @@ class Oracle:
         out.split_cap = split_cap
         out.group_page_cap = arrs["group_page_indices"].shape[0]
         out.chunk_cap = prefix_tiles
+        out.req_level_cap = arrs["req_level_group"].shape[0]
         # the read-once minimums default to none (every group with full pages reads its prefix
         # once) and the bytes per token to the case's own
         params = dict({"read_once_min_tokens": -1, "read_once_min_mib": -1,
@@ -167,10 +173,12 @@ class Oracle:
         kv_len, pind, pidx = _i32(case.kv_len), _i32(case.page_indptr), _i32(case.page_indices)
         pg = _i32(case.prefix_group)
         gpl = _i32(case.group_prefix_len) if ng else np.zeros(1, np.int32)
+        parent = getattr(case, "group_parent", None)
+        gpar = _i32(parent) if parent is not None else None
         rc = self.lib.oracle_plan(
             ctypes.c_int(B), ctypes.c_int(w.num_q_heads), ctypes.c_int(w.num_kv_heads),
             ctypes.c_int(case.page_size), ctypes.c_int(case.num_pages),
-            _p(kv_len), _p(pind), _p(pidx), _p(pg), ctypes.c_int(ng), _p(gpl),
+            _p(kv_len), _p(pind), _p(pidx), _p(pg), ctypes.c_int(ng), _p(gpl), _p(gpar),
             ctypes.byref(pp), ctypes.byref(out))
         if rc:
             raise OracleError(rc)
@@ -185,6 +193,7 @@ class Oracle:
         res["group_page_indices"] = arrs["group_page_indices"][:int(arrs["group_page_indptr"][ng])]
         res["chunk_begin"] = arrs["chunk_begin"][:nc]
         res["chunk_end"] = arrs["chunk_end"][:nc]
+        res["req_level_group"] = arrs["req_level_group"][:int(arrs["req_level_indptr"][B])]
         return res
 
     def attend(self, case, rows_b, rows_hq, t0=None, t1=None) -> tuple:

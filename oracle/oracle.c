@@ -23,8 +23,10 @@
  *  - Plan: block-aligned prefix sharing (floor(P/ps) shared pages, the tail
  *    stays private: "Track C Document 10", block size answer: 2,003 tokens at
  *    16 share 125 blocks), M_eff = members x GQA group and the dense/cascade
- *    rule M_eff >= threshold ("GraniKV", section 3 Per-step dispatcher), and
- *    the split-KV partition.  The pages fix neither the partition rule nor the
+ *    rule M_eff >= threshold ("GraniKV", section 3 Per-step dispatcher),
+ *    nested groups (a radix tree of shared beginnings, each level matched
+ *    block-aligned and read once for all requests below it), and the
+ *    split-KV partition.  The pages fix neither the partition rule nor the
  *    threshold value; the rule implemented here is the library's documented
  *    rule (token units, independent of page size), restated from its
  *    description with every constant passed in.
@@ -160,23 +162,51 @@ typedef struct {
   int32_t* split_begin;           /* token offsets within the suffix */
   int32_t* split_end;             int64_t split_cap;
   /* per group */
-  int32_t* group_shared_len;      /* [num_groups] tokens read once */
+  int32_t* group_shared_len;      /* [num_groups] tokens of the group's own segment read once */
   int32_t* group_page_indptr;     /* [num_groups+1] */
   int32_t* group_page_indices;    int64_t group_page_cap;
   int32_t* group_m_eff;           /* [num_groups] */
   int32_t* group_branch;          /* [num_groups] */
   int32_t* group_row_blocks;      /* [num_groups] */
   int32_t* group_chunk_indptr;    /* [num_groups+1] */
-  int32_t* chunk_begin;           /* token offsets within the shared prefix */
+  int32_t* chunk_begin;           /* token offsets within the context (the group's own segment) */
   int32_t* chunk_end;             int64_t chunk_cap;
+  /* per request: the groups whose prefix partials it merges, outermost first */
+  int32_t* req_level_indptr;      /* [B+1] */
+  int32_t* req_level_group;       int64_t req_level_cap;
 } oracle_plan_out;
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+/* Nested prefixes.  A group may extend the prefix of another: group_parent[g] (NULL: every
+ * group is a root) is -1 or a group of lower index whose prefix is no longer than g's, so the
+ * groups form a radix tree of shared beginnings ("Track C Document 10 -- Shrinking the
+ * footprint": the vLLM-or-SGLang answer keeps caches in a radix tree keyed on shared
+ * beginnings, and the cache table's per-user personalisation row shares per user on top of
+ * what every user shares).  A request of group g is a member of g and of every ancestor of g.
+ * Matching stays block-aligned at every level: g shares the first floor(P_g / ps) pages, and
+ * its own segment is the pages from floor(P_parent / ps) on. */
+static int parent_of(const int32_t* group_parent, int g) { return group_parent ? group_parent[g] : -1; }
+
+/* 1 if a request of group `leaf` is a member of group a */
+static int member_of(const int32_t* group_parent, int leaf, int a) {
+  for (int g = leaf; g >= 0; g = parent_of(group_parent, g))
+    if (g == a) return 1;
+  return 0;
+}
+
+/* full pages group g shares (0 for "no group") */
+static int64_t shared_pages(const int32_t* group_prefix_len, int g, int ps) {
+  return g >= 0 ? group_prefix_len[g] / ps : 0;
+}
+
+/* branches whose segment is read once per step */
+static int read_once(int branch) { return branch == OR_BRANCH_DENSE || branch == OR_BRANCH_CASCADE; }
+
 int oracle_plan(int B, int Hq, int Hkv, int ps, int num_pages,
                 const int32_t* kv_len, const int32_t* page_indptr, const int32_t* page_indices,
                 const int32_t* prefix_group, int num_groups, const int32_t* group_prefix_len,
-                const oracle_plan_params* pp, oracle_plan_out* out) {
+                const int32_t* group_parent, const oracle_plan_params* pp, oracle_plan_out* out) {
   if (Hkv < 1 || Hq < 1 || Hq % Hkv) return OR_EARG;
   if (num_groups < 0 || (num_groups > 0 && !group_prefix_len)) return OR_EARG;
   if (pp->num_sms < 1 || pp->tile_tokens < 1 || pp->split_min_tiles < 1 ||
@@ -188,58 +218,86 @@ int oracle_plan(int B, int Hq, int Hkv, int ps, int num_pages,
   const int G = Hq / Hkv;
   const int64_t tile = pp->tile_tokens;
 
-  /* groups: prefix length, member count, shared pages agree with the first member */
-  for (int g = 0; g < num_groups; ++g) if (group_prefix_len[g] < 0) return OR_EARG;
+  /* the group tree: a parent has a lower index and a prefix no longer than its child's */
+  for (int g = 0; g < num_groups; ++g) {
+    if (group_prefix_len[g] < 0) return OR_EARG;
+    int par = parent_of(group_parent, g);
+    if (par < -1 || par >= g) return OR_EARG;
+    if (par >= 0 && group_prefix_len[par] > group_prefix_len[g]) return OR_EARG;
+  }
+  for (int b = 0; b < B; ++b) {
+    int g = prefix_group ? prefix_group[b] : -1;
+    if (g < -1 || g >= num_groups) return OR_EARG;
+    if (g >= 0 && group_prefix_len[g] > kv_len[b]) return OR_EPREFIX;
+  }
+
+  /* per group: its members (its own requests and its descendants'), the first of them, and
+     agreement of every member with the first on the group's shared pages */
   int32_t* first_member = (int32_t*)malloc(sizeof(int32_t) * (num_groups > 0 ? num_groups : 1));
   int32_t* members = (int32_t*)calloc(num_groups > 0 ? num_groups : 1, sizeof(int32_t));
   if (!first_member || !members) { free(first_member); free(members); return OR_ENOMEM; }
-  for (int g = 0; g < num_groups; ++g) first_member[g] = -1;
-  for (int b = 0; b < B; ++b) {
-    int g = prefix_group ? prefix_group[b] : -1;
-    if (g < -1 || g >= num_groups) { rc = OR_EARG; goto done; }
-    if (g < 0) continue;
-    if (group_prefix_len[g] > kv_len[b]) { rc = OR_EPREFIX; goto done; }
-    int64_t n_sh = group_prefix_len[g] / ps;
-    if (first_member[g] < 0) {
-      first_member[g] = b;
-    } else {
-      int f = first_member[g];
-      for (int64_t i = 0; i < n_sh; ++i)
-        if (page_indices[page_indptr[b] + i] != page_indices[page_indptr[f] + i]) {
-          rc = OR_EPREFIX; goto done;
-        }
+  for (int g = 0; g < num_groups; ++g) {
+    first_member[g] = -1;
+    int64_t n_sh = shared_pages(group_prefix_len, g, ps);
+    for (int b = 0; b < B; ++b) {
+      int leaf = prefix_group ? prefix_group[b] : -1;
+      if (leaf < 0 || !member_of(group_parent, leaf, g)) continue;
+      if (first_member[g] < 0) {
+        first_member[g] = b;
+      } else {
+        int f = first_member[g];
+        for (int64_t i = 0; i < n_sh; ++i)
+          if (page_indices[page_indptr[b] + i] != page_indices[page_indptr[f] + i]) {
+            rc = OR_EPREFIX; goto done;
+          }
+      }
+      members[g] += 1;
     }
-    members[g] += 1;
   }
 
   /* per group: the dispatcher's branch (GraniKV section 3: M_eff = members x G against the
-     dense threshold), after the read-once test: a prefix is read once only if it has at least
-     read_once_min_tokens shared tokens and reading it once saves (members - 1) x shared
-     tokens x token_bytes >= read_once_min_mib MiB; otherwise every member reads it through
-     its own block table (the paged branch, nothing shared) */
+     dense threshold), after the read-once test on the group's own segment: it is read once
+     only if it has at least read_once_min_tokens shared tokens and reading it once saves
+     (members - 1) x shared tokens x token_bytes >= read_once_min_mib MiB; otherwise every
+     member reads it through its own block table (the paged branch, nothing shared).  Below a
+     paged group every group is paged too, so that the tokens a request reads through its own
+     block table stay one range at the end of its context. */
   for (int g = 0; g < num_groups; ++g) {
-    int64_t n_sh = (members[g] > 0) ? group_prefix_len[g] / ps : 0;
+    int par = parent_of(group_parent, g);
+    int64_t seg = (members[g] > 0) ? shared_pages(group_prefix_len, g, ps) - shared_pages(group_prefix_len, par, ps) : 0;
     int64_t m_eff = (int64_t)members[g] * G;
     out->group_m_eff[g] = (int32_t)m_eff;
+    int below_paged = 0;
+    for (int a = par; a >= 0; a = parent_of(group_parent, a))
+      if (out->group_branch[a] == OR_BRANCH_PAGED) below_paged = 1;
     int branch = OR_BRANCH_NONE;
-    if (m_eff > 0 && n_sh > 0) {
-      int64_t shared = n_sh * ps;
+    if (m_eff > 0 && seg > 0) {
+      int64_t shared = seg * ps;
       int64_t saved = (int64_t)(members[g] - 1) * shared * pp->token_bytes;
       int too_short = pp->read_once_min_tokens > 0 && shared < pp->read_once_min_tokens;
       int too_little = pp->read_once_min_mib > 0 && saved < ((int64_t)pp->read_once_min_mib << 20);
-      if (too_short || too_little) branch = OR_BRANCH_PAGED;
+      if (below_paged || too_short || too_little) branch = OR_BRANCH_PAGED;
       else branch = (m_eff >= pp->dense_threshold) ? OR_BRANCH_DENSE : OR_BRANCH_CASCADE;
     }
     out->group_branch[g] = branch;
   }
 
-  /* per request: block-aligned split of the block table (members of a paged group share nothing) */
+  /* per request: the read-once groups it belongs to, outermost first (ancestors have lower
+     indices), and the block-aligned split of its block table after the last of them */
   {
-    int64_t np_out = 0;
+    int64_t np_out = 0, nl = 0;
     out->suffix_page_indptr[0] = 0;
+    out->req_level_indptr[0] = 0;
     for (int b = 0; b < B; ++b) {
-      int g = prefix_group ? prefix_group[b] : -1;
-      int64_t n_sh = (g >= 0 && out->group_branch[g] != OR_BRANCH_PAGED) ? group_prefix_len[g] / ps : 0;
+      int leaf = prefix_group ? prefix_group[b] : -1;
+      int64_t n_sh = 0;
+      for (int a = 0; a < num_groups; ++a) {
+        if (leaf < 0 || !member_of(group_parent, leaf, a) || !read_once(out->group_branch[a])) continue;
+        if (nl >= out->req_level_cap) { rc = OR_ECAP; goto done; }
+        out->req_level_group[nl++] = a;
+        n_sh = group_prefix_len[a] / ps;
+      }
+      out->req_level_indptr[b + 1] = (int32_t)nl;
       out->suffix_start[b] = (int32_t)(n_sh * ps);
       out->suffix_len[b] = (int32_t)(kv_len[b] - n_sh * ps);
       for (int64_t i = page_indptr[b] + n_sh; i < page_indptr[b + 1]; ++i) {
@@ -275,15 +333,17 @@ int oracle_plan(int B, int Hq, int Hkv, int ps, int num_pages,
     }
   }
 
-  /* groups: shared pages, M_eff, branch, prefix chunks */
+  /* groups: shared pages (the whole prefix, ancestors' pages first), the own segment's
+     tokens, row blocks and prefix chunks over the segment */
   {
     int64_t gp = 0, nc = 0;
     out->group_page_indptr[0] = 0;
     out->group_chunk_indptr[0] = 0;
     for (int g = 0; g < num_groups; ++g) {
       int branch = out->group_branch[g];
-      int64_t n_sh = (members[g] > 0 && branch != OR_BRANCH_PAGED) ? group_prefix_len[g] / ps : 0;
-      out->group_shared_len[g] = (int32_t)(n_sh * ps);
+      int64_t n_sh = read_once(branch) ? group_prefix_len[g] / ps : 0;
+      int64_t seg0 = read_once(branch) ? shared_pages(group_prefix_len, parent_of(group_parent, g), ps) * ps : 0;
+      out->group_shared_len[g] = (int32_t)(n_sh * ps - seg0);
       for (int64_t i = 0; i < n_sh; ++i) {
         if (gp >= out->group_page_cap) { rc = OR_ECAP; goto done; }
         out->group_page_indices[gp++] = page_indices[page_indptr[first_member[g]] + i];
@@ -291,7 +351,7 @@ int oracle_plan(int B, int Hq, int Hkv, int ps, int num_pages,
       out->group_page_indptr[g + 1] = (int32_t)gp;
       int64_t m_eff = out->group_m_eff[g];
       int64_t rows = 0, n_chunks = 0, per_chunk = 0;
-      if (branch == OR_BRANCH_DENSE || branch == OR_BRANCH_CASCADE) {
+      if (read_once(branch)) {
         int64_t rows_per = (branch == OR_BRANCH_DENSE) ? pp->prefix_rows_dense : pp->prefix_rows_cascade;
         rows = ceil_div(m_eff, rows_per);
         int64_t tiles = ceil_div(out->group_shared_len[g], tile);
@@ -307,8 +367,8 @@ int oracle_plan(int B, int Hq, int Hkv, int ps, int num_pages,
       for (int64_t c = 0; c < n_chunks; ++c) {
         if (nc >= out->chunk_cap) { rc = OR_ECAP; goto done; }
         int64_t lo = tile * c * per_chunk, hi = tile * (c + 1) * per_chunk;
-        out->chunk_begin[nc] = (int32_t)lo;
-        out->chunk_end[nc] = (int32_t)(hi < out->group_shared_len[g] ? hi : out->group_shared_len[g]);
+        out->chunk_begin[nc] = (int32_t)(seg0 + lo);
+        out->chunk_end[nc] = (int32_t)(seg0 + (hi < out->group_shared_len[g] ? hi : out->group_shared_len[g]));
         ++nc;
       }
       out->group_chunk_indptr[g + 1] = (int32_t)nc;

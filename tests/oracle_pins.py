@@ -381,6 +381,129 @@ def pin_validation(orc):
     rejects(dataclasses.replace(c, group_prefix_len=gl), -5)
 
 
+def _three_level_tables():
+    """Hand-built block tables of a three-level tree at page size 16 (ids fixed here, nothing
+    generated): group 0 = 64 tokens (4 pages) shared by all six requests, group 1 = 256 tokens
+    under it for requests 2-5, group 2 = 328 tokens under group 1 for requests 4 and 5 (20 full
+    pages, 8 tokens private), and group 3 = 96 tokens under group 0 for request 1 alone."""
+    import dataclasses
+    ps = 16
+    root = [40, 41, 42, 43]
+    mid = root + list(range(50, 62))
+    leaf = mid + [62, 63, 64, 65]
+    side = root + [70, 71]
+    tables = [root + [1, 2], side + [3, 4], mid + [5], mid + [6, 7], leaf + [80, 8, 9], leaf + [81, 10]]
+    kv_len = np.array([64 + 20, 96 + 30, 256 + 16, 256 + 17, 328 + 28, 328 + 9], np.int32)
+    for b, t in enumerate(tables):
+        assert len(t) == -(-int(kv_len[b]) // ps)
+    base = workloads.make_case("agent", 0, batch=6, num_q_heads=4, num_kv_heads=2, head_dim=16,
+                               tables_only=True)
+    return dataclasses.replace(
+        base, page_size=ps, num_pages=100, kv_len=kv_len,
+        page_indptr=np.concatenate([[0], np.cumsum([len(t) for t in tables])]).astype(np.int32),
+        page_indices=np.concatenate(tables).astype(np.int32),
+        prefix_group=np.array([0, 3, 1, 1, 2, 2], np.int32),
+        group_prefix_len=np.array([64, 256, 328, 96], np.int32),
+        group_parent=np.array([-1, 0, 1, 0], np.int32))
+
+
+def _covered_once(p, b, kv_len):
+    """Token coverage of request b by its levels' prefix chunks and its suffix splits."""
+    cover = np.zeros(int(kv_len), np.int64)
+    for l in range(p["req_level_indptr"][b], p["req_level_indptr"][b + 1]):
+        g = p["req_level_group"][l]
+        for c in range(p["group_chunk_indptr"][g], p["group_chunk_indptr"][g + 1]):
+            cover[p["chunk_begin"][c]:p["chunk_end"][c]] += 1
+    s0 = p["suffix_start"][b]
+    for s in range(p["split_indptr"][b], p["split_indptr"][b + 1]):
+        cover[s0 + p["split_begin"][s]:s0 + p["split_end"][s]] += 1
+    return cover
+
+
+def pin_nested_prefix(orc):
+    """Nested groups (a tree of shared beginnings, each level read once for every request
+    below it): the members of a group are its own requests and its descendants' (M_eff
+    counted by hand), each request merges the read-once levels on its path from the root in
+    order, every context token is covered exactly once by those levels' chunks and the
+    request's splits, the merged parts equal full attention (and torch SDPA on contiguous
+    K/V), a level below a paged level is paged, and bad trees are rejected."""
+    import dataclasses
+    from oracle import OracleError
+    params = dict(PLAN_PARAMS, dense_threshold=8, read_once_min_tokens=-1, read_once_min_mib=-1)
+    t = _three_level_tables()
+    p = orc.plan(t, params)
+    assert list(p["group_m_eff"]) == [12, 8, 4, 2], "members counted through descendants (G = 2)"
+    assert list(p["group_branch"]) == [2, 2, 1, 1]
+    assert list(p["group_shared_len"]) == [64, 192, 64, 32], "own segments only"
+    assert list(p["suffix_start"]) == [64, 96, 256, 256, 320, 320]
+    assert p["req_level_indptr"].tolist() == [0, 1, 3, 5, 7, 10, 13]
+    assert p["req_level_group"].tolist() == [0, 0, 3, 0, 1, 0, 1, 0, 1, 2, 0, 1, 2]
+    g2 = p["group_page_indices"][p["group_page_indptr"][2]:p["group_page_indptr"][3]]
+    assert g2.tolist() == [40, 41, 42, 43] + list(range(50, 66)), "whole prefix, root first"
+    for b in range(t.batch):
+        assert np.all(_covered_once(p, b, t.kv_len[b]) == 1), b
+    # a short root segment (64 tokens) under a 100-token minimum: the root is paged and so is
+    # every level below it, the 192-token segment of group 1 too; the plan is then the plan
+    # without sharing
+    paged = orc.plan(t, dict(params, read_once_min_tokens=100))
+    alone = orc.plan(t.without_sharing(), dict(params, read_once_min_tokens=100))
+    assert list(paged["group_branch"]) == [3, 3, 3, 3]
+    for f in ("suffix_start", "suffix_len", "split_indptr", "split_begin", "split_end"):
+        assert np.array_equal(paged[f], alone[f]), f
+    # a 40-token minimum: the 32-token side segment (group 3) alone is paged
+    part = orc.plan(t, dict(params, read_once_min_tokens=40))
+    assert list(part["group_branch"]) == [2, 2, 1, 3] and part["suffix_start"][1] == 64
+
+    # values: the generator's two-level tree, parts merged in plan order = full attention
+    for kv in ("bf16", "fp8_e4m3"):
+        c = workloads.make_case("agent", 11, batch=7, prefix_len=100, private_range=(1, 90), page_size=16,
+                                num_q_heads=4, num_kv_heads=2, head_dim=16, kv_dtype=kv, nested=(3, 70),
+                                keep_logical=True)
+        p = orc.plan(c, dict(params, tile_tokens=16, prefix_min_tiles=1, split_min_tiles=1))
+        assert p["group_m_eff"].tolist() == [14] + [2 * int(np.sum(c.prefix_group == k)) for k in (1, 2, 3)]
+        for b in range(c.batch):
+            assert np.all(_covered_once(p, b, c.kv_len[b]) == 1), b
+            hh = np.arange(4)
+            bb = np.full(4, b)
+            ranges = []
+            for l in range(p["req_level_indptr"][b], p["req_level_indptr"][b + 1]):
+                g = p["req_level_group"][l]
+                ranges += [(p["chunk_begin"][k], p["chunk_end"][k])
+                           for k in range(p["group_chunk_indptr"][g], p["group_chunk_indptr"][g + 1])]
+            s0 = p["suffix_start"][b]
+            ranges += [(s0 + p["split_begin"][s], s0 + p["split_end"][s])
+                       for s in range(p["split_indptr"][b], p["split_indptr"][b + 1])]
+            o, lse = orc.attend(c, bb, hh, np.full(4, ranges[0][0]), np.full(4, ranges[0][1]))
+            for lo, hi in ranges[1:]:
+                po, pl = orc.attend(c, bb, hh, np.full(4, lo), np.full(4, hi))
+                o, lse = orc.merge(o, lse, po, pl)
+            full = orc.attend(c, bb, hh)
+            assert np.max(np.abs(o - full[0])) <= 1e-12 and np.max(np.abs(lse - full[1])) <= 1e-12
+            so, sl = sdpa_rows(c, b)
+            assert np.max(np.abs(full[0] - so)) <= 1e-12 and np.max(np.abs(full[1] - sl)) <= 1e-12
+
+    def rejects(case, code):
+        try:
+            orc.plan(case, params)
+        except OracleError as e:
+            assert e.code == code, (e.code, code)
+            return
+        raise AssertionError(f"accepted an invalid tree (expected {code})")
+
+    rejects(dataclasses.replace(t, group_parent=np.array([-1, 0, 3, 0], np.int32)), -1)   # parent after child
+    rejects(dataclasses.replace(t, group_parent=np.array([-1, 1, 1, 0], np.int32)), -1)   # own parent
+    rejects(dataclasses.replace(t, group_prefix_len=np.array([64, 128, 120, 96], np.int32)), -1)  # shorter than parent
+    bad = t.page_indices.copy()
+    bad[t.page_indptr[5] + 5] = 99          # request 5 leaves group 1's segment
+    rejects(dataclasses.replace(t, page_indices=bad), -5)
+    bad = t.page_indices.copy()
+    bad[t.page_indptr[1] + 2] = 98          # request 1 leaves the root's pages
+    rejects(dataclasses.replace(t, page_indices=bad), -5)
+    bad = t.page_indices.copy()
+    bad[t.page_indptr[4] + 17] = 97         # request 4 leaves group 2's own segment
+    rejects(dataclasses.replace(t, page_indices=bad), -5)
+
+
 ALL_PINS = [pin_paged_branch, pin_fp8_decode_all_codes, pin_bf16_decode_all_patterns, pin_sdpa_fp64,
             pin_closed_forms, pin_paging_invariance, pin_merge_identity, pin_kv_indices,
-            pin_block_aligned_prefix, pin_dispatcher, pin_partition, pin_validation]
+            pin_block_aligned_prefix, pin_dispatcher, pin_partition, pin_validation, pin_nested_prefix]

@@ -21,15 +21,24 @@ MUTATIONS = [
     ("fp8_subnormal_exponent", "ldexp((double)mantissa / 8.0, 1 - 7)", "ldexp((double)mantissa / 8.0, -7)"),
     ("bf16_shift", "((uint32_t)bits) << 16;", "((uint32_t)bits) << 15;"),
     ("merge_weight_swapped", "w2 * o2[(int64_t)r * d + i];", "w1 * o2[(int64_t)r * d + i];"),
-    ("prefix_pages_rounded_up",
-     "int64_t n_sh = (g >= 0 && out->group_branch[g] != OR_BRANCH_PAGED) ? group_prefix_len[g] / ps : 0;",
-     "int64_t n_sh = (g >= 0 && out->group_branch[g] != OR_BRANCH_PAGED) ? (group_prefix_len[g] + ps - 1) / ps : 0;"),
+    ("prefix_pages_rounded_up", "n_sh = group_prefix_len[a] / ps;", "n_sh = (group_prefix_len[a] + ps - 1) / ps;"),
     ("paged_saving_counts_every_member", "int64_t saved = (int64_t)(members[g] - 1) * shared * pp->token_bytes;",
      "int64_t saved = (int64_t)members[g] * shared * pp->token_bytes;"),
     ("paged_minimum_tokens_inclusive", "shared < pp->read_once_min_tokens;", "shared <= pp->read_once_min_tokens;"),
     ("paged_members_keep_their_prefix",
-     "int64_t n_sh = (g >= 0 && out->group_branch[g] != OR_BRANCH_PAGED) ? group_prefix_len[g] / ps : 0;",
-     "int64_t n_sh = (g >= 0) ? group_prefix_len[g] / ps : 0;"),
+     "if (leaf < 0 || !member_of(group_parent, leaf, a) || !read_once(out->group_branch[a])) continue;",
+     "if (leaf < 0 || !member_of(group_parent, leaf, a) || out->group_branch[a] == OR_BRANCH_NONE) continue;"),
+    ("nested_segment_start_dropped", "out->chunk_begin[nc] = (int32_t)(seg0 + lo);", "out->chunk_begin[nc] = (int32_t)(lo);"),
+    ("nested_members_only_direct", "if (leaf < 0 || !member_of(group_parent, leaf, g)) continue;",
+     "if (leaf != g) continue;"),
+    ("nested_paged_not_inherited", "if (below_paged || too_short || too_little)", "if (too_short || too_little)"),
+    ("nested_no_grandparents", "for (int g = leaf; g >= 0; g = parent_of(group_parent, g))",
+     "for (int g = leaf; g >= 0; g = (g == leaf) ? parent_of(group_parent, g) : -1)"),
+    ("nested_segment_counts_whole_prefix",
+     "shared_pages(group_prefix_len, g, ps) - shared_pages(group_prefix_len, par, ps) : 0;",
+     "shared_pages(group_prefix_len, g, ps) : 0;"),
+    ("nested_shared_len_whole_prefix", "out->group_shared_len[g] = (int32_t)(n_sh * ps - seg0);",
+     "out->group_shared_len[g] = (int32_t)(n_sh * ps);"),
     ("v_from_k_pool", "out[i] += w * (elem(v_pool, base + i, kv_dtype) * vs);",
      "out[i] += w * (elem(k_pool, base + i, kv_dtype) * vs);"),
     ("q_row_transposed", "qv[i] = elem(q, ((int64_t)b * Hq + hq) * d + i, q_dtype);",

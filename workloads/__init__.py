@@ -127,6 +127,7 @@ class Case:
     k_logical: Optional[np.ndarray] = None
     v_logical: Optional[np.ndarray] = None
     logical_rows: Optional[list] = None
+    group_parent: Optional[np.ndarray] = None  # [G] int32 parent group (-1 root), or None: all roots
 
     @property
     def batch(self) -> int:
@@ -141,7 +142,7 @@ class Case:
         return dataclasses.replace(
             self,
             prefix_group=np.full_like(self.prefix_group, -1),
-            group_prefix_len=np.zeros((0,), np.int32))
+            group_prefix_len=np.zeros((0,), np.int32), group_parent=None)
 
     def kv_token_bytes(self) -> int:
         """Bytes of K plus V for one token over all KV heads."""
@@ -223,7 +224,8 @@ def make_case(name: str, seed: int = 0, *, page_size: Optional[int] = None,
               layout: str = "scatter", num_q_heads: Optional[int] = None,
               num_kv_heads: Optional[int] = None, head_dim: Optional[int] = None,
               kv_dtype: Optional[str] = None, private_lengths: Optional[list] = None,
-              keep_logical: bool = False, tables_only: bool = False) -> Case:
+              keep_logical: bool = False, tables_only: bool = False,
+              nested: Optional[tuple] = None) -> Case:
     """Generate one seeded decode step of workload `name`.
 
     Overrides shrink or reshape a workload for tests (batch, prefix length,
@@ -234,7 +236,16 @@ def make_case(name: str, seed: int = 0, *, page_size: Optional[int] = None,
     `keep_logical`, the encoded rows before paging are kept (contiguous
     per-request K/V for brute-force checks).  With `tables_only`, only the
     lengths and block tables are generated (q and the pools are None).
+    With `nested=(n_sub, seg_len)`, the prefix is shared on two levels: group 0
+    holds the prefix_len-token prefix of every request, and groups 1..n_sub
+    (parent 0) each extend it by seg_len more tokens shared by a contiguous block
+    of the requests, stored once in pages of their own.
     """
+    if nested is not None:
+        return _make_nested_case(name, seed, page_size=page_size, batch=batch, prefix_len=prefix_len,
+                                 private_range=private_range, layout=layout, num_q_heads=num_q_heads,
+                                 num_kv_heads=num_kv_heads, head_dim=head_dim, kv_dtype=kv_dtype,
+                                 n_sub=int(nested[0]), seg_len=int(nested[1]), keep_logical=keep_logical)
     w = WORKLOADS[name]
     w = dataclasses.replace(
         w,
@@ -358,6 +369,84 @@ def make_case(name: str, seed: int = 0, *, page_size: Optional[int] = None,
     return Case(w, seed, ps, n_pages, layout, kv_len, page_indptr, page_indices,
                 prefix_group, group_prefix_len, q, k_pool, v_pool, k_scale, v_scale,
                 k_enc if keep_logical else None, v_enc if keep_logical else None, rows_of)
+
+
+def _make_nested_case(name, seed, *, page_size, batch, prefix_len, private_range, layout, num_q_heads,
+                      num_kv_heads, head_dim, kv_dtype, n_sub, seg_len, keep_logical) -> Case:
+    """Two-level shared prefix (see make_case): root prefix P, then per block of requests a
+    segment of seg_len tokens, then private tokens; logical rows [0, P) root, then each
+    block's segment, then every request's private rows."""
+    w = WORKLOADS[name]
+    w = dataclasses.replace(
+        w, batch=batch if batch is not None else w.batch,
+        prefix_len=prefix_len if prefix_len is not None else w.prefix_len,
+        private_lo=private_range[0] if private_range else w.private_lo,
+        private_hi=private_range[1] if private_range else w.private_hi,
+        num_q_heads=num_q_heads or w.num_q_heads, num_kv_heads=num_kv_heads or w.num_kv_heads,
+        head_dim=head_dim or w.head_dim, kv_dtype=kv_dtype or w.kv_dtype, num_pages=None)
+    B, Hq, Hkv, d = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    ps = page_size or w.page_size
+    P, S = int(w.prefix_len), int(seg_len)
+    if not (1 <= n_sub <= B):
+        raise ValueError("nested needs 1 <= n_sub <= batch")
+    rng = np.random.default_rng([seed, 0, 7])
+    priv = rng.integers(w.private_lo, w.private_hi + 1, size=B).astype(np.int64)
+    sub = (np.arange(B) * n_sub) // B                        # block of each request
+    kv_len = (P + S + priv).astype(np.int32)
+    n_tok = P + n_sub * S + int(priv.sum())
+    q32 = normal_f32((B, Hq, d), seed, 1)
+    k_log = normal_f32((n_tok, Hkv, d), seed, 2)
+    v_log = normal_f32((n_tok, Hkv, d), seed, 3)
+    k_scale = v_scale = None
+    if w.kv_dtype == "fp8_e4m3":
+        k_scale = (np.abs(k_log).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
+        v_scale = (np.abs(v_log).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
+    k_enc = _encode(k_log, w.kv_dtype, k_scale)
+    v_enc = _encode(v_log, w.kv_dtype, v_scale)
+    q = _encode(q32, w.q_dtype)
+    priv_base = P + n_sub * S + np.concatenate([[0], np.cumsum(priv)[:-1]])
+
+    def rows_of(b):  # logical row of every context token of request b
+        return np.concatenate([np.arange(P), P + sub[b] * S + np.arange(S),
+                               priv_base[b] + np.arange(int(priv[b]))]).astype(np.int64)
+
+    n0 = P // ps                                             # root pages, shared by all
+    n1 = (P + S) // ps                                       # pages shared within a block
+    own_pages = (kv_len.astype(np.int64) - n1 * ps + ps - 1) // ps
+    needed = n0 + n_sub * (n1 - n0) + int(own_pages.sum())
+    n_pages = int(math.ceil(1.25 * needed))
+    lrng = np.random.default_rng([seed, ps, 3, {"scatter": 0, "contiguous": 1}[layout]])
+    phys = lrng.permutation(n_pages).astype(np.int64) if layout == "scatter" else np.arange(n_pages, dtype=np.int64)
+    root = phys[:n0]
+    pos = n0
+    seg_pages = []
+    for _ in range(n_sub):
+        seg_pages.append(phys[pos:pos + n1 - n0])
+        pos += n1 - n0
+    page_lists = []
+    for b in range(B):
+        mine = phys[pos:pos + own_pages[b]]
+        pos += int(own_pages[b])
+        page_lists.append(np.concatenate([root, seg_pages[sub[b]], mine]))
+    page_indptr = np.zeros(B + 1, np.int32)
+    page_indptr[1:] = np.cumsum([len(x) for x in page_lists])
+    page_indices = np.concatenate(page_lists).astype(np.int32)
+    elem = _np_dtype(w.kv_dtype)
+    k_pool = np.full((n_pages * ps, Hkv, d), _poison(w.kv_dtype), dtype=elem)
+    v_pool = np.full((n_pages * ps, Hkv, d), _poison(w.kv_dtype), dtype=elem)
+    for b in range(B):
+        t = np.arange(int(kv_len[b]))
+        slots = page_lists[b][t // ps] * ps + t % ps
+        r = rows_of(b)
+        k_pool[slots] = k_enc[r]
+        v_pool[slots] = v_enc[r]
+    prefix_group = (1 + sub).astype(np.int32)
+    group_prefix_len = np.array([P] + [P + S] * n_sub, np.int32)
+    group_parent = np.array([-1] + [0] * n_sub, np.int32)
+    logical = dict(k_logical=k_enc, v_logical=v_enc, logical_rows=[rows_of(b) for b in range(B)]) if keep_logical else {}
+    return Case(w, seed, ps, n_pages, layout, kv_len, page_indptr, page_indices, prefix_group,
+                group_prefix_len, q, k_pool.reshape(n_pages, ps, Hkv, d), v_pool.reshape(n_pages, ps, Hkv, d),
+                k_scale, v_scale, group_parent=group_parent, **logical)
 
 
 def unique_kv_bytes(case: Case) -> int:
