@@ -683,8 +683,7 @@ def main():
         oh = torch.empty(o.shape, dtype=torch.int16 if w.o_dtype == "bf16" else torch.float32).pin_memory()
         lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
         qd = torch.empty_like(tens["q"])
-        batch, keep = step.make_batch(case.kv_len, case.page_indptr, case.page_indices, case.prefix_group,
-                                      case.group_prefix_len)
+        batch, keep = step.make_case_batch(case)
         devt = step.tensors(qd, tens["k"], tens["v"], o, lse, tens["ks"], tens["vs"])
         e2e = []
         for i in range(3 + args.steps):

@@ -75,7 +75,7 @@
 extern "C" {
 #endif
 
-#define PSP_ABI_VERSION 2
+#define PSP_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define PSP_API __attribute__((visibility("default")))
@@ -85,12 +85,15 @@ extern "C" {
 
 typedef int32_t psp_status;
 #define PSP_OK 0
-#define PSP_ERR_INVALID_ARGUMENT (-1) /* null pointer, bad size, inconsistent arrays */
+#define PSP_ERR_INVALID_ARGUMENT (-1) /* null pointer, bad size, inconsistent arrays, a group
+                                         tree whose parent is not a lower group or whose
+                                         child prefix is shorter than its parent's */
 #define PSP_ERR_UNSUPPORTED (-2)      /* configuration not built (see psp_create); never coerced */
 #define PSP_ERR_PAGE_OUT_OF_RANGE (-3)/* a page id < 0 or >= num_pages */
 #define PSP_ERR_LENGTH (-4)           /* kv_len < 1, or page count != ceil(kv_len / page_size) */
-#define PSP_ERR_PREFIX_MISMATCH (-5)  /* group members disagree on their shared pages, or a
-                                         member's context is shorter than the group prefix */
+#define PSP_ERR_PREFIX_MISMATCH (-5)  /* group members (descendants' requests included)
+                                         disagree on their shared pages, or a member's context
+                                         is shorter than its group's prefix */
 #define PSP_ERR_NO_PLAN (-6)          /* run/upload/query before a successful plan/upload */
 #define PSP_ERR_WORKSPACE (-7)        /* workspace NULL, too small or not 256-byte aligned */
 #define PSP_ERR_CUDA (-8)             /* a CUDA runtime call failed (text in psp_last_error) */
@@ -104,12 +107,13 @@ typedef int32_t psp_status;
 #define PSP_DTYPE_FP8_E4M3 2 /* OCP e4m3 ("fn"): value = code * per-KV-head fp32 scale */
 
 /* Prefix branch chosen per group by the dispatcher. */
-#define PSP_BRANCH_NONE 0    /* no member, or the prefix is shorter than one page */
+#define PSP_BRANCH_NONE 0    /* no member, or the group's own segment is shorter than one page */
 #define PSP_BRANCH_CASCADE 1 /* small-M tiled loop over the stacked queries */
 #define PSP_BRANCH_DENSE 2   /* 128-row tensor-core tiles over the stacked queries */
-#define PSP_BRANCH_PAGED 3   /* reading the prefix once does not pay at this size: every member
-                                reads its whole context, prefix included, through its own block
-                                table (the group's plan equals the plan without the group) */
+#define PSP_BRANCH_PAGED 3   /* reading the group's segment once does not pay at this size, or
+                                the group lies below a paged group: every member reads it
+                                through its own block table, as unshared tokens (a root group's
+                                plan then equals the plan without the group) */
 
 /* Flags for psp_config.flags. */
 #define PSP_FLAG_TOKEN_FLAT 1 /* lower block tables to per-token kv_indices on the device
@@ -156,10 +160,18 @@ typedef struct psp_config {
  *   page_indices[...]    physical page ids in [0, num_pages); at page_size 1 these are the
  *                        token-flat kv_indices
  *   prefix_group[B]      group id in [0, num_groups) or -1; NULL = no sharing at all
- *   group_prefix_len[g]  tokens of group g's shared prefix; only its floor(P / page_size)
- *                        full pages are shared (block-aligned matching), the remaining
- *                        tokens stay in each member's private suffix
- * Every member of a group must list the same first floor(P / page_size) page ids.
+ *   group_prefix_len[g]  tokens of group g's shared prefix (counted from the context's first
+ *                        token); only its floor(P / page_size) full pages are shared
+ *                        (block-aligned matching), the remaining tokens stay in each
+ *                        member's private suffix
+ *   group_parent[g]      nested prefixes (a radix tree of shared beginnings, "Track C
+ *                        Document 10", the vLLM-or-SGLang answer; per-user sharing on top of
+ *                        a global prefix in its cache table): -1 for a root, else a group of
+ *                        lower index whose prefix is no longer than g's; NULL = every group
+ *                        is a root.  A request of group g is a member of g and of every
+ *                        ancestor of g; group g's own segment is its shared pages from
+ *                        floor(P_parent / page_size) on, read once for all of its members.
+ * Every member of a group must list the group's floor(P / page_size) shared page ids.
  */
 typedef struct psp_batch {
   int32_t batch_size;
@@ -169,6 +181,7 @@ typedef struct psp_batch {
   const int32_t* prefix_group;
   int32_t num_groups;
   const int32_t* group_prefix_len;
+  const int32_t* group_parent;
 } psp_batch;
 
 /*
@@ -198,10 +211,10 @@ typedef struct psp_plan_info {
   int32_t num_splits;          /* suffix splits over all requests */
   int32_t num_chunks;          /* prefix chunks over all groups */
   int64_t suffix_pages;        /* entries of the suffix page lists */
-  int64_t group_pages;         /* entries of the group prefix page lists */
+  int64_t group_pages;         /* entries of the group prefix page lists (whole prefixes) */
   int64_t kv_indices_len;      /* sum of kv_len (token-flat lowering length) */
   int64_t suffix_tokens;       /* sum of suffix lengths */
-  int64_t shared_tokens;       /* sum of group shared lengths (read once per step) */
+  int64_t shared_tokens;       /* sum of the groups' own segments read once per step */
   int64_t workspace_bytes;     /* device workspace the plan needs */
   int32_t suffix_ctas;         /* (split, kv head) work items */
   int32_t prefix_dense_ctas;   /* (chunk, row block, kv head) items of dense groups */
@@ -230,16 +243,21 @@ typedef struct psp_plan_info {
 #define PSP_FIELD_SPLIT_INDPTR 4        /* [B+1] splits of request b */
 #define PSP_FIELD_SPLIT_BEGIN 5         /* [num_splits] token offset within the suffix */
 #define PSP_FIELD_SPLIT_END 6           /* [num_splits] exclusive */
-#define PSP_FIELD_GROUP_SHARED_LEN 7    /* [num_groups] tokens read once (full pages only) */
+#define PSP_FIELD_GROUP_SHARED_LEN 7    /* [num_groups] tokens of the own segment read once */
 #define PSP_FIELD_GROUP_PAGE_INDPTR 8   /* [num_groups+1] */
-#define PSP_FIELD_GROUP_PAGE_INDICES 9  /* shared page lists */
-#define PSP_FIELD_GROUP_M_EFF 10        /* [num_groups] members x (Hq / Hkv) */
+#define PSP_FIELD_GROUP_PAGE_INDICES 9  /* per read-once group its whole shared page list,
+                                           ancestors' pages first */
+#define PSP_FIELD_GROUP_M_EFF 10        /* [num_groups] members (descendants' requests
+                                           included) x (Hq / Hkv) */
 #define PSP_FIELD_GROUP_BRANCH 11       /* [num_groups] PSP_BRANCH_* */
 #define PSP_FIELD_GROUP_ROW_BLOCKS 12   /* [num_groups] stacked-query row blocks */
 #define PSP_FIELD_GROUP_CHUNK_INDPTR 13 /* [num_groups+1] */
-#define PSP_FIELD_CHUNK_BEGIN 14        /* [num_chunks] token offset within the shared prefix */
+#define PSP_FIELD_CHUNK_BEGIN 14        /* [num_chunks] context token (inside the group's own
+                                           segment, which starts at its parent's shared end) */
 #define PSP_FIELD_CHUNK_END 15          /* [num_chunks] exclusive */
 #define PSP_FIELD_KV_INDPTR 16          /* [B+1] offsets of the token-flat lowering */
+#define PSP_FIELD_REQ_LEVEL_INDPTR 17   /* [B+1] CSR offsets of each request's read-once groups */
+#define PSP_FIELD_REQ_LEVEL_GROUP 18    /* those groups, outermost first (merge order) */
 
 typedef struct psp_handle psp_handle;
 
@@ -265,29 +283,32 @@ PSP_API const char* psp_last_error(const psp_handle* h);
  * Host-only planning of one step (no CUDA call unless cfg.num_sms == 0, which
  * queries the current device's SM count once).  Validates the batch (see
  * psp_batch) and builds, in token units independent of the page size:
- *  - per request: shared pages n_sh = floor(P_g / page_size) for a member of
- *    a group g whose prefix is read once (0 otherwise, PAGED groups included),
- *    suffix_start = n_sh * page_size, suffix_len =
- *    kv_len - suffix_start, the suffix page list = pages[n_sh:] ("Track C
- *    Document 10", block-aligned prefix matching);
- *  - per group: M_eff = members x (Hq / Hkv) and the branch ("GraniKV",
- *    section 3 Per-step dispatcher): NONE without members or full pages; PAGED
- *    when reading the prefix once does not pay (shared tokens below
- *    read_once_min_tokens, or (members - 1) x shared tokens x token_bytes below
+ *  - per group (its members: its own requests and its descendants'): M_eff =
+ *    members x (Hq / Hkv), its own segment (shared tokens from its parent's
+ *    floor(P_parent / page_size) pages to its floor(P_g / page_size) pages)
+ *    and the branch ("GraniKV", section 3 Per-step dispatcher): NONE without
+ *    members or without a full page in the segment; PAGED below a PAGED group,
+ *    or when reading the segment once does not pay (its tokens below
+ *    read_once_min_tokens, or (members - 1) x its tokens x token_bytes below
  *    read_once_min_mib MiB; the built-in values 1024 tokens and 64 MiB are the
  *    GB300 refit); else DENSE if M_eff >= dense_threshold, else CASCADE.  A
- *    DENSE or CASCADE group's shared page list is read once; a PAGED group
- *    shares nothing (shared length 0, no chunks) and its members' suffixes are
- *    their whole contexts;
+ *    DENSE or CASCADE group's segment is read once; a PAGED group shares
+ *    nothing (shared length 0, no chunks);
+ *  - per request: its read-once groups, outermost first (each contributes
+ *    its prefix partials to the merge), shared pages n_sh = floor(P / page_size)
+ *    of the deepest of them (0 without one), suffix_start = n_sh * page_size,
+ *    suffix_len = kv_len - suffix_start, the suffix page list = pages[n_sh:]
+ *    ("Track C Document 10", block-aligned prefix matching);
  *  - the split-KV partition: with granule tile_tokens, T_b = ceil(S_b / tile)
  *    granules per suffix, W = Hkv * sum T_b, C = max(split_min_tiles,
  *    ceil(W / (split_ctas_per_sm * num_sms))) granules per split, and split s
  *    of request b covering suffix tokens [tile*s*C, min(tile*(s+1)*C, S_b));
- *  - the prefix partition: R = ceil(M_eff / rows) row blocks (rows = 128
- *    dense, 64 cascade), TP = ceil(shared / tile) granules, n = max(1,
+ *  - the prefix partition of each read-once segment: R = ceil(M_eff / rows) row
+ *    blocks (rows = 256 dense, 64 cascade), TP = ceil(shared / tile) granules, n = max(1,
  *    min(floor(prefix_ctas_per_sm * num_sms / (Hkv * R)), floor(TP /
- *    prefix_min_tiles))), CP = ceil(TP / n), chunk c covering shared tokens
- *    [tile*c*CP, min(tile*(c+1)*CP, shared)).
+ *    prefix_min_tiles))), CP = ceil(TP / n), chunk c covering the segment's
+ *    tokens [tile*c*CP, min(tile*(c+1)*CP, shared)), offset by the segment's
+ *    first context token.
  * A successful plan replaces the previous one (its upload becomes invalid).
  * Errors: INVALID_ARGUMENT, PAGE_OUT_OF_RANGE, LENGTH, PREFIX_MISMATCH,
  * HOST_ALLOC, CUDA (only when querying the SM count). */

@@ -43,7 +43,7 @@ FIELDS = {
     "split_indptr": 4, "split_begin": 5, "split_end": 6, "group_shared_len": 7,
     "group_page_indptr": 8, "group_page_indices": 9, "group_m_eff": 10, "group_branch": 11,
     "group_row_blocks": 12, "group_chunk_indptr": 13, "chunk_begin": 14, "chunk_end": 15,
-    "kv_indptr": 16,
+    "kv_indptr": 16, "req_level_indptr": 17, "req_level_group": 18,
 }
 
 
@@ -57,7 +57,7 @@ class psp_batch(ctypes.Structure):
     _fields_ = [("batch_size", ctypes.c_int32), ("kv_len", ctypes.c_void_p),
                 ("page_indptr", ctypes.c_void_p), ("page_indices", ctypes.c_void_p),
                 ("prefix_group", ctypes.c_void_p), ("num_groups", ctypes.c_int32),
-                ("group_prefix_len", ctypes.c_void_p)]
+                ("group_prefix_len", ctypes.c_void_p), ("group_parent", ctypes.c_void_p)]
 
 
 class psp_tensors(ctypes.Structure):
@@ -188,23 +188,31 @@ class DecodeStep:
         if st != PSP_OK:
             raise PspError(st, where, (psp_last_error(self.handle) or b"").decode())
 
-    def make_batch(self, kv_len, page_indptr, page_indices, prefix_group=None, group_prefix_len=None):
+    def make_batch(self, kv_len, page_indptr, page_indices, prefix_group=None, group_prefix_len=None,
+                   group_parent=None):
         arrs = [_i32(kv_len), _i32(page_indptr), _i32(page_indices),
                 None if prefix_group is None else _i32(prefix_group),
-                _i32(group_prefix_len if group_prefix_len is not None else np.zeros(0, np.int32))]
+                _i32(group_prefix_len if group_prefix_len is not None else np.zeros(0, np.int32)),
+                None if group_parent is None else _i32(group_parent)]
         ng = int(arrs[4].shape[0])
         b = psp_batch(int(arrs[0].shape[0]), _ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), _ptr(arrs[3]), ng,
-                      _ptr(arrs[4]) if ng else None)
+                      _ptr(arrs[4]) if ng else None, _ptr(arrs[5]) if ng else None)
         return b, arrs
 
-    def plan(self, kv_len, page_indptr, page_indices, prefix_group=None, group_prefix_len=None):
-        b, arrs = self.make_batch(kv_len, page_indptr, page_indices, prefix_group, group_prefix_len)
+    def plan(self, kv_len, page_indptr, page_indices, prefix_group=None, group_prefix_len=None,
+             group_parent=None):
+        b, arrs = self.make_batch(kv_len, page_indptr, page_indices, prefix_group, group_prefix_len, group_parent)
         self._check(psp_plan(self.handle, ctypes.byref(b)), "psp_plan")
         return self
 
+    def make_case_batch(self, case):
+        """make_batch over a generated case's block tables (nested groups included)."""
+        return self.make_batch(case.kv_len, case.page_indptr, case.page_indices, case.prefix_group,
+                               case.group_prefix_len, getattr(case, "group_parent", None))
+
     def plan_case(self, case):
         return self.plan(case.kv_len, case.page_indptr, case.page_indices, case.prefix_group,
-                         case.group_prefix_len)
+                         case.group_prefix_len, getattr(case, "group_parent", None))
 
     def plan_info(self) -> dict:
         info = psp_plan_info()

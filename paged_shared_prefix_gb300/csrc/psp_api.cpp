@@ -72,7 +72,7 @@ struct HostPlan {
   std::vector<int32_t> suffix_page_indptr, suffix_page_indices, suffix_start, suffix_len;
   std::vector<int32_t> split_indptr, split_req, split_begin, split_end;
   std::vector<int32_t> split_desc;  // kSplitDescInts per split (psp::SplitDesc)
-  std::vector<int32_t> req_group, req_member;
+  std::vector<int32_t> req_group, req_member, req_level_indptr, req_level_group, req_level_member, req_prefix_chunks;
   std::vector<int32_t> group_page_indptr, group_page_indices, group_m_eff, group_shared_len;
   std::vector<int32_t> group_branch, group_row_blocks;
   std::vector<int32_t> group_member_indptr, group_members, group_chunk_indptr;
@@ -90,7 +90,8 @@ struct HostPlan {
     B = NG = NS = NC = 0;
     for (std::vector<int32_t>* v :
          {&suffix_page_indptr, &suffix_page_indices, &suffix_start, &suffix_len, &split_indptr, &split_req,
-          &split_begin, &split_end, &split_desc, &req_group, &req_member, &group_page_indptr, &group_page_indices,
+          &split_begin, &split_end, &split_desc, &req_group, &req_member, &req_level_indptr, &req_level_group,
+          &req_level_member, &req_prefix_chunks, &group_page_indptr, &group_page_indices,
           &group_m_eff, &group_shared_len, &group_branch, &group_row_blocks, &group_member_indptr, &group_members,
           &group_chunk_indptr, &chunk_group, &chunk_begin, &chunk_end, &chunk_row_offset, &item_chunk_dense,
           &item_rb_dense, &item_chunk_cascade, &item_rb_cascade, &kv_indptr})
@@ -207,6 +208,15 @@ psp_status validate_batch(psp_handle* h, const psp_batch* bt) {
   }
   for (int g = 0; g < bt->num_groups; ++g)
     if (bt->group_prefix_len[g] < 0) return fail(h, PSP_ERR_INVALID_ARGUMENT, "negative group prefix length");
+  // nested groups: a parent has a lower index and a prefix no longer than its child's
+  if (bt->group_parent)
+    for (int g = 0; g < bt->num_groups; ++g) {
+      const int par = bt->group_parent[g];
+      if (par < -1 || par >= g)
+        return fail(h, PSP_ERR_INVALID_ARGUMENT, "group_parent[" + std::to_string(g) + "] is not -1 or a lower group");
+      if (par >= 0 && bt->group_prefix_len[par] > bt->group_prefix_len[g])
+        return fail(h, PSP_ERR_INVALID_ARGUMENT, "group " + std::to_string(g) + " has a shorter prefix than its parent");
+    }
   return PSP_OK;
 }
 
@@ -238,69 +248,109 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   P.B = B;
   P.NG = NG;
 
-  // --- groups: members (increasing request id) and agreement on shared pages
-  std::vector<int32_t> first(NG, -1), count(NG, 0);
+  // --- groups: the tree (checked in validate_batch; NULL parents: every group a root), the
+  //     members of each group (its own requests and its descendants'), increasing request id
+  const int32_t* parent = bt->group_parent;
+  auto parent_of = [&](int g) { return parent ? parent[g] : -1; };
+  auto pages_of = [&](int g) -> int64_t { return g >= 0 ? bt->group_prefix_len[g] / ps : 0; };
+  std::vector<int32_t> lead(NG, -1), count(NG, 0);
   P.req_group.assign(B, -1);
   P.req_member.assign(B, -1);
+  int64_t chain_len = 0;
   for (int b = 0; b < B; ++b) {
     const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
     if (g == -1) continue;
     if (g < -1 || g >= NG) return fail(h, PSP_ERR_INVALID_ARGUMENT, "prefix_group out of range");
-    const int64_t plen = bt->group_prefix_len[g];
-    if (plen > bt->kv_len[b])
+    if (bt->group_prefix_len[g] > bt->kv_len[b])
       return fail(h, PSP_ERR_PREFIX_MISMATCH, "group prefix longer than the context of request " + std::to_string(b));
-    const int64_t n_sh = plen / ps;
-    if (first[g] < 0) {
-      first[g] = b;
-    } else {
-      const int32_t* mine = bt->page_indices + bt->page_indptr[b];
-      const int32_t* ref = bt->page_indices + bt->page_indptr[first[g]];
-      if (n_sh > 0 && std::memcmp(mine, ref, static_cast<size_t>(n_sh) * sizeof(int32_t)) != 0) {
-        const psp_status range = full_range_check(h, bt);
-        if (range) return range;
-        return fail(h, PSP_ERR_PREFIX_MISMATCH,
-                    "request " + std::to_string(b) + " does not share the prefix pages of its group");
-      }
+    if (lead[g] < 0) lead[g] = b;
+    for (int a = g; a >= 0; a = parent_of(a)) {
+      ++count[a];
+      ++chain_len;
     }
-    P.req_member[b] = count[g]++;
   }
   P.group_member_indptr.assign(NG + 1, 0);
   for (int g = 0; g < NG; ++g) P.group_member_indptr[g + 1] = P.group_member_indptr[g] + count[g];
   P.group_members.assign(std::max<int64_t>(P.group_member_indptr[NG], 0), 0);
+  // per request, its groups from its own up to the root with its index among each one's members
+  std::vector<int32_t> chain_indptr(B + 1, 0), chain_group(chain_len), chain_member(chain_len);
+  {
+    std::vector<int32_t> cursor(P.group_member_indptr.begin(), P.group_member_indptr.end() - 1);
+    int64_t k = 0;
+    for (int b = 0; b < B; ++b) {
+      const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
+      for (int a = g; a >= 0; a = parent_of(a), ++k) {
+        chain_group[k] = a;
+        chain_member[k] = cursor[a] - P.group_member_indptr[a];
+        P.group_members[cursor[a]++] = b;
+      }
+      chain_indptr[b + 1] = static_cast<int32_t>(k);
+    }
+  }
+  // every member lists its group's shared pages: against the first request of its own group
+  // over the whole prefix (that request's pages were range-checked in full), and against the
+  // first member of every group on its path over that group's own segment (needed only where
+  // the first member is not the first request of the group itself)
   for (int b = 0; b < B; ++b) {
     const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
-    if (g >= 0) P.group_members[P.group_member_indptr[g] + P.req_member[b]] = b;
+    if (g < 0) continue;
+    const int32_t* mine = bt->page_indices + bt->page_indptr[b];
+    bool same = true;
+    const int64_t n_sh = pages_of(g);
+    if (b != lead[g] && n_sh > 0)
+      same = std::memcmp(mine, bt->page_indices + bt->page_indptr[lead[g]], static_cast<size_t>(n_sh) * sizeof(int32_t)) == 0;
+    for (int a = g; same && a >= 0; a = parent_of(a)) {
+      const int rep = P.group_members[P.group_member_indptr[a]];
+      if (rep == b || (a == g && rep == lead[g])) continue;
+      const int64_t lo = pages_of(parent_of(a)), hi = pages_of(a);
+      if (hi > lo)
+        same = std::memcmp(mine + lo, bt->page_indices + bt->page_indptr[rep] + lo,
+                           static_cast<size_t>(hi - lo) * sizeof(int32_t)) == 0;
+    }
+    if (!same) {
+      const psp_status range = full_range_check(h, bt);
+      if (range) return range;
+      return fail(h, PSP_ERR_PREFIX_MISMATCH,
+                  "request " + std::to_string(b) + " does not share the prefix pages of its group");
+    }
   }
 
-  // --- per group: shared pages, M_eff, branch, row blocks, prefix chunks
+  // --- per group: M_eff, the branch of its own segment, shared pages, row blocks, chunks
+  //     (a group below a paged group is paged: a request's unshared tokens stay one range)
   P.group_shared_len.assign(NG, 0);
   P.group_m_eff.assign(NG, 0);
   P.group_branch.assign(NG, PSP_BRANCH_NONE);
   P.group_row_blocks.assign(NG, 0);
   P.group_page_indptr.assign(NG + 1, 0);
   P.group_chunk_indptr.assign(NG + 1, 0);
+  std::vector<char> below_paged(NG, 0);
   for (int g = 0; g < NG; ++g) {
-    int64_t n_sh = count[g] > 0 ? bt->group_prefix_len[g] / ps : 0;
+    const int par = parent_of(g);
+    if (par >= 0) below_paged[g] = below_paged[par] || P.group_branch[par] == PSP_BRANCH_PAGED;
+    const int64_t n_sh = pages_of(g);
+    const int64_t seg0 = pages_of(par) * ps;  // first token of the group's own segment
+    const int64_t seg = count[g] > 0 ? n_sh * ps - seg0 : 0;
     const int64_t m_eff = static_cast<int64_t>(count[g]) * G;
     int branch = PSP_BRANCH_NONE;
-    if (m_eff > 0 && n_sh > 0) {
-      const int64_t saved = static_cast<int64_t>(count[g] - 1) * n_sh * ps * token_bytes;
-      if ((min_tokens > 0 && n_sh * ps < min_tokens) || (min_mib > 0 && saved < (static_cast<int64_t>(min_mib) << 20)))
+    if (m_eff > 0 && seg > 0) {
+      const int64_t saved = static_cast<int64_t>(count[g] - 1) * seg * token_bytes;
+      if (below_paged[g] || (min_tokens > 0 && seg < min_tokens) ||
+          (min_mib > 0 && saved < (static_cast<int64_t>(min_mib) << 20)))
         branch = PSP_BRANCH_PAGED;
       else
         branch = m_eff >= threshold ? PSP_BRANCH_DENSE : PSP_BRANCH_CASCADE;
     }
-    if (branch == PSP_BRANCH_PAGED) n_sh = 0;  // nothing is read once
-    const int64_t shared = n_sh * ps;
+    const bool once = branch == PSP_BRANCH_DENSE || branch == PSP_BRANCH_CASCADE;
+    const int64_t shared = once ? seg : 0;
     P.group_shared_len[g] = static_cast<int32_t>(shared);
     P.group_m_eff[g] = static_cast<int32_t>(m_eff);
-    if (n_sh > 0) {
-      const int32_t* src = bt->page_indices + bt->page_indptr[first[g]];
+    if (once) {  // the whole prefix, the ancestors' pages first
+      const int32_t* src = bt->page_indices + bt->page_indptr[P.group_members[P.group_member_indptr[g]]];
       P.group_page_indices.insert(P.group_page_indices.end(), src, src + n_sh);
     }
     P.group_page_indptr[g + 1] = static_cast<int32_t>(P.group_page_indices.size());
     P.group_branch[g] = branch;
-    if (branch == PSP_BRANCH_DENSE || branch == PSP_BRANCH_CASCADE) {
+    if (once) {
       const int64_t rows = branch == PSP_BRANCH_DENSE ? psp::kDenseRows : psp::kCascadeRows;
       const int64_t rb = cdiv(m_eff, rows);
       const int64_t tiles = cdiv(shared, tile);
@@ -313,8 +363,8 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
       for (int64_t ci = 0; ci < n; ++ci) {
         const int32_t chunk_id = static_cast<int32_t>(P.chunk_begin.size());
         P.chunk_group.push_back(g);
-        P.chunk_begin.push_back(static_cast<int32_t>(ci * per * tile));
-        P.chunk_end.push_back(static_cast<int32_t>(std::min((ci + 1) * per * tile, shared)));
+        P.chunk_begin.push_back(static_cast<int32_t>(seg0 + ci * per * tile));
+        P.chunk_end.push_back(static_cast<int32_t>(seg0 + std::min((ci + 1) * per * tile, shared)));
         P.chunk_row_offset.push_back(static_cast<int32_t>(P.pre_rows));
         P.pre_rows += static_cast<int64_t>(Hkv) * m_eff;
         for (int64_t r = 0; r < rb; ++r) {
@@ -333,23 +383,28 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   }
   if (P.pre_rows > INT32_MAX) return fail(h, PSP_ERR_INVALID_ARGUMENT, "prefix partial rows exceed int32");
   P.NC = static_cast<int32_t>(P.chunk_begin.size());
-  // requests whose group runs no prefix kernel read everything as suffix
-  for (int b = 0; b < B; ++b) {
-    const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
-    if (g >= 0 && (P.group_branch[g] == PSP_BRANCH_NONE || P.group_branch[g] == PSP_BRANCH_PAGED))
-      P.req_group[b] = -1;
-    else
-      P.req_group[b] = g;
-  }
 
-  // --- per request: suffix after the group's shared pages
+  // --- per request: the read-once groups on its path, outermost first (their prefix partials
+  //     are merged in this order), and the suffix after the deepest of them
+  P.req_level_indptr.assign(B + 1, 0);
+  P.req_prefix_chunks.assign(B, 0);
   P.suffix_page_indptr.assign(B + 1, 0);
   P.suffix_start.assign(B, 0);
   P.suffix_len.assign(B, 0);
   P.kv_indptr.assign(B + 1, 0);
   for (int b = 0; b < B; ++b) {
-    const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
-    const int64_t n_sh = (g >= 0 && P.group_branch[g] != PSP_BRANCH_PAGED) ? bt->group_prefix_len[g] / ps : 0;
+    int64_t n_sh = 0;
+    for (int32_t k = chain_indptr[b + 1] - 1; k >= chain_indptr[b]; --k) {
+      const int a = chain_group[k];
+      if (P.group_branch[a] != PSP_BRANCH_DENSE && P.group_branch[a] != PSP_BRANCH_CASCADE) continue;
+      P.req_level_group.push_back(a);
+      P.req_level_member.push_back(chain_member[k]);
+      P.req_prefix_chunks[b] += P.group_chunk_indptr[a + 1] - P.group_chunk_indptr[a];
+      P.req_group[b] = a;
+      P.req_member[b] = chain_member[k];
+      n_sh = pages_of(a);
+    }
+    P.req_level_indptr[b + 1] = static_cast<int32_t>(P.req_level_group.size());
     P.suffix_start[b] = static_cast<int32_t>(n_sh * ps);
     P.suffix_len[b] = static_cast<int32_t>(bt->kv_len[b] - n_sh * ps);
     const int32_t* pages = bt->page_indices + bt->page_indptr[b];
@@ -387,11 +442,13 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
     d.t1 = P.split_end[si];
     d.list_paged = P.suffix_page_indptr[b];
     d.list_flat = P.kv_indptr[b] + P.suffix_start[b];
-    d.c0 = g >= 0 ? P.group_chunk_indptr[g] : 0;
-    d.n_chunks = g >= 0 ? P.group_chunk_indptr[g + 1] - d.c0 : 0;
+    d.levels = P.req_level_indptr[b + 1] - P.req_level_indptr[b];
+    const bool one = d.levels == 1;  // a single level is described in place
+    d.c0 = one ? P.group_chunk_indptr[g] : 0;
+    d.n_chunks = P.req_prefix_chunks[b];
     d.one_split = P.split_indptr[b + 1] - P.split_indptr[b] == 1 ? 1 : 0;
-    d.prow = g >= 0 ? P.req_member[b] * G : 0;
-    d.m_eff = g >= 0 ? P.group_m_eff[g] : 0;
+    d.prow = one ? P.req_member[b] * G : 0;
+    d.m_eff = one ? P.group_m_eff[g] : 0;
     for (int k = 0; k < psp::kDescPages; ++k) {
       const int64_t t = static_cast<int64_t>(d.t0) + 16 * k;
       d.first_page[k] = (ps >= 16 && t < d.t1) ? P.suffix_page_indices[d.list_paged + (t / ps)] : -1;
@@ -417,6 +474,10 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   place(L.split_desc, n32(P.split_desc));
   place(L.req_group, n32(P.req_group));
   place(L.req_member, n32(P.req_member));
+  place(L.req_level_indptr, n32(P.req_level_indptr));
+  place(L.req_level_group, n32(P.req_level_group));
+  place(L.req_level_member, n32(P.req_level_member));
+  place(L.req_prefix_chunks, n32(P.req_prefix_chunks));
   place(L.group_page_indptr, n32(P.group_page_indptr));
   place(L.group_page_indices, n32(P.group_page_indices));
   place(L.group_m_eff, n32(P.group_m_eff));
@@ -464,6 +525,10 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   put(L.split_desc, P.split_desc);
   put(L.req_group, P.req_group);
   put(L.req_member, P.req_member);
+  put(L.req_level_indptr, P.req_level_indptr);
+  put(L.req_level_group, P.req_level_group);
+  put(L.req_level_member, P.req_level_member);
+  put(L.req_prefix_chunks, P.req_prefix_chunks);
   put(L.group_page_indptr, P.group_page_indptr);
   put(L.group_page_indices, P.group_page_indices);
   put(L.group_m_eff, P.group_m_eff);
@@ -530,6 +595,8 @@ const std::vector<int32_t>* field_vector(const HostPlan& P, int32_t field) {
     case PSP_FIELD_CHUNK_BEGIN: return &P.chunk_begin;
     case PSP_FIELD_CHUNK_END: return &P.chunk_end;
     case PSP_FIELD_KV_INDPTR: return &P.kv_indptr;
+    case PSP_FIELD_REQ_LEVEL_INDPTR: return &P.req_level_indptr;
+    case PSP_FIELD_REQ_LEVEL_GROUP: return &P.req_level_group;
   }
   return nullptr;
 }
@@ -576,6 +643,10 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.split_desc = reinterpret_cast<const psp::SplitDesc*>(I(L.split_desc));
   p.req_group = I(L.req_group);
   p.req_member = I(L.req_member);
+  p.req_level_indptr = I(L.req_level_indptr);
+  p.req_level_group = I(L.req_level_group);
+  p.req_level_member = I(L.req_level_member);
+  p.req_prefix_chunks = I(L.req_prefix_chunks);
   p.group_page_indptr = I(L.group_page_indptr);
   p.group_page_indices = I(L.group_page_indices);
   p.group_m_eff = I(L.group_m_eff);
@@ -742,9 +813,10 @@ void log_plan(const psp_handle* h, const psp_batch* bt) {
   s += buf;
   for (int g = 0; g < P.NG; ++g) {
     std::snprintf(buf, sizeof buf,
-                  "%s{\"group\": %d, \"members\": %d, \"m_eff\": %d, \"shared_tokens\": %d, "
+                  "%s{\"group\": %d, \"parent\": %d, \"members\": %d, \"m_eff\": %d, \"shared_tokens\": %d, "
                   "\"branch\": \"%s\", \"chunks\": %d}",
-                  g ? ", " : "", g, P.group_member_indptr[g + 1] - P.group_member_indptr[g], P.group_m_eff[g],
+                  g ? ", " : "", g, bt->group_parent ? bt->group_parent[g] : -1,
+                  P.group_member_indptr[g + 1] - P.group_member_indptr[g], P.group_m_eff[g],
                   P.group_shared_len[g], kBranch[P.group_branch[g]],
                   P.group_chunk_indptr[g + 1] - P.group_chunk_indptr[g]);
     s += buf;

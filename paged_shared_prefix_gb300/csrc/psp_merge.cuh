@@ -2,9 +2,10 @@
 // (request, query head) row, performed by whichever CTA delivers the last
 // partial of its (request, KV head).
 //
-// Every (b, h) expects one partial per prefix chunk of b's group plus one per
-// suffix split of b.  A CTA that has written its partials fences them and adds
-// one arrival on the (b, h) counter; the CTA that brings the count to the
+// Every (b, h) expects one partial per prefix chunk of each read-once group b
+// belongs to (one group, or a path of nested groups) plus one per suffix split
+// of b.  A CTA that has written its partials fences them and adds one arrival
+// on the (b, h) counter; the CTA that brings the count to the
 // expected total merges the G rows of (b, h) and resets the counter to zero
 // for the next step.  No CTA ever waits for another.  A request with exactly
 // one suffix split skips the counter when the prefix kernels run before the
@@ -15,9 +16,9 @@
 // Merge of a row: with every O_i normalised and lse_i its log2 normaliser,
 //   M = max_i lse_i,  w_i = 2^(lse_i - M),  O = sum_i w_i O_i / sum_i w_i,
 //   LSE = (M + log2 sum_i w_i) * ln 2,
-// in a fixed order (prefix chunks, then splits), so the result does not depend
-// on which CTA merges ("GraniKV", section 3: the prefix result is merged with
-// each request's suffix attention).
+// in a fixed order (prefix chunks level by level from the outermost, then splits),
+// so the result does not depend on which CTA merges ("GraniKV", section 3: the
+// prefix result is merged with each request's suffix attention).
 #pragma once
 
 #include "psp_device.cuh"
@@ -28,9 +29,7 @@ namespace dev {
 
 // Number of partial results (b, h) receives this step.
 __device__ __forceinline__ int expected_parts(const StepParams& p, int b) {
-  const int g = p.req_group[b];
-  const int chunks = g >= 0 ? p.group_chunk_indptr[g + 1] - p.group_chunk_indptr[g] : 0;
-  return chunks + p.split_indptr[b + 1] - p.split_indptr[b];
+  return p.req_prefix_chunks[b] + p.split_indptr[b + 1] - p.split_indptr[b];
 }
 
 // One arrival on (b, h) after this CTA's partials for it are written and fenced.
@@ -47,39 +46,20 @@ __device__ __forceinline__ bool arrive_is_last(const StepParams& p, int b, int h
   return false;
 }
 
-// Warp-cooperative merge of rows j0 .. j0 + 32/LANES - 1 (those below G) of (b, h): LANES
-// lanes per row, each owning D/LANES consecutive elements, every row at once, and no
-// store before the last load, so that the loads of every part of every row can be in
-// flight together (a merge costs a few dependent global round trips, not a few per row).
-// LANES = 4 merges a whole (request, KV head) in one warp; more lanes per row use fewer
-// registers per lane.
+// Accumulation of one part of a merged row: weight 2^(lse - mmax) times the part's
+// D/LANES elements of this lane (row r of obuf / lbuf).
 template <int D, int LANES>
-__device__ __forceinline__ void merge_rows(const StepParams& p, int b, int h, int j0, int lane) {
-  constexpr int kPer = D / LANES;           // elements per lane
-  constexpr int kW = kPer % 4 == 0 ? 4 : 2;  // elements per vector access
+struct MergeAcc {
+  static constexpr int kPer = D / LANES;           // elements per lane
+  static constexpr int kW = kPer % 4 == 0 ? 4 : 2;  // elements per vector access
   static_assert(kPer % kW == 0, "whole vectors per lane");
-  const int G = p.group;
-  const int j = j0 + lane / LANES;
-  const int sub = lane % LANES;
-  if (j >= G) return;
-  const int g = p.req_group[b];
-  int c0 = 0, c1 = 0, m_eff = 0, prow = 0;
-  if (g >= 0) {
-    c0 = p.group_chunk_indptr[g];
-    c1 = p.group_chunk_indptr[g + 1];
-    m_eff = p.group_m_eff[g];
-    prow = p.req_member[b] * G + j;
-  }
-  const int s0 = p.split_indptr[b], s1 = p.split_indptr[b + 1];
-  float mmax = neg_inf();
-  for (int c = c0; c < c1; ++c)
-    mmax = fmaxf(mmax, __ldcg(p.lse_pre + p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow));
-  for (int s = s0; s < s1; ++s) mmax = fmaxf(mmax, __ldcg(p.lse_suf + (static_cast<int64_t>(s) * p.hkv + h) * G + j));
   float acc[kPer];
+  float sum;
+  __device__ __forceinline__ MergeAcc() : sum(0.f) {
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
-  float sum = 0.f;
-  auto add = [&](int64_t r, const float* obuf, const float* lbuf) {
+    for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  }
+  __device__ __forceinline__ void add(int64_t r, const float* obuf, const float* lbuf, float mmax, int sub) {
     const float w = exp2f(__ldcg(lbuf + r) - mmax);
     sum += w;
     const float* src = obuf + r * D + sub * kPer;
@@ -97,22 +77,84 @@ __device__ __forceinline__ void merge_rows(const StepParams& p, int b, int h, in
         acc[v + 1] = fmaf(w, x.y, acc[v + 1]);
       }
     }
-  };
-  for (int c = c0; c < c1; ++c) add(p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow, p.o_pre, p.lse_pre);
-  for (int s = s0; s < s1; ++s) add((static_cast<int64_t>(s) * p.hkv + h) * G + j, p.o_suf, p.lse_suf);
-  const float inv = 1.f / sum;
-  const int64_t row = static_cast<int64_t>(b) * p.hq + h * G + j;
-  const int64_t obase = row * D + sub * kPer;
-  if (p.o_dtype == PSP_KV_BF16) {
-    uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.o) + obase);
-#pragma unroll
-    for (int v = 0; v < kPer; v += 2) o[v / 2] = pack_bf16(acc[v] * inv, acc[v + 1] * inv);
-  } else {
-    float* o = static_cast<float*>(p.o) + obase;
-#pragma unroll
-    for (int v = 0; v < kPer; ++v) o[v] = acc[v] * inv;
   }
-  if (p.lse && sub == 0) p.lse[row] = (mmax + log2f(sum)) * 0.6931471805599453f;
+  // o and lse of row (b, h * G + j)
+  __device__ __forceinline__ void store(const StepParams& p, int b, int h, int j, int sub, float mmax) const {
+    const float inv = 1.f / sum;
+    const int64_t row = static_cast<int64_t>(b) * p.hq + h * p.group + j;
+    const int64_t obase = row * D + sub * kPer;
+    if (p.o_dtype == PSP_KV_BF16) {
+      uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.o) + obase);
+#pragma unroll
+      for (int v = 0; v < kPer; v += 2) o[v / 2] = pack_bf16(acc[v] * inv, acc[v + 1] * inv);
+    } else {
+      float* o = static_cast<float*>(p.o) + obase;
+#pragma unroll
+      for (int v = 0; v < kPer; ++v) o[v] = acc[v] * inv;
+    }
+    if (p.lse && sub == 0) p.lse[row] = (mmax + log2f(sum)) * 0.6931471805599453f;
+  }
+};
+
+// merge_rows for a request of nested groups: one level per read-once group on its path,
+// outermost first, each with its own chunks, stacked rows and member index.  Out of line,
+// so that the single-level merge inlined into the kernels keeps its registers.
+template <int D, int LANES>
+__device__ __noinline__ void merge_rows_nested(const StepParams& p, int b, int h, int j, int sub, int l0, int l1) {
+  const int G = p.group;
+  const int s0 = p.split_indptr[b], s1 = p.split_indptr[b + 1];
+  float mmax = neg_inf();
+  for (int l = l0; l < l1; ++l) {
+    const int g = p.req_level_group[l], prow = p.req_level_member[l] * G + j, m_eff = p.group_m_eff[g];
+    for (int c = p.group_chunk_indptr[g]; c < p.group_chunk_indptr[g + 1]; ++c)
+      mmax = fmaxf(mmax, __ldcg(p.lse_pre + p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow));
+  }
+  for (int s = s0; s < s1; ++s) mmax = fmaxf(mmax, __ldcg(p.lse_suf + (static_cast<int64_t>(s) * p.hkv + h) * G + j));
+  MergeAcc<D, LANES> a;
+  for (int l = l0; l < l1; ++l) {
+    const int g = p.req_level_group[l], prow = p.req_level_member[l] * G + j, m_eff = p.group_m_eff[g];
+    for (int c = p.group_chunk_indptr[g]; c < p.group_chunk_indptr[g + 1]; ++c)
+      a.add(p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow, p.o_pre, p.lse_pre, mmax, sub);
+  }
+  for (int s = s0; s < s1; ++s) a.add((static_cast<int64_t>(s) * p.hkv + h) * G + j, p.o_suf, p.lse_suf, mmax, sub);
+  a.store(p, b, h, j, sub, mmax);
+}
+
+// Warp-cooperative merge of rows j0 .. j0 + 32/LANES - 1 (those below G) of (b, h): LANES
+// lanes per row, each owning D/LANES consecutive elements, every row at once, and no
+// store before the last load, so that the loads of every part of every row can be in
+// flight together (a merge costs a few dependent global round trips, not a few per row).
+// LANES = 4 merges a whole (request, KV head) in one warp; more lanes per row use fewer
+// registers per lane.  A request with prefix partials from one group reads them through
+// req_group / req_member; one of nested groups (several levels) merges out of line.
+template <int D, int LANES>
+__device__ __forceinline__ void merge_rows(const StepParams& p, int b, int h, int j0, int lane) {
+  const int G = p.group;
+  const int j = j0 + lane / LANES;
+  const int sub = lane % LANES;
+  if (j >= G) return;
+  const int g = p.req_group[b];
+  const int l0 = p.req_level_indptr[b], l1 = p.req_level_indptr[b + 1];
+  if (l1 - l0 > 1) {
+    merge_rows_nested<D, LANES>(p, b, h, j, sub, l0, l1);
+    return;
+  }
+  int c0 = 0, c1 = 0, m_eff = 0, prow = 0;
+  if (g >= 0) {
+    c0 = p.group_chunk_indptr[g];
+    c1 = p.group_chunk_indptr[g + 1];
+    m_eff = p.group_m_eff[g];
+    prow = p.req_member[b] * G + j;
+  }
+  const int s0 = p.split_indptr[b], s1 = p.split_indptr[b + 1];
+  float mmax = neg_inf();
+  for (int c = c0; c < c1; ++c)
+    mmax = fmaxf(mmax, __ldcg(p.lse_pre + p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow));
+  for (int s = s0; s < s1; ++s) mmax = fmaxf(mmax, __ldcg(p.lse_suf + (static_cast<int64_t>(s) * p.hkv + h) * G + j));
+  MergeAcc<D, LANES> a;
+  for (int c = c0; c < c1; ++c) a.add(p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow, p.o_pre, p.lse_pre, mmax, sub);
+  for (int s = s0; s < s1; ++s) a.add((static_cast<int64_t>(s) * p.hkv + h) * G + j, p.o_suf, p.lse_suf, mmax, sub);
+  a.store(p, b, h, j, sub, mmax);
 }
 
 // Writes one row's final result directly (the row has exactly one partial).

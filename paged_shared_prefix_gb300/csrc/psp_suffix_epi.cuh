@@ -16,7 +16,7 @@ namespace dev {
 
 constexpr int kPreRows = 16;  // prefix partial rows (chunks x query heads) prefetched per single-split request
 
-// The split's descriptor: three 16-byte loads, all issued together.
+// The split's descriptor (its first 48 bytes): three 16-byte loads, all issued together.
 __device__ __forceinline__ SplitDesc load_split_desc(const StepParams& p, int split) {
   const int4* src = reinterpret_cast<const int4*>(p.split_desc + split);
   const int4 a = __ldg(src), b = __ldg(src + 1), c = __ldg(src + 2);
@@ -31,6 +31,7 @@ __device__ __forceinline__ SplitDesc load_split_desc(const StepParams& p, int sp
   d.one_split = b.w;
   d.prow = c.x;
   d.m_eff = c.y;
+  d.levels = c.z;
   return d;
 }
 
@@ -40,6 +41,7 @@ struct SuffixCta {
   int c0, n_chunks;  // b's shared-prefix chunks [c0, c0 + n_chunks)
   int prow, m_eff;   // b's first stacked prefix row and its group's stacked rows
   bool one_split;    // b has exactly one suffix split
+  bool one_level;    // b's prefix partials (if any) come from one group: c0 / prow / m_eff describe them
   bool solo;         // one suffix split and the prefix kernels complete before its rows are read
   bool pre_smem;     // solo, and the prefix rows fit the shared-memory prefetch area
   bool wait_prefix;  // dependent launch, sequential form: prefix rows only after the prefix grid
@@ -58,9 +60,10 @@ __device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, const Split
   c.prow = d.prow;
   c.m_eff = d.m_eff;
   c.one_split = d.one_split != 0;
+  c.one_level = d.levels <= 1;
   c.solo = !p.concurrent && c.one_split;
   c.late = false;
-  c.pre_smem = c.solo && c.n_chunks > 0 && c.n_chunks * p.group <= pre_rows;
+  c.pre_smem = c.solo && c.one_level && c.n_chunks > 0 && c.n_chunks * p.group <= pre_rows;
   c.wait_prefix = p.pdl && !p.concurrent;
   return c;
 }
@@ -80,7 +83,7 @@ __device__ __forceinline__ bool suffix_cta_late(const StepParams& p, SuffixCta& 
   __threadfence();  // the prefix partials were fenced before their rows were counted
   c.late = true;
   c.solo = true;
-  c.pre_smem = c.n_chunks * p.group <= pre_rows;
+  c.pre_smem = c.one_level && c.n_chunks * p.group <= pre_rows;
   return c.pre_smem;
 }
 

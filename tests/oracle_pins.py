@@ -381,7 +381,7 @@ def pin_validation(orc):
     rejects(dataclasses.replace(c, group_prefix_len=gl), -5)
 
 
-def _three_level_tables():
+def _three_level_tables(num_q_heads=4, num_kv_heads=2, head_dim=16):
     """Hand-built block tables of a three-level tree at page size 16 (ids fixed here, nothing
     generated): group 0 = 64 tokens (4 pages) shared by all six requests, group 1 = 256 tokens
     under it for requests 2-5, group 2 = 328 tokens under group 1 for requests 4 and 5 (20 full
@@ -396,8 +396,8 @@ def _three_level_tables():
     kv_len = np.array([64 + 20, 96 + 30, 256 + 16, 256 + 17, 328 + 28, 328 + 9], np.int32)
     for b, t in enumerate(tables):
         assert len(t) == -(-int(kv_len[b]) // ps)
-    base = workloads.make_case("agent", 0, batch=6, num_q_heads=4, num_kv_heads=2, head_dim=16,
-                               tables_only=True)
+    base = workloads.make_case("agent", 0, batch=6, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                               head_dim=head_dim, tables_only=True)
     return dataclasses.replace(
         base, page_size=ps, num_pages=100, kv_len=kv_len,
         page_indptr=np.concatenate([[0], np.cumsum([len(t) for t in tables])]).astype(np.int32),

@@ -92,7 +92,7 @@ def _lib_plan(case, threshold=0, num_sms=NUM_SMS, **read_once):
 PLAN_FIELDS = ["suffix_start", "suffix_len", "suffix_page_indptr", "suffix_page_indices",
                "split_indptr", "split_begin", "split_end", "group_shared_len", "group_page_indptr",
                "group_page_indices", "group_m_eff", "group_branch", "group_row_blocks",
-               "group_chunk_indptr", "chunk_begin", "chunk_end"]
+               "group_chunk_indptr", "chunk_begin", "chunk_end", "req_level_indptr", "req_level_group"]
 
 
 def _check_plan_matches_oracle(case, threshold=0, num_sms=NUM_SMS, **read_once):
@@ -197,10 +197,77 @@ def test_plan_multi_group_matches_oracle():
     assert list(ref["group_branch"]) == [2 if thr <= 28 else 1, 3, 2 if thr <= 24 else 1]
 
 
+def _nested_cases():
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from oracle_pins import _three_level_tables
+    out = [("three-level-ps16", _three_level_tables(head_dim=64))]
+    for ps in (1, 16, 64):
+        out.append((f"two-level-ps{ps}", workloads.make_case(
+            "agent", 7, batch=40, prefix_len=1500, private_range=(1, 300), page_size=ps, nested=(5, 700),
+            tables_only=True)))
+    out.append(("two-level-one-block", workloads.make_case(
+        "fp8_large", 2, batch=12, prefix_len=2048, private_range=(1, 64), nested=(1, 2048), tables_only=True)))
+    out.append(("two-level-empty-segments", workloads.make_case(
+        "agent", 3, batch=9, prefix_len=300, private_range=(1, 40), nested=(3, 0), tables_only=True)))
+    out.append(("two-level-short-root", workloads.make_case(
+        "agent", 5, batch=30, prefix_len=40, private_range=(1, 50), nested=(3, 1200), tables_only=True)))
+    return out
+
+
+@pytest.mark.parametrize("label,case", _nested_cases(), ids=[c[0] for c in _nested_cases()])
+def test_plan_nested_matches_oracle(label, case):
+    """Nested groups: the library's plan equals the oracle's field by field (levels included)
+    under the built-in read-once minimums, none, every group dense or cascade, and a small GPU."""
+    for thr, ro, sms in ((0, {}, NUM_SMS), (0, NO_MINIMUM, NUM_SMS), (1, NO_MINIMUM, NUM_SMS),
+                         (1 << 20, NO_MINIMUM, NUM_SMS), (0, NO_MINIMUM, 7),
+                         (0, dict(read_once_min_tokens=100, read_once_min_mib=-1), NUM_SMS)):
+        info, ref = _check_plan_matches_oracle(case, threshold=thr, num_sms=sms, **ro)
+        assert info["num_groups"] == case.num_groups
+
+
+def test_plan_all_roots_equals_no_parents():
+    """group_parent of all -1 plans exactly like no group_parent array."""
+    import dataclasses
+    case = _multi_group_case()
+    roots = dataclasses.replace(case, group_parent=np.full(case.num_groups, -1, np.int32))
+    for ro in ({}, NO_MINIMUM):
+        a, b = _lib_plan(case, **ro), _lib_plan(roots, **ro)
+        for f in PLAN_FIELDS:
+            assert np.array_equal(a.plan_query(f), b.plan_query(f)), f
+        a.close()
+        b.close()
+
+
+def test_nested_invalid_trees_rejected_like_the_oracle():
+    import dataclasses
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from oracle_pins import _three_level_tables
+    t = _three_level_tables(head_dim=64)
+    bad_cases = [
+        ("parent after child", dataclasses.replace(t, group_parent=np.array([-1, 0, 3, 0], np.int32)), -1),
+        ("own parent", dataclasses.replace(t, group_parent=np.array([-1, 1, 1, 0], np.int32)), -1),
+        ("parent below -1", dataclasses.replace(t, group_parent=np.array([-2, 0, 1, 0], np.int32)), -1),
+        ("child shorter than parent", dataclasses.replace(t, group_prefix_len=np.array([64, 128, 120, 96], np.int32)), -1),
+    ]
+    for b, idx, label in ((5, 5, "leaves group 1's segment"), (1, 2, "leaves the root pages"),
+                          (4, 17, "leaves group 2's own segment"), (2, 1, "first member of group 1 leaves the root"),
+                          (3, 10, "second member of group 1 leaves its segment")):
+        pi = t.page_indices.copy()
+        pi[t.page_indptr[b] + idx] = 99
+        bad_cases.append((f"request {b} {label}", dataclasses.replace(t, page_indices=pi), -5))
+    pi = t.page_indices.copy()
+    pi[t.page_indptr[5] + 6] = 1000       # out of range inside a shared page of a later member
+    bad_cases.append(("out of range in a nested shared page", dataclasses.replace(t, page_indices=pi), -3))
+    for label, case, code in bad_cases:
+        assert _status_of_plan(case) == code, label
+        assert _oracle_status(case) == code, label
+
+
 def _status_of_plan(case):
     step = psp.DecodeStep.for_case(case, num_sms=NUM_SMS)
-    b, keep = step.make_batch(case.kv_len, case.page_indptr, case.page_indices, case.prefix_group,
-                              case.group_prefix_len)
+    b, keep = step.make_case_batch(case)
     st = psp.psp_plan(step.handle, ctypes.byref(b))
     step.close()
     return st

@@ -1,0 +1,103 @@
+"""GPU parity for nested prefix groups (a tree of shared beginnings): each level's own
+segment is read once for every request below it, and a request merges the partials of
+every read-once level on its path with its suffix splits.  Compared with the fp64 oracle's
+plain attention over each request's block table, at the tolerances of the other parity
+tests; the launch forms and the token-flat lowering must agree bit for bit."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_util import TOL, max_err, run_case
+from oracle_pins import _three_level_tables
+
+pytestmark = pytest.mark.gpu
+
+NESTED = [
+    ("agent", dict(name="agent", batch=24, prefix_len=600, private_range=(1, 300), nested=(4, 500))),
+    ("agent-ps1", dict(name="agent", batch=10, prefix_len=300, private_range=(1, 200), nested=(3, 170),
+                       page_size=1)),
+    ("agent-ps64-unaligned", dict(name="agent", batch=14, prefix_len=700, private_range=(1, 260),
+                                  nested=(3, 650), page_size=64)),
+    ("fp8", dict(name="fp8_large", batch=16, prefix_len=1024, private_range=(1, 400), nested=(3, 600))),
+    ("fp8-d64", dict(name="fp8_large", batch=9, prefix_len=256, private_range=(1, 150), nested=(2, 300),
+                     head_dim=64)),
+    ("agent-d64-g8", dict(name="agent", batch=8, prefix_len=320, private_range=(1, 120), nested=(3, 200),
+                          head_dim=64, num_q_heads=64)),
+    ("fp32", dict(name="tiny", batch=7, prefix_len=100, private_range=(1, 90), nested=(3, 70))),
+    ("one-split-each", dict(name="agent", batch=20, prefix_len=512, private_range=(1, 1), nested=(4, 256))),
+    ("one-subgroup", dict(name="fp8_large", batch=6, prefix_len=300, private_range=(1, 500), nested=(1, 900))),
+]
+
+
+def _make(kw, seed=3):
+    kw = dict(kw)
+    return workloads.make_case(kw.pop("name"), seed, **kw)
+
+
+def _check(case, out):
+    ref_o, ref_lse = oracle.attend_all(case)
+    tol = TOL[case.workload.kv_dtype]
+    o, lse = out
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert max_err(o, ref_o) <= tol and max_err(lse, ref_lse) <= tol
+
+
+@pytest.mark.parametrize("label,kw", NESTED, ids=[c[0] for c in NESTED])
+@pytest.mark.parametrize("branch", ["dense", "cascade", "mixed"])
+def test_nested_matches_oracle(label, kw, branch):
+    case = _make(kw)
+    G = case.workload.num_q_heads // case.workload.num_kv_heads
+    # mixed: the root (every request) dense, the subgroups cascade
+    thr = {"dense": 1, "cascade": 1 << 20, "mixed": case.batch * G}[branch]
+    _check(case, run_case(case, threshold=thr))
+
+
+def test_nested_forms_and_lowering_bit_identical(monkeypatch):
+    """Sequential and concurrent dependent launches, the forked prefix stream and the
+    token-flat lowering give the same bits on nested groups (a one-split request of several
+    levels merges in its suffix CTA or through its counter)."""
+    for kw in (NESTED[0][1], NESTED[3][1], dict(NESTED[7][1], private_range=(1, 80))):
+        case = _make(kw, seed=8)
+        outs = []
+        for form in ("1", "2", "2"):
+            monkeypatch.setenv("PSP_PDL_FORM", form)
+            outs.append(run_case(case))
+        monkeypatch.delenv("PSP_PDL_FORM")
+        outs.append(run_case(case, token_flat=True))
+        outs.append(run_case(case, concurrent=True))
+        for o, l in outs[1:]:
+            assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1]), kw["name"]
+        _check(case, outs[0])
+
+
+def _with_pools(case, seed):
+    """The case with seeded random queries and a fully written bf16 pool."""
+    w = case.workload
+    n = case.num_pages * case.page_size
+    q = workloads._encode(workloads.normal_f32((case.batch, w.num_q_heads, w.head_dim), seed, 1), w.q_dtype)
+    k = workloads._encode(workloads.normal_f32((n, w.num_kv_heads, w.head_dim), seed, 2), w.kv_dtype)
+    v = workloads._encode(workloads.normal_f32((n, w.num_kv_heads, w.head_dim), seed, 3), w.kv_dtype)
+    shape = (case.num_pages, case.page_size, w.num_kv_heads, w.head_dim)
+    return dataclasses.replace(case, q=q, k_pool=k.reshape(shape), v_pool=v.reshape(shape))
+
+
+def test_three_levels_match_oracle():
+    """Hand-built three-level tree plus a side branch: requests merge one, two or three
+    levels; every branch mix, both launch forms."""
+    case = _with_pools(_three_level_tables(num_q_heads=8, num_kv_heads=2, head_dim=64), 12)
+    for thr in (1, 1 << 20, 16):
+        _check(case, run_case(case, threshold=thr))
+        _check(case, run_case(case, threshold=thr, concurrent=True))
+
+
+def test_nested_paged_levels_match_oracle():
+    """Built-in read-once minimums on a tree whose root segment is short: the root is paged
+    and so is every level below it (the plan is the plan without sharing); with a long root
+    and short subgroup segments only the root is read once."""
+    short_root = _make(dict(name="agent", batch=12, prefix_len=200, private_range=(1, 100), nested=(2, 2048)))
+    long_root = _make(dict(name="agent", batch=12, prefix_len=2048, private_range=(1, 100), nested=(3, 200)))
+    for case in (short_root, long_root):
+        _check(case, run_case(case, read_once=None))

@@ -181,8 +181,7 @@ def test_step_host_matches_run():
     o_dev = torch.empty((case.batch, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda:0")
     l_dev = torch.empty((case.batch, w.num_q_heads), dtype=torch.float32, device="cuda:0")
     q_dev = torch.empty_like(tens["q"])
-    batch, keep = step.make_batch(case.kv_len, case.page_indptr, case.page_indices, case.prefix_group,
-                                  case.group_prefix_len)
+    batch, keep = step.make_case_batch(case)
     dev = step.tensors(q_dev, tens["k_pool"], tens["v_pool"], o_dev, l_dev)
     step.step_host(batch, q_host, o_host, l_host, dev, ws)
     o = o_host.view(torch.bfloat16).float().double().numpy()
