@@ -99,6 +99,8 @@ def parse():
     ap.add_argument("--sweep-read-once", action="store_true",
                     help="time the read-once step against the per-request paged step over prefix length x "
                          "members x dtype and report the refit minimum of saved bytes")
+    ap.add_argument("--sweep-nested", action="store_true",
+                    help="nested prefix groups: both levels read once vs the root alone vs no sharing")
     ap.add_argument("--sweep-threshold", action="store_true",
                     help="time the dense and cascade prefix kernels over an M_eff sweep and report the refit threshold")
     return ap.parse_args()
@@ -445,14 +447,15 @@ class Runner:
 
 
 def measure_case(psp, runner, case, steps, warmup, *, threshold=0, token_flat=False, concurrent=False,
-                 comparator=True, clocks=None, tensors=None):
+                 comparator=True, clocks=None, tensors=None, read_once=None):
     """One workload: whole-step times, per-kernel times, plan facts and the per-request paged
     comparator (the same batch with every request reading its prefix through its own table)."""
     import torch
     dev, stream = runner.dev, runner.stream
     tens = tensors or to_device(case, dev)
     o, lse = make_outputs(case, dev)
-    step = psp.DecodeStep.for_case(case, dense_threshold=threshold, token_flat=token_flat, concurrent=concurrent)
+    step = psp.DecodeStep.for_case(case, dense_threshold=threshold, token_flat=token_flat, concurrent=concurrent,
+                                   **(read_once or {}))
     t_plan = []
     for _ in range(5):
         t0 = time.perf_counter()
@@ -546,6 +549,52 @@ def sweep_read_once(args):
     return 0
 
 
+def sweep_nested(args):
+    """Nested prefix groups ("Track C Document 10": a radix tree of shared beginnings; sharing
+    per user on top of what every user shares): 256 requests share a 4096-token root prefix,
+    and each block of 256 / n requests shares one more segment on top of it, then private
+    suffixes U[128, 1024].  Three plans of the same batch and pool: both levels read once
+    (nested groups), the root alone read once (each request reads its block's segment through
+    its own block table), and no sharing.  bf16 (32 / 8 heads) and e4m3 (64 / 8 heads)."""
+    import dataclasses
+
+    import torch
+
+    import paged_shared_prefix_gb300 as psp
+    dev = torch.device("cuda:0")
+    runner = Runner(dev, torch.cuda.current_stream(dev))
+    rows = []
+    for name in ("agent", "fp8_large"):
+        for n_sub, seg in ((4, 2048), (16, 2048), (16, 8192), (16, 512), (64, 1024)):
+            case = workloads.make_case(name, 17, batch=256, prefix_len=4096, private_range=(128, 1024),
+                                       nested=(n_sub, seg))
+            nested = measure_case(psp, runner, case, args.steps, args.warmup)
+            root = dataclasses.replace(case, prefix_group=np.zeros(case.batch, np.int32),
+                                       group_prefix_len=case.group_prefix_len[:1].copy(), group_parent=None)
+            alone = measure_case(psp, runner, root, args.steps, args.warmup, comparator=False,
+                                 tensors=nested["tens"])
+            # every segment read once, whatever the dispatcher's read-once minimums say
+            forced = measure_case(psp, runner, case, args.steps, args.warmup, comparator=False,
+                                  tensors=nested["tens"], read_once=dict(read_once_min_tokens=-1,
+                                                                         read_once_min_mib=-1))
+            rows.append({"workload": name, "kv_dtype": case.workload.kv_dtype, "batch": case.batch, "root": 4096,
+                         "subgroups": n_sub, "segment": seg, "unique_kv_bytes": nested["unique_bytes"],
+                         "nested_us": nested["ms"] * 1e3, "root_only_us": alone["ms"] * 1e3,
+                         "no_sharing_us": nested["paged_comparator"]["us_per_step"],
+                         "speedup_vs_root_only": alone["ms"] / nested["ms"],
+                         "speedup_vs_no_sharing": nested["paged_comparator"]["speedup_read_once"],
+                         "nested_gbs": nested["unique_bytes"] / (nested["ms"] * 1e-3) / 1e9,
+                         "branches": nested["info"]["branches"][:2], "kernels_us":
+                             {k: v * 1e3 for k, v in nested["kernels_ms"].items()},
+                         "all_read_once_us": forced["ms"] * 1e3, "all_read_once_branches": forced["info"]["branches"][:2],
+                         "all_read_once_kernels_us": {k: v * 1e3 for k, v in forced["kernels_ms"].items()}})
+            for r in (nested, alone, forced):
+                r["step"].close()
+            del nested, alone, forced
+    print(json.dumps({"sweep_nested": rows, "gpu": torch.cuda.get_device_name(0)}))
+    return 0
+
+
 def sweep_control(args):
     """Control study of page size and index contiguity on the suffix kernel ("The 25% Page-Size
     Slowdown That Wasn't", "When source beats intuition": FlashInfer decode moved -1.0..+1.3%
@@ -602,6 +651,8 @@ def main():
         return sweep_read_once(args)
     if args.sweep_control:
         return sweep_control(args)
+    if args.sweep_nested:
+        return sweep_nested(args)
 
     import torch
     import torch.distributed as dist

@@ -101,3 +101,22 @@ def test_nested_paged_levels_match_oracle():
     long_root = _make(dict(name="agent", batch=12, prefix_len=2048, private_range=(1, 100), nested=(3, 200)))
     for case in (short_root, long_root):
         _check(case, run_case(case, read_once=None))
+
+
+@pytest.mark.parametrize("name,n_sub,seg", [("fp8_large", 16, 2048), ("agent", 64, 1024)])
+def test_nested_full_size_sampled(name, n_sub, seg):
+    """The benchmark's nested batches (256 requests, 4096-token root, one segment per block,
+    suffixes U[128, 1024]) under the built-in dispatcher and with every level read once:
+    1,024 sampled rows plus the longest and shortest requests against the oracle."""
+    case = workloads.make_case(name, 17, batch=256, prefix_len=4096, private_range=(128, 1024),
+                               nested=(n_sub, seg))
+    w = case.workload
+    rng = np.random.default_rng(5)
+    bb = np.concatenate([rng.integers(0, case.batch, 1024), np.repeat([np.argmax(case.kv_len),
+                                                                       np.argmin(case.kv_len)], w.num_q_heads)])
+    hh = np.concatenate([rng.integers(0, w.num_q_heads, 1024), np.tile(np.arange(w.num_q_heads), 2)])
+    ref_o, ref_lse = oracle.attend(case, bb, hh)
+    tol = TOL[w.kv_dtype]
+    for read_once in (None, dict(read_once_min_tokens=-1, read_once_min_mib=-1)):
+        o, lse = run_case(case, read_once=read_once)
+        assert max_err(o[bb, hh], ref_o) <= tol and max_err(lse[bb, hh], ref_lse) <= tol
