@@ -72,7 +72,8 @@ struct HostPlan {
   std::vector<int32_t> suffix_page_indptr, suffix_page_indices, suffix_start, suffix_len;
   std::vector<int32_t> split_indptr, split_req, split_begin, split_end;
   std::vector<int32_t> split_desc;  // kSplitDescInts per split (psp::SplitDesc)
-  std::vector<int32_t> req_group, req_member, req_level_indptr, req_level_group, req_level_member, req_prefix_chunks;
+  std::vector<int32_t> req_group, req_member, req_level_indptr, req_level_group;
+  std::vector<int32_t> req_part_indptr, req_part;  // req_part: (first row + member x G, M_eff) pairs
   std::vector<int32_t> group_page_indptr, group_page_indices, group_m_eff, group_shared_len;
   std::vector<int32_t> group_branch, group_row_blocks;
   std::vector<int32_t> group_member_indptr, group_members, group_chunk_indptr;
@@ -91,7 +92,7 @@ struct HostPlan {
     for (std::vector<int32_t>* v :
          {&suffix_page_indptr, &suffix_page_indices, &suffix_start, &suffix_len, &split_indptr, &split_req,
           &split_begin, &split_end, &split_desc, &req_group, &req_member, &req_level_indptr, &req_level_group,
-          &req_level_member, &req_prefix_chunks, &group_page_indptr, &group_page_indices,
+          &req_part_indptr, &req_part, &group_page_indptr, &group_page_indices,
           &group_m_eff, &group_shared_len, &group_branch, &group_row_blocks, &group_member_indptr, &group_members,
           &group_chunk_indptr, &chunk_group, &chunk_begin, &chunk_end, &chunk_row_offset, &item_chunk_dense,
           &item_rb_dense, &item_chunk_cascade, &item_rb_cascade, &kv_indptr})
@@ -387,7 +388,7 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   // --- per request: the read-once groups on its path, outermost first (their prefix partials
   //     are merged in this order), and the suffix after the deepest of them
   P.req_level_indptr.assign(B + 1, 0);
-  P.req_prefix_chunks.assign(B, 0);
+  P.req_part_indptr.assign(B + 1, 0);
   P.suffix_page_indptr.assign(B + 1, 0);
   P.suffix_start.assign(B, 0);
   P.suffix_len.assign(B, 0);
@@ -398,13 +399,16 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
       const int a = chain_group[k];
       if (P.group_branch[a] != PSP_BRANCH_DENSE && P.group_branch[a] != PSP_BRANCH_CASCADE) continue;
       P.req_level_group.push_back(a);
-      P.req_level_member.push_back(chain_member[k]);
-      P.req_prefix_chunks[b] += P.group_chunk_indptr[a + 1] - P.group_chunk_indptr[a];
+      for (int32_t c = P.group_chunk_indptr[a]; c < P.group_chunk_indptr[a + 1]; ++c) {
+        P.req_part.push_back(P.chunk_row_offset[c] + chain_member[k] * G);
+        P.req_part.push_back(P.group_m_eff[a]);
+      }
       P.req_group[b] = a;
       P.req_member[b] = chain_member[k];
       n_sh = pages_of(a);
     }
     P.req_level_indptr[b + 1] = static_cast<int32_t>(P.req_level_group.size());
+    P.req_part_indptr[b + 1] = static_cast<int32_t>(P.req_part.size() / 2);
     P.suffix_start[b] = static_cast<int32_t>(n_sh * ps);
     P.suffix_len[b] = static_cast<int32_t>(bt->kv_len[b] - n_sh * ps);
     const int32_t* pages = bt->page_indices + bt->page_indptr[b];
@@ -436,19 +440,14 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   for (int32_t si = 0; si < P.NS; ++si) {
     psp::SplitDesc d{};
     const int32_t b = P.split_req[si];
-    const int32_t g = P.req_group[b];
     d.b = b;
     d.t0 = P.split_begin[si];
     d.t1 = P.split_end[si];
     d.list_paged = P.suffix_page_indptr[b];
     d.list_flat = P.kv_indptr[b] + P.suffix_start[b];
-    d.levels = P.req_level_indptr[b + 1] - P.req_level_indptr[b];
-    const bool one = d.levels == 1;  // a single level is described in place
-    d.c0 = one ? P.group_chunk_indptr[g] : 0;
-    d.n_chunks = P.req_prefix_chunks[b];
+    d.part0 = P.req_part_indptr[b];
+    d.n_parts = P.req_part_indptr[b + 1] - d.part0;
     d.one_split = P.split_indptr[b + 1] - P.split_indptr[b] == 1 ? 1 : 0;
-    d.prow = one ? P.req_member[b] * G : 0;
-    d.m_eff = one ? P.group_m_eff[g] : 0;
     for (int k = 0; k < psp::kDescPages; ++k) {
       const int64_t t = static_cast<int64_t>(d.t0) + 16 * k;
       d.first_page[k] = (ps >= 16 && t < d.t1) ? P.suffix_page_indices[d.list_paged + (t / ps)] : -1;
@@ -473,11 +472,8 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   place(L.split_end, n32(P.split_end));
   place(L.split_desc, n32(P.split_desc));
   place(L.req_group, n32(P.req_group));
-  place(L.req_member, n32(P.req_member));
-  place(L.req_level_indptr, n32(P.req_level_indptr));
-  place(L.req_level_group, n32(P.req_level_group));
-  place(L.req_level_member, n32(P.req_level_member));
-  place(L.req_prefix_chunks, n32(P.req_prefix_chunks));
+  place(L.req_part_indptr, n32(P.req_part_indptr));
+  place(L.req_part, n32(P.req_part));
   place(L.group_page_indptr, n32(P.group_page_indptr));
   place(L.group_page_indices, n32(P.group_page_indices));
   place(L.group_m_eff, n32(P.group_m_eff));
@@ -524,11 +520,8 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   put(L.split_end, P.split_end);
   put(L.split_desc, P.split_desc);
   put(L.req_group, P.req_group);
-  put(L.req_member, P.req_member);
-  put(L.req_level_indptr, P.req_level_indptr);
-  put(L.req_level_group, P.req_level_group);
-  put(L.req_level_member, P.req_level_member);
-  put(L.req_prefix_chunks, P.req_prefix_chunks);
+  put(L.req_part_indptr, P.req_part_indptr);
+  put(L.req_part, P.req_part);
   put(L.group_page_indptr, P.group_page_indptr);
   put(L.group_page_indices, P.group_page_indices);
   put(L.group_m_eff, P.group_m_eff);
@@ -642,11 +635,8 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.split_end = I(L.split_end);
   p.split_desc = reinterpret_cast<const psp::SplitDesc*>(I(L.split_desc));
   p.req_group = I(L.req_group);
-  p.req_member = I(L.req_member);
-  p.req_level_indptr = I(L.req_level_indptr);
-  p.req_level_group = I(L.req_level_group);
-  p.req_level_member = I(L.req_level_member);
-  p.req_prefix_chunks = I(L.req_prefix_chunks);
+  p.req_part_indptr = I(L.req_part_indptr);
+  p.req_part = reinterpret_cast<const int2*>(I(L.req_part));
   p.group_page_indptr = I(L.group_page_indptr);
   p.group_page_indices = I(L.group_page_indices);
   p.group_m_eff = I(L.group_m_eff);

@@ -35,13 +35,10 @@ struct SplitDesc {
   int32_t t0, t1;      // suffix tokens [t0, t1) of b
   int32_t list_paged;  // b's first entry in suffix_page_indices
   int32_t list_flat;   // b's first suffix entry in kv_indices (kv_indptr[b] + suffix_start[b])
-  int32_t c0;          // b's shared-prefix chunks [c0, c0 + n_chunks) (none: 0, 0); with several
-  int32_t n_chunks;    //   levels, c0 = 0 and n_chunks = the chunks of all of them
+  int32_t part0;       // b's prefix parts [part0, part0 + n_parts) of req_part (none: 0, 0)
+  int32_t n_parts;
   int32_t one_split;   // 1: b has exactly one suffix split
-  int32_t prow;        // b's first stacked prefix row (member index x G); 0 with several levels
-  int32_t m_eff;       // stacked rows of b's group (0 without a prefix branch or with several levels)
-  int32_t levels;      // read-once prefix levels b merges (nested groups: more than one)
-  int32_t pad[5];
+  int32_t pad[8];
   // page size >= 16: the page of 16-token sub-tile s (tokens t0 + 16s ..) for s < kDescPages,
   // -1 past t1, so that a CTA's first copies need no block-table load; unused below 16
   int32_t first_page[16];
@@ -82,11 +79,10 @@ struct StepParams {
   const int32_t* split_end;            // [S]
   const SplitDesc* split_desc;         // [S]
   const int32_t* req_group;            // [B] deepest read-once group of b, else -1
-  const int32_t* req_member;           // [B] index of b among that group's members
-  const int32_t* req_level_indptr;     // [B+1] b's read-once groups, outermost first:
-  const int32_t* req_level_group;      //   req_level_group / req_level_member [indptr[b], indptr[b+1])
-  const int32_t* req_level_member;
-  const int32_t* req_prefix_chunks;    // [B] prefix chunks over all of b's levels
+  const int32_t* req_part_indptr;      // [B+1] b's prefix parts: one per chunk of each read-once
+  const int2* req_part;                //   group of b, outermost first; .x = the chunk's first partial
+                                       //   row + b's member index x G, .y = the group's M_eff, so that
+                                       //   query head j of KV head h is row .x + h * .y + j
   const int32_t* group_page_indptr;    // [NG+1]
   const int32_t* group_page_indices;
   const int32_t* group_m_eff;          // [NG]
@@ -121,7 +117,7 @@ struct StepParams {
 struct PlanLayout {
   size_t suffix_page_indptr, suffix_page_indices, suffix_start, suffix_len;
   size_t split_indptr, split_req, split_begin, split_end, split_desc;
-  size_t req_group, req_member, req_level_indptr, req_level_group, req_level_member, req_prefix_chunks;
+  size_t req_group, req_part_indptr, req_part;
   size_t group_page_indptr, group_page_indices, group_m_eff, group_shared_len;
   size_t group_member_indptr, group_members, group_chunk_indptr;
   size_t chunk_group, chunk_begin, chunk_end, chunk_row_offset;

@@ -29,7 +29,7 @@ namespace dev {
 
 // Number of partial results (b, h) receives this step.
 __device__ __forceinline__ int expected_parts(const StepParams& p, int b) {
-  return p.req_prefix_chunks[b] + p.split_indptr[b + 1] - p.split_indptr[b];
+  return p.req_part_indptr[b + 1] - p.req_part_indptr[b] + p.split_indptr[b + 1] - p.split_indptr[b];
 }
 
 // One arrival on (b, h) after this CTA's partials for it are written and fenced.
@@ -96,63 +96,31 @@ struct MergeAcc {
   }
 };
 
-// merge_rows for a request of nested groups: one level per read-once group on its path,
-// outermost first, each with its own chunks, stacked rows and member index.  Out of line,
-// so that the single-level merge inlined into the kernels keeps its registers.
-template <int D, int LANES>
-__device__ __noinline__ void merge_rows_nested(const StepParams& p, int b, int h, int j, int sub, int l0, int l1) {
-  const int G = p.group;
-  const int s0 = p.split_indptr[b], s1 = p.split_indptr[b + 1];
-  float mmax = neg_inf();
-  for (int l = l0; l < l1; ++l) {
-    const int g = p.req_level_group[l], prow = p.req_level_member[l] * G + j, m_eff = p.group_m_eff[g];
-    for (int c = p.group_chunk_indptr[g]; c < p.group_chunk_indptr[g + 1]; ++c)
-      mmax = fmaxf(mmax, __ldcg(p.lse_pre + p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow));
-  }
-  for (int s = s0; s < s1; ++s) mmax = fmaxf(mmax, __ldcg(p.lse_suf + (static_cast<int64_t>(s) * p.hkv + h) * G + j));
-  MergeAcc<D, LANES> a;
-  for (int l = l0; l < l1; ++l) {
-    const int g = p.req_level_group[l], prow = p.req_level_member[l] * G + j, m_eff = p.group_m_eff[g];
-    for (int c = p.group_chunk_indptr[g]; c < p.group_chunk_indptr[g + 1]; ++c)
-      a.add(p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow, p.o_pre, p.lse_pre, mmax, sub);
-  }
-  for (int s = s0; s < s1; ++s) a.add((static_cast<int64_t>(s) * p.hkv + h) * G + j, p.o_suf, p.lse_suf, mmax, sub);
-  a.store(p, b, h, j, sub, mmax);
-}
-
 // Warp-cooperative merge of rows j0 .. j0 + 32/LANES - 1 (those below G) of (b, h): LANES
 // lanes per row, each owning D/LANES consecutive elements, every row at once, and no
 // store before the last load, so that the loads of every part of every row can be in
-// flight together (a merge costs a few dependent global round trips, not a few per row).
-// LANES = 4 merges a whole (request, KV head) in one warp; more lanes per row use fewer
-// registers per lane.  A request with prefix partials from one group reads them through
-// req_group / req_member; one of nested groups (several levels) merges out of line.
+// flight together (a merge costs a few dependent global round trips, not a few per row:
+// the request's part list, then its partial rows).  LANES = 4 merges a whole (request,
+// KV head) in one warp; more lanes per row use fewer registers per lane.  The prefix
+// parts come in plan order (chunks of each read-once group, the outermost group first),
+// then the suffix splits.
 template <int D, int LANES>
 __device__ __forceinline__ void merge_rows(const StepParams& p, int b, int h, int j0, int lane) {
   const int G = p.group;
   const int j = j0 + lane / LANES;
   const int sub = lane % LANES;
   if (j >= G) return;
-  const int g = p.req_group[b];
-  const int l0 = p.req_level_indptr[b], l1 = p.req_level_indptr[b + 1];
-  if (l1 - l0 > 1) {
-    merge_rows_nested<D, LANES>(p, b, h, j, sub, l0, l1);
-    return;
-  }
-  int c0 = 0, c1 = 0, m_eff = 0, prow = 0;
-  if (g >= 0) {
-    c0 = p.group_chunk_indptr[g];
-    c1 = p.group_chunk_indptr[g + 1];
-    m_eff = p.group_m_eff[g];
-    prow = p.req_member[b] * G + j;
-  }
+  const int q0 = p.req_part_indptr[b], q1 = p.req_part_indptr[b + 1];
   const int s0 = p.split_indptr[b], s1 = p.split_indptr[b + 1];
+  auto pre_row = [&](int q) {
+    const int2 part = __ldg(p.req_part + q);
+    return static_cast<int64_t>(part.x) + static_cast<int64_t>(h) * part.y + j;
+  };
   float mmax = neg_inf();
-  for (int c = c0; c < c1; ++c)
-    mmax = fmaxf(mmax, __ldcg(p.lse_pre + p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow));
+  for (int q = q0; q < q1; ++q) mmax = fmaxf(mmax, __ldcg(p.lse_pre + pre_row(q)));
   for (int s = s0; s < s1; ++s) mmax = fmaxf(mmax, __ldcg(p.lse_suf + (static_cast<int64_t>(s) * p.hkv + h) * G + j));
   MergeAcc<D, LANES> a;
-  for (int c = c0; c < c1; ++c) a.add(p.chunk_row_offset[c] + static_cast<int64_t>(h) * m_eff + prow, p.o_pre, p.lse_pre, mmax, sub);
+  for (int q = q0; q < q1; ++q) a.add(pre_row(q), p.o_pre, p.lse_pre, mmax, sub);
   for (int s = s0; s < s1; ++s) a.add((static_cast<int64_t>(s) * p.hkv + h) * G + j, p.o_suf, p.lse_suf, mmax, sub);
   a.store(p, b, h, j, sub, mmax);
 }

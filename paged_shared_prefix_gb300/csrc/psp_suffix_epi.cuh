@@ -16,32 +16,27 @@ namespace dev {
 
 constexpr int kPreRows = 16;  // prefix partial rows (chunks x query heads) prefetched per single-split request
 
-// The split's descriptor (its first 48 bytes): three 16-byte loads, all issued together.
+// The split's descriptor (its first 32 bytes): two 16-byte loads, issued together.
 __device__ __forceinline__ SplitDesc load_split_desc(const StepParams& p, int split) {
   const int4* src = reinterpret_cast<const int4*>(p.split_desc + split);
-  const int4 a = __ldg(src), b = __ldg(src + 1), c = __ldg(src + 2);
+  const int4 a = __ldg(src), b = __ldg(src + 1);
   SplitDesc d;
   d.b = a.x;
   d.t0 = a.y;
   d.t1 = a.z;
   d.list_paged = a.w;
   d.list_flat = b.x;
-  d.c0 = b.y;
-  d.n_chunks = b.z;
+  d.part0 = b.y;
+  d.n_parts = b.z;
   d.one_split = b.w;
-  d.prow = c.x;
-  d.m_eff = c.y;
-  d.levels = c.z;
   return d;
 }
 
 // What the end of a suffix CTA needs to know about its request.
 struct SuffixCta {
   int split, h, b;
-  int c0, n_chunks;  // b's shared-prefix chunks [c0, c0 + n_chunks)
-  int prow, m_eff;   // b's first stacked prefix row and its group's stacked rows
-  bool one_split;    // b has exactly one suffix split
-  bool one_level;    // b's prefix partials (if any) come from one group: c0 / prow / m_eff describe them
+  int part0, n_parts;  // b's prefix parts [part0, part0 + n_parts) (one per chunk of each read-once group)
+  bool one_split;      // b has exactly one suffix split
   bool solo;         // one suffix split and the prefix kernels complete before its rows are read
   bool pre_smem;     // solo, and the prefix rows fit the shared-memory prefetch area
   bool wait_prefix;  // dependent launch, sequential form: prefix rows only after the prefix grid
@@ -55,15 +50,12 @@ __device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, const Split
   c.split = split;
   c.h = h;
   c.b = d.b;
-  c.c0 = d.c0;
-  c.n_chunks = d.n_chunks;
-  c.prow = d.prow;
-  c.m_eff = d.m_eff;
+  c.part0 = d.part0;
+  c.n_parts = d.n_parts;
   c.one_split = d.one_split != 0;
-  c.one_level = d.levels <= 1;
   c.solo = !p.concurrent && c.one_split;
   c.late = false;
-  c.pre_smem = c.solo && c.one_level && c.n_chunks > 0 && c.n_chunks * p.group <= pre_rows;
+  c.pre_smem = c.solo && c.n_parts > 0 && c.n_parts * p.group <= pre_rows;
   c.wait_prefix = p.pdl && !p.concurrent;
   return c;
 }
@@ -74,7 +66,7 @@ __device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, const Split
 // once the CTA's first copies are in flight (the check is a round trip); returns true when
 // the caller should prefetch the prefix rows now.
 __device__ __forceinline__ bool suffix_cta_late(const StepParams& p, SuffixCta& c, int pre_rows = kPreRows) {
-  if (!(p.pdl && p.concurrent && c.one_split && c.n_chunks > 0)) return false;
+  if (!(p.pdl && p.concurrent && c.one_split && c.n_parts > 0)) return false;
   __shared__ int prefix_complete;
   if (threadIdx.x == 0)
     prefix_complete = *reinterpret_cast<volatile int32_t*>(p.prefix_done) == p.prefix_rows_total;
@@ -83,26 +75,25 @@ __device__ __forceinline__ bool suffix_cta_late(const StepParams& p, SuffixCta& 
   __threadfence();  // the prefix partials were fenced before their rows were counted
   c.late = true;
   c.solo = true;
-  c.pre_smem = c.one_level && c.n_chunks * p.group <= pre_rows;
+  c.pre_smem = c.n_parts * p.group <= pre_rows;
   return c.pre_smem;
 }
 
-// cp.async of b's prefix partial rows of head h into pre_o [chunk * G + j][D] and
-// pre_l [chunk * G + j], by NT threads numbered tid = 0 .. NT - 1 (the caller commits
+// cp.async of b's prefix partial rows of head h into pre_o [part * G + j][D] and
+// pre_l [part * G + j], by NT threads numbered tid = 0 .. NT - 1 (the caller commits
 // and waits).
 template <int D, int NT>
 __device__ __forceinline__ void prefetch_prefix_rows(const StepParams& p, const SuffixCta& c, float* pre_o,
                                                      float* pre_l, int tid = threadIdx.x) {
   const int G = p.group;
-  const int m_eff = c.m_eff;
-  const int prow = c.prow;
   constexpr int kRowChunks = D * 4 / 16;
-  for (int e = tid; e < c.n_chunks * G * (kRowChunks + 1); e += NT) {
+  for (int e = tid; e < c.n_parts * G * (kRowChunks + 1); e += NT) {
     const int ch = e / (G * (kRowChunks + 1));
     const int rem = e - ch * G * (kRowChunks + 1);
     const int j = rem / (kRowChunks + 1);
     const int q = rem - j * (kRowChunks + 1);
-    const int64_t row = p.chunk_row_offset[c.c0 + ch] + static_cast<int64_t>(c.h) * m_eff + prow + j;
+    const int2 part = __ldg(p.req_part + c.part0 + ch);
+    const int64_t row = static_cast<int64_t>(part.x) + static_cast<int64_t>(c.h) * part.y + j;
     if (q < kRowChunks) {
       cp_async_16(smem_u32(pre_o + (ch * G + j) * D + q * 4), p.o_pre + row * D + q * 4, true);
     } else {
@@ -127,13 +118,13 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
   const int G = p.group;
   const int b = c.b, h = c.h;
   const bool one_split = c.one_split;
-  const bool only_part = one_split && c.n_chunks == 0;
+  const bool only_part = one_split && c.n_parts == 0;
   const bool direct = only_part || (c.solo && c.pre_smem);
   // Launched as a dependent of a still running prefix kernel: a one-split request whose
   // prefix partials are all complete (every prefix row counted done) merges them here like
   // a solo request; otherwise its part goes through the (request, KV head) counter.
   bool ready = c.late;
-  if (!c.late && p.pdl && p.concurrent && one_split && c.n_chunks > 0) {
+  if (!c.late && p.pdl && p.concurrent && one_split && c.n_parts > 0) {
     __shared__ int prefix_ready;
     if (threadIdx.x == 0) prefix_ready = *reinterpret_cast<volatile int32_t*>(p.prefix_done) == p.prefix_rows_total;
     __syncthreads();
@@ -154,7 +145,7 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
   // be written, then the parts weighted by 2^(lse - max), summed by fmaf in the fixed order,
   // times 1 / sum), so a row's result does not depend on which CTA merges it.
   __shared__ float s_coef[NSTATE * 8];  // [warp state][row]
-  __shared__ float s_cpre[kPreRows];    // [chunk * G + row]: 2^(lse_chunk - max)
+  __shared__ float s_cpre[kPreRows];    // [part * G + row]: 2^(lse_part - max)
   __shared__ float s_own[8], s_inv[8], s_lse[8];
   if (threadIdx.x < G) {
     const int g = threadIdx.x;
@@ -174,10 +165,10 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
     const float lse_own = mmax + log2f(sum);
     if (direct) {
       float big = neg_inf();
-      for (int ch = 0; ch < c.n_chunks; ++ch) big = fmaxf(big, pre_l[ch * G + g]);
+      for (int ch = 0; ch < c.n_parts; ++ch) big = fmaxf(big, pre_l[ch * G + g]);
       big = fmaxf(big, lse_own);
       float wsum = 0.f;
-      for (int ch = 0; ch < c.n_chunks; ++ch) {
+      for (int ch = 0; ch < c.n_parts; ++ch) {
         const float w = exp2f(pre_l[ch * G + g] - big);
         s_cpre[ch * G + g] = w;
         wsum += w;
@@ -209,7 +200,7 @@ __device__ __forceinline__ void suffix_finish(const StepParams& p, const SuffixC
       add(os, s_coef[w * 8 + g], *reinterpret_cast<const float4*>(red + (w * 8 + g) * D + d));
     if (direct) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int ch = 0; ch < c.n_chunks; ++ch)
+      for (int ch = 0; ch < c.n_parts; ++ch)
         add(acc, s_cpre[ch * G + g], *reinterpret_cast<const float4*>(pre_o + (ch * G + g) * D + d));
       add(acc, s_own[g], os);
       const float inv = s_inv[g];
