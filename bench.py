@@ -60,12 +60,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # M_eff 4096, e4m3 cache); the other workloads are measured beside it in the same process
 HEADLINE = "fp8_large"
 PER_CONFIG = ("llama8b_noshare", "agent", "short_prefix")
+# each kernel's translation unit and the headers it compiles (a recorded DRAM traffic figure
+# counts only while all of them are unchanged)
 KERNEL_SOURCES = {
-    "suffix_splitkv": "paged_shared_prefix_gb300/csrc/kernel_suffix.cu",
-    "prefix_cascade": "paged_shared_prefix_gb300/csrc/kernel_prefix_cascade.cu",
-    "prefix_dense": "paged_shared_prefix_gb300/csrc/kernel_prefix_dense.cu",
-    "expand_kv_indices": "paged_shared_prefix_gb300/csrc/kernel_merge.cu",
+    "suffix_splitkv": ("kernel_suffix.cu", "psp_suffix_epi.cuh", "psp_merge.cuh", "psp_device.cuh", "psp_internal.h"),
+    "prefix_cascade": ("kernel_prefix_cascade.cu", "psp_merge.cuh", "psp_device.cuh", "psp_internal.h"),
+    "prefix_dense": ("kernel_prefix_dense.cu", "psp_sm100.cuh", "psp_merge.cuh", "psp_device.cuh", "psp_internal.h"),
+    "expand_kv_indices": ("kernel_merge.cu", "psp_sm100.cuh", "psp_device.cuh", "psp_internal.h"),
 }
+CSRC = "paged_shared_prefix_gb300/csrc"
 
 
 def parse():
@@ -123,12 +126,16 @@ def describe(case) -> str:
             f"{case.num_pages} pages ({case.layout})")
 
 
-def src_hash(rel: str) -> str:
+def src_hash(files) -> str:
+    """First 16 hex digits of the SHA-256 of the named csrc files' bytes, in order."""
+    h = hashlib.sha256()
     try:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            return hashlib.sha256(f.read()).hexdigest()[:16]
+        for name in files:
+            with open(os.path.join(ROOT, CSRC, name), "rb") as f:
+                h.update(f.read())
     except OSError:
         return ""
+    return h.hexdigest()[:16] if files else ""
 
 
 def recorded_traffic(kernel: str, workload: str):
@@ -140,7 +147,7 @@ def recorded_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     ent = table.get(f"{kernel}@{workload}")
-    if not ent or ent.get("source_sha256_16") != src_hash(KERNEL_SOURCES.get(kernel, "")):
+    if not ent or ent.get("source_sha256_16") != src_hash(KERNEL_SOURCES.get(kernel, ())):
         return None
     return ent.get("dram_bytes_per_launch")
 
