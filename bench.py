@@ -104,6 +104,8 @@ def parse():
                          "members x dtype and report the refit minimum of saved bytes")
     ap.add_argument("--sweep-nested", action="store_true",
                     help="nested prefix groups: both levels read once vs the root alone vs no sharing")
+    ap.add_argument("--sweep-nested-read-once", action="store_true",
+                    help="nested segments read once or through each block table, over blocks x segment length")
     ap.add_argument("--sweep-threshold", action="store_true",
                     help="time the dense and cascade prefix kernels over an M_eff sweep and report the refit threshold")
     return ap.parse_args()
@@ -602,6 +604,44 @@ def sweep_nested(args):
     return 0
 
 
+def sweep_nested_read_once(args):
+    """Read-once choice for nested segments: 256 requests under a 4096-token root read once, n
+    blocks each sharing an S-token segment, suffixes U[128, 1024]; the step with every segment
+    read once against the same batch with the segments read through each request's block table
+    (the root alone shared), over n x S and both caches.  Reports the bytes a segment saves when
+    read once, (members - 1) x S x bytes per token, and the speedup."""
+    import dataclasses
+
+    import torch
+
+    import paged_shared_prefix_gb300 as psp
+    dev = torch.device("cuda:0")
+    runner = Runner(dev, torch.cuda.current_stream(dev))
+    rows = []
+    always = dict(read_once_min_tokens=-1, read_once_min_mib=-1)
+    for name in ("agent", "fp8_large"):
+        for n_sub in (4, 16, 64):
+            for seg in (256, 512, 1024, 2048, 4096):
+                case = workloads.make_case(name, 19, batch=256, prefix_len=4096, private_range=(128, 1024),
+                                           nested=(n_sub, seg))
+                once = measure_case(psp, runner, case, args.steps, args.warmup, comparator=False, read_once=always)
+                root = dataclasses.replace(case, prefix_group=np.zeros(case.batch, np.int32),
+                                           group_prefix_len=case.group_prefix_len[:1].copy(), group_parent=None)
+                paged = measure_case(psp, runner, root, args.steps, args.warmup, comparator=False,
+                                     tensors=once["tens"], read_once=always)
+                members = case.batch // n_sub
+                rows.append({"workload": name, "kv_dtype": case.workload.kv_dtype, "subgroups": n_sub, "segment": seg,
+                             "members": members, "m_eff": members * (case.workload.num_q_heads // 8),
+                             "saved_bytes": (members - 1) * seg * case.kv_token_bytes(),
+                             "read_once_us": once["ms"] * 1e3, "paged_us": paged["ms"] * 1e3,
+                             "speedup": paged["ms"] / once["ms"]})
+                for r in (once, paged):
+                    r["step"].close()
+                del once, paged
+    print(json.dumps({"sweep_nested_read_once": rows, "gpu": torch.cuda.get_device_name(0)}))
+    return 0
+
+
 def sweep_control(args):
     """Control study of page size and index contiguity on the suffix kernel ("The 25% Page-Size
     Slowdown That Wasn't", "When source beats intuition": FlashInfer decode moved -1.0..+1.3%
@@ -660,6 +700,8 @@ def main():
         return sweep_control(args)
     if args.sweep_nested:
         return sweep_nested(args)
+    if args.sweep_nested_read_once:
+        return sweep_nested_read_once(args)
 
     import torch
     import torch.distributed as dist
