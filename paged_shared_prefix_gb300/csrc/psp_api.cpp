@@ -448,9 +448,11 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
     d.part0 = P.req_part_indptr[b];
     d.n_parts = P.req_part_indptr[b + 1] - d.part0;
     d.one_split = P.split_indptr[b + 1] - P.split_indptr[b] == 1 ? 1 : 0;
+    const int32_t* spages = P.suffix_page_indices.data() + d.list_paged;
+    const int shift = h->page_shift;  // page_size == 1 << shift: no division per entry
     for (int k = 0; k < psp::kDescPages; ++k) {
-      const int64_t t = static_cast<int64_t>(d.t0) + 16 * k;
-      d.first_page[k] = (ps >= 16 && t < d.t1) ? P.suffix_page_indices[d.list_paged + (t / ps)] : -1;
+      const int32_t t = d.t0 + 16 * k;
+      d.first_page[k] = (ps >= 16 && t < d.t1) ? spages[t >> shift] : -1;
     }
     std::memcpy(P.split_desc.data() + static_cast<size_t>(si) * psp::kSplitDescInts, &d, sizeof(d));
   }
