@@ -482,6 +482,27 @@ def pin_nested_prefix(orc):
             so, sl = sdpa_rows(c, b)
             assert np.max(np.abs(full[0] - so)) <= 1e-12 and np.max(np.abs(full[1] - sl)) <= 1e-12
 
+    # random trees (up to six groups, zero-length segments, requests outside any group): every
+    # token covered once, a member's levels are the read-once groups on its path in order, and
+    # full attention over the paged layout equals torch SDPA on the contiguous logical rows
+    for seed in range(4):
+        spec = workloads.random_tree_spec(seed)
+        c = workloads.make_tree_case("agent", seed, page_size=16, num_q_heads=4, num_kv_heads=2, head_dim=16,
+                                     **spec)
+        p = orc.plan(c, dict(params, tile_tokens=16, prefix_min_tiles=1, split_min_tiles=1))
+        for b in range(c.batch):
+            assert np.all(_covered_once(p, b, c.kv_len[b]) == 1), (seed, b)
+            path, g = [], int(c.prefix_group[b])
+            while g >= 0:
+                path.insert(0, g)
+                g = int(c.group_parent[g])
+            levels = p["req_level_group"][p["req_level_indptr"][b]:p["req_level_indptr"][b + 1]].tolist()
+            assert levels == [a for a in path if p["group_branch"][a] in (1, 2)], (seed, b)
+        full = orc.attend_all(c)
+        for b in range(c.batch):
+            so, sl = sdpa_rows(c, b)
+            assert np.max(np.abs(full[0][b] - so)) <= 1e-12 and np.max(np.abs(full[1][b] - sl)) <= 1e-12
+
     def rejects(case, code):
         try:
             orc.plan(case, params)

@@ -226,6 +226,19 @@ def test_plan_nested_matches_oracle(label, case):
         assert info["num_groups"] == case.num_groups
 
 
+@pytest.mark.parametrize("ps", [1, 16, 64])
+def test_plan_random_trees_match_oracle(ps):
+    """Random trees of shared beginnings (up to six groups, zero-length segments, requests
+    outside any group): the library's plan equals the oracle's under several dispatcher
+    settings."""
+    for seed in range(12):
+        spec = workloads.random_tree_spec(100 + seed, batch=20, max_seg=600)
+        case = workloads.make_tree_case("agent", seed, page_size=ps, tables_only=True, **spec)
+        for thr, ro, sms in ((0, {}, NUM_SMS), (0, NO_MINIMUM, NUM_SMS), (40, NO_MINIMUM, 7),
+                             (0, dict(read_once_min_tokens=100, read_once_min_mib=-1), NUM_SMS)):
+            _check_plan_matches_oracle(case, threshold=thr, num_sms=sms, **ro)
+
+
 def test_plan_all_roots_equals_no_parents():
     """group_parent of all -1 plans exactly like no group_parent array."""
     import dataclasses

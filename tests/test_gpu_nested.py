@@ -120,3 +120,15 @@ def test_nested_full_size_sampled(name, n_sub, seg):
     for read_once in (None, dict(read_once_min_tokens=-1, read_once_min_mib=-1)):
         o, lse = run_case(case, read_once=read_once)
         assert max_err(o[bb, hh], ref_o) <= tol and max_err(lse[bb, hh], ref_lse) <= tol
+
+
+def test_random_trees_match_oracle():
+    """Random trees of shared beginnings on the GPU, cycling cache types, page sizes and
+    dispatcher thresholds, against the oracle."""
+    cells = [("agent", 16, 1), ("fp8_large", 16, 16), ("tiny", 16, 1 << 20), ("agent", 64, 40),
+             ("fp8_large", 1, 1), ("agent", 32, 1 << 20), ("fp8_large", 64, 64), ("agent", 16, 16)]
+    for i, (name, ps, thr) in enumerate(cells):
+        spec = workloads.random_tree_spec(200 + i, batch=14, max_seg=500)
+        heads = dict(num_q_heads=16, num_kv_heads=4) if name != "tiny" else {}
+        case = workloads.make_tree_case(name, i, page_size=ps, private_range=(1, 300), **heads, **spec)
+        _check(case, run_case(case, threshold=thr))

@@ -449,6 +449,103 @@ def _make_nested_case(name, seed, *, page_size, batch, prefix_len, private_range
                 k_scale, v_scale, group_parent=group_parent, **logical)
 
 
+def make_tree_case(name: str, seed: int, *, parents, seg_lens, request_groups, private_range=(1, 64),
+                   page_size: Optional[int] = None, num_q_heads: Optional[int] = None,
+                   num_kv_heads: Optional[int] = None, head_dim: Optional[int] = None,
+                   kv_dtype: Optional[str] = None, tables_only: bool = False) -> Case:
+    """A batch over an arbitrary tree of shared beginnings.  Group g (parents[g] = -1 or a lower
+    group) holds its parent's token sequence followed by seg_lens[g] tokens of its own, so
+    group_prefix_len[g] = P_parent + seg_lens[g]; request b belongs to group request_groups[b]
+    (-1: no group) and holds that group's sequence followed by U[private_range] tokens of its
+    own.  Pages follow block-aligned sharing: group g's floor(P_g / ps) pages are its parent's
+    floor(P_parent / ps) pages followed by pages of its own, stored once; every other token sits
+    in the request's own pages.  Logical K/V rows: each group's own tokens, then each request's."""
+    w = WORKLOADS[name]
+    w = dataclasses.replace(
+        w, batch=len(request_groups), num_q_heads=num_q_heads or w.num_q_heads,
+        num_kv_heads=num_kv_heads or w.num_kv_heads, head_dim=head_dim or w.head_dim,
+        kv_dtype=kv_dtype or w.kv_dtype, num_pages=None)
+    B, Hq, Hkv, d = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    ps = page_size or w.page_size
+    parents = np.asarray(parents, np.int32)
+    seg_lens = np.asarray(seg_lens, np.int64)
+    groups = np.asarray(request_groups, np.int32)
+    NG = parents.shape[0]
+    rng = np.random.default_rng([seed, 0, 11])
+    # token sequences (logical rows) of the groups, parents first
+    seq, pos = [], 0
+    for g in range(NG):
+        par = int(parents[g])
+        assert -1 <= par < g, "a parent is a lower group"
+        own = np.arange(pos, pos + int(seg_lens[g]), dtype=np.int64)
+        pos += int(seg_lens[g])
+        seq.append(np.concatenate([seq[par], own]) if par >= 0 else own)
+    plen = np.array([len(x) for x in seq], np.int32)
+    priv = rng.integers(private_range[0], private_range[1] + 1, size=B).astype(np.int64)
+    rows = []
+    for b in range(B):
+        g = int(groups[b])
+        base = seq[g] if g >= 0 else np.zeros(0, np.int64)
+        rows.append(np.concatenate([base, np.arange(pos, pos + int(priv[b]), dtype=np.int64)]))
+        pos += int(priv[b])
+    kv_len = np.array([len(r) for r in rows], np.int32)
+    # physical pages: each group's own shared pages once, then each request's own pages
+    n_sh = plen // ps
+    n_par = np.array([n_sh[p] if p >= 0 else 0 for p in parents], np.int64)
+    own_req = [(-(-int(kv_len[b]) // ps)) - (int(n_sh[groups[b]]) if groups[b] >= 0 else 0) for b in range(B)]
+    needed = int(np.sum(n_sh - n_par)) + int(sum(own_req))
+    n_pages = max(1, int(math.ceil(1.25 * needed)))
+    phys = np.random.default_rng([seed, ps, 12]).permutation(n_pages).astype(np.int64)
+    gpages, at = [], 0
+    for g in range(NG):
+        mine = phys[at:at + int(n_sh[g] - n_par[g])]
+        at += int(n_sh[g] - n_par[g])
+        gpages.append(np.concatenate([gpages[parents[g]], mine]) if parents[g] >= 0 else mine)
+    tables = []
+    for b in range(B):
+        g = int(groups[b])
+        shared = gpages[g] if g >= 0 else np.zeros(0, np.int64)
+        tables.append(np.concatenate([shared, phys[at:at + own_req[b]]]))
+        at += own_req[b]
+    page_indptr = np.zeros(B + 1, np.int32)
+    page_indptr[1:] = np.cumsum([len(t) for t in tables])
+    page_indices = np.concatenate(tables).astype(np.int32)
+    if tables_only:
+        return Case(w, seed, ps, n_pages, "scatter", kv_len, page_indptr, page_indices, groups, plen,
+                    None, None, None, None, None, group_parent=parents)
+    q = _encode(normal_f32((B, Hq, d), seed, 1), w.q_dtype)
+    k_log = normal_f32((pos, Hkv, d), seed, 2)
+    v_log = normal_f32((pos, Hkv, d), seed, 3)
+    k_scale = v_scale = None
+    if w.kv_dtype == "fp8_e4m3":
+        k_scale = (np.abs(k_log).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
+        v_scale = (np.abs(v_log).max(axis=(0, 2)) / np.float32(448.0)).astype(np.float32)
+    k_enc, v_enc = _encode(k_log, w.kv_dtype, k_scale), _encode(v_log, w.kv_dtype, v_scale)
+    elem = _np_dtype(w.kv_dtype)
+    k_pool = np.full((n_pages * ps, Hkv, d), _poison(w.kv_dtype), dtype=elem)
+    v_pool = np.full((n_pages * ps, Hkv, d), _poison(w.kv_dtype), dtype=elem)
+    for b in range(B):
+        t = np.arange(int(kv_len[b]))
+        slots = tables[b][t // ps] * ps + t % ps
+        k_pool[slots] = k_enc[rows[b]]
+        v_pool[slots] = v_enc[rows[b]]
+    return Case(w, seed, ps, n_pages, "scatter", kv_len, page_indptr, page_indices, groups, plen, q,
+                k_pool.reshape(n_pages, ps, Hkv, d), v_pool.reshape(n_pages, ps, Hkv, d), k_scale, v_scale,
+                k_logical=k_enc, v_logical=v_enc, logical_rows=rows, group_parent=parents)
+
+
+def random_tree_spec(seed: int, *, max_groups: int = 6, batch: int = 12, max_seg: int = 400) -> dict:
+    """A random tree for make_tree_case: up to max_groups groups, each the child of a random
+    earlier group (or a root), segment lengths U[0, max_seg] (a zero-length segment too), and
+    requests spread over the groups and no group."""
+    rng = np.random.default_rng([seed, 13])
+    ng = int(rng.integers(1, max_groups + 1))
+    parents = [-1] + [int(rng.integers(-1, g)) for g in range(1, ng)]
+    seg = [int(rng.integers(0, max_seg + 1)) if rng.random() > 0.1 else 0 for _ in range(ng)]
+    groups = [int(rng.integers(-1, ng)) for _ in range(batch)]
+    return dict(parents=parents, seg_lens=seg, request_groups=groups)
+
+
 def unique_kv_bytes(case: Case) -> int:
     """Distinct stored token slots a step must read, times K+V bytes per token.
 
