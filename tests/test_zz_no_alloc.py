@@ -36,11 +36,13 @@ NOALLOC_CASES = [
     ("agent", dict(batch=12, prefix_len=256, private_range=(1, 300)), dict(token_flat=True)),
     # the concurrent flag is ignored on this path (one stream, no side stream to create)
     ("fp8_large", dict(batch=8, prefix_len=320, private_range=(1, 200)), dict(token_flat=True, concurrent=True)),
+    # nested groups: per-request part lists in the scratch
+    ("agent", dict(batch=16, prefix_len=300, private_range=(1, 200), nested=(3, 260)), {}),
 ]
 
 
 @pytest.mark.parametrize("name,kw,flags", NOALLOC_CASES,
-                         ids=["agent", "fp8", "tiny", "agent-token-flat", "fp8-concurrent-token-flat"])
+                         ids=["agent", "fp8", "tiny", "agent-token-flat", "fp8-concurrent-token-flat", "agent-nested"])
 def test_noalloc_matches_workspace_run_twice(name, kw, flags):
     case = workloads.make_case(name, 3, **kw)
     ref_o, ref_lse = run_case(case, **flags)        # psp_run with a caller workspace
