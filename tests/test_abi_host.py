@@ -212,6 +212,10 @@ def _nested_cases():
         "agent", 3, batch=9, prefix_len=300, private_range=(1, 40), nested=(3, 0), tables_only=True)))
     out.append(("two-level-short-root", workloads.make_case(
         "agent", 5, batch=30, prefix_len=40, private_range=(1, 50), nested=(3, 1200), tables_only=True)))
+    # a chain of 24 levels, one request leaving at each level
+    out.append(("chain-24", workloads.make_tree_case(
+        "agent", 6, parents=[-1] + list(range(23)), seg_lens=[64 + 8 * g for g in range(24)],
+        request_groups=list(range(24)) + [-1, 23], page_size=16, tables_only=True)))
     return out
 
 
@@ -451,6 +455,16 @@ def test_plan_log_line_records_the_step():
     assert [g["m_eff"] for g in rec["groups"]] == want["m_eff"]
     assert [g["branch"] for g in rec["groups"]] == [names[b] for b in want["branch"]]
     assert {g["branch"] for g in rec["groups"]} == {"dense", "cascade"}
+    assert [g["parent"] for g in rec["groups"]] == [-1, -1, -1]
+    # a nested batch records each group's parent
+    code_nested = code.replace("case = _multi_group_case()",
+                               "case = workloads.make_case('agent', 2, batch=12, prefix_len=300, "
+                               "private_range=(1, 40), nested=(3, 200), tables_only=True)")
+    r = subprocess.run([sys.executable, "-c", code_nested], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    rec = json.loads([ln for ln in r.stderr.splitlines() if ln.startswith("psp_step ")][0][len("psp_step "):])
+    assert [g["parent"] for g in rec["groups"]] == [-1, 0, 0, 0]
+    assert [g["members"] for g in rec["groups"]] == [12, 4, 4, 4]
     # without the variable nothing is written
     r = subprocess.run([sys.executable, "-c", code], env={k: v for k, v in os.environ.items() if k != "PSP_LOG"},
                        capture_output=True, text=True, timeout=300)

@@ -132,3 +132,15 @@ def test_random_trees_match_oracle():
         heads = dict(num_q_heads=16, num_kv_heads=4) if name != "tiny" else {}
         case = workloads.make_tree_case(name, i, page_size=ps, private_range=(1, 300), **heads, **spec)
         _check(case, run_case(case, threshold=thr))
+
+
+def test_deep_chain_matches_oracle():
+    """A chain of 24 nested levels (one request leaving at each level, the last two at the
+    deepest): requests merge up to 24 levels of prefix partials with their suffix."""
+    case = workloads.make_tree_case("agent", 6, parents=[-1] + list(range(23)),
+                                    seg_lens=[64 + 8 * g for g in range(24)],
+                                    request_groups=list(range(24)) + [-1, 23], page_size=16,
+                                    num_q_heads=16, num_kv_heads=4, private_range=(1, 200))
+    for thr in (1, 1 << 20):
+        _check(case, run_case(case, threshold=thr))
+        _check(case, run_case(case, threshold=thr, concurrent=True))
