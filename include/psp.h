@@ -56,6 +56,11 @@
  *                           2 concurrent
  *   PSP_SUFFIX_STAGES       suffix ring depth per warp at d = 128 (default 2 for bf16,
  *                           3 for e4m3; once per process)
+ *   PSP_PLAN_THREADS        host threads (the calling one included, at most 16) that
+ *                           compare group members' shared pages in psp_plan when the batch
+ *                           lists at least 131072 page ids (default 8, never more than the
+ *                           host's hardware threads; 1 = the calling thread);
+ *                           the workers are made on first use and joined by psp_destroy
  *   PSP_LOG                 1: psp_plan writes one line per planned step to stderr,
  *                           "psp_step " and a JSON object: shapes and dtypes, page size,
  *                           block-table and kv_indices lengths, suffix and shared tokens,
@@ -272,8 +277,9 @@ PSP_API const char* psp_status_string(psp_status status);
  * UNSUPPORTED (a combination that is not built; nothing is coerced). */
 PSP_API psp_status psp_create(const psp_config* cfg, psp_handle** out);
 
-/* Frees the handle and its pinned staging.  Waits for nothing: the caller must
- * not destroy a handle whose upload is still in flight.  NULL is ignored. */
+/* Frees the handle, its pinned staging and its planning threads (joined).  Waits for no
+ * device work: the caller must not destroy a handle whose upload is still in flight.
+ * NULL is ignored. */
 PSP_API void psp_destroy(psp_handle* h);
 
 /* Description of the handle's last failure ("" if none; static to the handle). */

@@ -6,11 +6,16 @@
 
 #include <algorithm>
 #include <cmath>
+#include <condition_variable>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
+#include <memory>
+#include <mutex>
 #include <new>
 #include <string>
+#include <thread>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -66,6 +71,66 @@ int dtype_bytes(int32_t t) {
   }
   return 0;
 }
+
+// A few host threads for the plan's comparisons of members' shared pages in large batches
+// (made on first use, joined when the handle is destroyed).  run(parts, f) calls f(0) on the
+// calling thread and f(1) .. f(parts - 1) on the workers and returns when every call has.
+class HostPool {
+ public:
+  explicit HostPool(int workers) {
+    for (int i = 0; i < workers; ++i) threads_.emplace_back([this, i] { loop(i + 1); });
+  }
+  ~HostPool() {
+    {
+      std::lock_guard<std::mutex> g(m_);
+      stop_ = true;
+    }
+    cv_.notify_all();
+    for (std::thread& t : threads_) t.join();
+  }
+  int size() const { return static_cast<int>(threads_.size()) + 1; }
+  void run(int parts, const std::function<void(int)>& f) {
+    parts = std::max(1, std::min(parts, size()));
+    {
+      std::lock_guard<std::mutex> g(m_);
+      job_ = &f;
+      parts_ = parts;
+      pending_ = parts - 1;
+      ++gen_;
+    }
+    if (parts > 1) cv_.notify_all();
+    f(0);
+    std::unique_lock<std::mutex> l(m_);
+    done_.wait(l, [&] { return pending_ == 0; });
+    job_ = nullptr;
+  }
+
+ private:
+  void loop(int id) {
+    uint64_t seen = 0;
+    for (;;) {
+      const std::function<void(int)>* job = nullptr;
+      {
+        std::unique_lock<std::mutex> l(m_);
+        cv_.wait(l, [&] { return stop_ || gen_ != seen; });
+        if (stop_) return;
+        seen = gen_;
+        if (id >= parts_) continue;  // not part of this run (a run waits for all of its parts)
+        job = job_;
+      }
+      (*job)(id);
+      std::lock_guard<std::mutex> g(m_);
+      if (--pending_ == 0) done_.notify_one();
+    }
+  }
+  std::vector<std::thread> threads_;
+  std::mutex m_;
+  std::condition_variable cv_, done_;
+  const std::function<void(int)>* job_ = nullptr;
+  int parts_ = 0, pending_ = 0;
+  uint64_t gen_ = 0;
+  bool stop_ = false;
+};
 
 struct HostPlan {
   int32_t B = 0, NG = 0, NS = 0, NC = 0;
@@ -133,6 +198,8 @@ struct psp_handle {
   bool allow_concurrent = true;   // false on the workspace-free path (no object creation)
   int32_t pdl_form = 0;           // dependent-launch form: 0 by grid size, 1 sequential, 2 concurrent
   bool log = false;               // PSP_LOG: one structured line per plan on stderr
+  int32_t plan_threads = 1;       // PSP_PLAN_THREADS: threads comparing shared pages in large plans
+  std::unique_ptr<HostPool> pool; // its workers (made on first use)
 
   // per-kernel timing
   bool timing = false;
@@ -291,29 +358,56 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   // every member lists its group's shared pages: against the first request of its own group
   // over the whole prefix (that request's pages were range-checked in full), and against the
   // first member of every group on its path over that group's own segment (needed only where
-  // the first member is not the first request of the group itself)
-  for (int b = 0; b < B; ++b) {
-    const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
-    if (g < 0) continue;
-    const int32_t* mine = bt->page_indices + bt->page_indptr[b];
-    bool same = true;
-    const int64_t n_sh = pages_of(g);
-    if (b != lead[g] && n_sh > 0)
-      same = std::memcmp(mine, bt->page_indices + bt->page_indptr[lead[g]], static_cast<size_t>(n_sh) * sizeof(int32_t)) == 0;
-    for (int a = g; same && a >= 0; a = parent_of(a)) {
-      const int rep = P.group_members[P.group_member_indptr[a]];
-      if (rep == b || (a == g && rep == lead[g])) continue;
-      const int64_t lo = pages_of(parent_of(a)), hi = pages_of(a);
-      if (hi > lo)
-        same = std::memcmp(mine + lo, bt->page_indices + bt->page_indptr[rep] + lo,
-                           static_cast<size_t>(hi - lo) * sizeof(int32_t)) == 0;
+  // the first member is not the first request of the group itself).  Large batches split the
+  // requests over a few host threads; the first mismatching request in request order is the
+  // one reported either way.
+  auto first_mismatch = [&](int b0, int b1) {
+    for (int b = b0; b < b1; ++b) {
+      const int g = bt->prefix_group ? bt->prefix_group[b] : -1;
+      if (g < 0) continue;
+      const int32_t* mine = bt->page_indices + bt->page_indptr[b];
+      bool same = true;
+      const int64_t n_sh = pages_of(g);
+      if (b != lead[g] && n_sh > 0)
+        same = std::memcmp(mine, bt->page_indices + bt->page_indptr[lead[g]], static_cast<size_t>(n_sh) * sizeof(int32_t)) == 0;
+      for (int a = g; same && a >= 0; a = parent_of(a)) {
+        const int rep = P.group_members[P.group_member_indptr[a]];
+        if (rep == b || (a == g && rep == lead[g])) continue;
+        const int64_t lo = pages_of(parent_of(a)), hi = pages_of(a);
+        if (hi > lo)
+          same = std::memcmp(mine + lo, bt->page_indices + bt->page_indptr[rep] + lo,
+                             static_cast<size_t>(hi - lo) * sizeof(int32_t)) == 0;
+      }
+      if (!same) return b;
     }
-    if (!same) {
-      const psp_status range = full_range_check(h, bt);
-      if (range) return range;
-      return fail(h, PSP_ERR_PREFIX_MISMATCH,
-                  "request " + std::to_string(b) + " does not share the prefix pages of its group");
+    return -1;
+  };
+  int bad = -1;
+  const int64_t compared = chain_len > 0 ? static_cast<int64_t>(bt->page_indptr[B]) : 0;  // bounds the pages compared
+  const int parts = compared >= (int64_t{1} << 17) ? std::min<int>(h->plan_threads, B) : 1;
+  if (parts > 1 && !h->pool) {
+    try {
+      h->pool.reset(new HostPool(parts - 1));
+    } catch (...) {  // no threads to be had: compare on the calling thread
+      h->plan_threads = 1;
     }
+  }
+  if (parts > 1 && h->pool) {
+    const int n = std::min(parts, h->pool->size());
+    std::vector<int> found(n, -1);
+    const std::function<void(int)> part = [&](int i) {
+      found[i] = first_mismatch(static_cast<int>(static_cast<int64_t>(B) * i / n),
+                                static_cast<int>(static_cast<int64_t>(B) * (i + 1) / n));
+    };
+    h->pool->run(n, part);
+    for (int i = 0; i < n && bad < 0; ++i) bad = found[i];
+  } else {
+    bad = first_mismatch(0, B);
+  }
+  if (bad >= 0) {
+    const psp_status range = full_range_check(h, bt);
+    if (range) return range;
+    return fail(h, PSP_ERR_PREFIX_MISMATCH, "request " + std::to_string(bad) + " does not share the prefix pages of its group");
   }
 
   // --- per group: M_eff, the branch of its own segment, shared pages, row blocks, chunks
@@ -748,6 +842,10 @@ psp_status psp_create(const psp_config* cfg, psp_handle** out) {
   h->prefix_ctas_per_sm = env_int("PSP_PREFIX_CTAS_PER_SM", kPrefixCtasPerSm);
   h->pdl_form = env_int("PSP_PDL_FORM", 0);
   h->log = env_int("PSP_LOG", 0) > 0;
+  {
+    const int hw = std::max(1, static_cast<int>(std::thread::hardware_concurrency()));
+    h->plan_threads = std::max(1, std::min({16, hw, env_int("PSP_PLAN_THREADS", 8)}));
+  }
   if (c.dense_threshold == 0) {
     const int t = env_int("PSP_DENSE_THRESHOLD", 0);
     if (t > 0) h->cfg.dense_threshold = t;

@@ -338,6 +338,29 @@ def test_invalid_batches_rejected_like_the_oracle():
         assert _oracle_status(case) == code, label
 
 
+@pytest.mark.parametrize("threads", ["1", "3", "8"])
+def test_large_batch_mismatch_found_with_planning_threads(threads, monkeypatch):
+    """A batch large enough for the threaded page comparison: the plan equals the oracle's,
+    and a member that leaves its group's pages is reported (the first in request order, as
+    the error names it) however many threads compare."""
+    import dataclasses
+    monkeypatch.setenv("PSP_PLAN_THREADS", threads)
+    case = workloads.make_case("fp8_large", 1, batch=256, prefix_len=8192, private_range=(1, 64), tables_only=True)
+    assert case.page_indptr[-1] >= 1 << 17
+    _check_plan_matches_oracle(case)
+    for bad_bs in ([250], [77, 200], [3, 130, 254]):
+        pi = case.page_indices.copy()
+        for b in bad_bs:
+            pi[case.page_indptr[b] + 100] = case.num_pages - 1 - b
+        bad = dataclasses.replace(case, page_indices=pi)
+        step = psp.DecodeStep.for_case(bad, num_sms=NUM_SMS)
+        b, keep = step.make_case_batch(bad)
+        assert psp.psp_plan(step.handle, ctypes.byref(b)) == -5
+        assert f"request {bad_bs[0]} " in psp.psp_last_error(step.handle).decode()
+        step.close()
+        assert _oracle_status(bad) == -5
+
+
 def test_calls_before_plan_report_no_plan():
     step = psp.DecodeStep(8, 2, 64, "f32", "f32", "f32", 16, 64, num_sms=NUM_SMS)
     n = ctypes.c_size_t(0)
