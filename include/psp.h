@@ -56,6 +56,11 @@
  *                           2 concurrent
  *   PSP_SUFFIX_STAGES       suffix ring depth per warp at d = 128 (default 2 for bf16,
  *                           3 for e4m3; once per process)
+ *   PSP_NUM_SMS             SM count the partition is sized for when psp_config.num_sms
+ *                           is 0 (reproducible partitions across GPUs); unset or 0 = the
+ *                           current device's count
+ *   PSP_NVTX                1: psp_plan, psp_upload, psp_run and each kernel launch are named
+ *                           NVTX ranges (for a profiler's timeline); default 0
  *   PSP_PLAN_THREADS        host threads (the calling one included, at most 16) that
  *                           compare group members' shared pages in psp_plan when the batch
  *                           lists at least 131072 page ids (default 8, never more than the
@@ -145,7 +150,8 @@ typedef struct psp_config {
   int32_t o_dtype;
   int32_t page_size;       /* tokens per physical page */
   int32_t num_pages;       /* pages in the K pool (and the V pool) */
-  int32_t num_sms;         /* SMs the partition is sized for; 0 = current device's count */
+  int32_t num_sms;         /* SMs the partition is sized for; 0 = PSP_NUM_SMS if set, else the
+                              current device's count */
   int32_t dense_threshold; /* M_eff at or above which a group takes the dense branch;
                               0 = the built-in value measured on GB300 */
   int32_t flags;           /* PSP_FLAG_* */

@@ -19,6 +19,7 @@
 #include <vector>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "psp_internal.h"
 
@@ -171,6 +172,17 @@ struct HostPlan {
 
 }  // namespace
 
+// A named NVTX range over a scope when enabled (one push and one pop; nothing otherwise).
+struct NvtxRange {
+  bool on;
+  NvtxRange(bool enable, const char* name) : on(enable) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtxRangePop();
+  }
+};
+
 struct psp_handle {
   psp_config cfg{};
   int32_t group = 1;
@@ -199,6 +211,8 @@ struct psp_handle {
   int32_t pdl_form = 0;           // dependent-launch form: 0 by grid size, 1 sequential, 2 concurrent
   bool log = false;               // PSP_LOG: one structured line per plan on stderr
   int32_t plan_threads = 1;       // PSP_PLAN_THREADS: threads comparing shared pages in large plans
+  int32_t env_num_sms = 0;        // PSP_NUM_SMS: SM count used when cfg.num_sms is 0 (0 = query the device)
+  bool nvtx = false;              // PSP_NVTX: name psp_plan, psp_upload, psp_run and each launch as NVTX ranges
   std::unique_ptr<HostPool> pool; // its workers (made on first use)
 
   // per-kernel timing
@@ -842,6 +856,8 @@ psp_status psp_create(const psp_config* cfg, psp_handle** out) {
   h->prefix_ctas_per_sm = env_int("PSP_PREFIX_CTAS_PER_SM", kPrefixCtasPerSm);
   h->pdl_form = env_int("PSP_PDL_FORM", 0);
   h->log = env_int("PSP_LOG", 0) > 0;
+  h->env_num_sms = std::max(0, env_int("PSP_NUM_SMS", 0));
+  h->nvtx = env_int("PSP_NVTX", 0) > 0;
   {
     const int hw = std::max(1, static_cast<int>(std::thread::hardware_concurrency()));
     h->plan_threads = std::max(1, std::min({16, hw, env_int("PSP_PLAN_THREADS", 8)}));
@@ -923,9 +939,12 @@ psp_status psp_plan(psp_handle* h, const psp_batch* batch) {
   if (!h) return PSP_ERR_INVALID_ARGUMENT;
   h->planned = false;
   h->uploaded = false;
+  NvtxRange range(h->nvtx, "psp_plan");
   if (h->num_sms_resolved == 0) {
     if (h->cfg.num_sms > 0) {
       h->num_sms_resolved = h->cfg.num_sms;
+    } else if (h->env_num_sms > 0) {
+      h->num_sms_resolved = h->env_num_sms;
     } else {
       int dev = 0, n = 0;
       cudaError_t e = cudaGetDevice(&dev);
@@ -977,6 +996,7 @@ psp_status psp_plan_query(const psp_handle* h, int32_t field, void* dst, size_t 
 
 psp_status psp_upload(psp_handle* h, void* workspace, size_t workspace_bytes, void* stream) {
   if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  NvtxRange range(h->nvtx, "psp_upload");
   if (!h->planned) return fail(h, PSP_ERR_NO_PLAN, "psp_upload before psp_plan");
   const HostPlan& P = h->plan;
   const PlanLayout& L = P.layout;
@@ -1048,7 +1068,10 @@ static psp_status timed_launch(psp_handle* h, cudaStream_t s, const char* name, 
     e = cudaEventRecord(h->events[2 * slot], s);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventRecord");
   }
-  e = fn(p, n, s);
+  {
+    NvtxRange range(h->nvtx, name);
+    e = fn(p, n, s);
+  }
   if (e != cudaSuccess) return cuda_fail(h, e, name);
   if (h->timing) {
     e = cudaEventRecord(h->events[2 * slot + 1], s);
@@ -1065,6 +1088,7 @@ static cudaError_t expand_entry(const StepParams& p, int, cudaStream_t s) {
 
 psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
   if (!h) return PSP_ERR_INVALID_ARGUMENT;
+  NvtxRange range(h->nvtx, "psp_run");
   if (!h->planned || !h->uploaded) return fail(h, PSP_ERR_NO_PLAN, "psp_run needs psp_plan and psp_upload first");
   const psp_status bad = check_tensors(h, t);
   if (bad) return bad;

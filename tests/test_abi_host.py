@@ -361,6 +361,36 @@ def test_large_batch_mismatch_found_with_planning_threads(threads, monkeypatch):
         assert _oracle_status(bad) == -5
 
 
+def test_sm_count_override_and_nvtx_ranges():
+    """PSP_NUM_SMS sizes the partition when the configuration leaves num_sms at 0 (no device
+    is queried: this host has none), and PSP_NVTX=1 plans the same step with its NVTX ranges."""
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path[:0] = [%r, %r]\n"
+        "import json, workloads, paged_shared_prefix_gb300 as psp\n"
+        "case = workloads.make_case('agent', 3, batch=20, prefix_len=1024, private_range=(1, 300), tables_only=True)\n"
+        "step = psp.DecodeStep.for_case(case, num_sms=0)\n"
+        "step.plan_case(case)\n"
+        "print(json.dumps({'info': step.plan_info(), 'split': step.plan_query('split_end').tolist()}))\n"
+        % (here, os.path.dirname(here)))
+    outs = []
+    for extra in ({"PSP_NUM_SMS": "37"}, {"PSP_NUM_SMS": "37", "PSP_NVTX": "1"}):
+        env = dict(os.environ, **extra)
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs.append(r.stdout.strip().splitlines()[-1])
+    import json
+    got = json.loads(outs[0])
+    assert got["info"]["num_sms"] == 37
+    assert outs[0] == outs[1]
+    case = workloads.make_case("agent", 3, batch=20, prefix_len=1024, private_range=(1, 300), tables_only=True)
+    step = _lib_plan(case, num_sms=37)
+    assert step.plan_query("split_end").tolist() == got["split"]
+    step.close()
+
+
 def test_calls_before_plan_report_no_plan():
     step = psp.DecodeStep(8, 2, 64, "f32", "f32", "f32", 16, 64, num_sms=NUM_SMS)
     n = ctypes.c_size_t(0)

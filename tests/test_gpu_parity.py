@@ -424,3 +424,40 @@ def test_paged_branch_equals_the_plan_without_the_group():
         s.plan_case(c)
         assert list(s.plan_query("group_branch")) == [psp.BRANCH_DENSE]
         s.close()
+
+
+def test_outputs_and_workspace_guard_bands():
+    """Canary words before and after O, LSE and the workspace stay untouched by a step (nested
+    groups, e4m3 and bf16, both launch forms, the token-flat lowering): no kernel writes
+    outside its buffers."""
+    from gpu_util import device_tensors
+    for name, kw, flags in (("fp8_large", dict(batch=12, prefix_len=700, private_range=(1, 400), nested=(3, 300)), {}),
+                            ("agent", dict(batch=10, prefix_len=520, private_range=(1, 300)), dict(token_flat=True)),
+                            ("agent", dict(batch=10, prefix_len=520, private_range=(1, 300)), dict(concurrent=True))):
+        case = workloads.make_case(name, 9, **kw)
+        w = case.workload
+        tens = device_tensors(case)
+        step = psp.DecodeStep.for_case(case, **flags, read_once_min_tokens=-1, read_once_min_mib=-1)
+        step.plan_case(case)
+        guard = 4096  # bytes on each side (a multiple of 256, so alignment is kept)
+        nws = step.workspace_size()
+        ws_all = torch.full((nws + 2 * guard,), 0x5A, dtype=torch.uint8, device="cuda:0")
+        ws = ws_all[guard:guard + nws]
+        step.upload(ws)
+        n_o = case.batch * w.num_q_heads * w.head_dim
+        o_all = torch.full((n_o + 2 * guard // 2,), -7.0, dtype=torch.bfloat16, device="cuda:0")
+        o = o_all[guard // 2:guard // 2 + n_o].view(case.batch, w.num_q_heads, w.head_dim)
+        n_l = case.batch * w.num_q_heads
+        l_all = torch.full((n_l + 2 * guard // 4,), -7.0, dtype=torch.float32, device="cuda:0")
+        lse = l_all[guard // 4:guard // 4 + n_l].view(case.batch, w.num_q_heads)
+        step.run(tens["q"], tens["k_pool"], tens["v_pool"], o, lse, tens["k_scale"], tens["v_scale"])
+        torch.cuda.synchronize()
+        assert step.device_status() == 0
+        assert bool((ws_all[:guard] == 0x5A).all()) and bool((ws_all[guard + nws:] == 0x5A).all()), name
+        assert bool((o_all[:guard // 2] == -7.0).all()) and bool((o_all[guard // 2 + n_o:] == -7.0).all()), name
+        assert bool((l_all[:guard // 4] == -7.0).all()) and bool((l_all[guard // 4 + n_l:] == -7.0).all()), name
+        ref_o, ref_lse = oracle.attend_all(case)
+        tol = TOL[w.kv_dtype]
+        assert max_err(o.float().cpu().double().numpy(), ref_o) <= tol
+        assert max_err(lse.cpu().double().numpy(), ref_lse) <= tol
+        step.close()
