@@ -391,6 +391,24 @@ def test_sm_count_override_and_nvtx_ranges():
     step.close()
 
 
+def test_sizes_past_int32_are_refused():
+    """Contexts whose lengths sum past 2^31 - 1 tokens are refused before anything is planned
+    (the token-flat offsets are int32), and so is a pool of more than 2^31 - 1 slots."""
+    ps, L, B = 1024, (1 << 30) + 5, 2          # 2 x (2^30 + 5) tokens > 2^31 - 1
+    n = -(-L // ps)
+    step = psp.DecodeStep(1, 1, 64, "bf16", "bf16", "bf16", ps, n, num_sms=NUM_SMS)
+    ok = step.make_batch(np.array([L], np.int32), np.array([0, n], np.int32), np.arange(n, dtype=np.int32))[0]
+    assert psp.psp_plan(step.handle, ctypes.byref(ok)) == 0
+    kv = np.array([L] * B, np.int32)
+    indptr = np.array([0, n, 2 * n], np.int32)
+    pages = np.concatenate([np.arange(n), np.arange(n)]).astype(np.int32)
+    b, keep = step.make_batch(kv, indptr, pages)
+    assert psp.psp_plan(step.handle, ctypes.byref(b)) == -1
+    assert "int32" in psp.psp_last_error(step.handle).decode()
+    step.close()
+    assert _create_status(page_size=1024, num_pages=(1 << 21) + 1) == -1   # 2^31 + 1024 slots
+
+
 def test_calls_before_plan_report_no_plan():
     step = psp.DecodeStep(8, 2, 64, "f32", "f32", "f32", 16, 64, num_sms=NUM_SMS)
     n = ctypes.c_size_t(0)
