@@ -397,7 +397,7 @@ def test_sizes_past_int32_are_refused():
     ps, L, B = 1024, (1 << 30) + 5, 2          # 2 x (2^30 + 5) tokens > 2^31 - 1
     n = -(-L // ps)
     step = psp.DecodeStep(1, 1, 64, "bf16", "bf16", "bf16", ps, n, num_sms=NUM_SMS)
-    ok = step.make_batch(np.array([L], np.int32), np.array([0, n], np.int32), np.arange(n, dtype=np.int32))[0]
+    ok, keep1 = step.make_batch(np.array([L], np.int32), np.array([0, n], np.int32), np.arange(n, dtype=np.int32))
     assert psp.psp_plan(step.handle, ctypes.byref(ok)) == 0
     kv = np.array([L] * B, np.int32)
     indptr = np.array([0, n, 2 * n], np.int32)
