@@ -125,18 +125,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   dev::pdl_launch_dependents();  // the step's suffix kernel may start filling free SMs
   const int h = blockIdx.x % p.hkv;  // KV head fastest (neighbouring heads' rows are adjacent)
   const int item = blockIdx.x / p.hkv;
-  const int ci = p.item_chunk_dense[item];
-  const int rb = p.item_rb_dense[item];  // 256-row block
-  const int g = p.chunk_group[ci];
-  const int t0 = p.chunk_begin[ci];
-  const int t1 = p.chunk_end[ci];
+  // the work item's record: two 16-byte loads, issued together
+  const int4 da = __ldg(reinterpret_cast<const int4*>(p.item_desc_dense + item));
+  const int4 db = __ldg(reinterpret_cast<const int4*>(p.item_desc_dense + item) + 1);
+  const int rb = da.y;  // 256-row block
+  const int t0 = da.z;
+  const int t1 = da.w;
   const int n_tiles = (t1 - t0 + kTok - 1) / kTok;
   const int G = p.group;
-  const int m_eff = p.group_m_eff[g];
+  const int m_eff = db.x;
   const int row_base = rb * 2 * kRows;
   const int n_rows = min(2 * kRows, m_eff - row_base);
   const bool tile_b = n_rows > kRows;  // tile B holds live rows
-  const int32_t* members = p.group_members + p.group_member_indptr[g];
+  const int32_t* members = p.group_members + db.y;
+  const int list_base = db.z;    // the group's block list, or its first member's kv_indices
+  const int row_offset = db.w;   // the chunk's first prefix-partial row
   int32_t* status = p.status;
 
   if (threadIdx.x == 0) {
@@ -175,10 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* list;
       int shift;
       if (p.token_flat) {
-        list = p.kv_indices + p.kv_indptr[members[0]];
+        list = p.kv_indices + list_base;
         shift = 0;
       } else {
-        list = p.group_page_indices + p.group_page_indptr[g];
+        list = p.group_page_indices + list_base;
         shift = p.page_shift;
       }
       if (lane == 0) {
@@ -548,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* stage = reinterpret_cast<float*>(gbase + C::kOffQ + t * C::kQBytes + wq * 4096);  // [32][32]
       const int row0 = row_base + t * kRows + wq * 32;  // block row of lane 0
       const int live_rows = min(32, m_eff - row0);
-      const int64_t grow0 = p.chunk_row_offset[ci] + static_cast<int64_t>(h) * m_eff + row0;
+      const int64_t grow0 = row_offset + static_cast<int64_t>(h) * m_eff + row0;
       const float inv = out_scale / l;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {

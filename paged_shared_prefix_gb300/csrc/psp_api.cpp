@@ -145,6 +145,7 @@ struct HostPlan {
   std::vector<int32_t> group_member_indptr, group_members, group_chunk_indptr;
   std::vector<int32_t> chunk_group, chunk_begin, chunk_end, chunk_row_offset;
   std::vector<int32_t> item_chunk_dense, item_rb_dense, item_chunk_cascade, item_rb_cascade;
+  std::vector<int32_t> item_desc_dense;  // 8 ints per dense item (psp::DenseItemDesc)
   std::vector<int32_t> kv_indptr;
   int64_t kv_indices_len = 0, suffix_tokens = 0, shared_tokens = 0, pre_rows = 0;
   PlanLayout layout{};
@@ -161,7 +162,7 @@ struct HostPlan {
           &req_part_indptr, &req_part, &group_page_indptr, &group_page_indices,
           &group_m_eff, &group_shared_len, &group_branch, &group_row_blocks, &group_member_indptr, &group_members,
           &group_chunk_indptr, &chunk_group, &chunk_begin, &chunk_end, &chunk_row_offset, &item_chunk_dense,
-          &item_rb_dense, &item_chunk_cascade, &item_rb_cascade, &kv_indptr})
+          &item_rb_dense, &item_chunk_cascade, &item_rb_cascade, &kv_indptr, &item_desc_dense})
       v->clear();
     kv_indices_len = suffix_tokens = shared_tokens = pre_rows = 0;
     layout = PlanLayout{};
@@ -528,6 +529,23 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   }
   P.kv_indices_len = P.kv_indptr[B];
 
+  // --- one record per dense work item (its chunk, group, token range and list bases)
+  P.item_desc_dense.assign(P.item_chunk_dense.size() * 8, 0);
+  for (size_t it = 0; it < P.item_chunk_dense.size(); ++it) {
+    const int32_t ci = P.item_chunk_dense[it], g = P.chunk_group[ci];
+    const int32_t mb = P.group_member_indptr[g];
+    psp::DenseItemDesc d{};
+    d.chunk = ci;
+    d.rb = P.item_rb_dense[it];
+    d.t0 = P.chunk_begin[ci];
+    d.t1 = P.chunk_end[ci];
+    d.m_eff = P.group_m_eff[g];
+    d.member_base = mb;
+    d.list_base = (c.flags & PSP_FLAG_TOKEN_FLAT) ? P.kv_indptr[P.group_members[mb]] : P.group_page_indptr[g];
+    d.row_offset = P.chunk_row_offset[ci];
+    std::memcpy(P.item_desc_dense.data() + it * 8, &d, sizeof(d));
+  }
+
   // --- split-KV partition of the suffixes (token units, page-size independent)
   int64_t granules = 0;
   for (int b = 0; b < B; ++b) granules += cdiv(P.suffix_len[b], tile);
@@ -595,6 +613,7 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   place(L.chunk_begin, n32(P.chunk_begin));
   place(L.chunk_end, n32(P.chunk_end));
   place(L.chunk_row_offset, n32(P.chunk_row_offset));
+  place(L.item_desc_dense, n32(P.item_desc_dense));
   place(L.item_chunk_dense, n32(P.item_chunk_dense));
   place(L.item_rb_dense, n32(P.item_rb_dense));
   place(L.item_chunk_cascade, n32(P.item_chunk_cascade));
@@ -643,6 +662,7 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
   put(L.chunk_begin, P.chunk_begin);
   put(L.chunk_end, P.chunk_end);
   put(L.chunk_row_offset, P.chunk_row_offset);
+  put(L.item_desc_dense, P.item_desc_dense);
   put(L.item_chunk_dense, P.item_chunk_dense);
   put(L.item_rb_dense, P.item_rb_dense);
   put(L.item_chunk_cascade, P.item_chunk_cascade);
@@ -758,6 +778,7 @@ StepParams make_params(const psp_handle* h, const psp_tensors* t) {
   p.chunk_begin = I(L.chunk_begin);
   p.chunk_end = I(L.chunk_end);
   p.chunk_row_offset = I(L.chunk_row_offset);
+  p.item_desc_dense = reinterpret_cast<const psp::DenseItemDesc*>(I(L.item_desc_dense));
   p.item_chunk_dense = I(L.item_chunk_dense);
   p.item_rb_dense = I(L.item_rb_dense);
   p.item_chunk_cascade = I(L.item_chunk_cascade);

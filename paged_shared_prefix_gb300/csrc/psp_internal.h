@@ -47,6 +47,20 @@ constexpr int kDescPages = 16;
 static_assert(sizeof(SplitDesc) == 128, "one 128-byte record per split");
 constexpr int kSplitDescInts = static_cast<int>(sizeof(SplitDesc) / sizeof(int32_t));
 
+// Everything a dense prefix CTA needs about its work item in one 32-byte record (two 16-byte
+// loads), so that its member list and block list are one dependent load away, not four.
+struct DenseItemDesc {
+  int32_t chunk;       // prefix chunk
+  int32_t rb;          // 256-row block of the chunk's group
+  int32_t t0, t1;      // the chunk's context tokens [t0, t1)
+  int32_t m_eff;       // stacked rows of the group
+  int32_t member_base; // the group's first entry in group_members
+  int32_t list_base;   // the group's first entry in group_page_indices, or (token-flat) its first
+                       // member's first entry in kv_indices
+  int32_t row_offset;  // chunk_row_offset of the chunk
+};
+static_assert(sizeof(DenseItemDesc) == 32, "one 32-byte record per dense item");
+
 struct StepParams {
   // configuration
   int32_t batch;
@@ -94,6 +108,7 @@ struct StepParams {
   const int32_t* chunk_begin;          // [NC] context tokens (the group's own segment)
   const int32_t* chunk_end;            // [NC]
   const int32_t* chunk_row_offset;     // [NC] first prefix-partial row of the chunk
+  const DenseItemDesc* item_desc_dense;  // dense prefix work items, one record each
   const int32_t* item_chunk_dense;     // dense prefix work items: (chunk, row block)
   const int32_t* item_rb_dense;
   const int32_t* item_chunk_cascade;   // cascade prefix work items
@@ -121,7 +136,7 @@ struct PlanLayout {
   size_t group_page_indptr, group_page_indices, group_m_eff, group_shared_len;
   size_t group_member_indptr, group_members, group_chunk_indptr;
   size_t chunk_group, chunk_begin, chunk_end, chunk_row_offset;
-  size_t item_chunk_dense, item_rb_dense, item_chunk_cascade, item_rb_cascade;
+  size_t item_desc_dense, item_chunk_dense, item_rb_dense, item_chunk_cascade, item_rb_cascade;
   size_t kv_indptr;
   size_t plan_bytes;       // end of the uploaded integer region
   size_t status;
