@@ -25,7 +25,8 @@ the other kernels' (roofline_other), the per-request paged comparator (every
 request reading the prefix through its own block table) and the read-once
 speedup over it, the oracle's CPU baseline, the end-to-end figure through
 psp_step_host with host buffers (plan, plan upload, query copy in, output copy
-out, every step), sampled SM clocks, the launch count, a bare read of the same
+out, every step), the same per-step work as a serving loop that plans the next
+step while the device runs the current one (e2e_pipelined), sampled SM clocks, the launch count, a bare read of the same
 byte count for context (read_ceiling) and per_config.
 
 --impl reference times the fp64 CPU oracle (the reference arm of this path)
@@ -507,6 +508,69 @@ def measure_case(psp, runner, case, steps, warmup, *, threshold=0, token_flat=Fa
     return res
 
 
+def e2e_pipelined(psp, step, case, tens, ws, stream, steps, warmup):
+    """Serving loop through the C ABI with host buffers: every step copies its queries in from
+    pinned memory, plans (psp_plan), uploads the plan (psp_upload), runs (psp_run) and copies
+    its output and LSE back into pinned memory.  The host plans step i + 1 while the device
+    runs step i and waits for step i's output one step later; queries and outputs are
+    double-buffered on the device and the two copy directions run on streams of their own.
+    L2 is not flushed: the step's K/V bytes are several times the L2 size.  Returns
+    (seconds per step, H2D bytes per step, D2H bytes per step)."""
+    import torch
+    w = case.workload
+    dev = tens["k"].device
+    qh = torch.from_numpy(np.ascontiguousarray(case.q).view(np.int16 if w.q_dtype == "bf16" else np.float32))
+    qh = qh.pin_memory()
+    qd, od, ld, oh, lh = [], [], [], [], []
+    for _ in range(2):
+        qd.append(torch.empty_like(tens["q"]))
+        o, lse = make_outputs(case, dev)
+        od.append(o)
+        ld.append(lse)
+        oh.append(torch.empty(o.shape, dtype=torch.int16 if w.o_dtype == "bf16" else torch.float32).pin_memory())
+        lh.append(torch.empty(lse.shape, dtype=torch.float32).pin_memory())
+    batch, keep = step.make_case_batch(case)
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ring = 4
+    ev_q = [torch.cuda.Event() for _ in range(ring)]
+    ev_run = [torch.cuda.Event() for _ in range(ring)]
+    ev_o = [torch.cuda.Event() for _ in range(ring)]
+
+    def one(i):
+        k = i % 2
+        with torch.cuda.stream(h2d):
+            if i >= 2:
+                h2d.wait_event(ev_run[(i - 2) % ring])   # step i - 2 has read this query buffer
+            qd[k].view(qh.dtype).copy_(qh, non_blocking=True)
+            ev_q[i % ring].record(h2d)
+        step.plan_batch(batch)
+        step.upload(ws, stream)
+        stream.wait_event(ev_q[i % ring])
+        step.run(qd[k], tens["k"], tens["v"], od[k], ld[k], tens["ks"], tens["vs"], stream)
+        ev_run[i % ring].record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev_run[i % ring])
+            oh[k].copy_(od[k].view(oh[k].dtype), non_blocking=True)
+            lh[k].copy_(ld[k], non_blocking=True)
+            ev_o[i % ring].record(d2h)
+        if i >= 1:
+            ev_o[(i - 1) % ring].synchronize()           # step i - 1's output is on the host
+
+    for i in range(max(3, warmup)):
+        one(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    torch.cuda.synchronize()
+    per_step = (time.perf_counter() - t0) / steps
+    plan_bytes = sum(int(step.plan_query(f).nbytes) for f in psp.FIELDS)
+    h2d_bytes = int(qh.numel() * qh.element_size()) + plan_bytes
+    d2h_bytes = int(oh[0].numel() * oh[0].element_size() + lh[0].numel() * 4)
+    del keep
+    return per_step, h2d_bytes, d2h_bytes
+
+
 def config_summary(res, pk, pk_src):
     case, info = res["case"], res["info"]
     ub, ms = res["unique_bytes"], res["ms"]
@@ -800,6 +864,13 @@ def main():
                          "d2h_bytes_per_step": int(oh.numel() * oh.element_size() + lh.numel() * 4),
                          "path": "psp_step_host: plan + plan upload + q H2D + run + o/lse D2H, synchronous; "
                                  "the K/V cache stays resident in HBM"}
+        pipe_s, pipe_in, pipe_out = e2e_pipelined(psp, step, case, tens, ws, stream, args.steps, args.warmup)
+        result["e2e_pipelined"] = {
+            "value": world * ub / pipe_s / 1e9, "unit": UNIT, "us_per_step": pipe_s * 1e6,
+            "h2d_bytes_per_step": pipe_in, "d2h_bytes_per_step": pipe_out,
+            "path": "psp_plan + psp_upload + psp_run per step with q H2D and o/lse D2H through pinned host "
+                    "buffers on copy streams; the host plans step i+1 while the device runs step i and "
+                    "waits for step i's output one step later; no L2 flush (K/V larger than L2)"}
     step.close()
     del head, ws, tens
 

@@ -205,6 +205,11 @@ class DecodeStep:
         self._check(psp_plan(self.handle, ctypes.byref(b)), "psp_plan")
         return self
 
+    def plan_batch(self, batch: psp_batch):
+        """psp_plan over a psp_batch made by make_batch (the caller keeps its arrays alive)."""
+        self._check(psp_plan(self.handle, ctypes.byref(batch)), "psp_plan")
+        return self
+
     def make_case_batch(self, case):
         """make_batch over a generated case's block tables (nested groups included)."""
         return self.make_batch(case.kv_len, case.page_indptr, case.page_indices, case.prefix_group,

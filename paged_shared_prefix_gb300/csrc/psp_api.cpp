@@ -5,6 +5,7 @@
 #include "psp.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <condition_variable>
 #include <cstdio>
@@ -74,12 +75,14 @@ int dtype_bytes(int32_t t) {
 }
 
 // A few host threads for the plan's comparisons of members' shared pages in large batches
-// (made on first use, joined when the handle is destroyed).  run(parts, f) calls f(0) on the
-// calling thread and f(1) .. f(parts - 1) on the workers and returns when every call has.
+// (made on first use, joined when the handle is destroyed).  run(n, f) calls f(i) once for
+// every item i in [0, n): the calling thread starts on the items at once and the workers
+// take items from the same counter as they wake, so a worker that wakes late costs the call
+// nothing (it finds the items taken, or the job gone).  Returns when every call has.
 class HostPool {
  public:
   explicit HostPool(int workers) {
-    for (int i = 0; i < workers; ++i) threads_.emplace_back([this, i] { loop(i + 1); });
+    for (int i = 0; i < workers; ++i) threads_.emplace_back([this] { loop(); });
   }
   ~HostPool() {
     {
@@ -90,24 +93,29 @@ class HostPool {
     for (std::thread& t : threads_) t.join();
   }
   int size() const { return static_cast<int>(threads_.size()) + 1; }
-  void run(int parts, const std::function<void(int)>& f) {
-    parts = std::max(1, std::min(parts, size()));
+  void run(int n, const std::function<void(int)>& f) {
     {
       std::lock_guard<std::mutex> g(m_);
       job_ = &f;
-      parts_ = parts;
-      pending_ = parts - 1;
+      n_ = n;
+      next_.store(0, std::memory_order_relaxed);
       ++gen_;
     }
-    if (parts > 1) cv_.notify_all();
-    f(0);
+    cv_.notify_all();
+    drain(f);
+    // every item is taken: withdraw the job from workers still waking, then wait for the
+    // ones inside it to finish their items
     std::unique_lock<std::mutex> l(m_);
-    done_.wait(l, [&] { return pending_ == 0; });
     job_ = nullptr;
+    done_.wait(l, [&] { return active_ == 0; });
   }
 
  private:
-  void loop(int id) {
+  void drain(const std::function<void(int)>& f) {
+    for (int i = next_.fetch_add(1, std::memory_order_relaxed); i < n_; i = next_.fetch_add(1, std::memory_order_relaxed))
+      f(i);
+  }
+  void loop() {
     uint64_t seen = 0;
     for (;;) {
       const std::function<void(int)>* job = nullptr;
@@ -116,19 +124,21 @@ class HostPool {
         cv_.wait(l, [&] { return stop_ || gen_ != seen; });
         if (stop_) return;
         seen = gen_;
-        if (id >= parts_) continue;  // not part of this run (a run waits for all of its parts)
+        if (!job_) continue;  // the run has already ended
         job = job_;
+        ++active_;
       }
-      (*job)(id);
+      drain(*job);
       std::lock_guard<std::mutex> g(m_);
-      if (--pending_ == 0) done_.notify_one();
+      if (--active_ == 0) done_.notify_one();
     }
   }
   std::vector<std::thread> threads_;
   std::mutex m_;
   std::condition_variable cv_, done_;
   const std::function<void(int)>* job_ = nullptr;
-  int parts_ = 0, pending_ = 0;
+  int n_ = 0, active_ = 0;
+  std::atomic<int> next_{0};
   uint64_t gen_ = 0;
   bool stop_ = false;
 };
@@ -408,11 +418,12 @@ psp_status build_plan(psp_handle* h, const psp_batch* bt, HostPlan& P) {
     }
   }
   if (parts > 1 && h->pool) {
-    const int n = std::min(parts, h->pool->size());
+    // items of about 16k compared page ids, in request order
+    const int64_t per_item = std::max<int64_t>(1, (int64_t{1} << 14) * B / compared);
+    const int n = static_cast<int>(cdiv(B, per_item));
     std::vector<int> found(n, -1);
     const std::function<void(int)> part = [&](int i) {
-      found[i] = first_mismatch(static_cast<int>(static_cast<int64_t>(B) * i / n),
-                                static_cast<int>(static_cast<int64_t>(B) * (i + 1) / n));
+      found[i] = first_mismatch(static_cast<int>(per_item * i), static_cast<int>(std::min<int64_t>(B, per_item * (i + 1))));
     };
     h->pool->run(n, part);
     for (int i = 0; i < n && bad < 0; ++i) bad = found[i];
