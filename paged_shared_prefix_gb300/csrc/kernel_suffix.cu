@@ -53,7 +53,11 @@ struct SufCfg {
   __host__ __device__ static constexpr int min_ctas() { return (KV == PSP_KV_FP8 && D == 128 && NST == 3) ? 4 : 1; }
 };
 
-template <int KV, int D, int NW, int NST>
+// PT (page tiles): the block table is paged with pages of >= 16 tokens, so each 16-token
+// sub-tile lies in one page; a sub-tile then costs one table entry and one address
+// computation, its rows following at a fixed stride.  Otherwise (page size < 16, or the
+// token-flat kv_indices) every row is looked up on its own.
+template <int KV, int D, int NW, int NST, bool PT>
 __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>()) suffix_kernel(const StepParams p) {
   using C = SufCfg<KV, D>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -177,38 +181,71 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   // next row's table load above the previous row's copy.
   constexpr int kRowsPerPass = 32 / C::kChunks;
   constexpr int kRowIters = 16 / kRowsPerPass;
+  constexpr int kPgSlots = PT ? 1 : kRowIters;  // table entries a lane holds per sub-tile
   const int mask = (1 << shift) - 1;
-  auto load_pages = [&](int i, int32_t (&pg)[kRowIters]) {
+  // page tiles: this lane's first source bytes (its row within a pass, its 16-byte chunk)
+  const unsigned char* klane = nullptr;
+  const unsigned char* vlane = nullptr;
+  if constexpr (PT) {
+    const int64_t lane_off = static_cast<int64_t>(lane / C::kChunks) * row_stride + (lane % C::kChunks) * 16;
+    klane = kbase + lane_off;
+    vlane = vbase + lane_off;
+  }
+  auto load_pages = [&](int i, int32_t (&pg)[kPgSlots]) {
     const int tb = t0 + (warp + i * NW) * 16;
+    if constexpr (PT) {
+      pg[0] = __ldg(list + (tb >> shift));  // callers pass only sub-tiles of the split (tb < t1)
+    } else {
 #pragma unroll
-    for (int k = 0; k < kRowIters; ++k) {
-      const int t = tb + lane / C::kChunks + k * kRowsPerPass;
-      pg[k] = t < t1 ? __ldg(list + (t >> shift)) : -1;
+      for (int k = 0; k < kRowIters; ++k) {
+        const int t = tb + lane / C::kChunks + k * kRowsPerPass;
+        pg[k] = t < t1 ? __ldg(list + (t >> shift)) : -1;
+      }
     }
   };
   // the same for the ring's first NST sub-tiles, from the descriptor where it holds them
-  auto load_first_pages = [&](int i, int32_t (&pg)[kRowIters]) {
+  auto load_first_pages = [&](int i, int32_t (&pg)[kPgSlots]) {
     if (desc_pages && warp + i * NW < kDescPages) {
-      const int tb = t0 + (warp + i * NW) * 16;
+      if constexpr (PT) {
+        pg[0] = first_pg[i];
+      } else {
+        const int tb = t0 + (warp + i * NW) * 16;
 #pragma unroll
-      for (int k = 0; k < kRowIters; ++k) pg[k] = tb + lane / C::kChunks + k * kRowsPerPass < t1 ? first_pg[i] : -1;
+        for (int k = 0; k < kRowIters; ++k) pg[k] = tb + lane / C::kChunks + k * kRowsPerPass < t1 ? first_pg[i] : -1;
+      }
     } else {
       load_pages(i, pg);
     }
   };
-  auto issue = [&](int i, const int32_t (&pg)[kRowIters]) {
+  auto issue = [&](int i, const int32_t (&pg)[kPgSlots]) {
     const int tb = t0 + (warp + i * NW) * 16;
     unsigned char* kdst = ring + (i % NST) * C::kStageBytes;
     const int c = lane % C::kChunks;
+    if constexpr (PT) {
+      // one page holds the whole sub-tile: its first row, then kRowsPerPass rows per pass
+      const int64_t base = ((static_cast<int64_t>(pg[0]) << shift) | (tb & mask)) * row_stride;
+      const unsigned char* ks = klane + base;
+      const unsigned char* vs = vlane + base;
+      const int64_t pass = static_cast<int64_t>(kRowsPerPass) * row_stride;
 #pragma unroll
-    for (int k = 0; k < kRowIters; ++k) {
-      const int r = lane / C::kChunks + k * kRowsPerPass;
-      const bool valid = pg[k] >= 0;
-      const int64_t slot = (static_cast<int64_t>(pg[k]) << shift) | ((tb + r) & mask);
-      const int64_t off = valid ? slot * row_stride + c * 16 : 0;
-      const uint32_t d = smem_u32(kdst + r * C::kRowBytes + swz<C::kChunks>(r, c) * 16);
-      cp_async_16(d, kbase + off, valid);
-      cp_async_16(d + C::kTileBytes, vbase + off, valid);
+      for (int k = 0; k < kRowIters; ++k) {
+        const int r = lane / C::kChunks + k * kRowsPerPass;
+        const bool valid = tb + r < t1;
+        const uint32_t d = smem_u32(kdst + r * C::kRowBytes + swz<C::kChunks>(r, c) * 16);
+        cp_async_16(d, valid ? ks + k * pass : ks, valid);
+        cp_async_16(d + C::kTileBytes, valid ? vs + k * pass : vs, valid);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kRowIters; ++k) {
+        const int r = lane / C::kChunks + k * kRowsPerPass;
+        const bool valid = pg[k] >= 0;
+        const int64_t slot = (static_cast<int64_t>(pg[k]) << shift) | ((tb + r) & mask);
+        const int64_t off = valid ? slot * row_stride + c * 16 : 0;
+        const uint32_t d = smem_u32(kdst + r * C::kRowBytes + swz<C::kChunks>(r, c) * 16);
+        cp_async_16(d, kbase + off, valid);
+        cp_async_16(d + C::kTileBytes, vbase + off, valid);
+      }
     }
   };
 
@@ -232,7 +269,7 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   // sub-tiles NST-U further on, then waits for its own U, so NST-U sub-tiles stay in flight
   // while it computes.  The block-table entries of a sub-tile are loaded one iteration
   // before its copies, so no copy waits on a dependent table load.
-  int32_t pages[U][kRowIters];
+  int32_t pages[U][kPgSlots];
 #pragma unroll
   for (int i = 0; i < NST; ++i) {
     if (i < my_n) {
@@ -452,14 +489,14 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   suffix_grid_tail(p, grid_last);
 }
 
-template <int KV, int D, int NW, int NST>
-cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
+template <int KV, int D, int NW, int NST, bool PT>
+cudaError_t launch_pt(const StepParams& p, int num_splits, cudaStream_t s) {
   using C = SufCfg<KV, D>;
   const int ring = NW * NST * C::kStageBytes;
   const int epi = (NW * 8 * D + 2 * NW * 8) * 4;
   const int bytes = (ring > epi ? ring : epi) + C::template pre_rows<NST>() * (D + 1) * 4;
-  auto kern = suffix_kernel<KV, D, NW, NST>;
-  cudaError_t e = ensure_smem_limit<suffix_kernel<KV, D, NW, NST>>(bytes);
+  auto kern = suffix_kernel<KV, D, NW, NST, PT>;
+  cudaError_t e = ensure_smem_limit<suffix_kernel<KV, D, NW, NST, PT>>(bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_splits * p.hkv);
@@ -474,6 +511,12 @@ cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int KV, int D, int NW, int NST>
+cudaError_t launch_t(const StepParams& p, int num_splits, cudaStream_t s) {
+  if (!p.token_flat && p.page_shift >= 4) return launch_pt<KV, D, NW, NST, true>(p, num_splits, s);
+  return launch_pt<KV, D, NW, NST, false>(p, num_splits, s);
 }
 
 }  // namespace

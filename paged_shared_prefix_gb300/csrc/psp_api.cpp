@@ -1125,11 +1125,11 @@ psp_status psp_run(psp_handle* h, const psp_tensors* t, void* stream) {
   const psp_status bad = check_tensors(h, t);
   if (bad) return bad;
   const HostPlan& P = h->plan;
+  h->recorded = 0;  // an empty step launches nothing and reports no kernel times
   if (P.B == 0) return PSP_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StepParams p = make_params(h, t);
   int slot = 0;
-  h->recorded = 0;
   psp_status st;
   const int nd = static_cast<int>(P.item_chunk_dense.size());
   const int nc = static_cast<int>(P.item_chunk_cascade.size());

@@ -170,6 +170,38 @@ def test_edge_cases():
     assert max_err(o, ro) <= TOL["fp8_e4m3"] and max_err(lse, rl) <= TOL["fp8_e4m3"]
 
 
+def test_empty_batch_then_replan():
+    """A batch of no requests plans, uploads and runs (nothing is launched and the device
+    status stays clear); the same handle then plans and runs a real batch correctly."""
+    case = workloads.make_case("agent", 9, batch=6, prefix_len=160, private_range=(1, 90))
+    tens = device_tensors(case)
+    step = psp.DecodeStep.for_case(case, **READ_ONCE_ALWAYS)
+    z = np.zeros(0, np.int32)
+    step.plan(z, np.zeros(1, np.int32), z)
+    ws = torch.empty(max(step.workspace_size(), 256), dtype=torch.uint8, device="cuda:0")
+    step.upload(ws)
+    w = case.workload
+    o = torch.full((case.batch, w.num_q_heads, w.head_dim), float("nan"), dtype=torch.bfloat16, device="cuda:0")
+    lse = torch.full((case.batch, w.num_q_heads), float("nan"), dtype=torch.float32, device="cuda:0")
+    step.set_kernel_timing(True)
+    step.run(tens["q"], tens["k_pool"], tens["v_pool"], o, lse)
+    torch.cuda.synchronize()
+    assert step.kernel_times() == []
+    assert step.device_status() == 0
+    assert torch.isnan(lse).all()  # nothing was written
+    step.plan_case(case)
+    ws = torch.empty(step.workspace_size(), dtype=torch.uint8, device="cuda:0")
+    step.upload(ws)
+    step.run(tens["q"], tens["k_pool"], tens["v_pool"], o, lse)
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    assert len(step.kernel_times()) >= 1
+    ro, rl = oracle.attend_all(case)
+    assert max_err(o.float().cpu().numpy(), ro) <= TOL["bf16"]
+    assert max_err(lse.cpu().numpy(), rl) <= TOL["bf16"]
+    step.close()
+
+
 def test_step_host_matches_run():
     case = workloads.make_case("agent", 8, batch=10, prefix_len=192, private_range=(1, 200))
     w = case.workload
