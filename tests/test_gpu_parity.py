@@ -75,6 +75,36 @@ def test_page_sizes_and_layouts_bit_identical():
     assert max_err(outs[0][0], ref_o) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("name", ["llama8b_noshare", "fp8_large"])
+def test_every_page_size_bit_identical(name):
+    """Every supported page size gives the same bits: pages smaller than a 16-token sub-tile
+    (one table entry per row), pages holding whole sub-tiles (one entry per sub-tile) and a
+    page larger than any context; suffixes that end mid-page, with and without a shared prefix."""
+    kw = dict(batch=3, private_range=(1, 700)) if name == "llama8b_noshare" else dict(
+        batch=4, prefix_len=0, private_range=(1, 700))
+    outs = [run_case(workloads.make_case(name, 4, page_size=ps, **kw)) for ps in (1, 2, 4, 8, 16, 32, 256, 1024)]
+    for o, l in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
+    case = workloads.make_case(name, 4, page_size=16, **kw)
+    ref_o, ref_lse = oracle.attend_all(case)
+    tol = TOL[case.workload.kv_dtype]
+    assert max_err(outs[0][0], ref_o) <= tol and max_err(outs[0][1], ref_lse) <= tol
+
+
+@pytest.mark.parametrize("ps", [2, 4, 8, 32, 256])
+@pytest.mark.parametrize("name", ["agent", "fp8_large"])
+def test_shared_prefix_at_other_page_sizes(name, ps):
+    """Shared-prefix steps at page sizes the other tests leave out (the dense kernel's
+    per-page boxes of 2-8 tokens, a prefix tail kept private by large pages) against the
+    oracle, dense and cascade."""
+    case = workloads.make_case(name, 5, batch=12, prefix_len=600, private_range=(1, 300), page_size=ps)
+    tol = TOL[case.workload.kv_dtype]
+    ref_o, ref_lse = oracle.attend_all(case)
+    for thr in (1, 1 << 20):
+        o, lse = run_case(case, threshold=thr)
+        assert max_err(o, ref_o) <= tol and max_err(lse, ref_lse) <= tol, (thr, max_err(o, ref_o))
+
+
 def test_token_flat_lowering_bit_identical():
     for name, kw in (("agent", dict(batch=6, prefix_len=160, private_range=(1, 200))),
                      ("fp8_large", dict(batch=4, prefix_len=128, private_range=(1, 150))),
