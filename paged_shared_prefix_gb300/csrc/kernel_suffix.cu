@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
     sc1 *= __shfl_sync(0xffffffffu, q_scale, 8 * qc + 4);
   }
 
-  // -------- asynchronous gather of one 16-token sub-tile (K and V) into ring stage i % NST.
+  // -------- asynchronous gather of one 16-token sub-tile (K and V) into ring stage i % NST
+  // (the callers keep the stage index, so no division by a ring depth of 3 runs per copy).
   // The block-table entries of a sub-tile's rows are loaded one iteration ahead of its
   // copies (load_pages), so no copy waits on a dependent table load: the copies are
   // asm statements with a memory clobber, which keeps the compiler from hoisting the
@@ -217,9 +218,9 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
       load_pages(i, pg);
     }
   };
-  auto issue = [&](int i, const int32_t (&pg)[kPgSlots]) {
+  auto issue = [&](int i, int stage, const int32_t (&pg)[kPgSlots]) {
     const int tb = t0 + (warp + i * NW) * 16;
-    unsigned char* kdst = ring + (i % NST) * C::kStageBytes;
+    unsigned char* kdst = ring + stage * C::kStageBytes;
     const int c = lane % C::kChunks;
     if constexpr (PT) {
       // one page holds the whole sub-tile: its first row, then kRowsPerPass rows per pass
@@ -263,6 +264,9 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   // fp8: the running max is kept 8 below the true max, so P <= 2^8 (inside e4m3's range and
   // clear of its subnormals); l carries the same factor, so O / l and m + log2(l) are exact.
   constexpr float kPShift = (KV == PSP_KV_FP8) ? 8.f : 0.f;
+  // fp8: the running max moves (and O is rescaled) only when a head's tile max passes it by
+  // more than kLag, so P <= 2^(8 + kLag) = 445.7, still inside e4m3's largest code 448
+  constexpr float kLag = 0.8f;
 
   // Ring schedule: sub-tiles 0 .. NST-1 are issued before the loop (one cp.async group each).
   // Every later iteration first refills the U stages its predecessor consumed with the
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   for (int i = 0; i < NST; ++i) {
     if (i < my_n) {
       load_first_pages(i, pages[0]);
-      issue(i, pages[0]);
+      issue(i, i, pages[0]);
     }
     cp_async_commit();
   }
@@ -286,12 +290,15 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   // group, which the loop waits for one iteration later than its first sub-tiles.
   if (suffix_cta_late(p, cta, kPre)) prefetch_prefix_rows<D, NW * 32>(p, cta, pre_o, pre_l);
 
-  for (int i0 = 0; i0 < my_n; i0 += U) {
+  // ring stage of sub-tile i0 (i0 % NST, kept as a running index)
+  auto wrap = [](int x) { return x >= NST ? x - NST : x; };  // x < 2 * NST
+  int st0 = 0;
+  for (int i0 = 0; i0 < my_n; i0 += U, st0 = wrap(st0 + U)) {
     if (i0 > 0) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int nx = i0 + NST - U + u;
-        if (nx < my_n) issue(nx, pages[u]);
+        if (nx < my_n) issue(nx, wrap(st0 + NST - U + u), pages[u]);
         cp_async_commit();
         if (nx + U < my_n) load_pages(nx + U, pages[u]);  // in flight while this iteration computes
         // the block-table entries of a sub-tile kTablePrefetch iterations later, pulled into L2
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
     auto load_v = [&]() {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const unsigned char* vt = ring + ((i0 + u) % NST) * C::kStageBytes + C::kTileBytes;
+        const unsigned char* vt = ring + wrap(st0 + u) * C::kStageBytes + C::kTileBytes;
 #pragma unroll
         for (int f = 0; f < kVFrag; ++f)
           ldsm_x4_t(vf[u][f], smem_u32(vt + vrow * C::kRowBytes + swz<C::kChunks>(vrow, 2 * f + (lj & 1)) * 16));
@@ -333,7 +340,7 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
     };
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const unsigned char* kt = ring + ((i0 + u) % NST) * C::kStageBytes;
+      const unsigned char* kt = ring + wrap(st0 + u) * C::kStageBytes;
 #pragma unroll
       for (int f = 0; f < kKFrag; ++f)
         ldsm_x4(kf[u][f], smem_u32(kt + krow * C::kRowBytes + swz<C::kChunks>(krow, 2 * f + (lj >> 1)) * 16));
@@ -375,7 +382,11 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
     }
     mx0 = xor_max<4, 16>(mx0) - kPShift;
     mx1 = xor_max<4, 16>(mx1) - kPShift;
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    // fp8 (bound by its instruction count): rescale only when some running max passed its
+    // reference by more than kLag, which stops once the maxima settle; bf16 (bound by
+    // memory) moves the max and rescales every sub-tile
+    const bool move = KV != PSP_KV_FP8 || __any_sync(0xffffffffu, mx0 > m0 + kLag || mx1 > m1 + kLag);
+    const float mn0 = move ? fmaxf(m0, mx0) : m0, mn1 = move ? fmaxf(m1, mx1) : m1;
     float pr[U][4];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -384,9 +395,7 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
       pr[u][2] = ex2_ftz(x[u][2] - mn0);
       pr[u][3] = ex2_ftz(x[u][3] - mn1);
     }
-    // fp8 (bound by its instruction count): rescale only when some running max moved,
-    // which stops once the maxima settle; bf16 (bound by memory) rescales every sub-tile
-    if (KV != PSP_KV_FP8 || __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+    if (move) {
       const float a0 = ex2_ftz(m0 - mn0), a1 = ex2_ftz(m1 - mn1);
       l0 *= a0;
       l1 *= a1;
