@@ -264,9 +264,6 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   // fp8: the running max is kept 8 below the true max, so P <= 2^8 (inside e4m3's range and
   // clear of its subnormals); l carries the same factor, so O / l and m + log2(l) are exact.
   constexpr float kPShift = (KV == PSP_KV_FP8) ? 8.f : 0.f;
-  // fp8: the running max moves (and O is rescaled) only when a head's tile max passes it by
-  // more than kLag, so P <= 2^(8 + kLag) = 445.7, still inside e4m3's largest code 448
-  constexpr float kLag = 0.8f;
 
   // Ring schedule: sub-tiles 0 .. NST-1 are issued before the loop (one cp.async group each).
   // Every later iteration first refills the U stages its predecessor consumed with the
@@ -382,11 +379,7 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
     }
     mx0 = xor_max<4, 16>(mx0) - kPShift;
     mx1 = xor_max<4, 16>(mx1) - kPShift;
-    // fp8 (bound by its instruction count): rescale only when some running max passed its
-    // reference by more than kLag, which stops once the maxima settle; bf16 (bound by
-    // memory) moves the max and rescales every sub-tile
-    const bool move = KV != PSP_KV_FP8 || __any_sync(0xffffffffu, mx0 > m0 + kLag || mx1 > m1 + kLag);
-    const float mn0 = move ? fmaxf(m0, mx0) : m0, mn1 = move ? fmaxf(m1, mx1) : m1;
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
     float pr[U][4];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -395,7 +388,9 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
       pr[u][2] = ex2_ftz(x[u][2] - mn0);
       pr[u][3] = ex2_ftz(x[u][3] - mn1);
     }
-    if (move) {
+    // fp8 (bound by its instruction count): rescale only when some running max moved,
+    // which stops once the maxima settle; bf16 (bound by memory) rescales every sub-tile
+    if (KV != PSP_KV_FP8 || __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
       const float a0 = ex2_ftz(m0 - mn0), a1 = ex2_ftz(m1 - mn1);
       l0 *= a0;
       l1 *= a1;
