@@ -266,10 +266,14 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   constexpr float kPShift = (KV == PSP_KV_FP8) ? 8.f : 0.f;
 
   // Ring schedule: sub-tiles 0 .. NST-1 are issued before the loop (one cp.async group each).
-  // Every later iteration first refills the U stages its predecessor consumed with the
-  // sub-tiles NST-U further on, then waits for its own U, so NST-U sub-tiles stay in flight
-  // while it computes.  The block-table entries of a sub-tile are loaded one iteration
-  // before its copies, so no copy waits on a dependent table load.
+  // bf16 (U = 1): every later iteration first refills the stage its predecessor consumed
+  // with the sub-tile NST-1 further on, then waits for its own, which was issued one
+  // iteration earlier.  fp8 (U = 2): a refill at the top of the iteration would leave the
+  // second of its own sub-tiles only a moment to arrive, so each iteration refills its two
+  // stages as soon as their fragments are loaded, with the sub-tiles NST further on.  The
+  // block-table entries of a sub-tile are loaded one iteration before its copies, so no
+  // copy waits on a dependent table load.
+  constexpr bool kEarlyRefill = U == 2;
   int32_t pages[U][kPgSlots];
 #pragma unroll
   for (int i = 0; i < NST; ++i) {
@@ -291,11 +295,12 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   auto wrap = [](int x) { return x >= NST ? x - NST : x; };  // x < 2 * NST
   int st0 = 0;
   for (int i0 = 0; i0 < my_n; i0 += U, st0 = wrap(st0 + U)) {
-    if (i0 > 0) {
+    // refill the stages of sub-tiles i0 + u - dist with the sub-tiles NST further on
+    auto refill = [&](int dist) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int nx = i0 + NST - U + u;
-        if (nx < my_n) issue(nx, wrap(st0 + NST - U + u), pages[u]);
+        const int nx = i0 + NST - dist + u;
+        if (nx < my_n) issue(nx, wrap(st0 + (NST - dist) % NST + u), pages[u]);
         cp_async_commit();
         if (nx + U < my_n) load_pages(nx + U, pages[u]);  // in flight while this iteration computes
         // the block-table entries of a sub-tile kTablePrefetch iterations later, pulled into L2
@@ -304,7 +309,8 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
         const int pf = nx + U + kTablePrefetch;
         if (lane == 0 && pf < my_n) prefetch_l2(list + ((t0 + (warp + pf * NW) * 16) >> shift));
       }
-    }
+    };
+    if (!kEarlyRefill && i0 > 0) refill(U);  // the stages the previous iteration consumed
     cp_async_wait<NST - U>();
     __syncwarp();
 
@@ -369,6 +375,10 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
     }
 
     if constexpr (KV != PSP_KV_BF16) load_v();
+    if constexpr (kEarlyRefill) {
+      __syncwarp();  // every lane's fragment loads of these stages come first
+      refill(0);
+    }
 
     // ---- online softmax over the iteration's tokens
     float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
@@ -443,7 +453,8 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
         mma_e4m3(o[2 * cc + 1], ao, pb[0], pb[U - 1]);
       }
     }
-    __syncwarp();  // every lane's fragment loads are done before the next refill of these stages
+    // bf16: every lane's fragment loads are done before the next refill of these stages
+    if constexpr (!kEarlyRefill) __syncwarp();
   }
   const bool grid_last = suffix_grid_arrive(p);
   cp_async_commit();  // copies issued after the loop's last commit (a warp without refills)
