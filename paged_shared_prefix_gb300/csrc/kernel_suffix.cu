@@ -290,6 +290,9 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   // after every first copy is in flight; a late CTA's prefix rows join the next cp.async
   // group, which the loop waits for one iteration later than its first sub-tiles.
   if (suffix_cta_late(p, cta, kPre)) prefetch_prefix_rows<D, NW * 32>(p, cta, pre_o, pre_l);
+  // e4m3: only the late flag is carried through the loop, the rest of the CTA's request
+  // state is read again after it (registers are that kernel's limit; bf16 keeps it)
+  const bool late = cta.late;
 
   // ring stage of sub-tile i0 (i0 % NST, kept as a running index)
   auto wrap = [](int x) { return x >= NST ? x - NST : x; };  // x < 2 * NST
@@ -455,6 +458,10 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
     }
     // bf16: every lane's fragment loads are done before the next refill of these stages
     if constexpr (!kEarlyRefill) __syncwarp();
+  }
+  if constexpr (KV == PSP_KV_FP8) {
+    cta = suffix_cta(p, reload_split_desc(p, split), split, h, kPre);
+    if (late) suffix_cta_mark_late(p, cta, kPre);
   }
   const bool grid_last = suffix_grid_arrive(p);
   cp_async_commit();  // copies issued after the loop's last commit (a warp without refills)

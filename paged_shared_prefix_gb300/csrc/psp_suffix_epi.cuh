@@ -32,6 +32,25 @@ __device__ __forceinline__ SplitDesc load_split_desc(const StepParams& p, int sp
   return d;
 }
 
+// The same record read again late in a CTA (volatile, so the compiler keeps the first
+// read's registers free in between instead of reusing them).
+__device__ __forceinline__ SplitDesc reload_split_desc(const StepParams& p, int split) {
+  const int4* src = reinterpret_cast<const int4*>(p.split_desc + split);
+  int4 a, b;
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];\n" : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w) : "l"(src));
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];\n" : "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w) : "l"(src + 1));
+  SplitDesc d;
+  d.b = a.x;
+  d.t0 = a.y;
+  d.t1 = a.z;
+  d.list_paged = a.w;
+  d.list_flat = b.x;
+  d.part0 = b.y;
+  d.n_parts = b.z;
+  d.one_split = b.w;
+  return d;
+}
+
 // What the end of a suffix CTA needs to know about its request.
 struct SuffixCta {
   int split, h, b;
@@ -60,6 +79,13 @@ __device__ __forceinline__ SuffixCta suffix_cta(const StepParams& p, const Split
   return c;
 }
 
+// The state of a CTA that found its prefix rows complete (suffix_cta_late).
+__device__ __forceinline__ void suffix_cta_mark_late(const StepParams& p, SuffixCta& c, int pre_rows) {
+  c.late = true;
+  c.solo = true;
+  c.pre_smem = c.n_parts * p.group <= pre_rows;
+}
+
 // Concurrent form: a one-split request whose CTA finds every prefix row done (the prefix
 // CTAs count their rows after their partials and arrivals) merges like a solo request of
 // the sequential form, from prefetched rows, without its counter.  Called by every thread
@@ -73,9 +99,7 @@ __device__ __forceinline__ bool suffix_cta_late(const StepParams& p, SuffixCta& 
   __syncthreads();
   if (!prefix_complete) return false;
   __threadfence();  // the prefix partials were fenced before their rows were counted
-  c.late = true;
-  c.solo = true;
-  c.pre_smem = c.n_parts * p.group <= pre_rows;
+  suffix_cta_mark_late(p, c, pre_rows);
   return c.pre_smem;
 }
 
