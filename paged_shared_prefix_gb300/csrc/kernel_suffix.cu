@@ -48,9 +48,10 @@ struct SufCfg {
   template <int NST>
   __host__ __device__ static constexpr int pre_rows() { return (KV == PSP_KV_FP8 && D == 128 && NST == 3) ? 8 : kPreRows; }
   // resident CTAs per SM the register allocation must allow: four for that e4m3 ring (128
-  // registers a thread), otherwise whatever the compiler chooses
+  // registers a thread), three for the 2-stage bf16 ring (170; shared memory allows three),
+  // otherwise whatever the compiler chooses
   template <int NST>
-  __host__ __device__ static constexpr int min_ctas() { return (KV == PSP_KV_FP8 && D == 128 && NST == 3) ? 4 : 1; }
+  __host__ __device__ static constexpr int min_ctas() { return (KV == PSP_KV_FP8 && D == 128 && NST == 3) ? 4 : (KV == PSP_KV_BF16 && D == 128 && NST == 2) ? 3 : 1; }
 };
 
 // PT (page tiles): the block table is paged with pages of >= 16 tokens, so each 16-token
@@ -266,14 +267,12 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   constexpr float kPShift = (KV == PSP_KV_FP8) ? 8.f : 0.f;
 
   // Ring schedule: sub-tiles 0 .. NST-1 are issued before the loop (one cp.async group each).
-  // bf16 (U = 1): every later iteration first refills the stage its predecessor consumed
-  // with the sub-tile NST-1 further on, then waits for its own, which was issued one
-  // iteration earlier.  fp8 (U = 2): a refill at the top of the iteration would leave the
-  // second of its own sub-tiles only a moment to arrive, so each iteration refills its two
-  // stages as soon as their fragments are loaded, with the sub-tiles NST further on.  The
-  // block-table entries of a sub-tile are loaded one iteration before its copies, so no
-  // copy waits on a dependent table load.
-  constexpr bool kEarlyRefill = U == 2;
+  // Each iteration waits for its own U sub-tiles and refills their stages, with the sub-tiles
+  // NST further on, as soon as their fragments are in registers (after the score products),
+  // so every sub-tile is issued an iteration or more before it is needed (a refill at the top
+  // of the next iteration would leave the second of an e4m3 iteration's sub-tiles only a
+  // moment to arrive).  The block-table entries of a sub-tile are loaded one iteration
+  // before its copies, so no copy waits on a dependent table load.
   int32_t pages[U][kPgSlots];
 #pragma unroll
   for (int i = 0; i < NST; ++i) {
@@ -298,12 +297,12 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
   auto wrap = [](int x) { return x >= NST ? x - NST : x; };  // x < 2 * NST
   int st0 = 0;
   for (int i0 = 0; i0 < my_n; i0 += U, st0 = wrap(st0 + U)) {
-    // refill the stages of sub-tiles i0 + u - dist with the sub-tiles NST further on
-    auto refill = [&](int dist) {
+    // refill the stages of sub-tiles i0 + u with the sub-tiles NST further on
+    auto refill = [&]() {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int nx = i0 + NST - dist + u;
-        if (nx < my_n) issue(nx, wrap(st0 + (NST - dist) % NST + u), pages[u]);
+        const int nx = i0 + NST + u;
+        if (nx < my_n) issue(nx, wrap(st0 + u), pages[u]);
         cp_async_commit();
         if (nx + U < my_n) load_pages(nx + U, pages[u]);  // in flight while this iteration computes
         // the block-table entries of a sub-tile kTablePrefetch iterations later, pulled into L2
@@ -313,7 +312,6 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
         if (lane == 0 && pf < my_n) prefetch_l2(list + ((t0 + (warp + pf * NW) * 16) >> shift));
       }
     };
-    if (!kEarlyRefill && i0 > 0) refill(U);  // the stages the previous iteration consumed
     cp_async_wait<NST - U>();
     __syncwarp();
 
@@ -378,10 +376,8 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
     }
 
     if constexpr (KV != PSP_KV_BF16) load_v();
-    if constexpr (kEarlyRefill) {
-      __syncwarp();  // every lane's fragment loads of these stages come first
-      refill(0);
-    }
+    __syncwarp();  // every lane's fragment loads of these stages come first
+    refill();
 
     // ---- online softmax over the iteration's tokens
     float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
@@ -456,8 +452,6 @@ __global__ void __launch_bounds__(NW * 32, SufCfg<KV, D>::template min_ctas<NST>
         mma_e4m3(o[2 * cc + 1], ao, pb[0], pb[U - 1]);
       }
     }
-    // bf16: every lane's fragment loads are done before the next refill of these stages
-    if constexpr (!kEarlyRefill) __syncwarp();
   }
   if constexpr (KV == PSP_KV_FP8) {
     cta = suffix_cta(p, reload_split_desc(p, split), split, h, kPre);
