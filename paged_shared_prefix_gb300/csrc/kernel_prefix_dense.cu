@@ -222,18 +222,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         shift = p.page_shift;
       }
       if constexpr (GATHER) {
-        // small pages: the warp gathers every tile with cp.async (gather_tile).  A stage's
-        // barrier is arrived on once the next stage's copies are issued and its own have
-        // landed and been made visible to the tensor cores' proxy, so two stages are in
-        // flight at a time.
+        // small pages: the warp gathers every tile with cp.async (gather_tile).  Stage s (K_0
+        // is stage -1) is arrived on once its copies have landed and been made visible to the
+        // tensor cores' proxy, which the warp checks for at the top of iteration s + L, so the
+        // copies of L stages stay in flight (L = NS - 1 keeps the producer from waiting on a
+        // stage the consumer has yet to receive).
+        constexpr int L = NS - 1;
         const unsigned char* kpool = static_cast<const unsigned char*>(p.k_pool);
         const unsigned char* vpool = static_cast<const unsigned char*>(p.v_pool);
+        auto stage_bar = [&](int st) { return st < 0 ? bar(C::kBarK0) : bar(C::kBarFull + st % NS); };
         int cur[4], nxt[4];
         tile_slots(cur, list, shift, t0, t1, 0, lane);
         gather_tile<FP8>(kpool, p.hkv, h, base + C::kOffK0, cur, lane);
         cp_async_commit();
-        uint32_t pending = bar(C::kBarK0);
-        for (int j = 0; j < n_tiles; ++j) {
+        int arrived = -2;  // the last stage arrived on
+        int j = 0;
+        for (; j < n_tiles; ++j) {
+          if (j - L >= -1) {
+            cp_async_wait<L - 1>();  // stage j - L and every earlier one have landed
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(stage_bar(j - L));
+            arrived = j - L;
+          }
           const int st = j % NS;
           if (j >= NS) {
             int ok = 0;
@@ -249,18 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
           }
           cp_async_commit();
-          cp_async_wait<1>();  // every earlier stage (and K_0) has landed
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(pending);
-          pending = bar(C::kBarFull + st);
         }
-        // drain: every copy lands before the CTA may exit; the last stage's arrival (after an
-        // abort, on a stage nobody waits for)
+        // drain: every copy lands before the CTA may exit; the stages issued but not yet
+        // arrived on (after an abort, stages nobody waits for)
         cp_async_wait<0>();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(pending);
+        if (lane == 0)
+          for (int st = arrived + 1; st < j; ++st) mbar_arrive(stage_bar(st));
         __syncwarp();
       } else {
       if (lane == 0) {
