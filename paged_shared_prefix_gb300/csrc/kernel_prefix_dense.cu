@@ -692,9 +692,10 @@ cudaError_t launch_t(const StepParams& p, int num_items, cudaStream_t s) {
   static_assert(bytes <= 232448, "dense prefix CTA exceeds the shared memory of one SM");
   const int grid = num_items * p.hkv;
   // one TMA box per page costs the copy engine more than the producer warp's own 16-byte
-  // copies once pages hold 1 or 2 tokens (e4m3 batch, dense kernel: 1,144 against 372 us at
-  // page size 1; 229 against 368 us at page size 8 the other way)
-  if (p.token_flat || p.page_shift <= 1) {
+  // copies once pages hold few tokens: up to 2 for e4m3 (dense kernel on the e4m3 batch:
+  // 1,148 against 375 us at page size 1, 346 against ~375 us at 4), up to 4 for bf16 (agent
+  // batch: 49.2 against 43.5 us at page size 4, 34.9 against 43.2 us at 8)
+  if (p.token_flat || p.page_shift <= (FP8 ? 1 : 2)) {
     e = ensure_smem_limit<prefix_dense_kernel<FP8, true>>(bytes);
     if (e != cudaSuccess) return e;
     prefix_dense_kernel<FP8, true><<<grid, kThreads, bytes, s>>>(p, kmap, vmap, static_cast<int>(slots));
